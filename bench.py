@@ -1,0 +1,341 @@
+"""Benchmark of the single-GPU MoE layer forward.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload mixtral] [--no-cpu-baseline]
+
+One step = one whole layer forward (router GEMM, scoring/Top-k, statistics, dispatch, grouped
+SwiGLU expert GEMMs, shared experts, combine) over one batch of synthetic tokens already in HBM.
+The timed step issues the same kernels moe_forward issues, stage by stage through the C ABI,
+with CUDA events around the expert stage so that the grouped GEMM's share is measured live.
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own replica on its own token
+batch (the layer shards over tokens with no exchange), so the work scales weakly.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer fwd tokens/s on 1 B300; % of tensor-peak (prefill) / HBM BW (decode)"
+PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def workload_flops_bytes(wl):
+    """Algorithmic FLOPs and bytes of one layer forward (per step).
+
+    FLOPs = T * (2 d E  +  (k + shared) * 3 * 2 d F)  (router + SwiGLU experts)
+    bytes = touched expert weights + router weights + x read + out write.
+    """
+    T, d, E, k, F, Fs = wl.T, wl.d, wl.E, wl.k, wl.F, wl.F_sh
+    ffn = T * k * 3 * 2 * d * F + T * 3 * 2 * d * Fs
+    router = T * 2 * d * E
+    weights = (E * 3 * d * F + 3 * d * Fs + E * d) * 2
+    act = 2 * T * d * 2
+    return {"flops": ffn + router, "ffn_flops": ffn, "bytes": weights + act}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+        return int(n)
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(wl, inp_host, S):
+    """The oracle (as it stands) on an independent batch of the first S tokens."""
+    from oracle import moe_oracle as O
+    h = dict(inp_host)
+    h["x"] = h["x"][:S]
+    sub = wl.replace(T=S)
+    t0 = time.perf_counter()
+    if wl.routing == "expert_choice":
+        O.moe_forward_expert_choice(sub, h["x"], h["w_gate"], h["w13"], h["w2"], h["ws13"],
+                                    h["ws2"])
+    else:
+        O.moe_forward(sub, h["x"], h["w_gate"], h["bias"], h["w13"], h["w2"], h["ws13"], h["ws2"])
+    return time.perf_counter() - t0
+
+
+def host_inputs(inp):
+    import moe_inputs
+    return {k: moe_inputs.to_f64(v) for k, v in inp.items()}
+
+
+def run_cpu_baseline(wl, inp, target_s=12.0, steps=1):
+    hi = host_inputs(inp)
+    S = min(32, wl.T)
+    t = oracle_sample(wl, hi, S)
+    S = int(min(wl.T, max(S, S * target_s / max(t, 1e-3))))
+    times = [oracle_sample(wl, hi, S) for _ in range(steps)]
+    return S, times
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mixtral")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    import torch
+    import moe_inputs
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = moe_inputs.workload(args.workload)
+    flops = workload_flops_bytes(wl)
+    peaks, peak_kind = load_peaks()
+    config = {"workload": f"{wl.name}-shaped MoE layer: T={wl.T} d={wl.d} E={wl.E} k={wl.k} "
+                          f"F={wl.F} shared={wl.n_shared}x{wl.F_shared} score={wl.score} "
+                          f"routing={wl.routing} cf={wl.capacity_factor or 'none'}",
+              "T": wl.T, "d_model": wl.d, "E": wl.E, "k": wl.k, "d_ff": wl.F,
+              "shared_d_ff": wl.F_sh, "capacity_factor": wl.capacity_factor or None,
+              "l2": "inputs larger than L2 (expert weights "
+                    f"{wl.E * 3 * wl.d * wl.F * 2 / 1e9:.2f} GB > 126 MB)",
+              "parallelism": "replicas" if world == 1 else f"replicas x{world} (token shards)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        torch.manual_seed(0)
+        inp = moe_inputs.make_inputs(wl, device="cpu")
+        hi = host_inputs(inp)
+        S = min(wl.T, 128)
+        for _ in range(max(args.warmup, 0)):
+            oracle_sample(wl, hi, min(S, 16))
+        times = [oracle_sample(wl, hi, S) for _ in range(args.steps)]
+        ms = 1e3 * sum(times) / len(times)
+        val = S / (ms / 1e3)
+        cores = cpu_cores()
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config,
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"independent batch of the first {S} tokens per step"},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}))
+        return
+
+    import top_routing_expert_scoring_b300 as m
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = moe_inputs.make_inputs(wl, seed=rank, device="cuda")
+    cfg = m.make_config(wl.T, wl.d, wl.E, wl.k, wl.F, wl.F_sh, wl.score, wl.routing, wl.n_groups,
+                        wl.topk_groups, wl.renormalize, wl.route_scale, wl.capacity_factor,
+                        wl.dtype)
+    T, E, k, d = wl.T, wl.E, wl.k, wl.d
+    ws = m.workspace(cfg, dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    bf = dict(dtype=torch.bfloat16, device=dev)
+    logits, idx, w = torch.empty((T, E), **f32), torch.empty((T, k), **i32), torch.empty((T, k), **f32)
+    f, P, lb, z = (torch.empty(E, **f32), torch.empty(E, **f32), torch.empty(1, **f32),
+                   torch.empty(1, **f32))
+    counts, kept, offsets = torch.empty(E, **i32), torch.empty(E, **i32), torch.empty(E + 1, **i32)
+    pos, row_of, perm, nd = (torch.empty((T, k), **i32), torch.empty((T, k), **i32),
+                             torch.empty(T * k, **i32), torch.empty(1, **i32))
+    x_perm, y_perm = torch.empty((T * k, d), **bf), torch.empty((T * k, d), **bf)
+    shared = torch.empty((T, d), **bf) if wl.F_sh else None
+    out = torch.empty((T, d), **bf)
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    def step(gemm_events=None):
+        m.moe_router_topk(cfg, inp["x"], inp["w_gate"], inp["bias"], logits, idx, w, ws, stream)
+        m.moe_aux_stats(cfg, logits, idx, f, P, lb, z, ws, stream)
+        m.moe_dispatch(cfg, idx, inp["x"], counts, kept, offsets, pos, row_of, perm, x_perm, nd,
+                       ws, stream)
+        if gemm_events:
+            gemm_events[0].record(stream)
+        m.moe_expert_ffn(cfg, x_perm, offsets, inp["w13"], inp["w2"], y_perm, ws, stream)
+        if gemm_events:
+            gemm_events[1].record(stream)
+        if shared is not None:
+            m.moe_shared_ffn(cfg, inp["x"], inp["ws13"], inp["ws2"], shared, ws, stream)
+        m.moe_combine(cfg, y_perm, row_of, w, shared, out, stream)
+
+    launches_per_step = 1 + 1 + 2 + 4 + 1 + 2 + (2 if shared is not None else 0) + 1
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    barrier()
+    st = m.sync_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {m.status_string(st)}")
+
+    gemm_pairs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+                  for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(gemm_pairs[i])
+        t_end.record(stream)
+        barrier()
+    ms_total = t_start.elapsed_time(t_end)
+    gemm_ms = [a.elapsed_time(b) for a, b in gemm_pairs]
+    if world > 1:
+        tt = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / args.steps
+    value = world * T * args.steps / (ms_total / 1e3)
+
+    # end to end through the public call with host buffers (pinned), copies inside the region
+    x_host = inp["x"].cpu().pin_memory()
+    out_host = torch.empty((T, d), dtype=torch.bfloat16).pin_memory()
+    stats_host = torch.empty(E + 2, dtype=torch.float32).pin_memory()
+    x_dev = torch.empty_like(inp["x"])
+    stats_dev = torch.empty(E + 2, **f32)
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        m.moe_forward(cfg, x_dev, inp["w_gate"], inp["bias"], inp["w13"], inp["w2"], inp["ws13"],
+                      inp["ws2"], out, None, None, stats_dev[:E], None, stats_dev[E:E + 1],
+                      stats_dev[E + 1:E + 2], None, ws, stream)
+        out_host.copy_(out, non_blocking=True)
+        stats_host.copy_(stats_dev, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    t0 = time.perf_counter()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    st = m.sync_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {m.status_string(st)}")
+
+    if rank != 0:
+        return
+    gemm_avg = sum(gemm_ms) / len(gemm_ms)
+    tflops = flops["ffn_flops"] / (gemm_avg / 1e3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    layer_roof_ms = max(flops["flops"] / (peak * 1e12), flops["bytes"] / (peaks["hbm_gbs"] * 1e9)) * 1e3
+    res = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded i.i.d. normal tokens and random-init expert weights)",
+        "config": config,
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": tflops / peak, "traffic": None,
+                     "kernel": "grouped_gemm_tc_kernel (gate/up + down launches of one step)",
+                     "peak_kind": f"{peak_kind} bf16 burst"},
+        "layer_roofline": {"roofline_ms": layer_roof_ms, "frac": layer_roof_ms / ms_step,
+                           "flops_per_step": flops["flops"], "bytes_per_step": flops["bytes"]},
+        "stage_ms": {"expert_ffn": gemm_avg, "rest": ms_step - gemm_avg},
+        "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+                "d2h_bytes_per_step": out_host.numel() * out_host.element_size()
+                + stats_host.numel() * 4,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        S, times = run_cpu_baseline(wl, inp)
+        res["cpu_baseline"] = {"value": S / times[0], "unit": "tokens/s", "cores": cpu_cores(),
+                               "kind": "oracle",
+                               "sample": f"independent batch of the first {S} tokens "
+                                         f"({times[0]:.1f} s of float64 CPU work)"}
+    print(json.dumps(res))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,196 @@
+/*
+ * moe_b300.h — C ABI of the single-GPU MoE layer forward for NVIDIA B300 (sm_103a).
+ *
+ * One MoE layer forward, as the pages derive it:
+ *   route:    g = x W_gate; softmax (or sigmoid + selection bias with group limit) scores;
+ *             Top-k with renormalisation                 ["MoE 路由数学" §2.1; "Systems for
+ *                                                         Mixture-of-Experts Models" §2.1, §5.3]
+ *   dispatch: group (token, choice) pairs by expert, capacity C = ceil(cf*k*T/E), overflow
+ *             dropped in token order                     ["Systems for MoE Models" §2.2, §2.4]
+ *   experts:  SwiGLU FFN (SiLU(x W1) * x W3) W2 per expert, plus always-on shared experts
+ *                                                        ["Systems for MoE Models" §5.2;
+ *                                                         "MoE 路由数学" §2.2]
+ *   combine:  out = shared(x) + sum_{i in S} p~_i Expert_i(x)   ["MoE 路由数学" §2.1]
+ *   stats:    f_i, P_i, L_balance = E sum f_i P_i, z-loss  ["MoE 路由数学" §3.2; "Mixture of
+ *             Experts 架构" load_balancing_loss / router_z_loss code blocks]
+ *
+ * Conventions (every entry point):
+ *   - Returns 0 (MOE_OK) or a negative MOE_ERR_* status; moe_status_string() gives its text.
+ *   - Every pointer argument is DEVICE memory owned by the caller unless stated otherwise.
+ *     The library allocates and frees nothing and never synchronises the stream; all work is
+ *     enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *   - Tensors are row-major and contiguous.  "bf16" tensors hold IEEE bfloat16; with
+ *     cfg->dtype == MOE_DTYPE_F32 the same tensors hold float32 instead.
+ *   - Arguments are validated on the host before any launch (MOE_ERR_ARG / SHAPE /
+ *     UNSUPPORTED / WORKSPACE); a launch failure returns MOE_ERR_CUDA.  Faults found on the
+ *     device (a bounded wait that ran out) are written to the status word at the start of the
+ *     workspace and returned by moe_sync_status(); kernels never trap.
+ *   - `ws` is a caller-allocated device workspace of at least moe_workspace_size() bytes,
+ *     256-byte aligned.  Calls that share one workspace must not overlap on the GPU.
+ *
+ * Layouts:
+ *   x       [T, d]        tokens
+ *   w_gate  [E, d]        router, row e = expert e's vector (g[t,e] = sum_c x[t,c] w_gate[e,c])
+ *   bias    [E] float32   selection-only bias (sigmoid scoring); may be NULL (= zeros)
+ *   w13     [E, 2F, d]    rows [0,F) = W1 (gate projection), rows [F,2F) = W3 (up projection)
+ *   w2      [E, d, F]     down projection (y[c] = sum_f h[f] w2[c,f])
+ *   ws13    [2Fs, d], ws2 [d, Fs]   the shared experts concatenated into one SwiGLU expert of
+ *                         width Fs = cfg->d_ff_shared (sum of shared experts == concatenation)
+ *   topk_idx [T, k] int32 rank order (descending score; ties -> lower expert index)
+ *   topk_w   [T, k] float32
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  MOE_OK = 0,
+  MOE_ERR_ARG = -1,          /* NULL pointer or bad enum value */
+  MOE_ERR_SHAPE = -2,        /* sizes out of range or not aligned as required */
+  MOE_ERR_UNSUPPORTED = -3,  /* a valid request this build does not implement */
+  MOE_ERR_WORKSPACE = -4,    /* workspace NULL, too small or misaligned */
+  MOE_ERR_CUDA = -5,         /* a CUDA runtime call failed */
+  MOE_ERR_TIMEOUT = -6       /* a bounded device-side wait ran out */
+};
+
+enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 };
+enum { MOE_ROUTE_TOKEN_CHOICE = 0, MOE_ROUTE_EXPERT_CHOICE = 1 };
+enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_F32 = 1 };
+
+typedef struct moe_config {
+  int32_t T;            /* tokens, >= 1 */
+  int32_t d_model;      /* d; bf16 path: multiple of 128 */
+  int32_t E;            /* routed experts, 1..256 */
+  int32_t k;            /* experts per token, 1..min(E, 8); expert choice: C = T*k/E */
+  int32_t d_ff;         /* F of one routed expert; bf16 path: multiple of 128 */
+  int32_t d_ff_shared;  /* width of the concatenated shared experts, 0 = none */
+  int32_t score;        /* MOE_SCORE_* */
+  int32_t routing;      /* MOE_ROUTE_* */
+  int32_t n_groups;     /* expert groups (sigmoid scoring); 1 = no group limit */
+  int32_t topk_groups;  /* groups kept per token; == n_groups = no limit */
+  int32_t renormalize;  /* 1: w = p_S / sum_S p (default); 0: w = p_S (Switch, k = 1) */
+  float route_scale;    /* weights are multiplied by it (1.0; DeepSeek-V3: 2.5) */
+  float capacity_factor;/* C = ceil(cf*k*T/E); <= 0: no capacity limit */
+  int32_t dtype;        /* MOE_DTYPE_* */
+} moe_config;
+
+/* Text of a status code (static storage). */
+const char* moe_status_string(int status);
+
+/* Library version string, e.g. "moe_b300 1.0 sm_103a". */
+const char* moe_version(void);
+
+/* Validate cfg.  Returns MOE_OK or the first problem found. */
+int moe_check_config(const moe_config* cfg);
+
+/* Expert capacity C = ceil(cf*k*T/E) evaluated in double from the float cf
+ * ["Systems for MoE Models" §2.4]; T*k when cf <= 0 (no limit).  Host only. */
+int moe_capacity(const moe_config* cfg, int32_t* capacity);
+
+/* Bytes of device workspace that every call below needs for cfg (host only).  The same
+ * workspace size serves every entry point. */
+int moe_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* Reads and clears the device status word at the start of `ws` (copies 4 bytes to the host
+ * and synchronises `stream`).  Returns MOE_OK, or the first device-side error recorded since
+ * the last call, or MOE_ERR_CUDA if the copy itself failed. */
+int moe_sync_status(void* ws, void* stream);
+
+/* Router: logits, scores, Top-k and weights for every token ["MoE 路由数学" §2.1 (g, p, S,
+ * p~); "Mixture of Experts 架构" loss_free_balancing_routing code block; "Systems for MoE
+ * Models" §5.3 (sigmoid gate with groups, bias for selection only, route scale)].
+ *   x [T,d] bf16, w_gate [E,d] bf16, bias [E] f32 or NULL;
+ *   logits [T,E] f32 output or NULL (then kept in the workspace);
+ *   topk_idx [T,k] int32 and topk_w [T,k] f32 outputs.
+ * Token choice only (cfg->routing == MOE_ROUTE_TOKEN_CHOICE). */
+int moe_router_topk(const moe_config* cfg, const void* x, const void* w_gate, const float* bias,
+                    float* logits, int32_t* topk_idx, float* topk_w, void* ws, void* stream);
+
+/* Load-balance statistics from router logits and a selection ["MoE 路由数学" §3.2 (f_i, P_i,
+ * L_balance = E sum f_i P_i); "Mixture of Experts 架构" load_balancing_loss and router_z_loss
+ * code blocks].  f_i = (selections of expert i)/T before capacity drops (sum f = k);
+ * P_i = mean_t softmax(g_t)_i (sigmoid scoring: mean_t s_ti / sum_j s_tj);
+ * z = mean_t (logsumexp_i g_ti)^2.
+ *   logits [T,E] f32, topk_idx [T,k] int32 -> f [E], P [E], l_balance [1], z_loss [1] (f32).
+ * Reductions run in a fixed order (fp32 per token block, fp64 across blocks): results are
+ * bit-identical from run to run. */
+int moe_aux_stats(const moe_config* cfg, const float* logits, const int32_t* topk_idx, float* f,
+                  float* P, float* l_balance, float* z_loss, void* ws, void* stream);
+
+/* Dispatch: group (token, choice) pairs by expert in token order, apply the capacity and
+ * gather token rows into expert order ["Systems for MoE Models" §2.2 steps 2-3, §2.4].
+ *   counts[E]   selections per expert (before drops)
+ *   kept[E]     min(counts, C)
+ *   offsets[E+1] exclusive scan of kept (expert e's rows are [offsets[e], offsets[e+1]))
+ *   pos[T,k]    number of earlier tokens that chose the same expert
+ *   row_of[T,k] offsets[e] + pos when pos < C, else -1 (dropped)
+ *   perm[T*k]   perm[row] = t*k + j for kept pairs, -1 for rows >= offsets[E]
+ *   x_perm[T*k, d] bf16: x_perm[row] = x[t]; rows >= offsets[E] are left unwritten
+ *   n_dropped[1] pairs dropped by the capacity
+ * All outputs are bit-exact and deterministic.  x / x_perm may be NULL to skip the gather. */
+int moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const void* x, int32_t* counts,
+                 int32_t* kept, int32_t* offsets, int32_t* pos, int32_t* row_of, int32_t* perm,
+                 void* x_perm, int32_t* n_dropped, void* ws, void* stream);
+
+/* Routed expert FFNs on expert-grouped rows ["Systems for MoE Models" §5.2 SwiGLU]:
+ *   y_perm[r] = (SiLU(x_perm[r] W1_e^T) * (x_perm[r] W3_e^T)) W2_e^T for
+ *   r in [offsets[e], offsets[e+1]).  x_perm [T*k, d], y_perm [T*k, d] bf16 (rows beyond
+ *   offsets[E] untouched); offsets [E+1] device int32; w13, w2 as in the layout table.
+ * bf16: tcgen05 tensor-core grouped GEMMs with fp32 accumulation; the intermediate h is
+ * rounded to bf16.  f32: CUDA-core fp32 path. */
+int moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
+                   const void* w13, const void* w2, void* y_perm, void* ws, void* stream);
+
+/* Shared experts on every token ["MoE 路由数学" §2.2]: shared_out = SwiGLU(x; ws13, ws2),
+ * x [T,d] -> shared_out [T,d] bf16.  cfg->d_ff_shared must be > 0. */
+int moe_shared_ffn(const moe_config* cfg, const void* x, const void* ws13, const void* ws2,
+                   void* shared_out, void* ws, void* stream);
+
+/* Weighted combine ["MoE 路由数学" §2.1 Output; "Systems for MoE Models" §2.2 step 4]:
+ *   out[t] = shared_out[t] + sum_{j : row_of[t,j] >= 0} topk_w[t,j] * y_perm[row_of[t,j]]
+ * in fp32 in the order j = 0..k-1, then rounded once to bf16.  Dropped pairs add nothing and
+ * the remaining weights are not renormalised.  shared_out may be NULL.  No atomics. */
+int moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* row_of,
+                const float* topk_w, const void* shared_out, void* out, void* stream);
+
+/* Expert-choice routing ["MoE混合专家模型深度解析" §2.2 Expert Choice]: each expert takes the
+ * C = T*k/E tokens with the largest logit in its column (ties -> lower token index).
+ *   logits [T,E] f32 -> ec_tokens [E,C] int32 (ascending token order), ec_w [E,C] f32 =
+ *   softmax(g_t)_e, tok_ptr [T+1] int32, tok_rows [E*C] int32: for token t the rows e*C+i of
+ *   the experts that chose it, in ascending expert order (a CSR view used by the combine). */
+int moe_expert_choice(const moe_config* cfg, const float* logits, int32_t* ec_tokens, float* ec_w,
+                      int32_t* tok_ptr, int32_t* tok_rows, void* ws, void* stream);
+
+/* Whole layer forward: router -> dispatch -> routed experts (+ shared experts) -> combine,
+ * plus the statistics.  Every intermediate lives in `ws`.
+ *   x [T,d], w_gate [E,d], bias [E] or NULL, w13, w2, ws13/ws2 (NULL when d_ff_shared == 0)
+ *   out [T,d] bf16 (required)
+ *   optional outputs (NULL to skip): topk_idx [T,k], topk_w [T,k], f [E], P [E],
+ *   l_balance [1], z_loss [1], n_dropped [1] (token choice) */
+int moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const float* bias,
+                const void* w13, const void* w2, const void* ws13, const void* ws2, void* out,
+                int32_t* topk_idx, float* topk_w, float* f, float* P, float* l_balance,
+                float* z_loss, int32_t* n_dropped, void* ws, void* stream);
+
+/* Device addresses of the intermediates moe_forward leaves in `ws` (for inspection and
+ * tests): logits [T,E] f32, row_of [T,k] int32, offsets [E+1] int32, x_perm, y_perm. */
+int moe_workspace_views(const moe_config* cfg, void* ws, float** logits, int32_t** row_of,
+                        int32_t** offsets, void** x_perm, void** y_perm);
+
+/* Failure-path self test: launches one tiny kernel whose bounded wait on a flag that nothing
+ * sets runs out after about `limit_us` microseconds; it records MOE_ERR_TIMEOUT in the status
+ * word of `ws` and returns, leaving the context usable.  Read the result with
+ * moe_sync_status().  Exists so tests can exercise the timeout path without a fault. */
+int moe_selftest_timeout(void* ws, int32_t limit_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

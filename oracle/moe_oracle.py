@@ -409,3 +409,27 @@ def expert_choice_csr(tokens: np.ndarray, T: int):
     return {"ptr": ptr.astype(np.int32), "rows": rows.astype(np.int32),
             "experts": (rows // max(C, 1)).astype(np.int32),
             "counts": np.full(E, C, dtype=np.int64)}
+
+
+def moe_forward_sampled(x, idx, w, row_of, expert_weights, shared_weights=None, tokens=None):
+    """out[t] for the sampled tokens only, from a given selection (idx, w, row_of):
+    out[t] = Shared(x_t) + sum_{j : row_of[t,j] >= 0} w[t,j] Expert_{idx[t,j]}(x_t).
+
+    expert_weights(e) -> (w13 [2F,d], w2 [d,F]) as float64 arrays, fetched once per expert, so
+    that full-size layers can be checked without holding every expert in float64 at once;
+    shared_weights() -> (ws13, ws2) or None.  Same arithmetic as moe_forward_tokens.
+    """
+    tokens = np.asarray(tokens)
+    xs = np.asarray(x[tokens], F64)
+    out = np.zeros_like(xs)
+    if shared_weights is not None:
+        sw = shared_weights()
+        if sw is not None:
+            out += swiglu_expert(xs, sw[0], sw[1])
+    sel = idx[tokens]
+    keep = row_of[tokens] >= 0
+    for e in np.unique(sel[keep]):
+        w13, w2 = expert_weights(int(e))
+        rows, slots = np.nonzero((sel == e) & keep)
+        out[rows] += w[tokens][rows, slots][:, None] * swiglu_expert(xs[rows], w13, w2)
+    return out

@@ -1,0 +1,306 @@
+"""GPU-vs-oracle parity of the whole layer and of each stage, through the C ABI.
+
+Bars: selected expert indices, counts, offsets, positions, permutation and drop set
+bit-exact (tokens whose deciding scores differ by less than 1e-6 relative are reported and
+excluded); statistics within 1e-5 relative; layer output max-abs error <= 2e-2 x RMS (bf16) or
+1e-4 x RMS (float32 path).  Small cases span several tiles with ragged tails; the full-size
+cases (the benchmark's launch configuration) compare routing and dispatch on every token and
+the output on sampled tokens."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs
+from oracle import moe_oracle as O
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _inputs(wl, device=DEV, seed=0):
+    return moe_inputs.make_inputs(wl, seed=seed, device=device)
+
+
+def _full_check(wl, inp, report, out_tol):
+    """Whole-layer parity on a case small enough for the oracle's full forward."""
+    h = U.host(inp)
+    gpu = U.run_forward(wl, inp)
+    if wl.routing == "expert_choice":
+        ref = O.moe_forward_expert_choice(wl, h["x"], h["w_gate"], h["w13"], h["w2"], h["ws13"],
+                                          h["ws2"])
+        U.compare_stats(gpu, ref["stats"], report)
+        U.compare_out(gpu["out"].float().cpu().numpy(), ref["out"], out_tol, report)
+        return gpu, ref
+    ref = O.moe_forward(wl, h["x"], h["w_gate"], h["bias"], h["w13"], h["w2"], h["ws13"], h["ws2"])
+    ok = U.compare_routing(wl, gpu, ref, h["bias"], report)
+    if ok.all():
+        U.compare_stats(gpu, ref["stats"], report)
+        assert gpu["n_dropped"] == ref["disp"]["n_dropped"]
+        m = U.lib()
+        _, row_of_p, offsets_p, _, _ = m.moe_workspace_views(gpu["cfg"], gpu["ws"])
+        row_of = _read_i32(row_of_p, wl.T * wl.k).reshape(wl.T, wl.k)
+        offsets = _read_i32(offsets_p, wl.E + 1)
+        assert (row_of == ref["disp"]["row_of"]).all()
+        assert (offsets == ref["disp"]["offsets"]).all()
+    got = gpu["out"].float().cpu().numpy()
+    U.compare_out(got[ok], ref["out"][ok], out_tol, report)
+    return gpu, ref
+
+
+class _DevArray:
+    """Zero-copy view of n int32 values at a raw device address (the workspace views)."""
+    def __init__(self, ptr, n):
+        self.__cuda_array_interface__ = {"shape": (n,), "typestr": "<i4", "data": (ptr, False),
+                                         "version": 3, "strides": None}
+
+
+def _read_i32(ptr, n):
+    torch.cuda.synchronize()
+    return torch.as_tensor(_DevArray(ptr, n), device=DEV).cpu().numpy()
+
+
+# ---------------------------------------------------------------------------------------------
+# small cases: full oracle forward
+# ---------------------------------------------------------------------------------------------
+SMALL = {
+    # float32 path
+    "tiny": dict(name="tiny"),
+    "tiny_dense": dict(name="tiny_dense"),
+    "tiny_uniform": dict(name="tiny_uniform"),
+    # bf16: ragged M tiles, capacity drops, 3 N tiles in the gate/up GEMM
+    "softmax_cap": dict(name="mixtral", T=700, d=256, F=384, capacity_factor=1.25),
+    "softmax_collapsed_cap": dict(name="mixtral_collapsed", T=600, d=256, F=256,
+                                  capacity_factor=1.0),
+    # bf16 DeepSeek-V3-like gate: sigmoid + bias, 8 groups keep 4, top-8, scale 2.5, shared
+    "v3_like": dict(name="v3", T=333, d=256, E=64, F=256, F_shared=256),
+    # bf16 DeepSeekMoE-like: 2 shared experts, d not a multiple of 256 (N=128 down tiles)
+    "dsmoe_like": dict(name="dsmoe16b", T=1000, d=384, E=16, F=256, F_shared=128),
+    # expert choice
+    "ec_like": dict(name="dsmoe16b_ec", T=512, d=256, E=16, k=4, F=256, F_shared=128),
+    # single token (decode B = 1) and E = 1
+    "decode_b1": dict(name="v3", T=1, d=256, E=64, F=256, F_shared=256),
+    "one_expert": dict(name="mixtral", T=130, d=128, E=1, k=1, F=128),
+}
+
+
+@pytest.mark.parametrize("case", sorted(SMALL))
+def test_small_layer_parity(case):
+    spec = dict(SMALL[case])
+    wl = moe_inputs.workload(spec.pop("name"), **spec)
+    inp = _inputs(wl)
+    report = {}
+    tol = U.OUT_TOL_F32 if wl.dtype == "f32" else U.OUT_TOL_BF16
+    _full_check(wl, inp, report, tol)
+    print(case, report)
+
+
+def test_uniform_router_exact_ties():
+    # W_gate = 0: every logit is exactly 0 on both sides, the tie rule alone decides
+    wl = moe_inputs.workload("tiny_uniform")
+    gpu = U.run_forward(wl, _inputs(wl))
+    assert (gpu["idx"] == np.arange(wl.k)[None, :]).all()
+    assert np.abs(gpu["w"] - 1.0 / wl.k).max() == 0
+    assert gpu["l_balance"] == pytest.approx(wl.k, rel=1e-7)
+    assert gpu["z_loss"] == pytest.approx(np.log(wl.E) ** 2, rel=1e-6)
+    assert gpu["n_dropped"] == wl.T * wl.k - 160
+
+
+def test_forward_is_deterministic():
+    wl = moe_inputs.workload("v3", T=400, d=256, E=64, F=256, F_shared=256)
+    inp = _inputs(wl)
+    a = U.run_forward(wl, inp)
+    b = U.run_forward(wl, inp)
+    assert torch.equal(a["out"], b["out"])
+    assert (a["idx"] == b["idx"]).all() and (a["w"] == b["w"]).all()
+    assert (a["f"] == b["f"]).all() and (a["P"] == b["P"]).all()
+    assert a["l_balance"] == b["l_balance"] and a["z_loss"] == b["z_loss"]
+
+
+# ---------------------------------------------------------------------------------------------
+# stage entry points
+# ---------------------------------------------------------------------------------------------
+def test_stage_entry_points():
+    m = U.lib()
+    wl = moe_inputs.workload("v3", T=700, d=256, E=64, F=256, F_shared=256, capacity_factor=1.25)
+    cfg = U.config_of(wl)
+    inp = _inputs(wl)
+    h = U.host(inp)
+    ref = O.moe_forward(wl, h["x"], h["w_gate"], h["bias"], h["w13"], h["w2"], h["ws13"], h["ws2"])
+    T, E, k, d = wl.T, wl.E, wl.k, wl.d
+    ws = m.workspace(cfg)
+    i32 = dict(dtype=torch.int32, device=DEV)
+    f32 = dict(dtype=torch.float32, device=DEV)
+    logits = torch.empty((T, E), **f32)
+    idx = torch.empty((T, k), **i32)
+    w = torch.empty((T, k), **f32)
+    m.moe_router_topk(cfg, inp["x"], inp["w_gate"], inp["bias"], logits, idx, w, ws)
+    g = logits.cpu().numpy()
+    # logits: fp32 accumulation vs the correctly rounded exact value
+    assert np.abs(g - ref["g"]).max() <= 1e-5 * np.abs(ref["g"]).max()
+    report = {}
+    ok = U.compare_routing(wl, {"idx": idx.cpu().numpy(),
+                                "w": w.cpu().numpy().astype(np.float64)}, ref, h["bias"], report)
+    assert ok.all()
+    f = torch.empty(E, **f32)
+    P = torch.empty(E, **f32)
+    lb = torch.empty(1, **f32)
+    z = torch.empty(1, **f32)
+    m.moe_aux_stats(cfg, logits, idx, f, P, lb, z, ws)
+    U.compare_stats({"f": f.cpu().numpy(), "P": P.cpu().numpy(), "l_balance": lb.item(),
+                     "z_loss": z.item()}, ref["stats"], report)
+    # dispatch fed the oracle's indices: bit-exact
+    oidx = torch.from_numpy(ref["idx"].astype(np.int32)).to(DEV)
+    counts, kept = torch.empty(E, **i32), torch.empty(E, **i32)
+    offsets = torch.empty(E + 1, **i32)
+    pos, row_of = torch.empty((T, k), **i32), torch.empty((T, k), **i32)
+    perm, nd = torch.empty(T * k, **i32), torch.empty(1, **i32)
+    x_perm = torch.empty((T * k, d), dtype=torch.bfloat16, device=DEV)
+    m.moe_dispatch(cfg, oidx, inp["x"], counts, kept, offsets, pos, row_of, perm, x_perm, nd, ws)
+    D = ref["disp"]
+    for name, t in [("counts", counts), ("kept", kept), ("offsets", offsets), ("pos", pos),
+                    ("row_of", row_of), ("perm", perm)]:
+        assert (t.cpu().numpy() == D[name]).all(), name
+    assert nd.item() == D["n_dropped"] > 0
+    nk = int(D["offsets"][-1])
+    src = D["perm"][:nk] // k
+    assert torch.equal(x_perm[:nk].cpu(), inp["x"].cpu()[torch.from_numpy(src.astype(np.int64))])
+    # routed experts on the dispatched rows
+    y_perm = torch.zeros((T * k, d), dtype=torch.bfloat16, device=DEV)
+    m.moe_expert_ffn(cfg, x_perm, offsets, inp["w13"], inp["w2"], y_perm, ws)
+    U.compare_out(y_perm[:nk].float().cpu().numpy(), ref["y_rows"], U.OUT_TOL_BF16, report, "y")
+    shared = torch.empty((T, d), dtype=torch.bfloat16, device=DEV)
+    m.moe_shared_ffn(cfg, inp["x"], inp["ws13"], inp["ws2"], shared, ws)
+    U.compare_out(shared.float().cpu().numpy(), ref["shared"], U.OUT_TOL_BF16, report, "shared")
+    out = torch.empty((T, d), dtype=torch.bfloat16, device=DEV)
+    ow = torch.from_numpy(ref["w"].astype(np.float32)).to(DEV)
+    m.moe_combine(cfg, y_perm, row_of, ow, shared, out)
+    U.compare_out(out.float().cpu().numpy(), ref["out"], U.OUT_TOL_BF16, report)
+    torch.cuda.synchronize()
+    assert m.sync_status(ws) == 0
+    print(report)
+
+
+def test_expert_choice_entry_point():
+    m = U.lib()
+    wl = moe_inputs.workload("dsmoe16b_ec", T=777, d=256, E=16, k=4, F=256, F_shared=128)
+    cfg = U.config_of(wl)
+    inp = _inputs(wl)
+    h = U.host(inp)
+    g, g32 = O.router_logits(h["x"], h["w_gate"])
+    ws = m.workspace(cfg)
+    C = wl.T * wl.k // wl.E
+    logits = torch.from_numpy(g32).to(DEV)
+    tok = torch.empty((wl.E, C), dtype=torch.int32, device=DEV)
+    tw = torch.empty((wl.E, C), dtype=torch.float32, device=DEV)
+    ptr = torch.empty(wl.T + 1, dtype=torch.int32, device=DEV)
+    rows = torch.empty(wl.E * C, dtype=torch.int32, device=DEV)
+    m.moe_expert_choice(cfg, logits, tok, tw, ptr, rows, ws)
+    tokens, weights, _ = O.expert_choice_route(g32, wl.k)
+    csr = O.expert_choice_csr(tokens, wl.T)
+    assert (tok.cpu().numpy() == tokens).all()
+    assert np.abs(tw.cpu().numpy() - weights).max() <= U.WEIGHT_ATOL
+    assert (ptr.cpu().numpy() == csr["ptr"]).all()
+    assert (rows.cpu().numpy() == csr["rows"]).all()
+
+
+# ---------------------------------------------------------------------------------------------
+# failure paths (no fault: bounded waits and argument checks)
+# ---------------------------------------------------------------------------------------------
+def test_bounded_wait_reports_timeout_and_context_survives():
+    m = U.lib()
+    wl = moe_inputs.workload("tiny")
+    cfg = U.config_of(wl)
+    ws = m.workspace(cfg)
+    m.moe_selftest_timeout(ws, 2000)
+    torch.cuda.synchronize()
+    assert m.sync_status(ws) == -6
+    assert m.sync_status(ws) == 0          # cleared by the read
+    _full_check(wl, _inputs(wl), {}, U.OUT_TOL_F32)
+
+
+def test_bad_expert_index_is_reported_not_faulted():
+    m = U.lib()
+    wl = moe_inputs.workload("tiny")
+    cfg = U.config_of(wl)
+    ws = m.workspace(cfg)
+    T, E, k = wl.T, wl.E, wl.k
+    idx = torch.zeros((T, k), dtype=torch.int32, device=DEV)
+    idx[:, 1] = 1
+    idx[5, 1] = E            # out of range
+    idx[9, 1] = 0            # expert chosen twice
+    i32 = dict(dtype=torch.int32, device=DEV)
+    bufs = [torch.empty(E, **i32), torch.empty(E, **i32), torch.empty(E + 1, **i32),
+            torch.empty((T, k), **i32), torch.empty((T, k), **i32), torch.empty(T * k, **i32)]
+    nd = torch.empty(1, **i32)
+    m.moe_dispatch(cfg, idx, None, *bufs, None, nd, ws)
+    torch.cuda.synchronize()
+    assert m.sync_status(ws) == -1
+
+
+# ---------------------------------------------------------------------------------------------
+# full size: routing/dispatch on every token, output on sampled tokens
+# ---------------------------------------------------------------------------------------------
+FULL = {
+    "mixtral": dict(name="mixtral"),
+    "mixtral_collapsed": dict(name="mixtral_collapsed"),
+    "mixtral_cf1.0": dict(name="mixtral", capacity_factor=1.0),
+    "mixtral_collapsed_cf1.25": dict(name="mixtral_collapsed", capacity_factor=1.25),
+    "dsmoe16b": dict(name="dsmoe16b"),
+    "dsmoe16b_ec": dict(name="dsmoe16b_ec"),
+    "v3": dict(name="v3"),
+}
+
+
+@pytest.mark.parametrize("case", list(FULL))
+def test_full_size_parity(case):
+    spec = dict(FULL[case])
+    wl = moe_inputs.workload(spec.pop("name"), **spec)
+    inp = moe_inputs.make_inputs(wl, device=DEV)
+    report = {}
+    gpu = U.run_forward(wl, inp)
+    x = moe_inputs.to_f64(inp["x"])
+    wg = moe_inputs.to_f64(inp["w_gate"])
+    bias = moe_inputs.to_f64(inp["bias"])
+    rng = np.random.default_rng(0)
+    sample = np.sort(rng.choice(wl.T, size=16 if wl.E > 8 else 32, replace=False))
+    if wl.routing == "expert_choice":
+        g, g32 = O.router_logits(x, wg)
+        tokens, weights, p = O.expert_choice_route(g32, wl.k)
+        csr = O.expert_choice_csr(tokens, wl.T)
+        st = O.aux_stats_from_counts(g32, csr["counts"], wl.E)
+        U.compare_stats(gpu, st, report)
+        # per-token selection as a padded (idx, w, row) table for the sampled tokens
+        E, C = tokens.shape
+        kmax = int(np.diff(csr["ptr"]).max())
+        idx = np.zeros((wl.T, max(kmax, 1)), np.int64)
+        w = np.zeros((wl.T, max(kmax, 1)))
+        row_of = -np.ones((wl.T, max(kmax, 1)), np.int64)
+        for t in sample:
+            for n, r in enumerate(csr["rows"][csr["ptr"][t]:csr["ptr"][t + 1]]):
+                e, i = divmod(int(r), C)
+                idx[t, n], w[t, n], row_of[t, n] = e, weights[e, i], r
+        ok_tokens = sample
+    else:
+        r = O.route(wl, x, wg, bias)
+        ok = U.compare_routing(wl, gpu, r, bias, report)
+        disp = O.dispatch(r["idx"], wl.E, O.capacity(wl.capacity_factor, wl.k, wl.T, wl.E))
+        if ok.all():
+            U.compare_stats(gpu, O.aux_stats(r["g32"], r["idx"], wl.E, wl.score), report)
+            assert gpu["n_dropped"] == disp["n_dropped"]
+            m = U.lib()
+            _, row_of_p, offsets_p, _, _ = m.moe_workspace_views(gpu["cfg"], gpu["ws"])
+            assert (_read_i32(offsets_p, wl.E + 1) == disp["offsets"]).all()
+            assert (_read_i32(row_of_p, wl.T * wl.k).reshape(wl.T, wl.k) == disp["row_of"]).all()
+        idx, w, row_of = r["idx"], r["w"], disp["row_of"]
+        ok_tokens = sample[ok[sample]]
+        report["drop_rate"] = disp["n_dropped"] / (wl.T * wl.k)
+        report["f0"] = float(O.aux_stats(r["g32"], r["idx"], wl.E)["f"][0])
+    ref = O.moe_forward_sampled(x, idx, w, row_of, U.expert_weight_fetcher(inp),
+                                U.shared_fetcher(inp), ok_tokens)
+    got = gpu["out"][torch.from_numpy(ok_tokens).to(DEV)].float().cpu().numpy()
+    U.compare_out(got, ref, U.OUT_TOL_BF16, report)
+    print(case, report)
+    del inp, gpu
+    torch.cuda.empty_cache()

@@ -1,0 +1,111 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every entry point
+include/moe_b300.h declares, validates configurations, and computes capacity and workspace
+sizes.  No call here launches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import moe_inputs
+from oracle import moe_oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _lib():
+    import top_routing_expert_scoring_b300 as m
+    return m
+
+
+def declared_entry_points():
+    src = open(os.path.join(ROOT, "include", "moe_b300.h"), encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    m = _lib()
+    names = declared_entry_points()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(m.lib, n), n
+        assert n in m.EXPORTED, n
+    assert m.version().startswith("moe_b300")
+
+
+def config_of(wl, T=None):
+    m = _lib()
+    return m.make_config(T or wl.T, wl.d, wl.E, wl.k, wl.F, wl.F_sh, wl.score, wl.routing,
+                         wl.n_groups, wl.topk_groups, wl.renormalize, wl.route_scale,
+                         wl.capacity_factor, wl.dtype)
+
+
+@pytest.mark.parametrize("name", sorted(moe_inputs.WORKLOADS))
+def test_workload_configs_are_valid(name):
+    m = _lib()
+    cfg = config_of(moe_inputs.workload(name))
+    assert m.check_config(cfg) == 0
+    assert m.workspace_size(cfg) > 0
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("T", 0, -2), ("E", 0, -2), ("E", 257, -2), ("k", 9, -2), ("k", 0, -2),
+    ("d_model", 100, -2), ("d_ff", 1000, -2), ("score", 5, -1), ("dtype", 7, -1),
+    ("n_groups", 3, -2), ("renormalize", 2, -1), ("routing", 9, -1),
+])
+def test_config_rejections(field, value, status):
+    m = _lib()
+    cfg = config_of(moe_inputs.workload("mixtral"))
+    setattr(cfg, field, value)
+    assert m.check_config(cfg) == status
+
+
+def test_group_limit_needs_enough_experts():
+    m = _lib()
+    cfg = config_of(moe_inputs.workload("v3"))
+    cfg.topk_groups = 1          # 32 experts in one group >= k = 8: fine
+    assert m.check_config(cfg) == 0
+    cfg.E, cfg.n_groups, cfg.topk_groups = 64, 32, 2   # 2 groups x 2 experts < 8
+    assert m.check_config(cfg) == -2
+    cfg = config_of(moe_inputs.workload("mixtral"))
+    cfg.n_groups, cfg.topk_groups = 4, 2                 # group limit with softmax scoring
+    assert m.check_config(cfg) == -3
+
+
+@pytest.mark.parametrize("cf,k,T,E", [(1.25, 2, 2048, 16), (1.0, 2, 4096, 8), (1.25, 2, 4096, 8),
+                                      (1.1, 2, 4096, 8), (1.5, 8, 8192, 256), (0.3, 6, 333, 64),
+                                      (0.0, 2, 256, 8), (-1.0, 2, 256, 8), (1.25, 2, 100, 8)])
+def test_capacity_matches_oracle(cf, k, T, E):
+    m = _lib()
+    cfg = m.make_config(T, 128, E, k, 128, capacity_factor=cf)
+    want = O.capacity(cf, k, T, E)
+    assert m.capacity(cfg) == (T * k if want is None else min(want, T * k))
+
+
+def test_status_strings():
+    m = _lib()
+    for s in (0, -1, -2, -3, -4, -5, -6):
+        assert m.status_string(s) and "unknown" not in m.status_string(s)
+
+
+def test_null_arguments_rejected_before_any_launch():
+    m = _lib()
+    cfg = config_of(moe_inputs.workload("tiny"))
+    P = ctypes.c_void_p
+    assert m.lib.moe_forward(ctypes.byref(cfg), *([None] * 17)) == -1
+    # workspace checks: NULL and misaligned workspaces are refused
+    fake = P(0x1000)
+    assert m.lib.moe_router_topk(ctypes.byref(cfg), fake, fake, None, None, fake, fake, None,
+                                 None) == -4
+    assert m.lib.moe_router_topk(ctypes.byref(cfg), fake, fake, None, None, fake, fake,
+                                 P(0x1001), None) == -4
+    assert m.lib.moe_sync_status(None, None) == -4
+    assert m.lib.moe_selftest_timeout(P(0x1000), 0, None) == -1
+    assert m.lib.moe_check_config(None) == -1
+
+
+def test_workspace_grows_with_tokens():
+    m = _lib()
+    wl = moe_inputs.workload("mixtral")
+    assert m.workspace_size(config_of(wl, T=8192)) > m.workspace_size(config_of(wl, T=4096))

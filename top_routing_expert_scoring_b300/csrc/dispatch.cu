@@ -1,0 +1,190 @@
+// Dispatch: group the (token, choice) pairs by expert in token order, apply the expert
+// capacity and gather token rows into expert order.
+//   ["Systems for Mixture-of-Experts Models" §2.2 (group tokens by expert), §2.4 (capacity
+//    C = ceil(cf*k*n/E), overflow dropped)]
+//
+// Positions come from counting, never from atomic arrival order, so every output is
+// deterministic and bit-exact:
+//   D1  per block of 256 tokens, a bitmap bm[e][t/32] of the tokens that chose expert e and
+//       the block's count per expert;
+//   D2  one CTA scans the block counts (token-block order) per expert, clamps to the
+//       capacity and scans the kept counts over experts -> offsets, the M-tile schedule of
+//       the expert GEMMs and the drop count;
+//   D3  pos(t,j) = base[block][e] + popcount of bm[e] below t; row, perm;
+//   D4  x_perm[row] = x[t] with 16-byte vector copies, one warp per row.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+constexpr int kWords = kDispatchBlock / 32;   // bitmap words per expert per block
+
+__global__ void __launch_bounds__(kDispatchBlock) dispatch_count_kernel(
+    const int32_t* __restrict__ idx, int T, int E, int k, uint32_t* __restrict__ bitmap,
+    int32_t* __restrict__ blk_cnt, DevStatus* st) {
+  __shared__ uint32_t bm[256 * kWords];
+  const int tid = threadIdx.x;
+  for (int i = tid; i < E * kWords; i += blockDim.x) bm[i] = 0u;
+  __syncthreads();
+  const int t = blockIdx.x * kDispatchBlock + tid;
+  if (t < T) {
+    int sel[8];
+    for (int j = 0; j < k; ++j) {
+      int e = idx[(size_t)t * k + j];
+      bool bad = e < 0 || e >= E;
+      for (int q = 0; q < j; ++q) bad |= (sel[q] == e);   // an expert chosen twice
+      sel[j] = bad ? -1 : e;
+      if (bad) {
+        record_error(st, MOE_ERR_ARG, t);
+        continue;
+      }
+      atomicOr(&bm[e * kWords + tid / 32], 1u << (tid % 32));
+    }
+  }
+  __syncthreads();
+  uint32_t* gbm = bitmap + (size_t)blockIdx.x * E * kWords;
+  for (int i = tid; i < E * kWords; i += blockDim.x) gbm[i] = bm[i];
+  for (int e = tid; e < E; e += blockDim.x) {
+    int c = 0;
+#pragma unroll
+    for (int w = 0; w < kWords; ++w) c += __popc(bm[e * kWords + w]);
+    blk_cnt[(size_t)blockIdx.x * E + e] = c;
+  }
+}
+
+// One CTA of 256 threads (E <= 256).  blk_cnt is overwritten in place by the exclusive
+// per-expert base of every block.
+__global__ void __launch_bounds__(256) dispatch_scan_kernel(int32_t* __restrict__ blk_cnt,
+                                                           int nblk, int E, int capacity,
+                                                           int32_t* __restrict__ counts,
+                                                           int32_t* __restrict__ kept,
+                                                           int32_t* __restrict__ offsets,
+                                                           int32_t* __restrict__ mtile_prefix,
+                                                           int32_t* __restrict__ n_dropped) {
+  __shared__ int s_kept[256];
+  __shared__ int s_mt[256];
+  __shared__ int s_drop[256];
+  const int e = threadIdx.x;
+  int total = 0;
+  if (e < E) {
+    for (int b = 0; b < nblk; ++b) {
+      const int c = blk_cnt[(size_t)b * E + e];
+      blk_cnt[(size_t)b * E + e] = total;
+      total += c;
+    }
+  }
+  const int kp = e < E ? min(total, capacity) : 0;
+  s_kept[e] = kp;
+  s_mt[e] = ceil_div(kp, kTileM);
+  s_drop[e] = e < E ? total - kp : 0;
+  if (e < E) {
+    counts[e] = total;
+    kept[e] = kp;
+  }
+  __syncthreads();
+  // inclusive Hillis-Steele scans over 256 entries
+  for (int s = 1; s < 256; s <<= 1) {
+    int a = e >= s ? s_kept[e - s] : 0;
+    int b = e >= s ? s_mt[e - s] : 0;
+    int c = e >= s ? s_drop[e - s] : 0;
+    __syncthreads();
+    s_kept[e] += a;
+    s_mt[e] += b;
+    s_drop[e] += c;
+    __syncthreads();
+  }
+  if (e < E) {
+    offsets[e + 1] = s_kept[e];
+    mtile_prefix[e + 1] = s_mt[e];
+  }
+  if (e == 0) {
+    offsets[0] = 0;
+    mtile_prefix[0] = 0;
+    *n_dropped = s_drop[255];
+  }
+}
+
+__global__ void __launch_bounds__(kDispatchBlock) dispatch_scatter_kernel(
+    const int32_t* __restrict__ idx, int T, int E, int k, int capacity,
+    const uint32_t* __restrict__ bitmap, const int32_t* __restrict__ blk_base,
+    const int32_t* __restrict__ offsets, int32_t* __restrict__ pos, int32_t* __restrict__ row_of,
+    int32_t* __restrict__ perm) {
+  __shared__ uint32_t bm[256 * kWords];
+  const int tid = threadIdx.x;
+  const uint32_t* gbm = bitmap + (size_t)blockIdx.x * E * kWords;
+  for (int i = tid; i < E * kWords; i += blockDim.x) bm[i] = gbm[i];
+  __syncthreads();
+  const int t = blockIdx.x * kDispatchBlock + tid;
+  if (t >= T) return;
+  const int w_me = tid / 32;
+  const uint32_t below = (1u << (tid % 32)) - 1u;
+  for (int j = 0; j < k; ++j) {
+    const int e = idx[(size_t)t * k + j];
+    int p = -1, row = -1;
+    if (e >= 0 && e < E && ((bm[e * kWords + w_me] >> (tid % 32)) & 1u)) {
+      int r = __popc(bm[e * kWords + w_me] & below);
+      for (int w = 0; w < w_me; ++w) r += __popc(bm[e * kWords + w]);
+      p = blk_base[(size_t)blockIdx.x * E + e] + r;
+      if (p < capacity) {
+        row = offsets[e] + p;
+        perm[row] = t * k + j;
+      }
+    }
+    pos[(size_t)t * k + j] = p;
+    row_of[(size_t)t * k + j] = row;
+  }
+}
+
+// One warp per expert-ordered row; rows past offsets[E] get perm = -1.
+template <int VEC_BYTES>
+__global__ void __launch_bounds__(256) gather_rows_kernel(const int32_t* __restrict__ offsets,
+                                                         int E, int k, int total_rows,
+                                                         int row_bytes,
+                                                         int32_t* __restrict__ perm,
+                                                         const unsigned char* __restrict__ x,
+                                                         unsigned char* __restrict__ x_perm) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int nkept = offsets[E];
+  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < total_rows; r += warps) {
+    if (r >= nkept) {
+      if (lane == 0) perm[r] = -1;
+      continue;
+    }
+    if (x == nullptr) continue;
+    const int t = perm[r] / k;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * row_bytes);
+    uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)r * row_bytes);
+    const int n16 = row_bytes / 16;
+    for (int i = lane; i < n16; i += 32) dst[i] = __ldg(src + i);
+  }
+}
+
+cudaError_t launch_dispatch(const moe_config& c, int capacity, const int32_t* idx,
+                            const DispatchBufs& b, const void* x, void* x_perm, DevStatus* st,
+                            cudaStream_t s) {
+  const int nblk = ceil_div(c.T, kDispatchBlock);
+  dispatch_count_kernel<<<nblk, kDispatchBlock, 0, s>>>(idx, c.T, c.E, c.k, b.bitmap,
+                                                        b.blk_base, st);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  dispatch_scan_kernel<<<1, 256, 0, s>>>(b.blk_base, nblk, c.E, capacity, b.counts, b.kept,
+                                         b.offsets, b.mtile_prefix, b.n_dropped);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  dispatch_scatter_kernel<<<nblk, kDispatchBlock, 0, s>>>(idx, c.T, c.E, c.k, capacity, b.bitmap,
+                                                          b.blk_base, b.offsets, b.pos, b.row_of,
+                                                          b.perm);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  const int total_rows = c.T * c.k;
+  const int esz = c.dtype == MOE_DTYPE_F32 ? 4 : 2;
+  const int row_bytes = c.d_model * esz;
+  int blocks = ceil_div(total_rows, 8);
+  const int cap_blocks = num_sms() * 8;
+  if (blocks > cap_blocks) blocks = cap_blocks;
+  gather_rows_kernel<16><<<blocks, 256, 0, s>>>(b.offsets, c.E, c.k, total_rows, row_bytes,
+                                                b.perm, (const unsigned char*)x,
+                                                (unsigned char*)x_perm);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

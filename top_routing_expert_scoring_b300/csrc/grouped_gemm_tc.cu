@@ -1,0 +1,530 @@
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), sm_103a.
+//
+//   GEMM 1 (gate/up):  h = SiLU(X W1_e^T) * (X W3_e^T)     ["Systems for Mixture-of-Experts
+//   GEMM 2 (down):     y = h W2_e^T                          Models" §5.2 SwiGLU experts]
+//
+// over expert-ordered rows (expert e owns rows [offsets[e], offsets[e+1]), ragged).
+//
+// Design:
+//   * persistent CTAs (one per SM) walk a device-side tile list; tile -> (expert, N tile,
+//     M tile) with the M tile fastest, so the CTAs running at the same time share one weight
+//     tile, which is read from HBM once and from L2 by the others;
+//   * warp 0 issues TMA loads (128B-swizzled, K-major, 64-element K slices) into a 4-stage
+//     ring; warp 1 issues tcgen05.mma (M=128, N=256, K=16, bf16 in, fp32 accumulate in TMEM);
+//     warps 2-5 drain the accumulator (tcgen05.ld) and store bf16 rows.  Two TMEM
+//     accumulators (2 x 256 columns) let the epilogue of one tile overlap the MMAs of the next;
+//   * GEMM 1 puts 128 gate rows and the matching 128 up rows of W13 in one B tile, so one
+//     N=256 MMA yields both halves and the epilogue forms SiLU(gate) * up directly;
+//   * rows of an M tile past its expert's end are computed and never stored;
+//   * every mbarrier wait is bounded (about 2 s); on expiry the CTA records MOE_ERR_TIMEOUT in
+//     the status word, stops its loops, waits (bounded) for its own copies and MMAs in flight,
+//     frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BK = 64;                       // 64 bf16 = 128 bytes = one swizzle row
+constexpr int STAGES = 4;
+constexpr int A_STAGE = BM * BK * 2;         // 16 KB
+constexpr int B_BOX = 128 * BK * 2;          // 16 KB, one TMA box of 128 rows
+constexpr int B_STAGE = 2 * B_BOX;           // up to 256 rows
+constexpr int TMEM_COLS = 512;               // 2 accumulators x 256 fp32 columns
+constexpr int THREADS = 192;
+constexpr int NBARS = 2 * STAGES + 5;        // full, empty, tmem full x2, tmem empty x2, drain
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * (A_STAGE + B_STAGE) + 256;
+
+struct Params {
+  const int32_t* offsets;   // [E+1]
+  const int32_t* mtp;       // [E+1] prefix of M tiles
+  int E;
+  int uniform_rows;         // >= 0: one group of this many rows
+  int K;                    // reduction length (multiple of 64)
+  int n_tiles;              // N tiles per expert
+  int bn;                   // MMA N (128 or 256)
+  int swiglu;               // GEMM 1 epilogue
+  int b_rows;               // rows of B per expert
+  int up_off;               // GEMM 1: offset of the up rows inside an expert's B rows (F)
+  __nv_bfloat16* out;
+  int ldo;
+  DevStatus* st;
+};
+
+// ---------------------------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase of `bar` with the given parity.  Gives up when the CTA's abort flag is
+// raised (honor_abort) or after kWaitLimitNs, raising the flag and recording the timeout.
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
+                                          volatile int* abort_flag, DevStatus* st, int where,
+                                          bool honor_abort, uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 0u) {
+      if (honor_abort && *abort_flag) return false;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        *abort_flag = 1;
+        record_error(st, MOE_ERR_TIMEOUT, where);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand stored with the 128-byte swizzle:
+// rows of 128 bytes, 8-row atoms of 1024 bytes stacked along M/N (stride byte offset 1024).
+// Advancing K by 16 elements inside the atom adds 32 bytes to the start address.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address  [0,14)
+  d |= static_cast<uint64_t>(1) << 16;                     // leading byte offset (unused)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;             // stride byte offset [32,46)
+  d |= static_cast<uint64_t>(1) << 46;                     // descriptor version [46,48)
+  d |= static_cast<uint64_t>(2) << 61;                     // 128-byte swizzle [61,64)
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D = f32, A = B = bf16, both K-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane, then wait for the load.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------------------------
+// Tile list
+// ---------------------------------------------------------------------------------------------
+struct TileInfo {
+  int e, row0, rows, nt;
+};
+
+__device__ __forceinline__ int total_tiles(const Params& p) {
+  const int mt = p.uniform_rows >= 0 ? ceil_div(p.uniform_rows, BM) : p.mtp[p.E];
+  return mt * p.n_tiles;
+}
+
+__device__ __forceinline__ TileInfo decode_tile(int tile, const Params& p) {
+  TileInfo ti;
+  int base_m, mt_e, row_base, row_end;
+  if (p.uniform_rows >= 0) {
+    ti.e = 0;
+    base_m = 0;
+    mt_e = ceil_div(p.uniform_rows, BM);
+    row_base = 0;
+    row_end = p.uniform_rows;
+  } else {
+    int lo = 0, hi = p.E;   // largest e in [0, E) with mtp[e] * n_tiles <= tile
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (p.mtp[mid] * p.n_tiles <= tile) lo = mid; else hi = mid;
+    }
+    ti.e = lo;
+    base_m = p.mtp[lo];
+    mt_e = p.mtp[lo + 1] - base_m;
+    row_base = p.offsets[lo];
+    row_end = p.offsets[lo + 1];
+  }
+  const int tt = tile - base_m * p.n_tiles;
+  ti.nt = tt / mt_e;
+  const int mt = tt - ti.nt * mt_e;
+  ti.row0 = row_base + mt * BM;
+  ti.rows = min(BM, row_end - ti.row0);
+  return ti;
+}
+
+// ---------------------------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_STAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_STAGE);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * STAGES;
+  const uint32_t tfull0 = empty0 + 8 * STAGES;
+  const uint32_t tempty0 = tfull0 + 16;
+  const uint32_t drain = tempty0 + 16;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = total_tiles(p);
+  const int KB = p.K / BK;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------- TMA producer -------------------------------------------
+    int stage = 0;
+    uint32_t ph = 0;
+    uint32_t issued = 0, last_par = 0;   // per-stage bit masks for the drain
+    const int nbox = (p.swiglu || p.bn == 256) ? 2 : 1;
+    const uint32_t bytes = A_STAGE + nbox * B_BOX;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      const TileInfo ti = decode_tile(tile, p);
+      int b0, b1;
+      if (p.swiglu) {
+        b0 = ti.e * p.b_rows + ti.nt * 128;
+        b1 = b0 + p.up_off;
+      } else {
+        b0 = ti.e * p.b_rows + ti.nt * p.bn;
+        b1 = b0 + 128;
+      }
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!wait_bounded(empty0 + 8 * stage, ph ^ 1u, abort_flag, p.st, 1, true)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = full0 + 8 * stage;
+        mbar_expect_tx(fb, bytes);
+        tma_load_2d(smem_u32(sA + stage * A_STAGE), &tmA, fb, kb * BK, ti.row0);
+        tma_load_2d(smem_u32(sB + stage * B_STAGE), &tmB, fb, kb * BK, b0);
+        if (nbox == 2) tma_load_2d(smem_u32(sB + stage * B_STAGE + B_BOX), &tmB, fb, kb * BK, b1);
+        issued |= 1u << stage;
+        last_par = (last_par & ~(1u << stage)) | (ph << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+    if (!ok) {
+      // wait for this CTA's own copies in flight before the CTA may exit
+      for (int s = 0; s < STAGES; ++s)
+        if ((issued >> s) & 1u)
+          wait_bounded(full0 + 8 * s, (last_par >> s) & 1u, abort_flag, p.st, 5, false);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------- MMA issuer ---------------------------------------------
+    const uint32_t idesc = idesc_bf16_f32(BM, p.bn);
+    int stage = 0, acc = 0;
+    uint32_t ph = 0, aph = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      if (!wait_bounded(tempty0 + 8 * acc, aph ^ 1u, abort_flag, p.st, 2, true)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t dt = tmem_base + static_cast<uint32_t>(acc * 256);
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!wait_bounded(full0 + 8 * stage, ph, abort_flag, p.st, 3, true)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(sA + stage * A_STAGE);
+        const uint32_t b0 = smem_u32(sB + stage * B_STAGE);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          tc_mma(dt, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), idesc,
+                 (kb | kk) != 0 ? 1u : 0u);
+        tc_commit(empty0 + 8 * stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!ok) break;
+      tc_commit(tfull0 + 8 * acc);
+      acc ^= 1;
+      if (acc == 0) aph ^= 1u;
+    }
+    // every MMA this thread issued must finish before TMEM is released
+    tc_commit(drain);
+    wait_bounded(drain, 0u, abort_flag, p.st, 6, false);
+  } else if (warp >= 2) {
+    // ------------------------------- epilogue -----------------------------------------------
+    const int q = warp & 3;                 // TMEM lanes 32q .. 32q+31 belong to this warp
+    const int r = q * 32 + lane;            // row of the tile held by this thread
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const TileInfo ti = decode_tile(tile, p);
+      int ok = 1;
+      if (lane == 0) ok = wait_bounded(tfull0 + 8 * acc, aph, abort_flag, p.st, 4, true) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * 256) +
+                          (static_cast<uint32_t>(q * 32) << 16);
+      const bool live = r < ti.rows;
+      if (p.swiglu) {
+        __nv_bfloat16* orow = p.out + static_cast<size_t>(ti.row0 + r) * p.ldo + ti.nt * 128;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t gr[32], ur[32];
+          tmem_ld32(tb + c * 32, gr);
+          tmem_ld32(tb + 128 + c * 32, ur);
+          uint32_t packed[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float g0 = __uint_as_float(gr[2 * i]), g1 = __uint_as_float(gr[2 * i + 1]);
+            const float u0 = __uint_as_float(ur[2 * i]), u1 = __uint_as_float(ur[2 * i + 1]);
+            const float h0 = (g0 / (1.0f + __expf(-g0))) * u0;
+            const float h1 = (g1 / (1.0f + __expf(-g1))) * u1;
+            __nv_bfloat162 hv = __floats2bfloat162_rn(h0, h1);
+            packed[i] = *reinterpret_cast<uint32_t*>(&hv);
+          }
+          if (live) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
+                                  packed[4 * v + 3]);
+          }
+        }
+      } else {
+        __nv_bfloat16* orow = p.out + static_cast<size_t>(ti.row0 + r) * p.ldo + ti.nt * p.bn;
+        const int nchunks = p.bn / 32;
+#pragma unroll 1
+        for (int c = 0; c < nchunks; ++c) {
+          uint32_t vr[32];
+          tmem_ld32(tb + c * 32, vr);
+          uint32_t packed[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            __nv_bfloat162 hv =
+                __floats2bfloat162_rn(__uint_as_float(vr[2 * i]), __uint_as_float(vr[2 * i + 1]));
+            packed[i] = *reinterpret_cast<uint32_t*>(&hv);
+          }
+          if (live) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
+                                  packed[4 * v + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      acc ^= 1;
+      if (acc == 0) aph ^= 1u;
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// A kernel whose only wait is on a flag nothing ever sets: exercises the bounded-wait failure
+// path (status word set, kernel returns, context stays usable).
+__global__ void timeout_probe_kernel(DevStatus* st, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) wait_bounded(smem_u32(&bar), 0u, &abort_flag, st, 99, true, limit_ns);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor [rows, cols] (cols contiguous) read in boxes of 64 columns x 128 rows.
+static bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), 128};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const Params& p,
+                              int upper_tiles, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(SMEM_BYTES));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  int grid = num_sms();
+  if (upper_tiles < grid) grid = upper_tiles;
+  if (grid < 1) grid = 1;
+  grouped_gemm_tc_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(a, b, p);
+  return cudaGetLastError();
+}
+
+}  // namespace tc
+
+cudaError_t launch_ffn_tc(const GroupedFFN& g, DevStatus* st, cudaStream_t s) {
+  using namespace tc;
+  CUtensorMap mx, mw13, mh, mw2;
+  if (!make_map(&mx, g.x, (uint64_t)g.max_rows, (uint64_t)g.d) ||
+      !make_map(&mw13, g.w13, (uint64_t)g.E * 2 * g.F, (uint64_t)g.d) ||
+      !make_map(&mh, g.h, (uint64_t)g.max_rows, (uint64_t)g.F) ||
+      !make_map(&mw2, g.w2, (uint64_t)g.E * g.d, (uint64_t)g.F))
+    return cudaErrorInvalidValue;
+  const int mt_upper = g.uniform_rows >= 0 ? ceil_div(g.uniform_rows, BM)
+                                           : ceil_div(g.max_rows, BM) + g.E;
+  Params p1{};
+  p1.offsets = g.offsets;
+  p1.mtp = g.mtile_prefix;
+  p1.E = g.E;
+  p1.uniform_rows = g.uniform_rows;
+  p1.K = g.d;
+  p1.n_tiles = g.F / 128;
+  p1.bn = 256;
+  p1.swiglu = 1;
+  p1.b_rows = 2 * g.F;
+  p1.up_off = g.F;
+  p1.out = static_cast<__nv_bfloat16*>(g.h);
+  p1.ldo = g.F;
+  p1.st = st;
+  cudaError_t err = launch_one(mx, mw13, p1, mt_upper * p1.n_tiles, s);
+  if (err != cudaSuccess) return err;
+  Params p2 = p1;
+  p2.K = g.F;
+  p2.bn = (g.d % 256 == 0) ? 256 : 128;
+  p2.n_tiles = g.d / p2.bn;
+  p2.swiglu = 0;
+  p2.b_rows = g.d;
+  p2.up_off = 0;
+  p2.out = static_cast<__nv_bfloat16*>(g.y);
+  p2.ldo = g.d;
+  return launch_one(mh, mw2, p2, mt_upper * p2.n_tiles, s);
+}
+
+cudaError_t launch_timeout_probe(DevStatus* st, int limit_us, cudaStream_t s) {
+  tc::timeout_probe_kernel<<<1, 32, 0, s>>>(st, static_cast<uint64_t>(limit_us) * 1000ull);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

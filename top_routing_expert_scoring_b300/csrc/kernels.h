@@ -1,0 +1,80 @@
+// Host-side launchers of the MoE layer kernels.  Each returns cudaSuccess or the launch error.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+// ---- router ----------------------------------------------------------------------------------
+cudaError_t launch_router_logits(const moe_config& c, const void* x, const void* w_gate,
+                                 float* logits, cudaStream_t s);
+cudaError_t launch_route_topk(const moe_config& c, const float* logits, const float* bias,
+                              int32_t* idx, float* w, DevStatus* st, cudaStream_t s);
+cudaError_t launch_aux_stats(const moe_config& c, const float* logits, const int32_t* idx,
+                             const int32_t* ec_counts, float* part_P, int32_t* part_cnt,
+                             float* part_z, int nblocks, float* f, float* P, float* l_balance,
+                             float* z_loss, DevStatus* st, cudaStream_t s);
+int aux_blocks(const moe_config& c);
+
+// ---- dispatch --------------------------------------------------------------------------------
+struct DispatchBufs {
+  uint32_t* bitmap;     // [nblk][E][kDispatchBlock/32]
+  int32_t* blk_base;    // [nblk][E]
+  int32_t* counts;      // [E]
+  int32_t* kept;        // [E]
+  int32_t* offsets;     // [E+1]
+  int32_t* mtile_prefix;// [E+1] prefix of ceil(kept/kTileM)
+  int32_t* n_dropped;   // [1]
+  int32_t* pos;         // [T,k]
+  int32_t* row_of;      // [T,k]
+  int32_t* perm;        // [T*k]
+};
+cudaError_t launch_dispatch(const moe_config& c, int capacity, const int32_t* idx,
+                            const DispatchBufs& b, const void* x, void* x_perm, DevStatus* st,
+                            cudaStream_t s);
+
+// ---- expert FFN ------------------------------------------------------------------------------
+// Grouped SwiGLU over expert-ordered rows.  offsets/mtile_prefix describe the E groups; with
+// uniform_rows >= 0 there is one group of uniform_rows rows and the device arrays are unused.
+struct GroupedFFN {
+  const void* x;            // [rows, d]
+  const int32_t* offsets;   // [E+1]
+  const int32_t* mtile_prefix;  // [E+1]
+  int uniform_rows;
+  int E, d, F;
+  int max_rows;             // rows allocated in x / h / y
+  const void* w13;          // [E, 2F, d]
+  const void* w2;           // [E, d, F]
+  void* h;                  // [max_rows, F] scratch
+  void* y;                  // [max_rows, d]
+};
+cudaError_t launch_ffn_tc(const GroupedFFN& g, DevStatus* st, cudaStream_t s);
+cudaError_t launch_ffn_simt(const GroupedFFN& g, bool f32, DevStatus* st, cudaStream_t s);
+
+// ---- combine ---------------------------------------------------------------------------------
+cudaError_t launch_combine(const moe_config& c, const void* y_perm, const int32_t* row_of,
+                           const float* w, const void* shared_out, void* out, cudaStream_t s);
+cudaError_t launch_combine_ec(const moe_config& c, const void* y_perm, const int32_t* tok_ptr,
+                              const int32_t* tok_rows, const float* ec_w_flat,
+                              const void* shared_out, void* out, cudaStream_t s);
+
+// ---- expert choice ---------------------------------------------------------------------------
+// posmap [E][T]: position of token t in expert e's list or -1; ms [T]: softmax (max, sum).
+cudaError_t launch_expert_choice(const moe_config& c, const float* logits, int32_t* ec_tokens,
+                                 float* ec_w, int32_t* tok_cnt, int32_t* tok_ptr,
+                                 int32_t* tok_rows, int32_t* posmap, float2* ms, DevStatus* st,
+                                 cudaStream_t s);
+cudaError_t launch_gather_ec(const moe_config& c, const int32_t* ec_tokens, const void* x,
+                             void* x_perm, int32_t* offsets, int32_t* mtile_prefix,
+                             cudaStream_t s);
+
+// ---- failure-path self test ------------------------------------------------------------------
+cudaError_t launch_timeout_probe(DevStatus* st, int limit_us, cudaStream_t s);
+
+int num_sms();
+
+}  // namespace moe

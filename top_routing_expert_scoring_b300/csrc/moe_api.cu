@@ -1,0 +1,450 @@
+// C ABI of the MoE layer forward: argument checks, workspace layout and the launch sequence.
+// Every entry point validates on the host, enqueues on the caller's stream and returns; the
+// library allocates nothing and never synchronises (except moe_sync_status, which exists to).
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+      n = 148;
+  }
+  return n;
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+
+// Workspace layout.  Offsets are relative to the 256-byte aligned workspace base.
+struct Layout {
+  size_t status, logits, idx, w, bitmap, blk_base, counts, kept, offsets, mtp, n_dropped, pos,
+      row_of, perm, part_P, part_cnt, part_z, f, P, lb, z, x_perm, h, y_perm, shared_out,
+      ec_tokens, ec_w, tok_cnt, tok_ptr, tok_rows, posmap, tokstat, total;
+};
+
+int rows_max(const moe_config& c) { return c.T * c.k; }
+
+Layout layout(const moe_config& c) {
+  Layout L{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align_up(o + (bytes ? bytes : 1));
+    return at;
+  };
+  const size_t T = c.T, E = c.E, k = c.k, d = c.d_model, F = c.d_ff, Fs = c.d_ff_shared;
+  const size_t esz = c.dtype == MOE_DTYPE_F32 ? 4 : 2;
+  const size_t nblk = (T + kDispatchBlock - 1) / kDispatchBlock;
+  const size_t naux = aux_blocks(c);
+  const size_t R = rows_max(c);
+  L.status = take(sizeof(DevStatus));
+  L.logits = take(T * E * 4);
+  L.idx = take(T * k * 4);
+  L.w = take(T * k * 4);
+  L.bitmap = take(nblk * E * (kDispatchBlock / 32) * 4);
+  L.blk_base = take(nblk * E * 4);
+  L.counts = take(E * 4);
+  L.kept = take(E * 4);
+  L.offsets = take((E + 1) * 4);
+  L.mtp = take((E + 1) * 4);
+  L.n_dropped = take(4);
+  L.pos = take(T * k * 4);
+  L.row_of = take(T * k * 4);
+  L.perm = take(T * k * 4);
+  L.part_P = take(naux * E * 4);
+  L.part_cnt = take(naux * E * 4);
+  L.part_z = take(naux * 4);
+  L.f = take(E * 4);
+  L.P = take(E * 4);
+  L.lb = take(4);
+  L.z = take(4);
+  L.x_perm = take(R * d * esz);
+  const size_t hrows = R > T ? R : T;
+  const size_t hcols = F > Fs ? F : Fs;
+  L.h = take(hrows * hcols * esz);
+  L.y_perm = take(R * d * esz);
+  L.shared_out = take(Fs ? T * d * esz : 0);
+  if (c.routing == MOE_ROUTE_EXPERT_CHOICE) {
+    const size_t C = (T * k) / E;
+    L.ec_tokens = take(E * C * 4);
+    L.ec_w = take(E * C * 4);
+    L.tok_cnt = take(T * 4);
+    L.tok_ptr = take((T + 1) * 4);
+    L.tok_rows = take(E * C * 4);
+    L.posmap = take(E * T * 4);
+    L.tokstat = take(T * 8);
+  }
+  L.total = o;
+  return L;
+}
+
+template <typename P>
+P* at(void* ws, size_t off) {
+  return reinterpret_cast<P*>(static_cast<unsigned char*>(ws) + off);
+}
+
+int check_ws(void* ws) {
+  if (!ws) return MOE_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) % kAlign) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+int capacity_of(const moe_config& c) {
+  if (!(c.capacity_factor > 0.0f)) return c.T * c.k;
+  const double C = std::ceil(static_cast<double>(c.capacity_factor) * c.k * c.T / c.E);
+  const double lim = static_cast<double>(c.T) * c.k;
+  return static_cast<int>(C < lim ? C : lim);
+}
+
+bool bf16(const moe_config& c) { return c.dtype == MOE_DTYPE_BF16; }
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_ARG: return "invalid argument (NULL pointer, bad enum or bad index)";
+    case MOE_ERR_SHAPE: return "unsupported or inconsistent sizes";
+    case MOE_ERR_UNSUPPORTED: return "request not implemented by this build";
+    case MOE_ERR_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_TIMEOUT: return "a bounded device-side wait ran out";
+    default: return "unknown status";
+  }
+}
+
+const char* moe_version(void) { return "moe_b300 1.0 sm_103a"; }
+
+int moe_check_config(const moe_config* c) {
+  if (!c) return MOE_ERR_ARG;
+  if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID) return MOE_ERR_ARG;
+  if (c->routing != MOE_ROUTE_TOKEN_CHOICE && c->routing != MOE_ROUTE_EXPERT_CHOICE)
+    return MOE_ERR_ARG;
+  if (c->dtype != MOE_DTYPE_BF16 && c->dtype != MOE_DTYPE_F32) return MOE_ERR_ARG;
+  if (c->renormalize != 0 && c->renormalize != 1) return MOE_ERR_ARG;
+  if (!std::isfinite(c->route_scale) || !std::isfinite(c->capacity_factor)) return MOE_ERR_ARG;
+  if (c->T < 1 || c->T > (1 << 20)) return MOE_ERR_SHAPE;
+  if (c->E < 1 || c->E > 256) return MOE_ERR_SHAPE;
+  if (c->k < 1 || c->k > 8 || c->k > c->E) return MOE_ERR_SHAPE;
+  if (c->d_model < 1 || c->d_ff < 1 || c->d_ff_shared < 0) return MOE_ERR_SHAPE;
+  if ((long long)c->T * c->k * (c->d_model > c->d_ff ? c->d_model : c->d_ff) > (1ll << 40))
+    return MOE_ERR_SHAPE;
+  if (c->n_groups < 1 || c->n_groups > 32 || c->E % c->n_groups) return MOE_ERR_SHAPE;
+  if (c->topk_groups < 1 || c->topk_groups > c->n_groups) return MOE_ERR_SHAPE;
+  if (c->topk_groups < c->n_groups) {
+    if (c->score != MOE_SCORE_SIGMOID) return MOE_ERR_UNSUPPORTED;
+    if (c->topk_groups * (c->E / c->n_groups) < c->k) return MOE_ERR_SHAPE;
+  }
+  if (c->dtype == MOE_DTYPE_BF16) {
+    if (c->d_model % 128 || c->d_ff % 128 || c->d_ff_shared % 128) return MOE_ERR_SHAPE;
+  } else {
+    if (c->d_model % 4) return MOE_ERR_SHAPE;
+  }
+  if (c->routing == MOE_ROUTE_EXPERT_CHOICE) {
+    if (c->score != MOE_SCORE_SOFTMAX) return MOE_ERR_UNSUPPORTED;
+    const long long C = (long long)c->T * c->k / c->E;
+    if (C < 1 || C > c->T) return MOE_ERR_SHAPE;
+  }
+  return MOE_OK;
+}
+
+int moe_capacity(const moe_config* c, int32_t* capacity) {
+  int st = moe_check_config(c);
+  if (st) return st;
+  if (!capacity) return MOE_ERR_ARG;
+  *capacity = capacity_of(*c);
+  return MOE_OK;
+}
+
+int moe_workspace_size(const moe_config* c, size_t* bytes) {
+  int st = moe_check_config(c);
+  if (st) return st;
+  if (!bytes) return MOE_ERR_ARG;
+  *bytes = layout(*c).total;
+  return MOE_OK;
+}
+
+int moe_sync_status(void* ws, void* stream) {
+  if (check_ws(ws)) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DevStatus h{};
+  DevStatus* d = at<DevStatus>(ws, 0);
+  if (cudaMemcpyAsync(&h, d, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (h.code != 0) {
+    if (cudaMemsetAsync(d, 0, sizeof(DevStatus), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return h.code;
+}
+
+int moe_router_topk(const moe_config* c, const void* x, const void* w_gate, const float* bias,
+                    float* logits, int32_t* topk_idx, float* topk_w, void* ws, void* stream) {
+  int st = moe_check_config(c);
+  if (st) return st;
+  if (c->routing != MOE_ROUTE_TOKEN_CHOICE) return MOE_ERR_UNSUPPORTED;
+  if (!x || !w_gate || !topk_idx || !topk_w) return MOE_ERR_ARG;
+  if ((st = check_ws(ws))) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Layout L = layout(*c);
+  float* g = logits ? logits : at<float>(ws, L.logits);
+  cudaError_t e = launch_router_logits(*c, x, w_gate, g, s);
+  if (e == cudaSuccess)
+    e = launch_route_topk(*c, g, bias, topk_idx, topk_w, at<DevStatus>(ws, L.status), s);
+  return cuda_status(e);
+}
+
+int moe_aux_stats(const moe_config* c, const float* logits, const int32_t* topk_idx, float* f,
+                  float* P, float* l_balance, float* z_loss, void* ws, void* stream) {
+  int st = moe_check_config(c);
+  if (st) return st;
+  if (!logits) return MOE_ERR_ARG;
+  if (c->routing == MOE_ROUTE_TOKEN_CHOICE && !topk_idx) return MOE_ERR_ARG;
+  if ((st = check_ws(ws))) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Layout L = layout(*c);
+  return cuda_status(launch_aux_stats(
+      *c, logits, topk_idx, nullptr, at<float>(ws, L.part_P), at<int32_t>(ws, L.part_cnt),
+      at<float>(ws, L.part_z), aux_blocks(*c), f, P, l_balance, z_loss,
+      at<DevStatus>(ws, L.status), s));
+}
+
+int moe_dispatch(const moe_config* c, const int32_t* topk_idx, const void* x, int32_t* counts,
+                 int32_t* kept, int32_t* offsets, int32_t* pos, int32_t* row_of, int32_t* perm,
+                 void* x_perm, int32_t* n_dropped, void* ws, void* stream) {
+  int st = moe_check_config(c);
+  if (st) return st;
+  if (c->routing != MOE_ROUTE_TOKEN_CHOICE) return MOE_ERR_UNSUPPORTED;
+  if (!topk_idx || !counts || !kept || !offsets || !pos || !row_of || !perm || !n_dropped)
+    return MOE_ERR_ARG;
+  if ((x == nullptr) != (x_perm == nullptr)) return MOE_ERR_ARG;
+  if ((st = check_ws(ws))) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Layout L = layout(*c);
+  DispatchBufs b{at<uint32_t>(ws, L.bitmap), at<int32_t>(ws, L.blk_base), counts, kept,
+                 offsets, at<int32_t>(ws, L.mtp), n_dropped, pos, row_of, perm};
+  return cuda_status(launch_dispatch(*c, capacity_of(*c), topk_idx, b, x, x_perm,
+                                     at<DevStatus>(ws, L.status), s));
+}
+
+}  // extern "C"
+
+namespace moe {
+namespace {
+
+int run_ffn(const moe_config& c, const void* xin, const int32_t* offsets, const int32_t* mtp,
+            int uniform_rows, int E, int F, int max_rows, const void* w13, const void* w2,
+            void* y, void* ws, const Layout& L, cudaStream_t s) {
+  GroupedFFN g{};
+  g.x = xin;
+  g.offsets = offsets;
+  g.mtile_prefix = mtp;
+  g.uniform_rows = uniform_rows;
+  g.E = E;
+  g.d = c.d_model;
+  g.F = F;
+  g.max_rows = max_rows;
+  g.w13 = w13;
+  g.w2 = w2;
+  g.h = at<void>(ws, L.h);
+  g.y = y;
+  DevStatus* st = at<DevStatus>(ws, L.status);
+  cudaError_t e = bf16(c) ? launch_ffn_tc(g, st, s) : launch_ffn_simt(g, true, st, s);
+  return cuda_status(e);
+}
+
+// offsets [E+1] given by the caller: the M-tile prefix the GEMM scheduler needs is rebuilt
+// on the device from them.
+__global__ void mtp_from_offsets(const int32_t* offsets, int E, int32_t* mtp) {
+  __shared__ int s[256];
+  const int e = threadIdx.x;
+  int v = 0;
+  if (e < E) v = ceil_div(offsets[e + 1] - offsets[e], kTileM);
+  s[e] = v;
+  __syncthreads();
+  for (int o = 1; o < 256; o <<= 1) {
+    int a = e >= o ? s[e - o] : 0;
+    __syncthreads();
+    s[e] += a;
+    __syncthreads();
+  }
+  if (e < E) mtp[e + 1] = s[e];
+  if (e == 0) mtp[0] = 0;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" {
+
+int moe_expert_ffn(const moe_config* c, const void* x_perm, const int32_t* offsets,
+                   const void* w13, const void* w2, void* y_perm, void* ws, void* stream) {
+  int st = moe_check_config(c);
+  if (st) return st;
+  if (!x_perm || !offsets || !w13 || !w2 || !y_perm) return MOE_ERR_ARG;
+  if ((st = check_ws(ws))) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Layout L = layout(*c);
+  int32_t* mtp = at<int32_t>(ws, L.mtp);
+  mtp_from_offsets<<<1, 256, 0, s>>>(offsets, c->E, mtp);
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  return run_ffn(*c, x_perm, offsets, mtp, -1, c->E, c->d_ff, rows_max(*c), w13, w2, y_perm, ws,
+                 L, s);
+}
+
+int moe_shared_ffn(const moe_config* c, const void* x, const void* ws13, const void* ws2,
+                   void* shared_out, void* ws, void* stream) {
+  int st = moe_check_config(c);
+  if (st) return st;
+  if (c->d_ff_shared <= 0) return MOE_ERR_SHAPE;
+  if (!x || !ws13 || !ws2 || !shared_out) return MOE_ERR_ARG;
+  if ((st = check_ws(ws))) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Layout L = layout(*c);
+  return run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13, ws2, shared_out,
+                 ws, L, s);
+}
+
+int moe_combine(const moe_config* c, const void* y_perm, const int32_t* row_of,
+                const float* topk_w, const void* shared_out, void* out, void* stream) {
+  int st = moe_check_config(c);
+  if (st) return st;
+  if (c->routing != MOE_ROUTE_TOKEN_CHOICE) return MOE_ERR_UNSUPPORTED;
+  if (!y_perm || !row_of || !topk_w || !out) return MOE_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return cuda_status(launch_combine(*c, y_perm, row_of, topk_w, shared_out, out, s));
+}
+
+int moe_expert_choice(const moe_config* c, const float* logits, int32_t* ec_tokens, float* ec_w,
+                      int32_t* tok_ptr, int32_t* tok_rows, void* ws, void* stream) {
+  int st = moe_check_config(c);
+  if (st) return st;
+  if (c->routing != MOE_ROUTE_EXPERT_CHOICE) return MOE_ERR_ARG;
+  if (!logits || !ec_tokens || !ec_w || !tok_ptr || !tok_rows) return MOE_ERR_ARG;
+  if ((st = check_ws(ws))) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Layout L = layout(*c);
+  return cuda_status(launch_expert_choice(*c, logits, ec_tokens, ec_w, at<int32_t>(ws, L.tok_cnt),
+                                          tok_ptr, tok_rows, at<int32_t>(ws, L.posmap),
+                                          at<float2>(ws, L.tokstat), at<DevStatus>(ws, L.status),
+                                          s));
+}
+
+int moe_forward(const moe_config* c, const void* x, const void* w_gate, const float* bias,
+                const void* w13, const void* w2, const void* ws13, const void* ws2, void* out,
+                int32_t* topk_idx, float* topk_w, float* f, float* P, float* l_balance,
+                float* z_loss, int32_t* n_dropped, void* ws, void* stream) {
+  int st = moe_check_config(c);
+  if (st) return st;
+  if (!x || !w_gate || !w13 || !w2 || !out) return MOE_ERR_ARG;
+  if (c->d_ff_shared > 0 && (!ws13 || !ws2)) return MOE_ERR_ARG;
+  if ((st = check_ws(ws))) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Layout L = layout(*c);
+  DevStatus* dst = at<DevStatus>(ws, L.status);
+  float* g = at<float>(ws, L.logits);
+  f = f ? f : at<float>(ws, L.f);
+  P = P ? P : at<float>(ws, L.P);
+  l_balance = l_balance ? l_balance : at<float>(ws, L.lb);
+  z_loss = z_loss ? z_loss : at<float>(ws, L.z);
+  void* shared = c->d_ff_shared > 0 ? at<void>(ws, L.shared_out) : nullptr;
+
+  cudaError_t e = launch_router_logits(*c, x, w_gate, g, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  if (c->routing == MOE_ROUTE_TOKEN_CHOICE) {
+    int32_t* idx = topk_idx ? topk_idx : at<int32_t>(ws, L.idx);
+    float* w = topk_w ? topk_w : at<float>(ws, L.w);
+    if ((e = launch_route_topk(*c, g, bias, idx, w, dst, s)) != cudaSuccess) return MOE_ERR_CUDA;
+    if ((e = launch_aux_stats(*c, g, idx, nullptr, at<float>(ws, L.part_P),
+                              at<int32_t>(ws, L.part_cnt), at<float>(ws, L.part_z),
+                              aux_blocks(*c), f, P, l_balance, z_loss, dst, s)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    DispatchBufs b{at<uint32_t>(ws, L.bitmap), at<int32_t>(ws, L.blk_base),
+                   at<int32_t>(ws, L.counts), at<int32_t>(ws, L.kept),
+                   at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.mtp),
+                   n_dropped ? n_dropped : at<int32_t>(ws, L.n_dropped), at<int32_t>(ws, L.pos),
+                   at<int32_t>(ws, L.row_of), at<int32_t>(ws, L.perm)};
+    if ((e = launch_dispatch(*c, capacity_of(*c), idx, b, x, at<void>(ws, L.x_perm), dst, s)) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    if ((st = run_ffn(*c, at<void>(ws, L.x_perm), b.offsets, b.mtile_prefix, -1, c->E, c->d_ff,
+                      rows_max(*c), w13, w2, at<void>(ws, L.y_perm), ws, L, s)))
+      return st;
+    if (shared && (st = run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13,
+                                ws2, shared, ws, L, s)))
+      return st;
+    return cuda_status(launch_combine(*c, at<void>(ws, L.y_perm), b.row_of, w, shared, out, s));
+  }
+
+  // expert choice
+  const int C = (int)((long long)c->T * c->k / c->E);
+  int32_t* ec_tokens = at<int32_t>(ws, L.ec_tokens);
+  float* ec_w = at<float>(ws, L.ec_w);
+  if ((e = launch_expert_choice(*c, g, ec_tokens, ec_w, at<int32_t>(ws, L.tok_cnt),
+                                at<int32_t>(ws, L.tok_ptr), at<int32_t>(ws, L.tok_rows),
+                                at<int32_t>(ws, L.posmap), at<float2>(ws, L.tokstat), dst, s)) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  if ((e = launch_aux_stats(*c, g, nullptr, nullptr, at<float>(ws, L.part_P),
+                            at<int32_t>(ws, L.part_cnt), at<float>(ws, L.part_z), aux_blocks(*c),
+                            f, P, l_balance, z_loss, dst, s)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if ((e = launch_gather_ec(*c, ec_tokens, x, at<void>(ws, L.x_perm), at<int32_t>(ws, L.offsets),
+                            at<int32_t>(ws, L.mtp), s)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if ((st = run_ffn(*c, at<void>(ws, L.x_perm), at<int32_t>(ws, L.offsets),
+                    at<int32_t>(ws, L.mtp), -1, c->E, c->d_ff, c->E * C, w13, w2,
+                    at<void>(ws, L.y_perm), ws, L, s)))
+    return st;
+  if (shared && (st = run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13, ws2,
+                              shared, ws, L, s)))
+    return st;
+  return cuda_status(launch_combine_ec(*c, at<void>(ws, L.y_perm), at<int32_t>(ws, L.tok_ptr),
+                                       at<int32_t>(ws, L.tok_rows), ec_w, shared, out, s));
+}
+
+int moe_workspace_views(const moe_config* c, void* ws, float** logits, int32_t** row_of,
+                        int32_t** offsets, void** x_perm, void** y_perm) {
+  int st = moe_check_config(c);
+  if (st) return st;
+  if ((st = check_ws(ws))) return st;
+  const Layout L = layout(*c);
+  if (logits) *logits = at<float>(ws, L.logits);
+  if (row_of) *row_of = at<int32_t>(ws, L.row_of);
+  if (offsets) *offsets = at<int32_t>(ws, L.offsets);
+  if (x_perm) *x_perm = at<void>(ws, L.x_perm);
+  if (y_perm) *y_perm = at<void>(ws, L.y_perm);
+  return MOE_OK;
+}
+
+int moe_selftest_timeout(void* ws, int32_t limit_us, void* stream) {
+  int st = check_ws(ws);
+  if (st) return st;
+  if (limit_us < 1 || limit_us > 2000000) return MOE_ERR_ARG;
+  return cuda_status(launch_timeout_probe(at<DevStatus>(ws, 0), limit_us,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

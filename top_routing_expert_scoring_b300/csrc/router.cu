@@ -1,0 +1,391 @@
+// Router kernels: logits, scoring + Top-k + weights, and the load-balance statistics.
+//
+//   g = x W_gate                                   ["MoE 路由数学" §2.1]
+//   softmax:  p = softmax(g), S = TopK(g, k), w = p_S / sum_S p     (same section)
+//   sigmoid:  s = sigmoid(g), selection on s + b, groups limited by the sum of each group's
+//             two best biased scores, w = route_scale * s_S / sum_S s
+//                                                  ["Systems for Mixture-of-Experts Models"
+//                                                   §5.3 router walk-through]
+//   stats:    f_i, P_i, L = E sum f_i P_i, z = mean (logsumexp g)^2
+//                                                  ["MoE 路由数学" §3.2; "Mixture of Experts 架构"
+//                                                   load_balancing_loss / router_z_loss blocks]
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------------------------------
+// Logits on CUDA cores: one CTA computes a 32-token x 64-expert tile, K in chunks of 32.
+// Each output is a sequential fp32 sum over c in index order.
+// ------------------------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(256) router_logits_simt(const T* __restrict__ x,
+                                                         const T* __restrict__ w,
+                                                         float* __restrict__ g, int Tn, int d,
+                                                         int E) {
+  constexpr int TT = 32, TE = 64, TK = 32;
+  __shared__ float xs[TK][TT + 1];
+  __shared__ float wsm[TK][TE + 1];
+  const int t0 = blockIdx.x * TT, e0 = blockIdx.y * TE;
+  const int tid = threadIdx.x;
+  const int tx = tid % 16, ty = tid / 16;      // ty: token pair, tx: 4 experts
+  float acc[2][4] = {};
+  for (int k0 = 0; k0 < d; k0 += TK) {
+    for (int i = tid; i < TT * TK; i += 256) {
+      int r = i / TK, kk = i % TK;
+      int t = t0 + r, c = k0 + kk;
+      xs[kk][r] = (t < Tn && c < d) ? to_f32(x[(size_t)t * d + c]) : 0.f;
+    }
+    for (int i = tid; i < TE * TK; i += 256) {
+      int r = i / TK, kk = i % TK;
+      int e = e0 + r, c = k0 + kk;
+      wsm[kk][r] = (e < E && c < d) ? to_f32(w[(size_t)e * d + c]) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < TK; ++kk) {
+      float a0 = xs[kk][ty * 2], a1 = xs[kk][ty * 2 + 1];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float b = wsm[kk][tx * 4 + j];
+        acc[0][j] = fmaf(a0, b, acc[0][j]);
+        acc[1][j] = fmaf(a1, b, acc[1][j]);
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    int t = t0 + ty * 2 + r;
+    if (t >= Tn) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      int e = e0 + tx * 4 + j;
+      if (e < E) g[(size_t)t * E + e] = acc[r][j];
+    }
+  }
+}
+
+cudaError_t launch_router_logits(const moe_config& c, const void* x, const void* w_gate,
+                                 float* logits, cudaStream_t s) {
+  dim3 grid(ceil_div(c.T, 32), ceil_div(c.E, 64));
+  if (c.dtype == MOE_DTYPE_F32)
+    router_logits_simt<float><<<grid, 256, 0, s>>>((const float*)x, (const float*)w_gate, logits,
+                                                   c.T, c.d_model, c.E);
+  else
+    router_logits_simt<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16*)x,
+                                                           (const __nv_bfloat16*)w_gate, logits,
+                                                           c.T, c.d_model, c.E);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------------
+// Scoring, group limit, Top-k and weights: one warp per token.  Lane l holds experts
+// l*V .. l*V+V-1 (V = ceil(E/32)); the selection is k rounds of a warp-wide (key, index)
+// maximum, which ranks equal keys by the lower expert index.
+// ------------------------------------------------------------------------------------------
+struct RouteArgs {
+  const float* g;
+  const float* bias;
+  int T, E, k, score, n_groups, topk_groups, renorm;
+  float scale;
+  int32_t* idx;
+  float* w;
+};
+
+template <int V>
+__global__ void __launch_bounds__(256) route_topk_kernel(RouteArgs a) {
+  extern __shared__ float route_smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, wpb = blockDim.x >> 5;
+  const int E = a.E, k = a.k;
+  const bool grouped = a.score == MOE_SCORE_SIGMOID && a.n_groups > 1 && a.topk_groups < a.n_groups;
+  float* row = route_smem + warp * (E + 32);
+  float* gsc = row + E;
+  for (int t = blockIdx.x * wpb + warp; t < a.T; t += gridDim.x * wpb) {
+    float key[V], val[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int e = lane * V + i;
+      const float gv = e < E ? a.g[(size_t)t * E + e] : -INFINITY;
+      if (a.score == MOE_SCORE_SOFTMAX) {
+        key[i] = gv;
+        val[i] = gv;
+      } else {
+        const float sv = e < E ? 1.0f / (1.0f + expf(-gv)) : 0.f;
+        const float b = (e < E && a.bias) ? a.bias[e] : 0.f;
+        val[i] = sv;
+        key[i] = e < E ? sv + b : -INFINITY;
+      }
+    }
+    if (grouped) {
+      const int per = E / a.n_groups;
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        const int e = lane * V + i;
+        if (e < E) row[e] = key[i];
+      }
+      __syncwarp();
+      if (lane < a.n_groups) {
+        float b1 = -INFINITY, b2 = -INFINITY;      // two largest of the group
+        for (int q = 0; q < per; ++q) {
+          const float v = row[lane * per + q];
+          if (v > b1) { b2 = b1; b1 = v; } else if (v > b2) { b2 = v; }
+        }
+        gsc[lane] = b1 + b2;
+      }
+      __syncwarp();
+      float gk = lane < a.n_groups ? gsc[lane] : -INFINITY;
+      bool gtaken = lane >= a.n_groups;
+      uint32_t keep = 0;
+      for (int r = 0; r < a.topk_groups; ++r) {
+        float bk = gtaken ? -INFINITY : gk;
+        int bi = gtaken ? 0x7fffffff : lane;
+        warp_best(bk, bi);
+        keep |= 1u << bi;
+        if (lane == bi) gtaken = true;
+      }
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        const int e = lane * V + i;
+        if (e < E && !((keep >> (e / per)) & 1u)) key[i] = -INFINITY;
+      }
+      __syncwarp();
+    }
+    // k rounds of the warp-wide best remaining (key, index)
+    uint32_t taken = 0;
+    int my_sel = -1;
+    float my_val = 0.f;
+    float first_val = 0.f;
+    for (int j = 0; j < k; ++j) {
+      float bk = -INFINITY;
+      int bi = 0x7fffffff;
+      float bv = 0.f;
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        const int e = lane * V + i;
+        if (!((taken >> i) & 1u) && e < E && ranks_before(key[i], e, bk, bi)) {
+          bk = key[i];
+          bi = e;
+          bv = val[i];
+        }
+      }
+      const int mine = bi;
+      warp_best(bk, bi);
+      const int owner = bi / V;
+      if (lane == owner) {
+#pragma unroll
+        for (int i = 0; i < V; ++i)
+          if (lane * V + i == bi) taken |= 1u << i;
+      }
+      const float v = __shfl_sync(0xffffffffu, bv, owner);
+      (void)mine;
+      if (j == 0) first_val = v;
+      if (lane == j) { my_sel = bi; my_val = v; }
+    }
+    // weights of the k selected experts (lanes 0..k-1 hold one each)
+    float num = 0.f;
+    if (a.score == MOE_SCORE_SOFTMAX) {
+      // p_j = exp(g_j - m) / sum_all exp(g - m) with m = the largest logit (= first selected)
+      num = lane < k ? expf(my_val - first_val) : 0.f;
+    } else {
+      num = lane < k ? my_val : 0.f;
+    }
+    float den;
+    if (a.renorm) {
+      den = warp_sum(num);
+    } else if (a.score == MOE_SCORE_SOFTMAX) {
+      float part = 0.f;
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        const int e = lane * V + i;
+        if (e < E) part += expf(val[i] - first_val);
+      }
+      den = warp_sum(part);
+    } else {
+      den = 1.f;
+    }
+    if (lane < k) {
+      a.idx[(size_t)t * k + lane] = my_sel;
+      a.w[(size_t)t * k + lane] = (num / den) * a.scale;
+    }
+  }
+}
+
+cudaError_t launch_route_topk(const moe_config& c, const float* logits, const float* bias,
+                              int32_t* idx, float* w, DevStatus* st, cudaStream_t s) {
+  (void)st;
+  RouteArgs a{logits, bias, c.T, c.E, c.k, c.score, c.n_groups, c.topk_groups, c.renormalize,
+              c.route_scale, idx, w};
+  const int wpb = 8;
+  const int blocks = ceil_div(c.T, wpb);
+  const size_t smem = (size_t)wpb * (c.E + 32) * sizeof(float);
+  if (c.E <= 32) route_topk_kernel<1><<<blocks, wpb * 32, smem, s>>>(a);
+  else if (c.E <= 64) route_topk_kernel<2><<<blocks, wpb * 32, smem, s>>>(a);
+  else if (c.E <= 128) route_topk_kernel<4><<<blocks, wpb * 32, smem, s>>>(a);
+  else route_topk_kernel<8><<<blocks, wpb * 32, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------------
+// Statistics.  Each CTA owns a fixed set of tokens (warp w of CTA b takes tokens
+// b*8 + w + i*gridDim*8), accumulates per-expert sums in registers, reduces its warps in a
+// fixed order and writes one partial row; a single CTA then sums the rows in float64 in
+// block order.  No floating-point atomics, so the results are reproducible bit for bit.
+// ------------------------------------------------------------------------------------------
+struct AuxArgs {
+  const float* g;
+  const int32_t* idx;       // [T,k] or NULL when ec_C > 0
+  int T, E, k, score;
+  int ec_C;                 // expert choice: every expert holds ec_C tokens
+  float* part_P;            // [nblk][E]
+  int32_t* part_cnt;        // [nblk][E]
+  float* part_z;            // [nblk]
+};
+
+constexpr int kAuxWarps = 8;
+
+template <int V>
+__global__ void __launch_bounds__(kAuxWarps * 32) aux_partial_kernel(AuxArgs a) {
+  extern __shared__ unsigned char aux_smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int E = a.E;
+  float accP[V];
+  int cnt[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) { accP[i] = 0.f; cnt[i] = 0; }
+  float zacc = 0.f;
+  for (int t = blockIdx.x * kAuxWarps + warp; t < a.T; t += gridDim.x * kAuxWarps) {
+    float gv[V];
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int e = lane * V + i;
+      gv[i] = e < E ? a.g[(size_t)t * E + e] : -INFINITY;
+      m = fmaxf(m, gv[i]);
+    }
+    m = warp_max(m);
+    float ex[V], se = 0.f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      ex[i] = (lane * V + i) < E ? expf(gv[i] - m) : 0.f;
+      se += ex[i];
+    }
+    se = warp_sum(se);
+    const float lse = m + logf(se);
+    if (a.score == MOE_SCORE_SOFTMAX) {
+#pragma unroll
+      for (int i = 0; i < V; ++i) accP[i] += ex[i] / se;
+    } else {
+      float sv[V], ss = 0.f;
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        sv[i] = (lane * V + i) < E ? 1.0f / (1.0f + expf(-gv[i])) : 0.f;
+        ss += sv[i];
+      }
+      ss = warp_sum(ss);
+#pragma unroll
+      for (int i = 0; i < V; ++i) accP[i] += sv[i] / ss;
+    }
+    if (a.ec_C <= 0) {
+      for (int j = 0; j < a.k; ++j) {
+        const int e = a.idx[(size_t)t * a.k + j];
+        if (e >= 0 && e < E && e / V == lane) {
+#pragma unroll
+          for (int i = 0; i < V; ++i)
+            if (lane * V + i == e) cnt[i] += 1;
+        }
+      }
+    }
+    if (lane == 0) zacc += lse * lse;
+  }
+  // fixed-order reduction over the CTA's warps
+  double* sP = reinterpret_cast<double*>(aux_smem);                 // [warps][E]
+  int* sC = reinterpret_cast<int*>(sP + kAuxWarps * E);              // [warps][E]
+  double* sZ = reinterpret_cast<double*>(sC + kAuxWarps * E + (kAuxWarps * E & 1));
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int e = lane * V + i;
+    if (e < E) {
+      sP[warp * E + e] = accP[i];
+      sC[warp * E + e] = cnt[i];
+    }
+  }
+  if (lane == 0) sZ[warp] = zacc;
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    double p = 0.0;
+    int c = 0;
+    for (int w = 0; w < kAuxWarps; ++w) { p += sP[w * E + e]; c += sC[w * E + e]; }
+    a.part_P[(size_t)blockIdx.x * E + e] = (float)p;
+    a.part_cnt[(size_t)blockIdx.x * E + e] = c;
+  }
+  if (threadIdx.x == 0) {
+    double z = 0.0;
+    for (int w = 0; w < kAuxWarps; ++w) z += sZ[w];
+    a.part_z[blockIdx.x] = (float)z;
+  }
+}
+
+__global__ void __launch_bounds__(256) aux_final_kernel(const float* part_P,
+                                                       const int32_t* part_cnt,
+                                                       const float* part_z, int nblk, int T,
+                                                       int E, int ec_C, float* f, float* P,
+                                                       float* l_balance, float* z_loss) {
+  __shared__ double red[256];
+  const int e = threadIdx.x;
+  double prod = 0.0;
+  if (e < E) {
+    double p = 0.0;
+    long long c = 0;
+    for (int b = 0; b < nblk; ++b) {
+      p += part_P[(size_t)b * E + e];
+      c += part_cnt[(size_t)b * E + e];
+    }
+    if (ec_C > 0) c = ec_C;
+    const double fe = (double)c / T, Pe = p / T;
+    if (f) f[e] = (float)fe;
+    if (P) P[e] = (float)Pe;
+    prod = fe * Pe;
+  }
+  red[threadIdx.x] = prod;
+  __syncthreads();
+  for (int s = 128; s > 0; s >>= 1) {
+    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    if (l_balance) *l_balance = (float)(E * red[0]);
+    double z = 0.0;
+    for (int b = 0; b < nblk; ++b) z += part_z[b];
+    if (z_loss) *z_loss = (float)(z / T);
+  }
+}
+
+int aux_blocks(const moe_config& c) {
+  int b = ceil_div(c.T, kAuxWarps * 8);
+  return b < 1 ? 1 : (b > 512 ? 512 : b);
+}
+
+cudaError_t launch_aux_stats(const moe_config& c, const float* logits, const int32_t* idx,
+                             const int32_t* /*ec_counts*/, float* part_P, int32_t* part_cnt,
+                             float* part_z, int nblocks, float* f, float* P, float* l_balance,
+                             float* z_loss, DevStatus* st, cudaStream_t s) {
+  (void)st;
+  const int ecC = c.routing == MOE_ROUTE_EXPERT_CHOICE ? (int)((long long)c.T * c.k / c.E) : 0;
+  AuxArgs a{logits, idx, c.T, c.E, c.k, c.score, ecC, part_P, part_cnt, part_z};
+  const size_t smem = (size_t)kAuxWarps * c.E * (sizeof(double) + sizeof(int)) + 8 +
+                      kAuxWarps * sizeof(double) + 16;
+  if (c.E <= 32) aux_partial_kernel<1><<<nblocks, kAuxWarps * 32, smem, s>>>(a);
+  else if (c.E <= 64) aux_partial_kernel<2><<<nblocks, kAuxWarps * 32, smem, s>>>(a);
+  else if (c.E <= 128) aux_partial_kernel<4><<<nblocks, kAuxWarps * 32, smem, s>>>(a);
+  else aux_partial_kernel<8><<<nblocks, kAuxWarps * 32, smem, s>>>(a);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  aux_final_kernel<<<1, 256, 0, s>>>(part_P, part_cnt, part_z, nblocks, c.T, c.E, ecC, f, P,
+                                     l_balance, z_loss);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
