@@ -216,9 +216,9 @@ def main():
     counts, kept, offsets = torch.empty(E, **i32), torch.empty(E, **i32), torch.empty(E + 1, **i32)
     pos, row_of, perm, nd = (torch.empty((T, k), **i32), torch.empty((T, k), **i32),
                              torch.empty(T * k, **i32), torch.empty(1, **i32))
-    x_perm, y_perm = torch.empty((T * k, d), **bf), torch.empty((T * k, d), **bf)
-    shared = torch.empty((T, d), **bf) if wl.F_sh else None
-    out = torch.empty((T, d), **bf)
+    x_perm, y_perm = torch.empty((T * k, d), **bf), torch.empty((T * k, d), **f32)
+    shared = torch.empty((T, d), **f32) if wl.F_sh else None
+    out = torch.empty((T, d), **f32)      # fp32 layer output (out_dtype f32)
     stream = torch.cuda.current_stream()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
 
@@ -271,7 +271,7 @@ def main():
 
     # end to end through the public call with host buffers (pinned), copies inside the region
     x_host = inp["x"].cpu().pin_memory()
-    out_host = torch.empty((T, d), dtype=torch.bfloat16).pin_memory()
+    out_host = torch.empty((T, d), dtype=torch.float32).pin_memory()
     stats_host = torch.empty(E + 2, dtype=torch.float32).pin_memory()
     x_dev = torch.empty_like(inp["x"])
     stats_dev = torch.empty(E + 2, **f32)

@@ -38,6 +38,8 @@
  *                         width Fs = cfg->d_ff_shared (sum of shared experts == concatenation)
  *   topk_idx [T, k] int32 rank order (descending score; ties -> lower expert index)
  *   topk_w   [T, k] float32
+ *   y_perm   [T*k, d] float32 expert outputs in expert order; shared_out [T, d] float32
+ *   out      [T, d] in cfg->out_dtype
  */
 #ifndef MOE_B300_H
 #define MOE_B300_H
@@ -77,7 +79,9 @@ typedef struct moe_config {
   int32_t renormalize;  /* 1: w = p_S / sum_S p (default); 0: w = p_S (Switch, k = 1) */
   float route_scale;    /* weights are multiplied by it (1.0; DeepSeek-V3: 2.5) */
   float capacity_factor;/* C = ceil(cf*k*T/E); <= 0: no capacity limit */
-  int32_t dtype;        /* MOE_DTYPE_* */
+  int32_t dtype;        /* MOE_DTYPE_*: x, weights, x_perm and h (bf16: tensor cores) */
+  int32_t out_dtype;    /* MOE_DTYPE_*: layer output; F32 keeps the fp32 accumulation as is,
+                           BF16 rounds it once (up to 2^-8 relative) */
 } moe_config;
 
 /* Text of a status code (static storage). */
@@ -140,24 +144,27 @@ int moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const void* x, 
 
 /* Routed expert FFNs on expert-grouped rows ["Systems for MoE Models" §5.2 SwiGLU]:
  *   y_perm[r] = (SiLU(x_perm[r] W1_e^T) * (x_perm[r] W3_e^T)) W2_e^T for
- *   r in [offsets[e], offsets[e+1]).  x_perm [T*k, d], y_perm [T*k, d] bf16 (rows beyond
- *   offsets[E] untouched); offsets [E+1] device int32; w13, w2 as in the layout table.
+ *   r in [offsets[e], offsets[e+1]).  x_perm [T*k, d] (activation type), y_perm [T*k, d]
+ *   float32 (rows beyond offsets[E] untouched); offsets [E+1] device int32; w13, w2 as in the
+ *   layout table.
  * bf16: tcgen05 tensor-core grouped GEMMs with fp32 accumulation; the intermediate h is
- * rounded to bf16.  f32: CUDA-core fp32 path. */
+ * rounded to bf16 (it is the down GEMM's operand).  f32: CUDA-core fp32 path. */
 int moe_expert_ffn(const moe_config* cfg, const void* x_perm, const int32_t* offsets,
-                   const void* w13, const void* w2, void* y_perm, void* ws, void* stream);
+                   const void* w13, const void* w2, float* y_perm, void* ws, void* stream);
 
 /* Shared experts on every token ["MoE 路由数学" §2.2]: shared_out = SwiGLU(x; ws13, ws2),
- * x [T,d] -> shared_out [T,d] bf16.  cfg->d_ff_shared must be > 0. */
+ * x [T,d] -> shared_out [T,d] float32 (kept in fp32 so the combine rounds the layer output
+ * only once).  cfg->d_ff_shared must be > 0. */
 int moe_shared_ffn(const moe_config* cfg, const void* x, const void* ws13, const void* ws2,
-                   void* shared_out, void* ws, void* stream);
+                   float* shared_out, void* ws, void* stream);
 
 /* Weighted combine ["MoE 路由数学" §2.1 Output; "Systems for MoE Models" §2.2 step 4]:
  *   out[t] = shared_out[t] + sum_{j : row_of[t,j] >= 0} topk_w[t,j] * y_perm[row_of[t,j]]
- * in fp32 in the order j = 0..k-1, then rounded once to bf16.  Dropped pairs add nothing and
- * the remaining weights are not renormalised.  shared_out may be NULL.  No atomics. */
-int moe_combine(const moe_config* cfg, const void* y_perm, const int32_t* row_of,
-                const float* topk_w, const void* shared_out, void* out, void* stream);
+ * in fp32 in the order j = 0..k-1, written in cfg->out_dtype.  Dropped pairs add nothing and
+ * the remaining weights are not renormalised.  y_perm float32; shared_out [T,d] float32 or
+ * NULL.  No atomics. */
+int moe_combine(const moe_config* cfg, const float* y_perm, const int32_t* row_of,
+                const float* topk_w, const float* shared_out, void* out, void* stream);
 
 /* Expert-choice routing ["MoE混合专家模型深度解析" §2.2 Expert Choice]: each expert takes the
  * C = T*k/E tokens with the largest logit in its column (ties -> lower token index).
@@ -170,7 +177,7 @@ int moe_expert_choice(const moe_config* cfg, const float* logits, int32_t* ec_to
 /* Whole layer forward: router -> dispatch -> routed experts (+ shared experts) -> combine,
  * plus the statistics.  Every intermediate lives in `ws`.
  *   x [T,d], w_gate [E,d], bias [E] or NULL, w13, w2, ws13/ws2 (NULL when d_ff_shared == 0)
- *   out [T,d] bf16 (required)
+ *   out [T,d] in cfg->out_dtype (required)
  *   optional outputs (NULL to skip): topk_idx [T,k], topk_w [T,k], f [E], P [E],
  *   l_balance [1], z_loss [1], n_dropped [1] (token choice) */
 int moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const float* bias,
@@ -179,9 +186,9 @@ int moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const 
                 float* z_loss, int32_t* n_dropped, void* ws, void* stream);
 
 /* Device addresses of the intermediates moe_forward leaves in `ws` (for inspection and
- * tests): logits [T,E] f32, row_of [T,k] int32, offsets [E+1] int32, x_perm, y_perm. */
+ * tests): logits [T,E] f32, row_of [T,k] int32, offsets [E+1] int32, x_perm, y_perm (f32). */
 int moe_workspace_views(const moe_config* cfg, void* ws, float** logits, int32_t** row_of,
-                        int32_t** offsets, void** x_perm, void** y_perm);
+                        int32_t** offsets, void** x_perm, float** y_perm);
 
 /* Failure-path self test: launches one tiny kernel whose bounded wait on a flag that nothing
  * sets runs out after about `limit_us` microseconds; it records MOE_ERR_TIMEOUT in the status

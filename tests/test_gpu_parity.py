@@ -96,6 +96,27 @@ def test_small_layer_parity(case):
     print(case, report)
 
 
+@pytest.mark.parametrize("case", ["v3_like", "softmax_cap"])
+def test_bf16_output(case):
+    # the layer output rounded once to bf16: the bound adds that rounding (2^-8 |out|)
+    spec = dict(SMALL[case])
+    wl = moe_inputs.workload(spec.pop("name"), **spec)
+    inp = _inputs(wl)
+    cfg = U.config_of(wl, out_dtype="bf16")
+    gpu = U.run_forward(wl, inp, cfg)
+    assert gpu["out"].dtype == torch.bfloat16
+    h = U.host(inp)
+    ref = O.moe_forward(wl, h["x"], h["w_gate"], h["bias"], h["w13"], h["w2"], h["ws13"], h["ws2"])
+    report = {}
+    ok = U.compare_routing(wl, gpu, ref, h["bias"], report)
+    U.compare_out(gpu["out"].float().cpu().numpy()[ok], ref["out"][ok], U.OUT_TOL_BF16, report,
+                  bf16_rounded=True)
+    f32 = U.run_forward(wl, inp)
+    # the bf16 output is the float32 output rounded to nearest
+    assert torch.equal(f32["out"].to(torch.bfloat16), gpu["out"])
+    print(case, report)
+
+
 def test_uniform_router_exact_ties():
     # W_gate = 0: every logit is exactly 0 on both sides, the tie rule alone decides
     wl = moe_inputs.workload("tiny_uniform")
@@ -167,13 +188,13 @@ def test_stage_entry_points():
     src = D["perm"][:nk] // k
     assert torch.equal(x_perm[:nk].cpu(), inp["x"].cpu()[torch.from_numpy(src.astype(np.int64))])
     # routed experts on the dispatched rows
-    y_perm = torch.zeros((T * k, d), dtype=torch.bfloat16, device=DEV)
+    y_perm = torch.zeros((T * k, d), dtype=torch.float32, device=DEV)
     m.moe_expert_ffn(cfg, x_perm, offsets, inp["w13"], inp["w2"], y_perm, ws)
     U.compare_out(y_perm[:nk].float().cpu().numpy(), ref["y_rows"], U.OUT_TOL_BF16, report, "y")
-    shared = torch.empty((T, d), dtype=torch.bfloat16, device=DEV)
+    shared = torch.empty((T, d), dtype=torch.float32, device=DEV)
     m.moe_shared_ffn(cfg, inp["x"], inp["ws13"], inp["ws2"], shared, ws)
     U.compare_out(shared.float().cpu().numpy(), ref["shared"], U.OUT_TOL_BF16, report, "shared")
-    out = torch.empty((T, d), dtype=torch.bfloat16, device=DEV)
+    out = torch.empty((T, d), dtype=torch.float32, device=DEV)
     ow = torch.from_numpy(ref["w"].astype(np.float32)).to(DEV)
     m.moe_combine(cfg, y_perm, row_of, ow, shared, out)
     U.compare_out(out.float().cpu().numpy(), ref["out"], U.OUT_TOL_BF16, report)

@@ -52,7 +52,7 @@ def test_workload_configs_are_valid(name):
 @pytest.mark.parametrize("field,value,status", [
     ("T", 0, -2), ("E", 0, -2), ("E", 257, -2), ("k", 9, -2), ("k", 0, -2),
     ("d_model", 100, -2), ("d_ff", 1000, -2), ("score", 5, -1), ("dtype", 7, -1),
-    ("n_groups", 3, -2), ("renormalize", 2, -1), ("routing", 9, -1),
+    ("n_groups", 3, -2), ("renormalize", 2, -1), ("routing", 9, -1), ("out_dtype", 4, -1),
 ])
 def test_config_rejections(field, value, status):
     m = _lib()

@@ -41,7 +41,7 @@ class MoeConfig(ctypes.Structure):
         ("score", ctypes.c_int32), ("routing", ctypes.c_int32), ("n_groups", ctypes.c_int32),
         ("topk_groups", ctypes.c_int32), ("renormalize", ctypes.c_int32),
         ("route_scale", ctypes.c_float), ("capacity_factor", ctypes.c_float),
-        ("dtype", ctypes.c_int32),
+        ("dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
     ]
 
     def __repr__(self):
@@ -94,11 +94,12 @@ def version() -> str:
 
 def make_config(T, d_model, E, k, d_ff, d_ff_shared=0, score="softmax",
                 routing="token_choice", n_groups=1, topk_groups=None, renormalize=True,
-                route_scale=1.0, capacity_factor=0.0, dtype="bf16") -> MoeConfig:
+                route_scale=1.0, capacity_factor=0.0, dtype="bf16", out_dtype="f32") -> MoeConfig:
+    """out_dtype: "f32" returns the fp32-accumulated layer output as is; "bf16" rounds it."""
     return MoeConfig(int(T), int(d_model), int(E), int(k), int(d_ff), int(d_ff_shared),
                      SCORE[score], ROUTING[routing], int(n_groups),
                      int(n_groups if topk_groups is None else topk_groups), int(bool(renormalize)),
-                     float(route_scale), float(capacity_factor), DTYPE[dtype])
+                     float(route_scale), float(capacity_factor), DTYPE[dtype], DTYPE[out_dtype])
 
 
 def _ptr(t):

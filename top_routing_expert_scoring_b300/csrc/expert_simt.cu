@@ -6,6 +6,8 @@
 // whatever the buffer holds and never stored.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -49,6 +51,7 @@ __device__ __forceinline__ void locate_tile(int tile, const int32_t* mtp, const 
 
 template <typename T, bool SWIGLU>
 __global__ void __launch_bounds__(256) ffn_simt_kernel(SimtArgs a) {
+  using TO = typename std::conditional<SWIGLU, T, float>::type;   // h in T, y in float32
   constexpr int TM = kTileM, TN = 64, TK = 16;
   __shared__ float As[TK][TM + 4];
   __shared__ float Bs[TK][TN + 4];
@@ -96,7 +99,7 @@ __global__ void __launch_bounds__(256) ffn_simt_kernel(SimtArgs a) {
     }
     __syncthreads();
   }
-  T* out = (T*)a.out;
+  TO* out = (TO*)a.out;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int r = tr * 8 + i;
@@ -107,7 +110,7 @@ __global__ void __launch_bounds__(256) ffn_simt_kernel(SimtArgs a) {
       if (n >= a.N) continue;
       float v = acc[i][j];
       if constexpr (SWIGLU) v = (v / (1.0f + expf(-v))) * accu[i][j];
-      out[(size_t)(row0 + r) * a.N + n] = from_f32<T>(v);
+      out[(size_t)(row0 + r) * a.N + n] = from_f32<TO>(v);
     }
   }
 }

@@ -51,7 +51,8 @@ struct Params {
   int swiglu;               // GEMM 1 epilogue
   int b_rows;               // rows of B per expert
   int up_off;               // GEMM 1: offset of the up rows inside an expert's B rows (F)
-  __nv_bfloat16* out;
+  void* out;                // bf16 rows, or float32 rows when out_f32
+  int out_f32;
   int ldo;
   DevStatus* st;
 };
@@ -357,7 +358,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                           (static_cast<uint32_t>(q * 32) << 16);
       const bool live = r < ti.rows;
       if (p.swiglu) {
-        __nv_bfloat16* orow = p.out + static_cast<size_t>(ti.row0 + r) * p.ldo + ti.nt * 128;
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
+                              static_cast<size_t>(ti.row0 + r) * p.ldo + ti.nt * 128;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t gr[32], ur[32];
@@ -368,8 +370,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int i = 0; i < 16; ++i) {
             const float g0 = __uint_as_float(gr[2 * i]), g1 = __uint_as_float(gr[2 * i + 1]);
             const float u0 = __uint_as_float(ur[2 * i]), u1 = __uint_as_float(ur[2 * i + 1]);
-            const float h0 = (g0 / (1.0f + __expf(-g0))) * u0;
-            const float h1 = (g1 / (1.0f + __expf(-g1))) * u1;
+            const float h0 = (g0 / (1.0f + expf(-g0))) * u0;
+            const float h1 = (g1 / (1.0f + expf(-g1))) * u1;
             __nv_bfloat162 hv = __floats2bfloat162_rn(h0, h1);
             packed[i] = *reinterpret_cast<uint32_t*>(&hv);
           }
@@ -381,8 +383,24 @@ __global__ void __launch_bounds__(THREADS, 1)
                                   packed[4 * v + 3]);
           }
         }
+      } else if (p.out_f32) {
+        float* orow = static_cast<float*>(p.out) + static_cast<size_t>(ti.row0 + r) * p.ldo +
+                      ti.nt * p.bn;
+        const int nchunks = p.bn / 32;
+#pragma unroll 1
+        for (int c = 0; c < nchunks; ++c) {
+          uint32_t vr[32];
+          tmem_ld32(tb + c * 32, vr);
+          if (live) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[v] = make_uint4(vr[4 * v], vr[4 * v + 1], vr[4 * v + 2], vr[4 * v + 3]);
+          }
+        }
       } else {
-        __nv_bfloat16* orow = p.out + static_cast<size_t>(ti.row0 + r) * p.ldo + ti.nt * p.bn;
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
+                              static_cast<size_t>(ti.row0 + r) * p.ldo + ti.nt * p.bn;
         const int nchunks = p.bn / 32;
 #pragma unroll 1
         for (int c = 0; c < nchunks; ++c) {
@@ -505,7 +523,8 @@ cudaError_t launch_ffn_tc(const GroupedFFN& g, DevStatus* st, cudaStream_t s) {
   p1.swiglu = 1;
   p1.b_rows = 2 * g.F;
   p1.up_off = g.F;
-  p1.out = static_cast<__nv_bfloat16*>(g.h);
+  p1.out = g.h;
+  p1.out_f32 = 0;
   p1.ldo = g.F;
   p1.st = st;
   cudaError_t err = launch_one(mx, mw13, p1, mt_upper * p1.n_tiles, s);
@@ -517,7 +536,8 @@ cudaError_t launch_ffn_tc(const GroupedFFN& g, DevStatus* st, cudaStream_t s) {
   p2.swiglu = 0;
   p2.b_rows = g.d;
   p2.up_off = 0;
-  p2.out = static_cast<__nv_bfloat16*>(g.y);
+  p2.out = g.y;
+  p2.out_f32 = 1;
   p2.ldo = g.d;
   return launch_one(mh, mw2, p2, mt_upper * p2.n_tiles, s);
 }

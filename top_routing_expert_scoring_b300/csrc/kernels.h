@@ -50,17 +50,18 @@ struct GroupedFFN {
   const void* w13;          // [E, 2F, d]
   const void* w2;           // [E, d, F]
   void* h;                  // [max_rows, F] scratch
-  void* y;                  // [max_rows, d]
+  float* y;                 // [max_rows, d] float32
 };
 cudaError_t launch_ffn_tc(const GroupedFFN& g, DevStatus* st, cudaStream_t s);
 cudaError_t launch_ffn_simt(const GroupedFFN& g, bool f32, DevStatus* st, cudaStream_t s);
 
 // ---- combine ---------------------------------------------------------------------------------
-cudaError_t launch_combine(const moe_config& c, const void* y_perm, const int32_t* row_of,
-                           const float* w, const void* shared_out, void* out, cudaStream_t s);
-cudaError_t launch_combine_ec(const moe_config& c, const void* y_perm, const int32_t* tok_ptr,
+// y_perm and shared_out (or NULL) are float32 [*, d]; out follows c.out_dtype.
+cudaError_t launch_combine(const moe_config& c, const float* y_perm, const int32_t* row_of,
+                           const float* w, const float* shared_out, void* out, cudaStream_t s);
+cudaError_t launch_combine_ec(const moe_config& c, const float* y_perm, const int32_t* tok_ptr,
                               const int32_t* tok_rows, const float* ec_w_flat,
-                              const void* shared_out, void* out, cudaStream_t s);
+                              const float* shared_out, void* out, cudaStream_t s);
 
 // ---- expert choice ---------------------------------------------------------------------------
 // posmap [E][T]: position of token t in expert e's list or -1; ms [T]: softmax (max, sum).

@@ -75,8 +75,8 @@ Layout layout(const moe_config& c) {
   const size_t hrows = R > T ? R : T;
   const size_t hcols = F > Fs ? F : Fs;
   L.h = take(hrows * hcols * esz);
-  L.y_perm = take(R * d * esz);
-  L.shared_out = take(Fs ? T * d * esz : 0);
+  L.y_perm = take(R * d * 4);          // float32 expert outputs
+  L.shared_out = take(Fs ? T * d * 4 : 0);   // float32 for both activation types
   if (c.routing == MOE_ROUTE_EXPERT_CHOICE) {
     const size_t C = (T * k) / E;
     L.ec_tokens = take(E * C * 4);
@@ -141,6 +141,7 @@ int moe_check_config(const moe_config* c) {
   if (c->routing != MOE_ROUTE_TOKEN_CHOICE && c->routing != MOE_ROUTE_EXPERT_CHOICE)
     return MOE_ERR_ARG;
   if (c->dtype != MOE_DTYPE_BF16 && c->dtype != MOE_DTYPE_F32) return MOE_ERR_ARG;
+  if (c->out_dtype != MOE_DTYPE_BF16 && c->out_dtype != MOE_DTYPE_F32) return MOE_ERR_ARG;
   if (c->renormalize != 0 && c->renormalize != 1) return MOE_ERR_ARG;
   if (!std::isfinite(c->route_scale) || !std::isfinite(c->capacity_factor)) return MOE_ERR_ARG;
   if (c->T < 1 || c->T > (1 << 20)) return MOE_ERR_SHAPE;
@@ -255,7 +256,7 @@ namespace {
 
 int run_ffn(const moe_config& c, const void* xin, const int32_t* offsets, const int32_t* mtp,
             int uniform_rows, int E, int F, int max_rows, const void* w13, const void* w2,
-            void* y, void* ws, const Layout& L, cudaStream_t s) {
+            float* y, void* ws, const Layout& L, cudaStream_t s) {
   GroupedFFN g{};
   g.x = xin;
   g.offsets = offsets;
@@ -299,7 +300,7 @@ __global__ void mtp_from_offsets(const int32_t* offsets, int E, int32_t* mtp) {
 extern "C" {
 
 int moe_expert_ffn(const moe_config* c, const void* x_perm, const int32_t* offsets,
-                   const void* w13, const void* w2, void* y_perm, void* ws, void* stream) {
+                   const void* w13, const void* w2, float* y_perm, void* ws, void* stream) {
   int st = moe_check_config(c);
   if (st) return st;
   if (!x_perm || !offsets || !w13 || !w2 || !y_perm) return MOE_ERR_ARG;
@@ -314,7 +315,7 @@ int moe_expert_ffn(const moe_config* c, const void* x_perm, const int32_t* offse
 }
 
 int moe_shared_ffn(const moe_config* c, const void* x, const void* ws13, const void* ws2,
-                   void* shared_out, void* ws, void* stream) {
+                   float* shared_out, void* ws, void* stream) {
   int st = moe_check_config(c);
   if (st) return st;
   if (c->d_ff_shared <= 0) return MOE_ERR_SHAPE;
@@ -326,8 +327,8 @@ int moe_shared_ffn(const moe_config* c, const void* x, const void* ws13, const v
                  ws, L, s);
 }
 
-int moe_combine(const moe_config* c, const void* y_perm, const int32_t* row_of,
-                const float* topk_w, const void* shared_out, void* out, void* stream) {
+int moe_combine(const moe_config* c, const float* y_perm, const int32_t* row_of,
+                const float* topk_w, const float* shared_out, void* out, void* stream) {
   int st = moe_check_config(c);
   if (st) return st;
   if (c->routing != MOE_ROUTE_TOKEN_CHOICE) return MOE_ERR_UNSUPPORTED;
@@ -368,7 +369,7 @@ int moe_forward(const moe_config* c, const void* x, const void* w_gate, const fl
   P = P ? P : at<float>(ws, L.P);
   l_balance = l_balance ? l_balance : at<float>(ws, L.lb);
   z_loss = z_loss ? z_loss : at<float>(ws, L.z);
-  void* shared = c->d_ff_shared > 0 ? at<void>(ws, L.shared_out) : nullptr;
+  float* shared = c->d_ff_shared > 0 ? at<float>(ws, L.shared_out) : nullptr;
 
   cudaError_t e = launch_router_logits(*c, x, w_gate, g, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -390,12 +391,12 @@ int moe_forward(const moe_config* c, const void* x, const void* w_gate, const fl
         cudaSuccess)
       return MOE_ERR_CUDA;
     if ((st = run_ffn(*c, at<void>(ws, L.x_perm), b.offsets, b.mtile_prefix, -1, c->E, c->d_ff,
-                      rows_max(*c), w13, w2, at<void>(ws, L.y_perm), ws, L, s)))
+                      rows_max(*c), w13, w2, at<float>(ws, L.y_perm), ws, L, s)))
       return st;
     if (shared && (st = run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13,
                                 ws2, shared, ws, L, s)))
       return st;
-    return cuda_status(launch_combine(*c, at<void>(ws, L.y_perm), b.row_of, w, shared, out, s));
+    return cuda_status(launch_combine(*c, at<float>(ws, L.y_perm), b.row_of, w, shared, out, s));
   }
 
   // expert choice
@@ -416,17 +417,17 @@ int moe_forward(const moe_config* c, const void* x, const void* w_gate, const fl
     return MOE_ERR_CUDA;
   if ((st = run_ffn(*c, at<void>(ws, L.x_perm), at<int32_t>(ws, L.offsets),
                     at<int32_t>(ws, L.mtp), -1, c->E, c->d_ff, c->E * C, w13, w2,
-                    at<void>(ws, L.y_perm), ws, L, s)))
+                    at<float>(ws, L.y_perm), ws, L, s)))
     return st;
   if (shared && (st = run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13, ws2,
                               shared, ws, L, s)))
     return st;
-  return cuda_status(launch_combine_ec(*c, at<void>(ws, L.y_perm), at<int32_t>(ws, L.tok_ptr),
+  return cuda_status(launch_combine_ec(*c, at<float>(ws, L.y_perm), at<int32_t>(ws, L.tok_ptr),
                                        at<int32_t>(ws, L.tok_rows), ec_w, shared, out, s));
 }
 
 int moe_workspace_views(const moe_config* c, void* ws, float** logits, int32_t** row_of,
-                        int32_t** offsets, void** x_perm, void** y_perm) {
+                        int32_t** offsets, void** x_perm, float** y_perm) {
   int st = moe_check_config(c);
   if (st) return st;
   if ((st = check_ws(ws))) return st;
@@ -435,7 +436,7 @@ int moe_workspace_views(const moe_config* c, void* ws, float** logits, int32_t**
   if (row_of) *row_of = at<int32_t>(ws, L.row_of);
   if (offsets) *offsets = at<int32_t>(ws, L.offsets);
   if (x_perm) *x_perm = at<void>(ws, L.x_perm);
-  if (y_perm) *y_perm = at<void>(ws, L.y_perm);
+  if (y_perm) *y_perm = at<float>(ws, L.y_perm);
   return MOE_OK;
 }
 
