@@ -149,6 +149,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="mixtral")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override T (smaller cases for profiler captures; not a bench line)")
     args = ap.parse_args()
 
     import torch
@@ -158,6 +160,8 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     wl = moe_inputs.workload(args.workload)
+    if args.tokens:
+        wl = wl.replace(T=args.tokens)
     flops = workload_flops_bytes(wl)
     peaks, peak_kind = load_peaks()
     config = {"workload": f"{wl.name}-shaped MoE layer: T={wl.T} d={wl.d} E={wl.E} k={wl.k} "

@@ -24,7 +24,7 @@ lib_path = os.path.join(_HERE, "libmoe_b300.so")
 
 if not os.path.exists(lib_path):
     raise ImportError(
-        f"{lib_path} is missing: build it with `python -m top_routing_expert_scoring_b300.build` "
+        f"{lib_path} is missing: build it with `python top_routing_expert_scoring_b300/build.py` "
         "(needs nvcc with sm_103a support)")
 
 lib = ctypes.CDLL(lib_path)

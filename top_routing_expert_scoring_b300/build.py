@@ -1,6 +1,8 @@
 """Builds the CUDA library libmoe_b300.so in this package directory (sm_103a only).
 
-    python -m top_routing_expert_scoring_b300.build [--debug]
+    python top_routing_expert_scoring_b300/build.py [--force] [-v]
+
+(Run it as a script: importing the package itself loads the library it builds.)
 
 Each .cu file under csrc/ is compiled with nvcc for sm_103a (in parallel) and linked into one
 shared library that exports the C ABI declared in include/moe_b300.h.  The CUDA runtime is
