@@ -142,6 +142,24 @@ int moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const void* x, 
                  int32_t* kept, int32_t* offsets, int32_t* pos, int32_t* row_of, int32_t* perm,
                  void* x_perm, int32_t* n_dropped, void* ws, void* stream);
 
+/* moe_dispatch for callers that cannot allocate device memory.  The pages have no
+ * counterpart: this entry point exists for integration only.  Some callers may not call
+ * cudaMalloc (inside another framework's memory pool, in a plugin host that hands over only
+ * the tensors it owns, under a locked-down embedded allocator), so this variant takes no
+ * workspace: its scratch is one fixed array inside the library, about 2.3 MB on every GPU that
+ * loads it, held until the process exits.
+ *   Same inputs and outputs as moe_dispatch, and bit-identical results, plus
+ *   status [2] int32 (device): cleared on entry, then (code, detail) of the first device-side
+ *   error (MOE_ERR_ARG for an out-of-range or repeated expert index).
+ * Limits: T <= 65536 and E <= 256, else MOE_ERR_SHAPE before any launch.  All calls share the
+ * one array and it keeps the last call's contents: calls that overlap on the GPU race, so
+ * issue them one after another.  The first call on a device looks up the array's device
+ * address and caches it; make that first call before any stream capture.  Allocates nothing. */
+int moe_dispatch_noalloc(const moe_config* cfg, const int32_t* topk_idx, const void* x,
+                         int32_t* counts, int32_t* kept, int32_t* offsets, int32_t* pos,
+                         int32_t* row_of, int32_t* perm, void* x_perm, int32_t* n_dropped,
+                         int32_t* status, void* stream);
+
 /* Routed expert FFNs on expert-grouped rows ["Systems for MoE Models" §5.2 SwiGLU]:
  *   y_perm[r] = (SiLU(x_perm[r] W1_e^T) * (x_perm[r] W3_e^T)) W2_e^T for
  *   r in [offsets[e], offsets[e+1]).  x_perm [T*k, d] (activation type), y_perm [T*k, d]

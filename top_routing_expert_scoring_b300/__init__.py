@@ -14,7 +14,7 @@ import os
 __all__ = [
     "MoeConfig", "MoeError", "make_config", "lib", "lib_path", "workspace", "capacity",
     "workspace_size", "check_config", "sync_status", "status_string", "version",
-    "moe_router_topk", "moe_aux_stats", "moe_dispatch", "moe_expert_ffn", "moe_shared_ffn",
+    "moe_router_topk", "moe_aux_stats", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_shared_ffn",
     "moe_combine", "moe_expert_choice", "moe_forward", "moe_workspace_views",
     "moe_selftest_timeout", "EXPORTED", "SCORE", "ROUTING", "DTYPE",
 ]
@@ -68,6 +68,7 @@ _SIGS = {
     "moe_router_topk": ([_CFG, _P, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "moe_aux_stats": ([_CFG, _P, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "moe_dispatch": ([_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "moe_dispatch_noalloc": ([_CFG] + [_P] * 12, ctypes.c_int),
     "moe_expert_ffn": ([_CFG, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "moe_shared_ffn": ([_CFG, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "moe_combine": ([_CFG, _P, _P, _P, _P, _P, _P], ctypes.c_int),
@@ -171,6 +172,17 @@ def moe_dispatch(cfg, topk_idx, x, counts, kept, offsets, pos, row_of, perm, x_p
     _check("moe_dispatch", lib.moe_dispatch(
         ctypes.byref(cfg), _ptr(topk_idx), _ptr(x), _ptr(counts), _ptr(kept), _ptr(offsets),
         _ptr(pos), _ptr(row_of), _ptr(perm), _ptr(x_perm), _ptr(n_dropped), _ptr(ws),
+        _stream(stream)))
+
+
+def moe_dispatch_noalloc(cfg, topk_idx, x, counts, kept, offsets, pos, row_of, perm, x_perm,
+                         n_dropped, status, stream=None):
+    """moe_dispatch without a workspace, for callers that may not allocate device memory (the
+    scratch is a fixed array inside the library; T <= 65536, E <= 256).  status: int32[2] on
+    the device, (code, detail) of the first device-side error."""
+    _check("moe_dispatch_noalloc", lib.moe_dispatch_noalloc(
+        ctypes.byref(cfg), _ptr(topk_idx), _ptr(x), _ptr(counts), _ptr(kept), _ptr(offsets),
+        _ptr(pos), _ptr(row_of), _ptr(perm), _ptr(x_perm), _ptr(n_dropped), _ptr(status),
         _stream(stream)))
 
 
