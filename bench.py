@@ -16,7 +16,6 @@ import argparse
 import json
 import os
 import statistics
-import subprocess
 import sys
 import time
 
@@ -51,56 +50,106 @@ def workload_flops_bytes(wl):
     return {"flops": ffn + router, "ffn_flops": ffn, "bytes": weights + act}
 
 
-class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+class _Nvml:
+    """Read-only NVML queries through ctypes (libnvidia-ml.so.1 ships with the driver)."""
+    CLOCK_SM = 1
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
+    def __init__(self):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+
+    def handle(self, cuda_index):
+        ct = self.ct
+        h = ct.c_void_p()
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(cuda_index).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            if self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ct.byref(h)) == 0:
+                return h
+        except Exception:
+            pass
+        if self.lib.nvmlDeviceGetHandleByIndex_v2(ct.c_uint(cuda_index), ct.byref(h)) != 0:
+            raise RuntimeError("nvmlDeviceGetHandleByIndex failed")
+        return h
+
+    def clock(self, h, maximum=False):
+        v = self.ct.c_uint()
+        fn = self.lib.nvmlDeviceGetMaxClockInfo if maximum else self.lib.nvmlDeviceGetClockInfo
+        if fn(h, self.ct.c_int(self.CLOCK_SM), self.ct.byref(v)) != 0:
+            raise RuntimeError("nvml clock query failed")
+        return v.value
+
+    def reasons(self, h):
+        v = self.ct.c_ulonglong()
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        if fn is None or fn(h, self.ct.byref(v)) != 0:
+            if self.lib.nvmlDeviceGetCurrentClocksThrottleReasons(h, self.ct.byref(v)) != 0:
+                raise RuntimeError("nvml reasons query failed")
+        return v.value
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
+class ClockSampler:
+    """Samples the SM clock and the clock-event (throttle) reasons of the benchmarked GPU
+    through NVML (read-only) every few milliseconds while the timed region runs."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, cuda_index: int, interval_s: float = 0.002):
+        self.cuda_index = cuda_index
+        self.interval = interval_s
+        self.samples = []
+        self.max_mhz = None
+        self.error = None
+        self.recording = False
+
+    def start(self):
+        """Begin recording (call right before the timed region)."""
+        self.recording = True
+
+    def _run(self):
+        try:
+            nv = _Nvml()
+            h = nv.handle(self.cuda_index)
+            self.max_mhz = nv.clock(h, maximum=True)
+            while not self._stop.is_set():
+                if self.recording:
+                    self.samples.append((nv.clock(h), nv.reasons(h)))
+                self._stop.wait(self.interval)
+            nv.close()
+        except Exception as e:          # sampling is best effort; reported as unsampled
+            self.error = repr(e)
 
     def __enter__(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
+        import threading
+        self._stop = threading.Event()
+        self._thread = threading.Thread(target=self._run, daemon=True)
+        self._thread.start()
+        time.sleep(0.05)                 # first sample before the timed region starts
         return self
 
     def __exit__(self, *a):
-        self.lines = []
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                out, _ = self.proc.communicate(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+        self._stop.set()
+        self._thread.join(timeout=5)
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in getattr(self, "lines", []):
-            parts = [p.strip() for p in l.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"],
+                    "samples": 0, "error": self.error}
+        reasons = set()
+        for _, r in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples),
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
+                "samples": len(self.samples)}
 
 
 def cpu_cores():
@@ -132,19 +181,22 @@ def host_inputs(inp):
     return {k: moe_inputs.to_f64(v) for k, v in inp.items()}
 
 
-def run_cpu_baseline(wl, inp, target_s=12.0, steps=1):
+def run_cpu_baseline(wl, inp, target_s=12.0):
+    """Sizes the oracle's sample so that it takes about target_s seconds (two probe sizes give
+    the per-token cost), then times it once."""
     hi = host_inputs(inp)
-    S = min(32, wl.T)
-    t = oracle_sample(wl, hi, S)
-    S = int(min(wl.T, max(S, S * target_s / max(t, 1e-3))))
-    times = [oracle_sample(wl, hi, S) for _ in range(steps)]
-    return S, times
+    s1, s2 = min(32, wl.T), min(256, wl.T)
+    t1 = oracle_sample(wl, hi, s1)
+    t2 = oracle_sample(wl, hi, s2) if s2 > s1 else t1
+    per_tok = max((t2 - t1) / max(s2 - s1, 1), 1e-6)
+    S = int(min(wl.T, max(s2, s1 + (target_s - t1) / per_tok)))
+    return S, [oracle_sample(wl, hi, S)]
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="mixtral")
@@ -257,8 +309,9 @@ def main():
     gemm_pairs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
                   for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
+    with ClockSampler(torch.cuda.current_device()) as clk:
         barrier()
+        clk.start()
         t_start.record(stream)
         for i in range(args.steps):
             step(gemm_pairs[i])

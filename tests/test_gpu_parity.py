@@ -325,3 +325,59 @@ def test_full_size_parity(case):
     print(case, report)
     del inp, gpu
     torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------------------------------------
+# both tensor-core GEMM kernels (single CTA, CTA pair) on the same dispatched rows
+# ---------------------------------------------------------------------------------------------
+PAIR_CASES = {
+    # ~1024 rows per expert, ragged: odd and even numbers of 128-row blocks
+    "rows1024": dict(name="mixtral", T=2048, d=256, E=4, k=2, F=384),
+    # few rows per expert (pairs with an empty half), several N tiles in both GEMMs
+    "rows_small": dict(name="mixtral", T=300, d=512, E=8, k=2, F=256),
+}
+
+
+@pytest.mark.parametrize("kernel", ["single", "pair"])
+@pytest.mark.parametrize("case", sorted(PAIR_CASES))
+def test_expert_gemm_kernels(case, kernel, monkeypatch):
+    monkeypatch.setenv("MOE_B300_GEMM", kernel)
+    m = U.lib()
+    spec = dict(PAIR_CASES[case])
+    wl = moe_inputs.workload(spec.pop("name"), **spec)
+    cfg = U.config_of(wl)
+    inp = _inputs(wl)
+    h = U.host(inp)
+    ref = O.moe_forward(wl, h["x"], h["w_gate"], h["bias"], h["w13"], h["w2"], h["ws13"], h["ws2"])
+    D = ref["disp"]
+    T, k, d = wl.T, wl.k, wl.d
+    nk = int(D["offsets"][-1])
+    x_perm = torch.zeros((T * k, d), dtype=torch.bfloat16, device=DEV)
+    src = torch.from_numpy((D["perm"][:nk] // k).astype(np.int64))
+    x_perm[:nk] = inp["x"].cpu()[src].to(DEV)
+    offsets = torch.from_numpy(D["offsets"].astype(np.int32)).to(DEV)
+    y = torch.full((T * k, d), float("nan"), dtype=torch.float32, device=DEV)
+    ws = m.workspace(cfg)
+    m.moe_expert_ffn(cfg, x_perm, offsets, inp["w13"], inp["w2"], y, ws)
+    torch.cuda.synchronize()
+    assert m.sync_status(ws) == 0
+    report = {}
+    U.compare_out(y[:nk].cpu().numpy(), ref["y_rows"], U.OUT_TOL_BF16, report, "y")
+    assert torch.isnan(y[nk:]).all()          # rows past the last expert are never written
+    print(case, kernel, report)
+
+
+def test_shared_expert_on_pair_kernel(monkeypatch):
+    monkeypatch.setenv("MOE_B300_GEMM", "pair")
+    m = U.lib()
+    wl = moe_inputs.workload("dsmoe16b", T=777, d=256, E=8, k=2, F=128, F_shared=256)
+    cfg = U.config_of(wl)
+    inp = _inputs(wl)
+    h = U.host(inp)
+    ws = m.workspace(cfg)
+    shared = torch.empty((wl.T, wl.d), dtype=torch.float32, device=DEV)
+    m.moe_shared_ffn(cfg, inp["x"], inp["ws13"], inp["ws2"], shared, ws)
+    torch.cuda.synchronize()
+    assert m.sync_status(ws) == 0
+    U.compare_out(shared.cpu().numpy(), O.shared_out(h["x"], h["ws13"], h["ws2"]),
+                  U.OUT_TOL_BF16, {}, "shared")

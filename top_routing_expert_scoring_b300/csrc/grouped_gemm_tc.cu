@@ -23,8 +23,12 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
+#include <cstdlib>
+#include <cstring>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_ptx.cuh"
 
 namespace moe {
 namespace tc {
@@ -56,119 +60,6 @@ struct Params {
   int ldo;
   DevStatus* st;
 };
-
-// ---------------------------------------------------------------------------------------------
-// PTX wrappers
-// ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Waits for the phase of `bar` with the given parity.  Gives up when the CTA's abort flag is
-// raised (honor_abort) or after kWaitLimitNs, raising the flag and recording the timeout.
-__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
-                                          volatile int* abort_flag, DevStatus* st, int where,
-                                          bool honor_abort, uint64_t limit_ns = kWaitLimitNs) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 15u) == 0u) {
-      if (honor_abort && *abort_flag) return false;
-      if (globaltimer_ns() - t0 > limit_ns) {
-        *abort_flag = 1;
-        record_error(st, MOE_ERR_TIMEOUT, where);
-        return false;
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int c0, int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
-      : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor of a K-major operand stored with the 128-byte swizzle:
-// rows of 128 bytes, 8-row atoms of 1024 bytes stacked along M/N (stride byte offset 1024).
-// Advancing K by 16 elements inside the atom adds 32 bytes to the start address.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address  [0,14)
-  d |= static_cast<uint64_t>(1) << 16;                     // leading byte offset (unused)
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;             // stride byte offset [32,46)
-  d |= static_cast<uint64_t>(1) << 46;                     // descriptor version [46,48)
-  d |= static_cast<uint64_t>(2) << 61;                     // 128-byte swizzle [61,64)
-  return d;
-}
-
-// Instruction descriptor, kind::f16: D = f32, A = B = bf16, both K-major, shape M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (static_cast<uint32_t>(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                       uint32_t idesc, uint32_t accum) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
-      : "memory");
-}
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-// 32 consecutive fp32 columns of this thread's TMEM lane, then wait for the load.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
-      "%28, %29, %30, %31}, [%32];\n"
-      "tcgen05.wait::ld.sync.aligned;\n"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-        "=r"(r[31])
-      : "r"(taddr)
-      : "memory");
-}
 
 // ---------------------------------------------------------------------------------------------
 // Tile list
@@ -265,7 +156,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int stage = 0;
     uint32_t ph = 0;
     uint32_t issued = 0, last_par = 0;   // per-stage bit masks for the drain
-    const int nbox = (p.swiglu || p.bn == 256) ? 2 : 1;
+    const int nbox = (p.swiglu || p.bn > 128) ? 2 : 1;
     const uint32_t bytes = A_STAGE + nbox * B_BOX;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
@@ -471,7 +362,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2-D bf16 tensor [rows, cols] (cols contiguous) read in boxes of 64 columns x 128 rows.
-static bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -502,8 +393,21 @@ static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const 
 
 }  // namespace tc
 
+static bool use_pair_kernel(const GroupedFFN& g) {
+  if (g.d % 256 != 0) return false;
+  const char* env = getenv("MOE_B300_GEMM");
+  if (env && strcmp(env, "single") == 0) return false;
+  if (env && strcmp(env, "pair") == 0) return true;
+  // One group (shared experts): pairs carry no padding and run ~4% faster.  Ragged groups pay
+  // on average half a 128-row block per expert for 256-row pair tiles, so pairs only win once
+  // experts average >= 2048 rows.
+  if (g.uniform_rows >= 0) return g.uniform_rows >= 512;
+  return (long long)g.max_rows / g.E >= 2048;
+}
+
 cudaError_t launch_ffn_tc(const GroupedFFN& g, DevStatus* st, cudaStream_t s) {
   using namespace tc;
+  if (use_pair_kernel(g)) return launch_ffn_tc2(g, st, s);
   CUtensorMap mx, mw13, mh, mw2;
   if (!make_map(&mx, g.x, (uint64_t)g.max_rows, (uint64_t)g.d) ||
       !make_map(&mw13, g.w13, (uint64_t)g.E * 2 * g.F, (uint64_t)g.d) ||
@@ -540,6 +444,34 @@ cudaError_t launch_ffn_tc(const GroupedFFN& g, DevStatus* st, cudaStream_t s) {
   p2.out_f32 = 1;
   p2.ldo = g.d;
   return launch_one(mh, mw2, p2, mt_upper * p2.n_tiles, s);
+}
+
+// Router logits through the same kernel: one group of T rows, B = W_gate [E, d], fp32 output.
+// N tile = E (E <= 128) or 128 (E a multiple of 128, several N tiles); rows of the B box past
+// E are zero-filled by the TMA and their columns are never stored.
+cudaError_t launch_router_tc(const moe_config& c, const void* x, const void* w_gate,
+                             float* logits, cudaStream_t s) {
+  using namespace tc;
+  CUtensorMap mx, mw;
+  if (!make_map(&mx, x, (uint64_t)c.T, (uint64_t)c.d_model) ||
+      !make_map(&mw, w_gate, (uint64_t)c.E, (uint64_t)c.d_model))
+    return cudaErrorInvalidValue;
+  Params p{};
+  p.offsets = nullptr;
+  p.mtp = nullptr;
+  p.E = 1;
+  p.uniform_rows = c.T;
+  p.K = c.d_model;
+  p.bn = c.E <= 128 ? c.E : (c.E % 128 == 0 ? 128 : c.E);
+  p.n_tiles = c.E / p.bn;
+  p.swiglu = 0;
+  p.b_rows = c.E;
+  p.up_off = 0;
+  p.out = logits;
+  p.out_f32 = 1;
+  p.ldo = c.E;
+  p.st = nullptr;
+  return launch_one(mx, mw, p, ceil_div(c.T, BM) * p.n_tiles, s);
 }
 
 cudaError_t launch_timeout_probe(DevStatus* st, int limit_us, cudaStream_t s) {

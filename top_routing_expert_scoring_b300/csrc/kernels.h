@@ -12,6 +12,9 @@ namespace moe {
 // ---- router ----------------------------------------------------------------------------------
 cudaError_t launch_router_logits(const moe_config& c, const void* x, const void* w_gate,
                                  float* logits, cudaStream_t s);
+// Router logits on the tensor cores (bf16, E a multiple of 32): g = x W_gate^T in fp32.
+cudaError_t launch_router_tc(const moe_config& c, const void* x, const void* w_gate,
+                             float* logits, cudaStream_t s);
 cudaError_t launch_route_topk(const moe_config& c, const float* logits, const float* bias,
                               int32_t* idx, float* w, DevStatus* st, cudaStream_t s);
 cudaError_t launch_aux_stats(const moe_config& c, const float* logits, const int32_t* idx,
@@ -52,7 +55,12 @@ struct GroupedFFN {
   void* h;                  // [max_rows, F] scratch
   float* y;                 // [max_rows, d] float32
 };
+// Tensor-core path.  Picks the CTA-pair kernel (cta_group::2, 256-row tiles) for one group of
+// >= 512 rows or for experts averaging >= 2048 rows (d % 256 == 0), else the single-CTA
+// kernel; the environment variable MOE_B300_GEMM=single|pair|auto overrides the choice (pair
+// falls back to single when d % 256 != 0).
 cudaError_t launch_ffn_tc(const GroupedFFN& g, DevStatus* st, cudaStream_t s);
+cudaError_t launch_ffn_tc2(const GroupedFFN& g, DevStatus* st, cudaStream_t s);
 cudaError_t launch_ffn_simt(const GroupedFFN& g, bool f32, DevStatus* st, cudaStream_t s);
 
 // ---- combine ---------------------------------------------------------------------------------

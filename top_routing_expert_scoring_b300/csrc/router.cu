@@ -17,8 +17,8 @@
 namespace moe {
 
 // ------------------------------------------------------------------------------------------
-// Logits on CUDA cores: one CTA computes a 32-token x 64-expert tile, K in chunks of 32.
-// Each output is a sequential fp32 sum over c in index order.
+// Logits on CUDA cores, general case (float32 path, or shapes the other two kernels do not
+// take): one CTA computes a 32-token x 64-expert tile, K in chunks of 32.
 // ------------------------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(256) router_logits_simt(const T* __restrict__ x,
@@ -68,8 +68,92 @@ __global__ void __launch_bounds__(256) router_logits_simt(const T* __restrict__ 
   }
 }
 
+// ------------------------------------------------------------------------------------------
+// Logits for a small expert count (E <= 32, bf16): the router weights stay in shared memory
+// and each warp streams one token row with 16-byte loads, keeping E partial dot products per
+// lane; a butterfly reduction (fixed order) finishes them.  HBM-bound on reading x.
+// ------------------------------------------------------------------------------------------
+template <int EP>
+__global__ void __launch_bounds__(256) router_logits_stream(const uint4* __restrict__ x,
+                                                           const uint4* __restrict__ w,
+                                                           float* __restrict__ g, int Tn,
+                                                           int d8, int E) {
+  extern __shared__ uint4 wsm[];                  // [EP][d8]: 8 bf16 per uint4
+  for (int i = threadIdx.x; i < EP * d8; i += blockDim.x) {
+    const int e = i / d8;
+    wsm[i] = e < E ? w[i] : make_uint4(0u, 0u, 0u, 0u);
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tn; t += warps) {
+    float acc[EP];
+#pragma unroll
+    for (int e = 0; e < EP; ++e) acc[e] = 0.f;
+    const uint4* xr = x + (size_t)t * d8;
+    for (int c = lane; c < d8; c += 32) {
+      const uint4 xv = __ldg(xr + c);
+      const __nv_bfloat162* xh = reinterpret_cast<const __nv_bfloat162*>(&xv);
+      float xf[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(xh[i]);
+        xf[2 * i] = f.x;
+        xf[2 * i + 1] = f.y;
+      }
+#pragma unroll
+      for (int e = 0; e < EP; ++e) {
+        const uint4 wv = wsm[e * d8 + c];
+        const __nv_bfloat162* wh = reinterpret_cast<const __nv_bfloat162*>(&wv);
+        float a = acc[e];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(wh[i]);
+          a = fmaf(xf[2 * i], f.x, a);
+          a = fmaf(xf[2 * i + 1], f.y, a);
+        }
+        acc[e] = a;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < EP; ++e) acc[e] = warp_sum(acc[e]);
+#pragma unroll
+    for (int e = 0; e < EP; ++e)
+      if (lane == e && e < E) g[(size_t)t * E + e] = acc[e];
+  }
+}
+
+template <int EP>
+static cudaError_t launch_stream(const moe_config& c, const void* x, const void* w_gate,
+                                 float* logits, cudaStream_t s) {
+  const int d8 = c.d_model / 8;
+  const size_t smem = (size_t)EP * d8 * sizeof(uint4);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(router_logits_stream<EP>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int per_sm = smem <= 64 * 1024 ? 3 : (smem <= 100 * 1024 ? 2 : 1);
+  int blocks = ceil_div(c.T, 8);
+  if (blocks > num_sms() * per_sm) blocks = num_sms() * per_sm;
+  router_logits_stream<EP><<<blocks, 256, smem, s>>>((const uint4*)x, (const uint4*)w_gate, logits,
+                                                     c.T, d8, c.E);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_router_logits(const moe_config& c, const void* x, const void* w_gate,
                                  float* logits, cudaStream_t s) {
+  if (c.dtype == MOE_DTYPE_BF16) {
+    if (c.E >= 32 && c.E % 32 == 0) return launch_router_tc(c, x, w_gate, logits, s);
+    const size_t row_bytes = (size_t)c.d_model * 2;
+    if (c.E <= 8 && 8 * row_bytes <= 200 * 1024) return launch_stream<8>(c, x, w_gate, logits, s);
+    if (c.E <= 16 && 16 * row_bytes <= 200 * 1024)
+      return launch_stream<16>(c, x, w_gate, logits, s);
+    if (c.E <= 32 && 32 * row_bytes <= 200 * 1024)
+      return launch_stream<32>(c, x, w_gate, logits, s);
+  }
   dim3 grid(ceil_div(c.T, 32), ceil_div(c.E, 64));
   if (c.dtype == MOE_DTYPE_F32)
     router_logits_simt<float><<<grid, 256, 0, s>>>((const float*)x, (const float*)w_gate, logits,
@@ -328,38 +412,49 @@ __global__ void __launch_bounds__(kAuxWarps * 32) aux_partial_kernel(AuxArgs a) 
   }
 }
 
-__global__ void __launch_bounds__(256) aux_final_kernel(const float* part_P,
-                                                       const int32_t* part_cnt,
-                                                       const float* part_z, int nblk, int T,
-                                                       int E, int ec_C, float* f, float* P,
-                                                       float* l_balance, float* z_loss) {
-  __shared__ double red[256];
-  const int e = threadIdx.x;
-  double prod = 0.0;
-  if (e < E) {
-    double p = 0.0;
-    long long c = 0;
-    for (int b = 0; b < nblk; ++b) {
+// One warp per expert: lanes sum blocks lane, lane+32, ... in float64, then a butterfly in a
+// fixed order; warp 0 also sums the z partials.  Deterministic for a given block count.
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__global__ void __launch_bounds__(1024) aux_final_kernel(const float* part_P,
+                                                        const int32_t* part_cnt,
+                                                        const float* part_z, int nblk, int T,
+                                                        int E, int ec_C, float* f, float* P,
+                                                        float* l_balance, float* z_loss) {
+  __shared__ double prod[256];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int e = warp; e < E; e += nw) {
+    double p = 0.0, c = 0.0;
+    for (int b = lane; b < nblk; b += 32) {
       p += part_P[(size_t)b * E + e];
       c += part_cnt[(size_t)b * E + e];
     }
+    p = warp_sum_d(p);
+    c = warp_sum_d(c);
     if (ec_C > 0) c = ec_C;
-    const double fe = (double)c / T, Pe = p / T;
-    if (f) f[e] = (float)fe;
-    if (P) P[e] = (float)Pe;
-    prod = fe * Pe;
+    const double fe = c / T, Pe = p / T;
+    if (lane == 0) {
+      if (f) f[e] = (float)fe;
+      if (P) P[e] = (float)Pe;
+      prod[e] = fe * Pe;
+    }
   }
-  red[threadIdx.x] = prod;
   __syncthreads();
-  for (int s = 128; s > 0; s >>= 1) {
-    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) {
-    if (l_balance) *l_balance = (float)(E * red[0]);
+  if (warp == 0) {
+    double acc = 0.0;
+    for (int e = lane; e < E; e += 32) acc += prod[e];
+    acc = warp_sum_d(acc);
     double z = 0.0;
-    for (int b = 0; b < nblk; ++b) z += part_z[b];
-    if (z_loss) *z_loss = (float)(z / T);
+    for (int b = lane; b < nblk; b += 32) z += part_z[b];
+    z = warp_sum_d(z);
+    if (lane == 0) {
+      if (l_balance) *l_balance = (float)(E * acc);
+      if (z_loss) *z_loss = (float)(z / T);
+    }
   }
 }
 
@@ -383,8 +478,8 @@ cudaError_t launch_aux_stats(const moe_config& c, const float* logits, const int
   else aux_partial_kernel<8><<<nblocks, kAuxWarps * 32, smem, s>>>(a);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  aux_final_kernel<<<1, 256, 0, s>>>(part_P, part_cnt, part_z, nblocks, c.T, c.E, ecC, f, P,
-                                     l_balance, z_loss);
+  aux_final_kernel<<<1, 1024, 0, s>>>(part_P, part_cnt, part_z, nblocks, c.T, c.E, ecC, f, P,
+                                      l_balance, z_loss);
   return cudaGetLastError();
 }
 
