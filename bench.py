@@ -5,8 +5,8 @@
 
 One step = one whole layer forward (router GEMM, scoring/Top-k, statistics, dispatch, grouped
 SwiGLU expert GEMMs, shared experts, combine) over one batch of synthetic tokens already in HBM.
-The timed step issues the same kernels moe_forward issues, stage by stage through the C ABI,
-with CUDA events around the expert stage so that the grouped GEMM's share is measured live.
+The timed step is moe_forward_timed: moe_forward's kernels, with two CUDA events recorded
+around the expert GEMM launches so that the grouped GEMM's share is measured live.
 Prints one JSON line (rank 0).  Under torchrun every rank runs its own replica on its own token
 batch (the layer shards over tokens with no exchange), so the work scales weakly.
 """
@@ -193,6 +193,105 @@ def run_cpu_baseline(wl, inp, target_s=12.0):
     return S, [oracle_sample(wl, hi, S)]
 
 
+def decode_sweep(args):
+    """Decode-sized batches: B tokens per step, 100 seeded steps per B with fresh x and router
+    weights (expert weights fixed), timed through moe_forward.  Reports tokens/s and the HBM
+    bandwidth reached on the bytes a step must read: the experts it actually touches (counted
+    from its own selection), the shared experts, the router, x and the output.  Also reports
+    the distinct experts touched per step against E(1-(1-k/E)^B), as configured and with a
+    zero selection bias (exchangeable experts, where the formula holds in expectation)."""
+    import math
+    import torch
+    import moe_inputs
+    import top_routing_expert_scoring_b300 as m
+    torch.cuda.set_device(0)
+    peaks, peak_kind = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    for name in args.decode_workloads.split(","):
+        wl0 = moe_inputs.workload(name)
+        weights = moe_inputs.make_expert_weights(wl0, device="cuda")
+        per_expert = 3 * wl0.d * wl0.F * 2
+        shared_bytes = 3 * wl0.d * wl0.F_sh * 2
+        for B in [int(b) for b in args.decode_batches.split(",")]:
+            wl = wl0.replace(T=B)
+            cfg = m.make_config(B, wl.d, wl.E, wl.k, wl.F, wl.F_sh, wl.score, wl.routing,
+                                wl.n_groups, wl.topk_groups, wl.renormalize, wl.route_scale,
+                                wl.capacity_factor, wl.dtype)
+            steps = args.decode_steps
+            routers = [moe_inputs.make_router_inputs(wl, seed=1000 + i, device="cuda")
+                       for i in range(steps)]
+            ws = m.workspace(cfg)
+            out = torch.empty((B, wl.d), dtype=torch.float32, device="cuda")
+            idx_all = torch.empty((steps, B, wl.k), dtype=torch.int32, device="cuda")
+
+            def fwd(i):
+                r = routers[i]
+                m.moe_forward(cfg, r["x"], r["w_gate"], r["bias"], weights["w13"], weights["w2"],
+                              weights["ws13"], weights["ws2"], out, topk_idx=idx_all[i], ws=ws)
+            for i in range(min(5, steps)):
+                fwd(i)
+            torch.cuda.synchronize()
+            graphs = []
+            if not args.no_graphs:
+                # one CUDA graph per step (its own inputs), captured outside the timed region
+                for i in range(steps):
+                    gr = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(gr):
+                        fwd(i)
+                    graphs.append(gr)
+                torch.cuda.synchronize()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+            with ClockSampler(torch.cuda.current_device()) as clk:
+                clk.start()
+                ev[0].record()
+                for i in range(steps):
+                    if graphs:
+                        graphs[i].replay()
+                    else:
+                        fwd(i)
+                    ev[i + 1].record()
+                torch.cuda.synchronize()
+            st = m.sync_status(ws)
+            if st != 0:
+                raise RuntimeError(f"device status {st}: {m.status_string(st)}")
+            ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+            distinct = [int(torch.unique(idx_all[i]).numel()) for i in range(steps)]
+            step_bytes = [dn * per_expert + shared_bytes + wl.E * wl.d * 2 + B * wl.d * 2 +
+                          B * wl.d * 4 for dn in distinct]
+            total_s = sum(ms) / 1e3
+            gbs = sum(step_bytes) / total_s / 1e9
+            # routing-only statistic with the selection bias at zero
+            zero = wl.replace(bias_range=0.0)
+            cfg0 = cfg
+            logits = torch.empty((B, wl.E), dtype=torch.float32, device="cuda")
+            w0 = torch.empty((B, wl.k), dtype=torch.float32, device="cuda")
+            dz = []
+            for i in range(steps):
+                r = moe_inputs.make_router_inputs(zero, seed=5000 + i, device="cuda")
+                m.moe_router_topk(cfg0, r["x"], r["w_gate"], None, logits, idx_all[i], w0, ws)
+                dz.append(int(torch.unique(idx_all[i]).numel()))
+            formula = wl.E * (1 - (1 - wl.k / wl.E) ** B)
+            mean_z = sum(dz) / len(dz)
+            se_z = (sum((v - mean_z) ** 2 for v in dz) / max(len(dz) - 1, 1)) ** 0.5 / math.sqrt(len(dz))
+            print(json.dumps({
+                "metric": "MoE layer fwd tokens/s, decode batch; % of HBM BW on touched expert "
+                          "weights", "mode": "decode", "workload": f"{name} B={B}",
+                "value": B * steps / total_s, "unit": "tokens/s", "steps": steps,
+                "ms_per_step": sum(ms) / steps, "dtype": "bf16", "data": "synthetic",
+                "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                             "frac": gbs / hbm, "peak_kind": f"{peak_kind} copy bandwidth"},
+                "bytes_per_step_mean": sum(step_bytes) / steps,
+                "distinct_experts": {"as_configured_mean": sum(distinct) / steps,
+                                     "zero_bias_mean": mean_z, "zero_bias_se": se_z,
+                                     "formula": formula},
+                "clocks": clk.summary(), "cuda_graphs": bool(graphs),
+                "l2": "each step reads >= 0.35 GB of expert weights (> 126 MB L2)"}))
+            del routers, ws, graphs
+            torch.cuda.empty_cache()
+        del weights
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -201,9 +300,20 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="mixtral")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-sweep", action="store_true",
+                    help="decode-sized batches instead of the prefill step (one line per B)")
+    ap.add_argument("--decode-workloads", default="v3,mixtral")
+    ap.add_argument("--decode-batches", default="1,8,64,256")
+    ap.add_argument("--decode-steps", type=int, default=100)
+    ap.add_argument("--no-graphs", action="store_true",
+                    help="decode sweep: launch each forward directly instead of a CUDA graph")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override T (smaller cases for profiler captures; not a bench line)")
     args = ap.parse_args()
+
+    if args.decode_sweep:
+        decode_sweep(args)
+        return
 
     import torch
     import moe_inputs
@@ -269,38 +379,33 @@ def main():
     logits, idx, w = torch.empty((T, E), **f32), torch.empty((T, k), **i32), torch.empty((T, k), **f32)
     f, P, lb, z = (torch.empty(E, **f32), torch.empty(E, **f32), torch.empty(1, **f32),
                    torch.empty(1, **f32))
-    counts, kept, offsets = torch.empty(E, **i32), torch.empty(E, **i32), torch.empty(E + 1, **i32)
-    pos, row_of, perm, nd = (torch.empty((T, k), **i32), torch.empty((T, k), **i32),
-                             torch.empty(T * k, **i32), torch.empty(1, **i32))
-    x_perm, y_perm = torch.empty((T * k, d), **bf), torch.empty((T * k, d), **f32)
-    shared = torch.empty((T, d), **f32) if wl.F_sh else None
+    nd = torch.empty(1, **i32)
+    shared = wl.F_sh > 0
     out = torch.empty((T, d), **f32)      # fp32 layer output (out_dtype f32)
     stream = torch.cuda.current_stream()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
 
-    def step(gemm_events=None):
-        m.moe_router_topk(cfg, inp["x"], inp["w_gate"], inp["bias"], logits, idx, w, ws, stream)
-        m.moe_aux_stats(cfg, logits, idx, f, P, lb, z, ws, stream)
-        m.moe_dispatch(cfg, idx, inp["x"], counts, kept, offsets, pos, row_of, perm, x_perm, nd,
-                       ws, stream)
-        if gemm_events:
-            gemm_events[0].record(stream)
-        m.moe_expert_ffn(cfg, x_perm, offsets, inp["w13"], inp["w2"], y_perm, ws, stream)
-        if gemm_events:
-            gemm_events[1].record(stream)
-        if shared is not None:
-            m.moe_shared_ffn(cfg, inp["x"], inp["ws13"], inp["ws2"], shared, ws, stream)
-        m.moe_combine(cfg, y_perm, row_of, w, shared, out, stream)
+    def step(gemm_events):
+        m.moe_forward_timed(cfg, inp["x"], inp["w_gate"], inp["bias"], inp["w13"], inp["w2"],
+                            inp["ws13"], inp["ws2"], out, idx, w, f, P, lb, z, nd, ws, stream,
+                            gemm_events[0], gemm_events[1])
 
-    launches_per_step = 1 + 1 + 2 + 4 + 1 + 2 + (2 if shared is not None else 0) + 1
+    # our kernels per forward: router logits, Top-k (+statistics partials), dispatch (1 kernel
+    # for T <= 256, else 4), 2 expert GEMMs, 2 shared-expert GEMMs, combine, statistics final
+    launches_per_step = 1 + 1 + (1 if T <= 256 else 4) + 2 + (2 if shared else 0) + 1 + 1
+    if wl.routing == "expert_choice":
+        launches_per_step = 1 + 5 + 2 + 2 + (2 if shared else 0) + 1 + 2
 
     def barrier():
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
+    warm_events = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    for ev_ in warm_events:
+        ev_.record(stream)              # torch creates the event handle on first record
     for _ in range(max(args.warmup, 3)):
-        step()
+        step(warm_events)
     barrier()
     st = m.sync_status(ws)
     if st != 0:
@@ -308,6 +413,9 @@ def main():
 
     gemm_pairs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
                   for _ in range(args.steps)]
+    for pair in gemm_pairs:
+        for ev_ in pair:
+            ev_.record(stream)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(torch.cuda.current_device()) as clk:
         barrier()
@@ -370,7 +478,8 @@ def main():
         "config": config,
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": tflops / peak, "traffic": None,
-                     "kernel": "grouped_gemm_tc_kernel (gate/up + down launches of one step)",
+                     "kernel": ("whole expert-choice forward" if wl.routing == "expert_choice"
+                                else "grouped GEMM kernel (gate/up + down launches of one step)"),
                      "peak_kind": f"{peak_kind} bf16 burst"},
         "layer_roofline": {"roofline_ms": layer_roof_ms, "frac": layer_roof_ms / ms_step,
                            "flops_per_step": flops["flops"], "bytes_per_step": flops["bytes"]},

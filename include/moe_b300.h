@@ -203,6 +203,16 @@ int moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const 
                 int32_t* topk_idx, float* topk_w, float* f, float* P, float* l_balance,
                 float* z_loss, int32_t* n_dropped, void* ws, void* stream);
 
+/* moe_forward that also records two caller-created CUDA events (cudaEvent_t, timing enabled)
+ * on `stream` around the expert GEMM launches: the routed experts' grouped GEMMs (prefill),
+ * or the routed and shared experts' decode GEMMs.  Same kernels and results as moe_forward;
+ * for measuring the GEMM share of a forward.  Both events are required. */
+int moe_forward_timed(const moe_config* cfg, const void* x, const void* w_gate, const float* bias,
+                      const void* w13, const void* w2, const void* ws13, const void* ws2,
+                      void* out, int32_t* topk_idx, float* topk_w, float* f, float* P,
+                      float* l_balance, float* z_loss, int32_t* n_dropped, void* ws,
+                      void* stream, void* ev_expert_begin, void* ev_expert_end);
+
 /* Device addresses of the intermediates moe_forward leaves in `ws` (for inspection and
  * tests): logits [T,E] f32, row_of [T,k] int32, offsets [E+1] int32, x_perm, y_perm (f32). */
 int moe_workspace_views(const moe_config* cfg, void* ws, float** logits, int32_t** row_of,

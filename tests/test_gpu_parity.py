@@ -79,9 +79,17 @@ SMALL = {
     "dsmoe_like": dict(name="dsmoe16b", T=1000, d=384, E=16, F=256, F_shared=128),
     # expert choice
     "ec_like": dict(name="dsmoe16b_ec", T=512, d=256, E=16, k=4, F=256, F_shared=128),
-    # single token (decode B = 1) and E = 1
+    # decode-sized batches (<= 64 rows per expert on average): swap-AB decode kernel, shared
+    # experts folded into the same tile list
     "decode_b1": dict(name="v3", T=1, d=256, E=64, F=256, F_shared=256),
+    "decode_b8": dict(name="v3", T=8, d=512, E=64, F=256, F_shared=384),
+    "decode_b64": dict(name="v3", T=64, d=256, E=64, F=384, F_shared=256),
+    "decode_mixtral_b32": dict(name="mixtral", T=32, d=512, F=384),
+    "decode_collapsed_b256": dict(name="mixtral_collapsed", T=256, d=256, F=256),
+    "decode_dsmoe_b100": dict(name="dsmoe16b", T=100, d=256, E=64, F=128, F_shared=128),
     "one_expert": dict(name="mixtral", T=130, d=128, E=1, k=1, F=128),
+    # prefill path with E = 1, k = 1 and d = 256 (decode regime needs <= 64 rows per expert)
+    "one_expert_d256": dict(name="mixtral", T=300, d=256, E=1, k=1, F=128),
 }
 
 
@@ -381,3 +389,103 @@ def test_shared_expert_on_pair_kernel(monkeypatch):
     assert m.sync_status(ws) == 0
     U.compare_out(shared.cpu().numpy(), O.shared_out(h["x"], h["ws13"], h["ws2"]),
                   U.OUT_TOL_BF16, {}, "shared")
+
+
+@pytest.mark.parametrize("T", [1, 100, 256, 257, 700])
+def test_dispatch_oracle_indices_bitexact(T):
+    # T <= 256 takes the single-CTA dispatch, larger T the three-kernel path; both must give
+    # the oracle's counts, positions, rows, permutation and drops bit for bit
+    m = U.lib()
+    wl = moe_inputs.workload("mixtral_collapsed", T=T, d=256, F=128, capacity_factor=1.0)
+    cfg = U.config_of(wl)
+    inp = moe_inputs.make_router_inputs(wl, device=DEV)
+    h = {k: moe_inputs.to_f64(v) for k, v in inp.items()}
+    r = O.route(wl, h["x"], h["w_gate"], h["bias"])
+    D = O.dispatch(r["idx"], wl.E, O.capacity(wl.capacity_factor, wl.k, T, wl.E))
+    E, k, d = wl.E, wl.k, wl.d
+    i32 = dict(dtype=torch.int32, device=DEV)
+    outs = {n: torch.full(sh, -9, **i32) for n, sh in
+            [("counts", (E,)), ("kept", (E,)), ("offsets", (E + 1,)), ("pos", (T, k)),
+             ("row_of", (T, k)), ("perm", (T * k,))]}
+    nd = torch.full((1,), -9, **i32)
+    x_perm = torch.zeros((T * k, d), dtype=torch.bfloat16, device=DEV)
+    ws = m.workspace(cfg)
+    oidx = torch.from_numpy(r["idx"].astype(np.int32)).to(DEV)
+    m.moe_dispatch(cfg, oidx, inp["x"], outs["counts"], outs["kept"], outs["offsets"],
+                   outs["pos"], outs["row_of"], outs["perm"], x_perm, nd, ws)
+    torch.cuda.synchronize()
+    assert m.sync_status(ws) == 0
+    for n, t in outs.items():
+        assert (t.cpu().numpy() == D[n]).all(), n
+    assert nd.item() == D["n_dropped"]
+    nk = int(D["offsets"][-1])
+    src = torch.from_numpy((D["perm"][:nk] // k).astype(np.int64))
+    assert torch.equal(x_perm[:nk].cpu(), inp["x"].cpu()[src])
+
+
+def test_forward_replays_in_a_cuda_graph():
+    # every launch of moe_forward is stream-ordered and allocation-free, so a captured forward
+    # replays with identical results
+    m = U.lib()
+    wl = moe_inputs.workload("v3", T=16, d=256, E=64, F=256, F_shared=256)
+    cfg = U.config_of(wl)
+    inp = _inputs(wl)
+    ws = m.workspace(cfg)
+    out = torch.empty((wl.T, wl.d), dtype=torch.float32, device=DEV)
+
+    def fwd():
+        m.moe_forward(cfg, inp["x"], inp["w_gate"], inp["bias"], inp["w13"], inp["w2"],
+                      inp["ws13"], inp["ws2"], out, ws=ws)
+    fwd()
+    torch.cuda.synchronize()
+    eager = out.clone()
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fwd()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert m.sync_status(ws) == 0
+    assert torch.equal(out, eager)
+
+
+@pytest.mark.parametrize("case", ["v3_like", "softmax_cap", "decode_b8"])
+def test_forward_timed_and_fused_statistics(case):
+    # moe_forward_timed runs moe_forward's kernels (identical output) and brackets the expert
+    # GEMMs with the caller's events; the statistics moe_forward fuses into its Top-k pass
+    # equal moe_aux_stats on the same logits and selection bit for bit
+    m = U.lib()
+    spec = dict(SMALL[case])
+    wl = moe_inputs.workload(spec.pop("name"), **spec)
+    cfg = U.config_of(wl)
+    inp = _inputs(wl)
+    a = U.run_forward(wl, inp, cfg)
+    ws = m.workspace(cfg)
+    out = torch.empty_like(a["out"])
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    for e in ev:
+        e.record()
+    m.moe_forward_timed(cfg, inp["x"], inp["w_gate"], inp["bias"], inp["w13"], inp["w2"],
+                        inp["ws13"], inp["ws2"], out, ws=ws, ev_begin=ev[0], ev_end=ev[1])
+    torch.cuda.synchronize()
+    assert m.sync_status(ws) == 0
+    assert torch.equal(out, a["out"])
+    assert ev[0].elapsed_time(ev[1]) > 0
+    logits_p, _, _, _, _ = m.moe_workspace_views(a["cfg"], a["ws"])
+    logits = torch.as_tensor(_DevF32(logits_p, wl.T * wl.E), device=DEV).reshape(wl.T, wl.E)
+    idx = torch.from_numpy(a["idx"]).to(DEV)
+    f = torch.empty(wl.E, dtype=torch.float32, device=DEV)
+    P = torch.empty(wl.E, dtype=torch.float32, device=DEV)
+    lb = torch.empty(1, dtype=torch.float32, device=DEV)
+    z = torch.empty(1, dtype=torch.float32, device=DEV)
+    m.moe_aux_stats(cfg, logits.contiguous(), idx, f, P, lb, z, ws)
+    torch.cuda.synchronize()
+    assert (f.cpu().numpy() == a["f"]).all() and (P.cpu().numpy() == a["P"]).all()
+    assert lb.item() == a["l_balance"] and z.item() == a["z_loss"]
+
+
+class _DevF32:
+    def __init__(self, ptr, n):
+        self.__cuda_array_interface__ = {"shape": (n,), "typestr": "<f4", "data": (ptr, False),
+                                         "version": 3, "strides": None}

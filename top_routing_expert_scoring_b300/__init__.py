@@ -15,7 +15,7 @@ __all__ = [
     "MoeConfig", "MoeError", "make_config", "lib", "lib_path", "workspace", "capacity",
     "workspace_size", "check_config", "sync_status", "status_string", "version",
     "moe_router_topk", "moe_aux_stats", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_shared_ffn",
-    "moe_combine", "moe_expert_choice", "moe_forward", "moe_workspace_views",
+    "moe_combine", "moe_expert_choice", "moe_forward", "moe_forward_timed", "moe_workspace_views",
     "moe_selftest_timeout", "EXPORTED", "SCORE", "ROUTING", "DTYPE",
 ]
 
@@ -74,6 +74,7 @@ _SIGS = {
     "moe_combine": ([_CFG, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "moe_expert_choice": ([_CFG, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "moe_forward": ([_CFG] + [_P] * 17, ctypes.c_int),
+    "moe_forward_timed": ([_CFG] + [_P] * 19, ctypes.c_int),
     "moe_workspace_views": ([_CFG, _P] + [ctypes.POINTER(_P)] * 5, ctypes.c_int),
     "moe_selftest_timeout": ([_P, ctypes.c_int32, _P], ctypes.c_int),
 }
@@ -217,6 +218,17 @@ def moe_forward(cfg, x, w_gate, bias, w13, w2, ws13, ws2, out, topk_idx=None, to
         ctypes.byref(cfg), _ptr(x), _ptr(w_gate), _ptr(bias), _ptr(w13), _ptr(w2), _ptr(ws13),
         _ptr(ws2), _ptr(out), _ptr(topk_idx), _ptr(topk_w), _ptr(f), _ptr(P), _ptr(l_balance),
         _ptr(z_loss), _ptr(n_dropped), _ptr(ws), _stream(stream)))
+
+
+def moe_forward_timed(cfg, x, w_gate, bias, w13, w2, ws13, ws2, out, topk_idx=None, topk_w=None,
+                      f=None, P=None, l_balance=None, z_loss=None, n_dropped=None, ws=None,
+                      stream=None, ev_begin=None, ev_end=None):
+    """moe_forward plus two torch.cuda.Event (enable_timing) recorded around the expert GEMMs."""
+    _check("moe_forward_timed", lib.moe_forward_timed(
+        ctypes.byref(cfg), _ptr(x), _ptr(w_gate), _ptr(bias), _ptr(w13), _ptr(w2), _ptr(ws13),
+        _ptr(ws2), _ptr(out), _ptr(topk_idx), _ptr(topk_w), _ptr(f), _ptr(P), _ptr(l_balance),
+        _ptr(z_loss), _ptr(n_dropped), _ptr(ws), _stream(stream), ev_begin.cuda_event,
+        ev_end.cuda_event))
 
 
 def moe_workspace_views(cfg, ws):

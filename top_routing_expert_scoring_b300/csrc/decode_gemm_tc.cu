@@ -1,0 +1,457 @@
+// Expert GEMMs for decode-sized batches (few tokens per expert), tcgen05, sm_103a.
+//
+// Same SwiGLU products as the prefill kernels ["Systems for Mixture-of-Experts Models" §5.2],
+// computed transposed so that the weights fill the MMA's M = 128 rows and the few tokens of an
+// expert fill N (16..128):
+//   GEMM 1:  G^T = W1_e X^T and U^T = W3_e X^T  ->  h[t, f] = SiLU(G[f,t]) * U[f,t]
+//   GEMM 2:  Y^T = W2_e H^T (two 128-row halves of a 256-row W2 block)
+// At decode sizes the layer is bound by reading the touched experts' weights once
+// ("Systems for MoE Models" §1.4: a batch touches about E(1-(1-k/E)^B) experts), so each tile
+// streams 256 weight rows through a 4-stage TMA ring while the token rows stay small.  The
+// shared experts are one more entry of the same tile list (their token rows are appended to the
+// expert-ordered rows), so every SM streams weights even for a single token.
+//
+// Tile list: entry j in [0, E) is routed expert j, entry E the shared expert (if any); entry j
+// has n_j rows, cut into chunks of NP rows; its tiles are (weight block, chunk) with the chunk
+// fastest so the CTAs reading one weight block run together.  Every wait is bounded as in the
+// prefill kernels.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace dec {
+
+using namespace tc;
+
+constexpr int BK = 64;
+constexpr int MAX_STAGES = 8;
+constexpr int A_BOX = 128 * BK * 2;           // 16 KB: 128 weight rows
+constexpr int A_STAGE = 2 * A_BOX;            // two 128-row weight blocks
+constexpr int NP_MAX = 128;                   // token rows per chunk (B box height)
+constexpr int TMEM_COLS = 512;                // 2 buffers x (2 x 128 columns)
+constexpr int THREADS = 192;
+constexpr int MAX_J = 257;
+constexpr int NBARS = 2 * MAX_STAGES + 5;
+constexpr size_t CTRL_BYTES = 8 * NBARS + 16 + (MAX_J + 1) * 4;
+constexpr size_t SMEM_LIMIT = 227 * 1024;
+// The ring's stage holds 256 weight rows and the largest token chunk (np_max rows) of one
+// 64-wide K slice; as many stages as fit (up to 8): 6 for 16-row chunks, 4 for 128-row chunks.
+inline int stage_bytes(int np_max) { return A_STAGE + ((np_max * BK * 2 + 1023) / 1024) * 1024; }
+inline int num_stages(int np_max) {
+  const int n = static_cast<int>((SMEM_LIMIT - 1024 - CTRL_BYTES) / stage_bytes(np_max));
+  return n < MAX_STAGES ? n : MAX_STAGES;
+}
+
+struct Params {
+  const int32_t* offsets;   // [E+1] routed row offsets
+  int E;
+  int has_shared;
+  int T;                    // tokens (rows of the shared entry, appended after offsets[E])
+  int NP;                   // routed chunk rows = routed B box height (16, 32, 64 or 128)
+  int NPs;                  // shared chunk rows = shared B box height
+  int gemm;                 // 1 = gate/up + SwiGLU, 2 = down
+  int K_routed, K_shared;   // reduction lengths (GEMM 1: d, d; GEMM 2: F, Fs)
+  int wb_routed, wb_shared; // weight blocks per entry (GEMM 1: F/128, Fs/128; GEMM 2: d/256)
+  int a_rows_routed;        // rows of A per routed expert (GEMM 1: 2F; GEMM 2: d)
+  int up_routed, up_shared; // GEMM 1: offset of the up rows (F, Fs)
+  void* out;                // GEMM 1: h bf16 [rows, ldo]; GEMM 2: y f32 [rows, ldo]
+  float* out_shared;        // GEMM 2: shared output f32 [T, ldo]
+  int ldo;
+  int ksplit;               // K is cut into ksplit slices, each a tile of its own
+  float* gu;                // GEMM 1 with ksplit > 1: fp32 gate | up partials [ksplit][rows][2 ldo]
+  size_t part_stride;       // elements between consecutive K-slice partials of the outputs
+  size_t shared_stride;     // GEMM 2: elements between K-slice partials of out_shared
+  int stages;               // ring depth
+  int stage;                // bytes per ring stage
+  DevStatus* st;
+};
+
+struct DTile {
+  int j, wb, ks, row0, n;   // entry, weight block, K slice, first row of the chunk, valid rows
+};
+
+__device__ __forceinline__ int entry_rows(const Params& p, int j) {
+  return j < p.E ? p.offsets[j + 1] - p.offsets[j] : p.T;
+}
+__device__ __forceinline__ int entry_row0(const Params& p, int j) {
+  return j < p.E ? p.offsets[j] : p.offsets[p.E];
+}
+
+__device__ __forceinline__ int entry_np(const Params& p, int j) {
+  return j < p.E ? p.NP : p.NPs;
+}
+
+__device__ __forceinline__ DTile decode_dtile(int tile, const Params& p, const int* prefix,
+                                              int J) {
+  int lo = 0, hi = J;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (prefix[mid] <= tile) lo = mid; else hi = mid;
+  }
+  DTile t;
+  t.j = lo;
+  const int n_j = entry_rows(p, lo);
+  const int np = entry_np(p, lo);
+  const int chunks = ceil_div(n_j, np);
+  int tt = tile - prefix[lo];
+  const int c = tt % chunks;          // chunk fastest: CTAs on one weight slice run together
+  tt /= chunks;
+  t.ks = tt % p.ksplit;
+  t.wb = tt / p.ksplit;
+  t.row0 = entry_row0(p, lo) + c * np;
+  t.n = min(np, n_j - c * np);
+  return t;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    decode_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                       const __grid_constant__ CUtensorMap tmAs,
+                       const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmBs, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int STAGES = p.stages;
+  const int STAGE = p.stage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* prefix = reinterpret_cast<int*>(tmem_slot + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * STAGES;
+  const uint32_t tfull0 = empty0 + 8 * STAGES;
+  const uint32_t tempty0 = tfull0 + 16;
+  const uint32_t drain = tempty0 + 16;
+  const int J = p.E + (p.has_shared ? 1 : 0);
+
+  for (int j = threadIdx.x; j < J; j += blockDim.x)
+    prefix[j + 1] = ceil_div(entry_rows(p, j), entry_np(p, j)) *
+                    (j < p.E ? p.wb_routed : p.wb_shared) * p.ksplit;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    prefix[0] = 0;
+    for (int j = 1; j <= J; ++j) prefix[j] += prefix[j - 1];
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = prefix[J];
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------- TMA producer -------------------------------------------
+    int stage = 0;
+    uint32_t ph = 0, issued = 0, last_par = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      const DTile t = decode_dtile(tile, p, prefix, J);
+      const bool sh = t.j >= p.E;
+      const CUtensorMap* am = sh ? &tmAs : &tmA;
+      const CUtensorMap* bm = sh ? &tmBs : &tmB;
+      const uint32_t b_bytes = static_cast<uint32_t>(entry_np(p, t.j)) * BK * 2;
+      int a0, a1;
+      if (p.gemm == 1) {
+        const int base = sh ? 0 : t.j * p.a_rows_routed;
+        a0 = base + t.wb * 128;
+        a1 = a0 + (sh ? p.up_shared : p.up_routed);
+      } else {
+        a0 = (sh ? 0 : t.j * p.a_rows_routed) + t.wb * 256;
+        a1 = a0 + 128;
+      }
+      const int KB = (sh ? p.K_shared : p.K_routed) / BK;
+      const int kb0 = t.ks * KB / p.ksplit, kb1 = (t.ks + 1) * KB / p.ksplit;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!wait_bounded(empty0 + 8 * stage, ph ^ 1u, abort_flag, p.st, 21, true)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = full0 + 8 * stage;
+        const uint32_t sa = smem_u32(smem + stage * STAGE);
+        mbar_expect_tx(fb, A_STAGE + b_bytes);
+        tma_load_2d(sa, am, fb, kb * BK, a0);
+        tma_load_2d(sa + A_BOX, am, fb, kb * BK, a1);
+        tma_load_2d(sa + A_STAGE, bm, fb, kb * BK, t.row0);
+        issued |= 1u << stage;
+        last_par = (last_par & ~(1u << stage)) | (ph << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+    if (!ok) {
+      for (int s = 0; s < STAGES; ++s)
+        if ((issued >> s) & 1u)
+          wait_bounded(full0 + 8 * s, (last_par >> s) & 1u, abort_flag, p.st, 25, false);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------- MMA issuer ---------------------------------------------
+    int stage = 0, acc = 0;
+    uint32_t ph = 0, aph = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      const DTile t = decode_dtile(tile, p, prefix, J);
+      const int n16 = (t.n + 15) & ~15;
+      const uint32_t idesc = idesc_bf16_f32(128, n16);
+      const int KB = (t.j >= p.E ? p.K_shared : p.K_routed) / BK;
+      const int kb0 = t.ks * KB / p.ksplit, kb1 = (t.ks + 1) * KB / p.ksplit;
+      if (!wait_bounded(tempty0 + 8 * acc, aph ^ 1u, abort_flag, p.st, 22, true)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * 256);
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!wait_bounded(full0 + 8 * stage, ph, abort_flag, p.st, 23, true)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = smem_u32(smem + stage * STAGE);
+        const uint32_t sb = sa + A_STAGE;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint64_t bdesc = sw128_desc(sb + kk * 32);
+          const uint32_t accum = (kb != kb0 || kk != 0) ? 1u : 0u;
+          tc_mma(d0, sw128_desc(sa + kk * 32), bdesc, idesc, accum);
+          tc_mma(d0 + 128, sw128_desc(sa + A_BOX + kk * 32), bdesc, idesc, accum);
+        }
+        tc_commit(empty0 + 8 * stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!ok) break;
+      tc_commit(tfull0 + 8 * acc);
+      acc ^= 1;
+      if (acc == 0) aph ^= 1u;
+    }
+    tc_commit(drain);
+    wait_bounded(drain, 0u, abort_flag, p.st, 26, false);
+  } else if (warp >= 2) {
+    // ------------------------------- epilogue -----------------------------------------------
+    // Thread = one weight row f (TMEM lane); columns = tokens.  For each token the warp's 32
+    // lanes write 32 consecutive outputs.
+    const int q = warp & 3;
+    const int f = q * 32 + lane;
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const DTile t = decode_dtile(tile, p, prefix, J);
+      int ok = 1;
+      if (lane == 0) ok = wait_bounded(tfull0 + 8 * acc, aph, abort_flag, p.st, 24, true) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * 256) +
+                          (static_cast<uint32_t>(q * 32) << 16);
+      const bool sh = t.j >= p.E;
+#pragma unroll 1
+      for (int c0 = 0; c0 < t.n; c0 += 32) {
+        uint32_t lo[32], hi[32];
+        tmem_ld32(tb + c0, lo);
+        tmem_ld32(tb + 128 + c0, hi);
+        const int m = min(32, t.n - c0);
+        if (p.gemm == 1 && p.ksplit == 1) {
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (i < m) {
+              const float g = __uint_as_float(lo[i]), u = __uint_as_float(hi[i]);
+              const float hv = (g / (1.0f + expf(-g))) * u;
+              out[static_cast<size_t>(t.row0 + c0 + i) * p.ldo + t.wb * 128 + f] =
+                  __float2bfloat16_rn(hv);
+            }
+          }
+        } else if (p.gemm == 1) {
+          // raw gate | up partial sums of this K slice; a finalize pass forms SiLU(g) * u
+          float* gu = p.gu + static_cast<size_t>(t.ks) * p.part_stride;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (i < m) {
+              float* o = gu + static_cast<size_t>(t.row0 + c0 + i) * (2 * p.ldo) + t.wb * 128 + f;
+              o[0] = __uint_as_float(lo[i]);
+              o[p.ldo] = __uint_as_float(hi[i]);
+            }
+          }
+        } else {
+          float* out = sh ? p.out_shared + static_cast<size_t>(t.ks) * p.shared_stride
+                          : static_cast<float*>(p.out) + static_cast<size_t>(t.ks) * p.part_stride;
+          const int rbase = sh ? t.row0 - p.offsets[p.E] : t.row0;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (i < m) {
+              float* o = out + static_cast<size_t>(rbase + c0 + i) * p.ldo + t.wb * 256 + f;
+              o[0] = __uint_as_float(lo[i]);
+              o[128] = __uint_as_float(hi[i]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      acc ^= 1;
+      if (acc == 0) aph ^= 1u;
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// h[r][f] = SiLU(sum_s gate_s[r][f]) * sum_s up_s[r][f], slices summed in order s = 0.. ;
+// routed rows r < offsets[E] have F columns, the appended shared rows F_shared.
+__global__ void __launch_bounds__(256) swiglu_finalize_kernel(const float* __restrict__ gu,
+                                                             size_t part_stride, int S,
+                                                             const int32_t* __restrict__ offsets,
+                                                             int E, int T, int F, int Fs, int ldo,
+                                                             __nv_bfloat16* __restrict__ h) {
+  const int nk = offsets[E];
+  const int rows = nk + T;
+  const size_t total = static_cast<size_t>(rows) * ldo;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const int r = static_cast<int>(i / ldo), f = static_cast<int>(i - (size_t)r * ldo);
+    if (f >= (r < nk ? F : Fs)) continue;
+    float g = 0.f, u = 0.f;
+    const float* src = gu + static_cast<size_t>(r) * (2 * ldo) + f;
+    for (int sl = 0; sl < S; ++sl) {
+      g += src[sl * part_stride];
+      u += src[sl * part_stride + ldo];
+    }
+    h[i] = __float2bfloat16_rn((g / (1.0f + expf(-g))) * u);
+  }
+}
+
+static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& as, const CUtensorMap& b,
+                          const CUtensorMap& bs, Params p, int upper_tiles, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(decode_gemm_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(SMEM_LIMIT));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int np_max = p.NP > p.NPs ? p.NP : p.NPs;
+  p.stage = stage_bytes(np_max);
+  p.stages = num_stages(np_max);
+  const size_t smem = 1024 + static_cast<size_t>(p.stages) * p.stage + CTRL_BYTES;
+  int grid = num_sms();
+  if (upper_tiles < grid) grid = upper_tiles;
+  if (grid < 1) grid = 1;
+  decode_gemm_kernel<<<grid, THREADS, smem, s>>>(a, as, b, bs, p);
+  return cudaGetLastError();
+}
+
+}  // namespace dec
+
+cudaError_t launch_ffn_decode(const DecodeFFN& g, DevStatus* st, cudaStream_t s) {
+  using namespace dec;
+  const bool sh = g.F_shared > 0;
+  const int Fmax = g.F > g.F_shared ? g.F : g.F_shared;
+  CUtensorMap ma1, mas1, mb1, mbs1, ma2, mas2, mb2, mbs2;
+  if (!tc::make_map_box(&ma1, g.w13, (uint64_t)g.E * 2 * g.F, (uint64_t)g.d, 128) ||
+      !tc::make_map_box(&ma2, g.w2, (uint64_t)g.E * g.d, (uint64_t)g.F, 128) ||
+      !tc::make_map_box(&mb1, g.x, (uint64_t)g.max_rows, (uint64_t)g.d, g.np) ||
+      !tc::make_map_box(&mb2, g.h, (uint64_t)g.max_rows, (uint64_t)Fmax, g.np) ||
+      !tc::make_map_box(&mbs1, g.x, (uint64_t)g.max_rows, (uint64_t)g.d, g.np_shared) ||
+      !tc::make_map_box(&mbs2, g.h, (uint64_t)g.max_rows, (uint64_t)Fmax, g.np_shared))
+    return cudaErrorInvalidValue;
+  if (sh) {
+    if (!tc::make_map_box(&mas1, g.ws13, (uint64_t)2 * g.F_shared, (uint64_t)g.d, 128) ||
+        !tc::make_map_box(&mas2, g.ws2, (uint64_t)g.d, (uint64_t)g.F_shared, 128))
+      return cudaErrorInvalidValue;
+  } else {
+    mas1 = ma1;
+    mas2 = ma2;
+  }
+  Params p1{};
+  p1.offsets = g.offsets;
+  p1.E = g.E;
+  p1.has_shared = sh ? 1 : 0;
+  p1.T = g.T;
+  p1.NP = g.np;
+  p1.NPs = g.np_shared;
+  p1.gemm = 1;
+  p1.K_routed = g.d;
+  p1.K_shared = g.d;
+  p1.wb_routed = g.F / 128;
+  p1.wb_shared = sh ? g.F_shared / 128 : 0;
+  p1.a_rows_routed = 2 * g.F;
+  p1.up_routed = g.F;
+  p1.up_shared = g.F_shared;
+  p1.out = g.h;
+  p1.out_shared = nullptr;
+  p1.ldo = Fmax;
+  p1.ksplit = g.ksplit1;
+  p1.gu = g.gu;
+  p1.part_stride = static_cast<size_t>(g.max_rows) * 2 * Fmax;
+  p1.shared_stride = 0;
+  p1.st = st;
+  // upper bound of the tile count: every routed row in its own chunk is impossible to exceed
+  const int chunks_upper = ceil_div(g.max_rows, g.np) + g.E + ceil_div(g.T, g.np_shared) + 1;
+  const int wbmax1 = p1.wb_routed > p1.wb_shared ? p1.wb_routed : p1.wb_shared;
+  cudaError_t err = launch(ma1, mas1, mb1, mbs1, p1, chunks_upper * wbmax1 * g.ksplit1, s);
+  if (err != cudaSuccess) return err;
+  if (g.ksplit1 > 1) {
+    const long long work = static_cast<long long>(g.max_rows) * Fmax;
+    int blocks = static_cast<int>((work + 255) / 256);
+    if (blocks > num_sms() * 8) blocks = num_sms() * 8;
+    swiglu_finalize_kernel<<<blocks, 256, 0, s>>>(g.gu, p1.part_stride, g.ksplit1, g.offsets, g.E,
+                                                  g.T, g.F, sh ? g.F_shared : 0, Fmax,
+                                                  static_cast<__nv_bfloat16*>(g.h));
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  }
+  Params p2 = p1;
+  p2.gemm = 2;
+  p2.K_routed = g.F;
+  p2.K_shared = g.F_shared;
+  p2.wb_routed = g.d / 256;
+  p2.wb_shared = sh ? g.d / 256 : 0;
+  p2.a_rows_routed = g.d;
+  p2.up_routed = 0;
+  p2.up_shared = 0;
+  p2.out = g.y;
+  p2.out_shared = g.shared_out;
+  p2.ldo = g.d;
+  p2.ksplit = g.ksplit2;
+  p2.gu = nullptr;
+  p2.part_stride = g.y_part_stride;
+  p2.shared_stride = g.shared_part_stride;
+  return launch(ma2, mas2, mb2, mbs2, p2, chunks_upper * p2.wb_routed * g.ksplit2, s);
+}
+
+}  // namespace moe

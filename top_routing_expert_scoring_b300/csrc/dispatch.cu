@@ -135,6 +135,121 @@ __global__ void __launch_bounds__(kDispatchBlock) dispatch_scatter_kernel(
   }
 }
 
+// T <= 256 (one token block): count, scan, scatter and the row gather in one launch.  Every
+// CTA recomputes the (small) dispatch in shared memory with the same counting scheme as the
+// three-kernel path (bitmap of the tokens per expert, scans, popcount ranks), so the results
+// are identical; CTA 0 publishes it, and all CTAs copy their share of the rows: routed rows
+// [0, nkept), then (append_shared) the T token rows after them for the shared experts.
+__global__ void __launch_bounds__(kDispatchBlock) dispatch_small_kernel(
+    const int32_t* __restrict__ idx, int T, int E, int k, int capacity,
+    int32_t* __restrict__ counts, int32_t* __restrict__ kept, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ mtile_prefix, int32_t* __restrict__ n_dropped,
+    int32_t* __restrict__ pos, int32_t* __restrict__ row_of, int32_t* __restrict__ perm,
+    DevStatus* st, const unsigned char* __restrict__ x, unsigned char* __restrict__ x_perm,
+    int row_bytes, int append_shared) {
+  __shared__ uint32_t bm[256 * kWords];
+  __shared__ int s_kept[256];
+  __shared__ int s_mt[256];
+  __shared__ int s_drop[256];
+  __shared__ int s_off[257];
+  __shared__ int s_perm[256 * 8];
+  const bool lead = blockIdx.x == 0;
+  const int tid = threadIdx.x;
+  for (int i = tid; i < E * kWords; i += blockDim.x) bm[i] = 0u;
+  __syncthreads();
+  const int t = tid;
+  if (t < T) {
+    int sel[8];
+    for (int j = 0; j < k; ++j) {
+      const int e = idx[(size_t)t * k + j];
+      bool bad = e < 0 || e >= E;
+      for (int q = 0; q < j; ++q) bad |= (sel[q] == e);
+      sel[j] = bad ? -1 : e;
+      if (bad) {
+        if (lead) record_error(st, MOE_ERR_ARG, t);
+        continue;
+      }
+      atomicOr(&bm[e * kWords + tid / 32], 1u << (tid % 32));
+    }
+  }
+  __syncthreads();
+  const int e = tid;
+  int total = 0;
+  if (e < E) {
+#pragma unroll
+    for (int w = 0; w < kWords; ++w) total += __popc(bm[e * kWords + w]);
+  }
+  const int kp = e < E ? min(total, capacity) : 0;
+  s_kept[e] = kp;
+  s_mt[e] = ceil_div(kp, kTileM);
+  s_drop[e] = e < E ? total - kp : 0;
+  if (lead && e < E) {
+    counts[e] = total;
+    kept[e] = kp;
+  }
+  __syncthreads();
+  for (int sft = 1; sft < 256; sft <<= 1) {
+    const int a = e >= sft ? s_kept[e - sft] : 0;
+    const int b = e >= sft ? s_mt[e - sft] : 0;
+    const int c = e >= sft ? s_drop[e - sft] : 0;
+    __syncthreads();
+    s_kept[e] += a;
+    s_mt[e] += b;
+    s_drop[e] += c;
+    __syncthreads();
+  }
+  if (e < E) s_off[e + 1] = s_kept[e];
+  if (e == 0) s_off[0] = 0;
+  if (lead) {
+    if (e < E) {
+      offsets[e + 1] = s_kept[e];
+      mtile_prefix[e + 1] = s_mt[e];
+    }
+    if (e == 0) {
+      offsets[0] = 0;
+      mtile_prefix[0] = 0;
+      *n_dropped = s_drop[255];
+    }
+  }
+  __syncthreads();
+  if (t < T) {
+    const int w_me = tid / 32;
+    const uint32_t below = (1u << (tid % 32)) - 1u;
+    for (int j = 0; j < k; ++j) {
+      const int ex = idx[(size_t)t * k + j];
+      int p = -1, row = -1;
+      if (ex >= 0 && ex < E && ((bm[ex * kWords + w_me] >> (tid % 32)) & 1u)) {
+        int r = __popc(bm[ex * kWords + w_me] & below);
+        for (int w = 0; w < w_me; ++w) r += __popc(bm[ex * kWords + w]);
+        p = r;
+        if (p < capacity) {
+          row = s_off[ex] + p;
+          s_perm[row] = t * k + j;
+        }
+      }
+      if (lead) {
+        pos[(size_t)t * k + j] = p;
+        row_of[(size_t)t * k + j] = row;
+      }
+    }
+  }
+  __syncthreads();
+  const int nkept = s_off[E];
+  if (lead)
+    for (int r = tid; r < T * k; r += blockDim.x) perm[r] = r < nkept ? s_perm[r] : -1;
+  if (x == nullptr) return;
+  // row copies: warp-granular, grid-strided over routed rows then appended rows
+  const int lane = tid & 31;
+  const int nrows = nkept + (append_shared ? T : 0);
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int r = (blockIdx.x * blockDim.x + tid) >> 5; r < nrows; r += warps) {
+    const int src_t = r < nkept ? s_perm[r] / k : r - nkept;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)src_t * row_bytes);
+    uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)r * row_bytes);
+    for (int i = lane; i < row_bytes / 16; i += 32) dst[i] = __ldg(src + i);
+  }
+}
+
 // One warp per expert-ordered row; rows past offsets[E] get perm = -1.
 template <int VEC_BYTES>
 __global__ void __launch_bounds__(256) gather_rows_kernel(const int32_t* __restrict__ offsets,
@@ -160,31 +275,69 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const int32_t* __restr
   }
 }
 
+// x_perm[offsets[E] + t] = x[t]: the shared experts' rows after the routed rows (decode path).
+__global__ void __launch_bounds__(256) append_rows_kernel(const int32_t* __restrict__ offsets,
+                                                         int E, int T, int row_bytes,
+                                                         const unsigned char* __restrict__ x,
+                                                         unsigned char* __restrict__ x_perm) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const size_t base = (size_t)offsets[E];
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * row_bytes);
+    uint4* dst = reinterpret_cast<uint4*>(x_perm + (base + t) * row_bytes);
+    for (int i = lane; i < row_bytes / 16; i += 32) dst[i] = __ldg(src + i);
+  }
+}
+
+cudaError_t launch_append_rows(const moe_config& c, const int32_t* offsets, const void* x,
+                               void* x_perm, cudaStream_t s) {
+  const int row_bytes = c.d_model * (c.dtype == MOE_DTYPE_F32 ? 4 : 2);
+  int blocks = ceil_div(c.T, 8);
+  if (blocks > num_sms() * 4) blocks = num_sms() * 4;
+  append_rows_kernel<<<blocks, 256, 0, s>>>(offsets, c.E, c.T, row_bytes,
+                                            (const unsigned char*)x, (unsigned char*)x_perm);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_dispatch(const moe_config& c, int capacity, const int32_t* idx,
                             const DispatchBufs& b, const void* x, void* x_perm, DevStatus* st,
-                            cudaStream_t s) {
+                            cudaStream_t s, bool append_shared) {
   const int nblk = ceil_div(c.T, kDispatchBlock);
-  dispatch_count_kernel<<<nblk, kDispatchBlock, 0, s>>>(idx, c.T, c.E, c.k, b.bitmap,
-                                                        b.blk_base, st);
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  dispatch_scan_kernel<<<1, 256, 0, s>>>(b.blk_base, nblk, c.E, capacity, b.counts, b.kept,
-                                         b.offsets, b.mtile_prefix, b.n_dropped);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  dispatch_scatter_kernel<<<nblk, kDispatchBlock, 0, s>>>(idx, c.T, c.E, c.k, capacity, b.bitmap,
-                                                          b.blk_base, b.offsets, b.pos, b.row_of,
-                                                          b.perm);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  const int total_rows = c.T * c.k;
+  cudaError_t err;
   const int esz = c.dtype == MOE_DTYPE_F32 ? 4 : 2;
   const int row_bytes = c.d_model * esz;
+  if (nblk == 1) {
+    const int rows = c.T * c.k + (append_shared ? c.T : 0);
+    int blocks = x ? ceil_div(rows, 8) : 1;
+    if (blocks > num_sms()) blocks = num_sms();
+    dispatch_small_kernel<<<blocks, kDispatchBlock, 0, s>>>(
+        idx, c.T, c.E, c.k, capacity, b.counts, b.kept, b.offsets, b.mtile_prefix, b.n_dropped,
+        b.pos, b.row_of, b.perm, st, (const unsigned char*)x, (unsigned char*)x_perm, row_bytes,
+        append_shared ? 1 : 0);
+    return cudaGetLastError();
+  } else {
+    dispatch_count_kernel<<<nblk, kDispatchBlock, 0, s>>>(idx, c.T, c.E, c.k, b.bitmap,
+                                                          b.blk_base, st);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    dispatch_scan_kernel<<<1, 256, 0, s>>>(b.blk_base, nblk, c.E, capacity, b.counts, b.kept,
+                                           b.offsets, b.mtile_prefix, b.n_dropped);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    dispatch_scatter_kernel<<<nblk, kDispatchBlock, 0, s>>>(idx, c.T, c.E, c.k, capacity,
+                                                            b.bitmap, b.blk_base, b.offsets,
+                                                            b.pos, b.row_of, b.perm);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  }
+  const int total_rows = c.T * c.k;
   int blocks = ceil_div(total_rows, 8);
   const int cap_blocks = num_sms() * 8;
   if (blocks > cap_blocks) blocks = cap_blocks;
   gather_rows_kernel<16><<<blocks, 256, 0, s>>>(b.offsets, c.E, c.k, total_rows, row_bytes,
                                                 b.perm, (const unsigned char*)x,
                                                 (unsigned char*)x_perm);
-  return cudaGetLastError();
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if (append_shared && x) return launch_append_rows(c, b.offsets, x, x_perm, s);
+  return cudaSuccess;
 }
 
 }  // namespace moe

@@ -15,8 +15,16 @@ cudaError_t launch_router_logits(const moe_config& c, const void* x, const void*
 // Router logits on the tensor cores (bf16, E a multiple of 32): g = x W_gate^T in fp32.
 cudaError_t launch_router_tc(const moe_config& c, const void* x, const void* w_gate,
                              float* logits, cudaStream_t s);
+// With part_P/part_cnt/part_z the kernel also writes the load-balance partials of
+// aux_blocks(c) fixed token sets (the same values launch_aux_stats' first kernel produces);
+// launch_aux_final then reduces them.
 cudaError_t launch_route_topk(const moe_config& c, const float* logits, const float* bias,
-                              int32_t* idx, float* w, DevStatus* st, cudaStream_t s);
+                              int32_t* idx, float* w, DevStatus* st, cudaStream_t s,
+                              float* part_P = nullptr, int32_t* part_cnt = nullptr,
+                              float* part_z = nullptr);
+cudaError_t launch_aux_final(const moe_config& c, const float* part_P, const int32_t* part_cnt,
+                             const float* part_z, int nblocks, float* f, float* P,
+                             float* l_balance, float* z_loss, cudaStream_t s);
 cudaError_t launch_aux_stats(const moe_config& c, const float* logits, const int32_t* idx,
                              const int32_t* ec_counts, float* part_P, int32_t* part_cnt,
                              float* part_z, int nblocks, float* f, float* P, float* l_balance,
@@ -36,9 +44,14 @@ struct DispatchBufs {
   int32_t* row_of;      // [T,k]
   int32_t* perm;        // [T*k]
 };
+// append_shared: also copy the T token rows after the kept rows (decode path's shared rows).
 cudaError_t launch_dispatch(const moe_config& c, int capacity, const int32_t* idx,
                             const DispatchBufs& b, const void* x, void* x_perm, DevStatus* st,
-                            cudaStream_t s);
+                            cudaStream_t s, bool append_shared = false);
+
+// x_perm[offsets[E] + t] = x[t] for t < T (rows of the shared experts on the decode path).
+cudaError_t launch_append_rows(const moe_config& c, const int32_t* offsets, const void* x,
+                               void* x_perm, cudaStream_t s);
 
 // ---- expert FFN ------------------------------------------------------------------------------
 // Grouped SwiGLU over expert-ordered rows.  offsets/mtile_prefix describe the E groups; with
@@ -63,10 +76,35 @@ cudaError_t launch_ffn_tc(const GroupedFFN& g, DevStatus* st, cudaStream_t s);
 cudaError_t launch_ffn_tc2(const GroupedFFN& g, DevStatus* st, cudaStream_t s);
 cudaError_t launch_ffn_simt(const GroupedFFN& g, bool f32, DevStatus* st, cudaStream_t s);
 
+// Decode-sized batches: swap-AB tensor-core GEMMs (weights on M, tokens on N) over the routed
+// experts plus the shared experts in one tile list.  x holds the expert-ordered token rows
+// with the T shared rows appended after offsets[E]; h has ldo = max(F, F_shared).
+struct DecodeFFN {
+  const void* x;            // [max_rows, d] bf16
+  const int32_t* offsets;   // [E+1]
+  int E, T, d, F, F_shared;
+  int max_rows;
+  int np, np_shared;        // token rows per chunk (16, 32, 64, 128)
+  const void* w13;
+  const void* w2;
+  const void* ws13;
+  const void* ws2;
+  void* h;                  // [max_rows, max(F, F_shared)] bf16
+  float* y;                 // [ksplit2][max_rows, d] f32 partials (routed rows)
+  float* shared_out;        // [ksplit2][T, d] f32 partials
+  int ksplit1, ksplit2;     // K slices of the gate/up and down GEMMs (1 = no split)
+  float* gu;                // [ksplit1][max_rows, 2 max(F, F_shared)] f32 when ksplit1 > 1
+  size_t y_part_stride;     // elements between y partials (max_rows * d)
+  size_t shared_part_stride;// elements between shared partials (T * d)
+};
+cudaError_t launch_ffn_decode(const DecodeFFN& g, DevStatus* st, cudaStream_t s);
+
 // ---- combine ---------------------------------------------------------------------------------
-// y_perm and shared_out (or NULL) are float32 [*, d]; out follows c.out_dtype.
+// y_perm and shared_out (or NULL) are float32 [*, d]; out follows c.out_dtype.  With nsplit > 1
+// they hold nsplit K-slice partials, y_stride / shared_stride elements apart, summed in order.
 cudaError_t launch_combine(const moe_config& c, const float* y_perm, const int32_t* row_of,
-                           const float* w, const float* shared_out, void* out, cudaStream_t s);
+                           const float* w, const float* shared_out, void* out, cudaStream_t s,
+                           int nsplit = 1, size_t y_stride = 0, size_t shared_stride = 0);
 cudaError_t launch_combine_ec(const moe_config& c, const float* y_perm, const int32_t* tok_ptr,
                               const int32_t* tok_rows, const float* ec_w_flat,
                               const float* shared_out, void* out, cudaStream_t s);

@@ -32,10 +32,45 @@ size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 struct Layout {
   size_t status, logits, idx, w, bitmap, blk_base, counts, kept, offsets, mtp, n_dropped, pos,
       row_of, perm, part_P, part_cnt, part_z, f, P, lb, z, x_perm, h, y_perm, shared_out,
-      ec_tokens, ec_w, tok_cnt, tok_ptr, tok_rows, posmap, tokstat, total;
+      ec_tokens, ec_w, tok_cnt, tok_ptr, tok_rows, posmap, tokstat, dec_gu, dec_y, dec_sh, total;
 };
 
+// K-split of the decode GEMMs: up to kMaxSplit slices, partial buffers only for small batches.
+constexpr int kMaxSplit = 8;
+constexpr long long kSplitRows = 1024;
+
 int rows_max(const moe_config& c) { return c.T * c.k; }
+
+// Decode regime: bf16 with few rows per expert (<= 64 on average); the swap-AB kernel streams
+// each touched expert's weights once with the tokens on the MMA's N side.
+bool decode_regime(const moe_config& c) {
+  return c.dtype == MOE_DTYPE_BF16 && c.routing == MOE_ROUTE_TOKEN_CHOICE &&
+         (long long)c.T * c.k <= 64ll * c.E && c.d_model % 256 == 0;
+}
+
+bool decode_split_possible(const moe_config& c) {
+  return decode_regime(c) && (long long)c.T * c.k <= kSplitRows;
+}
+
+// Expected experts touched by T tokens, E(1 - (1 - k/E)^T) ("Systems for MoE Models" §1.4),
+// plus the shared experts, sets how many tiles a decode GEMM has; K is split until there are
+// about two waves of tiles.
+int decode_split(const moe_config& c, int tiles_per_entry, int kblocks) {
+  if (!decode_split_possible(c)) return 1;
+  const double touched = c.E * (1.0 - std::pow(1.0 - (double)c.k / c.E, (double)c.T));
+  const double entries = touched + (c.d_ff_shared > 0 ? 1.0 : 0.0);
+  const double tiles = entries * tiles_per_entry;
+  int sp = (int)std::ceil(2.0 * num_sms() / (tiles > 1 ? tiles : 1));
+  if (sp > kMaxSplit) sp = kMaxSplit;
+  if (sp > kblocks) sp = kblocks;
+  return sp < 1 ? 1 : sp;
+}
+
+int pow2_clamp(long long v, int lo, int hi) {
+  int p = lo;
+  while (p < v && p < hi) p <<= 1;
+  return p;
+}
 
 Layout layout(const moe_config& c) {
   Layout L{};
@@ -71,8 +106,9 @@ Layout layout(const moe_config& c) {
   L.P = take(E * 4);
   L.lb = take(4);
   L.z = take(4);
-  L.x_perm = take(R * d * esz);
-  const size_t hrows = R > T ? R : T;
+  // the decode path appends the T shared-expert rows after the routed rows
+  L.x_perm = take((R + T) * d * esz);
+  const size_t hrows = R + T;
   const size_t hcols = F > Fs ? F : Fs;
   L.h = take(hrows * hcols * esz);
   L.y_perm = take(R * d * 4);          // float32 expert outputs
@@ -86,6 +122,12 @@ Layout layout(const moe_config& c) {
     L.tok_rows = take(E * C * 4);
     L.posmap = take(E * T * 4);
     L.tokstat = take(T * 8);
+  }
+  if (decode_split_possible(c)) {
+    const size_t Fmax = F > Fs ? F : Fs;
+    L.dec_gu = take((size_t)kMaxSplit * (R + T) * 2 * Fmax * 4);
+    L.dec_y = take((size_t)kMaxSplit * R * d * 4);
+    L.dec_sh = take((size_t)kMaxSplit * T * d * 4);
   }
   L.total = o;
   return L;
@@ -307,6 +349,30 @@ int moe_expert_ffn(const moe_config* c, const void* x_perm, const int32_t* offse
   if ((st = check_ws(ws))) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Layout L = layout(*c);
+  if (decode_regime(*c)) {
+    DecodeFFN g{};
+    g.x = x_perm;
+    g.offsets = offsets;
+    g.E = c->E;
+    g.T = c->T;
+    g.d = c->d_model;
+    g.F = c->d_ff;
+    g.F_shared = 0;
+    g.max_rows = rows_max(*c);
+    g.np = pow2_clamp(2ll * c->T * c->k / c->E, 16, 128);
+    g.np_shared = 16;
+    g.w13 = w13;
+    g.w2 = w2;
+    g.h = at<void>(ws, L.h);
+    g.y = y_perm;
+    g.ksplit1 = decode_split(*c, c->d_ff / 128, c->d_model / 64);
+    g.ksplit2 = 1;                          // the caller's y_perm holds one slice
+    g.gu = g.ksplit1 > 1 ? at<float>(ws, L.dec_gu) : nullptr;
+    g.y_part_stride = (size_t)rows_max(*c) * c->d_model;
+    g.shared_part_stride = 0;
+    return launch_ffn_decode(g, at<DevStatus>(ws, L.status), s) == cudaSuccess ? MOE_OK
+                                                                             : MOE_ERR_CUDA;
+  }
   int32_t* mtp = at<int32_t>(ws, L.mtp);
   mtp_from_offsets<<<1, 256, 0, s>>>(offsets, c->E, mtp);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
@@ -352,16 +418,21 @@ int moe_expert_choice(const moe_config* c, const float* logits, int32_t* ec_toke
                                           s));
 }
 
-int moe_forward(const moe_config* c, const void* x, const void* w_gate, const float* bias,
-                const void* w13, const void* w2, const void* ws13, const void* ws2, void* out,
-                int32_t* topk_idx, float* topk_w, float* f, float* P, float* l_balance,
-                float* z_loss, int32_t* n_dropped, void* ws, void* stream) {
+}  // extern "C"
+
+namespace moe {
+namespace {
+
+int forward_impl(const moe_config* c, const void* x, const void* w_gate, const float* bias,
+                 const void* w13, const void* w2, const void* ws13, const void* ws2, void* out,
+                 int32_t* topk_idx, float* topk_w, float* f, float* P, float* l_balance,
+                 float* z_loss, int32_t* n_dropped, void* ws, cudaStream_t s,
+                 cudaEvent_t ev_begin, cudaEvent_t ev_end) {
   int st = moe_check_config(c);
   if (st) return st;
   if (!x || !w_gate || !w13 || !w2 || !out) return MOE_ERR_ARG;
   if (c->d_ff_shared > 0 && (!ws13 || !ws2)) return MOE_ERR_ARG;
   if ((st = check_ws(ws))) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Layout L = layout(*c);
   DevStatus* dst = at<DevStatus>(ws, L.status);
   float* g = at<float>(ws, L.logits);
@@ -370,6 +441,12 @@ int moe_forward(const moe_config* c, const void* x, const void* w_gate, const fl
   l_balance = l_balance ? l_balance : at<float>(ws, L.lb);
   z_loss = z_loss ? z_loss : at<float>(ws, L.z);
   float* shared = c->d_ff_shared > 0 ? at<float>(ws, L.shared_out) : nullptr;
+  float* part_P = at<float>(ws, L.part_P);
+  int32_t* part_cnt = at<int32_t>(ws, L.part_cnt);
+  float* part_z = at<float>(ws, L.part_z);
+  auto mark = [&](cudaEvent_t ev) {
+    return ev ? cudaEventRecord(ev, s) : cudaSuccess;
+  };
 
   cudaError_t e = launch_router_logits(*c, x, w_gate, g, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -377,26 +454,68 @@ int moe_forward(const moe_config* c, const void* x, const void* w_gate, const fl
   if (c->routing == MOE_ROUTE_TOKEN_CHOICE) {
     int32_t* idx = topk_idx ? topk_idx : at<int32_t>(ws, L.idx);
     float* w = topk_w ? topk_w : at<float>(ws, L.w);
-    if ((e = launch_route_topk(*c, g, bias, idx, w, dst, s)) != cudaSuccess) return MOE_ERR_CUDA;
-    if ((e = launch_aux_stats(*c, g, idx, nullptr, at<float>(ws, L.part_P),
-                              at<int32_t>(ws, L.part_cnt), at<float>(ws, L.part_z),
-                              aux_blocks(*c), f, P, l_balance, z_loss, dst, s)) != cudaSuccess)
+    // Top-k with the load-balance partials of the same pass; the partials are reduced after
+    // the combine, off the path to the output
+    if ((e = launch_route_topk(*c, g, bias, idx, w, dst, s, part_P, part_cnt, part_z)) !=
+        cudaSuccess)
       return MOE_ERR_CUDA;
+    const bool dec = decode_regime(*c);
     DispatchBufs b{at<uint32_t>(ws, L.bitmap), at<int32_t>(ws, L.blk_base),
                    at<int32_t>(ws, L.counts), at<int32_t>(ws, L.kept),
                    at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.mtp),
                    n_dropped ? n_dropped : at<int32_t>(ws, L.n_dropped), at<int32_t>(ws, L.pos),
                    at<int32_t>(ws, L.row_of), at<int32_t>(ws, L.perm)};
-    if ((e = launch_dispatch(*c, capacity_of(*c), idx, b, x, at<void>(ws, L.x_perm), dst, s)) !=
-        cudaSuccess)
+    if ((e = launch_dispatch(*c, capacity_of(*c), idx, b, x, at<void>(ws, L.x_perm), dst, s,
+                             dec && shared != nullptr)) != cudaSuccess)
       return MOE_ERR_CUDA;
-    if ((st = run_ffn(*c, at<void>(ws, L.x_perm), b.offsets, b.mtile_prefix, -1, c->E, c->d_ff,
-                      rows_max(*c), w13, w2, at<float>(ws, L.y_perm), ws, L, s)))
-      return st;
-    if (shared && (st = run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13,
-                                ws2, shared, ws, L, s)))
-      return st;
-    return cuda_status(launch_combine(*c, at<float>(ws, L.y_perm), b.row_of, w, shared, out, s));
+    if (dec) {
+      DecodeFFN g{};
+      g.x = at<void>(ws, L.x_perm);
+      g.offsets = b.offsets;
+      g.E = c->E;
+      g.T = c->T;
+      g.d = c->d_model;
+      g.F = c->d_ff;
+      g.F_shared = c->d_ff_shared;
+      g.max_rows = rows_max(*c) + c->T;
+      g.np = pow2_clamp(2ll * c->T * c->k / c->E, 16, 128);
+      g.np_shared = pow2_clamp(c->T, 16, 128);
+      g.w13 = w13;
+      g.w2 = w2;
+      g.ws13 = ws13;
+      g.ws2 = ws2;
+      g.h = at<void>(ws, L.h);
+      g.ksplit1 = decode_split(*c, c->d_ff / 128, c->d_model / 64);
+      // every K slice must hold at least one 64-wide block of both the routed and shared K
+      const int kb2 = (c->d_ff_shared > 0 && c->d_ff_shared < c->d_ff ? c->d_ff_shared
+                                                                      : c->d_ff) / 64;
+      g.ksplit2 = decode_split(*c, c->d_model / 256, kb2);
+      g.gu = g.ksplit1 > 1 ? at<float>(ws, L.dec_gu) : nullptr;
+      g.y = g.ksplit2 > 1 ? at<float>(ws, L.dec_y) : at<float>(ws, L.y_perm);
+      g.shared_out = g.ksplit2 > 1 ? at<float>(ws, L.dec_sh) : shared;
+      g.y_part_stride = (size_t)rows_max(*c) * c->d_model;
+      g.shared_part_stride = (size_t)c->T * c->d_model;
+      if (mark(ev_begin) != cudaSuccess || launch_ffn_decode(g, dst, s) != cudaSuccess ||
+          mark(ev_end) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      if ((e = launch_combine(*c, g.y, b.row_of, w, shared ? g.shared_out : nullptr, out, s,
+                              g.ksplit2, g.y_part_stride, g.shared_part_stride)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    } else {
+      if (mark(ev_begin) != cudaSuccess) return MOE_ERR_CUDA;
+      if ((st = run_ffn(*c, at<void>(ws, L.x_perm), b.offsets, b.mtile_prefix, -1, c->E,
+                        c->d_ff, rows_max(*c), w13, w2, at<float>(ws, L.y_perm), ws, L, s)))
+        return st;
+      if (mark(ev_end) != cudaSuccess) return MOE_ERR_CUDA;
+      if (shared && (st = run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13,
+                                  ws2, shared, ws, L, s)))
+        return st;
+      if ((e = launch_combine(*c, at<float>(ws, L.y_perm), b.row_of, w, shared, out, s)) !=
+          cudaSuccess)
+        return MOE_ERR_CUDA;
+    }
+    return cuda_status(launch_aux_final(*c, part_P, part_cnt, part_z, aux_blocks(*c), f, P,
+                                        l_balance, z_loss, s));
   }
 
   // expert choice
@@ -408,22 +527,49 @@ int moe_forward(const moe_config* c, const void* x, const void* w_gate, const fl
                                 at<int32_t>(ws, L.posmap), at<float2>(ws, L.tokstat), dst, s)) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
-  if ((e = launch_aux_stats(*c, g, nullptr, nullptr, at<float>(ws, L.part_P),
-                            at<int32_t>(ws, L.part_cnt), at<float>(ws, L.part_z), aux_blocks(*c),
-                            f, P, l_balance, z_loss, dst, s)) != cudaSuccess)
-    return MOE_ERR_CUDA;
   if ((e = launch_gather_ec(*c, ec_tokens, x, at<void>(ws, L.x_perm), at<int32_t>(ws, L.offsets),
                             at<int32_t>(ws, L.mtp), s)) != cudaSuccess)
     return MOE_ERR_CUDA;
+  if (mark(ev_begin) != cudaSuccess) return MOE_ERR_CUDA;
   if ((st = run_ffn(*c, at<void>(ws, L.x_perm), at<int32_t>(ws, L.offsets),
                     at<int32_t>(ws, L.mtp), -1, c->E, c->d_ff, c->E * C, w13, w2,
                     at<float>(ws, L.y_perm), ws, L, s)))
     return st;
+  if (mark(ev_end) != cudaSuccess) return MOE_ERR_CUDA;
   if (shared && (st = run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13, ws2,
                               shared, ws, L, s)))
     return st;
-  return cuda_status(launch_combine_ec(*c, at<float>(ws, L.y_perm), at<int32_t>(ws, L.tok_ptr),
-                                       at<int32_t>(ws, L.tok_rows), ec_w, shared, out, s));
+  if ((e = launch_combine_ec(*c, at<float>(ws, L.y_perm), at<int32_t>(ws, L.tok_ptr),
+                             at<int32_t>(ws, L.tok_rows), ec_w, shared, out, s)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return cuda_status(launch_aux_stats(*c, g, nullptr, nullptr, part_P, part_cnt, part_z,
+                                      aux_blocks(*c), f, P, l_balance, z_loss, dst, s));
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" {
+
+int moe_forward(const moe_config* c, const void* x, const void* w_gate, const float* bias,
+                const void* w13, const void* w2, const void* ws13, const void* ws2, void* out,
+                int32_t* topk_idx, float* topk_w, float* f, float* P, float* l_balance,
+                float* z_loss, int32_t* n_dropped, void* ws, void* stream) {
+  return forward_impl(c, x, w_gate, bias, w13, w2, ws13, ws2, out, topk_idx, topk_w, f, P,
+                      l_balance, z_loss, n_dropped, ws, static_cast<cudaStream_t>(stream),
+                      nullptr, nullptr);
+}
+
+int moe_forward_timed(const moe_config* c, const void* x, const void* w_gate, const float* bias,
+                      const void* w13, const void* w2, const void* ws13, const void* ws2,
+                      void* out, int32_t* topk_idx, float* topk_w, float* f, float* P,
+                      float* l_balance, float* z_loss, int32_t* n_dropped, void* ws,
+                      void* stream, void* ev_expert_begin, void* ev_expert_end) {
+  if (!ev_expert_begin || !ev_expert_end) return MOE_ERR_ARG;
+  return forward_impl(c, x, w_gate, bias, w13, w2, ws13, ws2, out, topk_idx, topk_w, f, P,
+                      l_balance, z_loss, n_dropped, ws, static_cast<cudaStream_t>(stream),
+                      static_cast<cudaEvent_t>(ev_expert_begin),
+                      static_cast<cudaEvent_t>(ev_expert_end));
 }
 
 int moe_workspace_views(const moe_config* c, void* ws, float** logits, int32_t** row_of,

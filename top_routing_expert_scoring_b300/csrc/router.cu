@@ -143,8 +143,77 @@ static cudaError_t launch_stream(const moe_config& c, const void* x, const void*
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------------------------------
+// Logits for a handful of tokens (T <= 16, bf16): one CTA per expert streams that expert's
+// router row once (16-byte loads; its 8 warps take one eighth of d each) and forms the T dot
+// products against the token rows, which stay in L1/L2; the 8 partial sums are added in a
+// fixed order.  Spreads the router weights over every SM instead of one tile.
+// ------------------------------------------------------------------------------------------
+template <int TP>
+__global__ void __launch_bounds__(256) router_logits_few(const uint4* __restrict__ x,
+                                                        const uint4* __restrict__ w,
+                                                        float* __restrict__ g, int Tn, int d8,
+                                                        int E) {
+  __shared__ float part[8][TP];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int e = blockIdx.x;
+  float acc[TP];
+#pragma unroll
+  for (int t = 0; t < TP; ++t) acc[t] = 0.f;
+  const uint4* wr = w + (size_t)e * d8;
+  const int per = ceil_div(d8, 8);
+  const int c0 = warp * per, c1 = min(d8, c0 + per);
+  for (int c = c0 + lane; c < c1; c += 32) {
+    const uint4 wv = __ldg(wr + c);
+    const __nv_bfloat162* wh = reinterpret_cast<const __nv_bfloat162*>(&wv);
+    float wf[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f2 = __bfloat1622float2(wh[i]);
+      wf[2 * i] = f2.x;
+      wf[2 * i + 1] = f2.y;
+    }
+#pragma unroll
+    for (int t = 0; t < TP; ++t) {
+      if (t < Tn) {
+        const uint4 xv = __ldg(x + (size_t)t * d8 + c);
+        const __nv_bfloat162* xh = reinterpret_cast<const __nv_bfloat162*>(&xv);
+        float a = acc[t];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f2 = __bfloat1622float2(xh[i]);
+          a = fmaf(wf[2 * i], f2.x, a);
+          a = fmaf(wf[2 * i + 1], f2.y, a);
+        }
+        acc[t] = a;
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < TP; ++t) {
+    const float v = warp_sum(acc[t]);
+    if (lane == 0) part[warp][t] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x < TP && threadIdx.x < Tn) {
+    float v = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v += part[q][threadIdx.x];
+    g[(size_t)threadIdx.x * E + e] = v;
+  }
+}
+
 cudaError_t launch_router_logits(const moe_config& c, const void* x, const void* w_gate,
                                  float* logits, cudaStream_t s) {
+  if (c.dtype == MOE_DTYPE_BF16 && c.T <= 16) {
+    if (c.T <= 4)
+      router_logits_few<4><<<c.E, 256, 0, s>>>((const uint4*)x, (const uint4*)w_gate, logits, c.T,
+                                               c.d_model / 8, c.E);
+    else
+      router_logits_few<16><<<c.E, 256, 0, s>>>((const uint4*)x, (const uint4*)w_gate, logits,
+                                                c.T, c.d_model / 8, c.E);
+    return cudaGetLastError();
+  }
   if (c.dtype == MOE_DTYPE_BF16) {
     if (c.E >= 32 && c.E % 32 == 0) return launch_router_tc(c, x, w_gate, logits, s);
     const size_t row_bytes = (size_t)c.d_model * 2;
@@ -177,7 +246,81 @@ struct RouteArgs {
   float scale;
   int32_t* idx;
   float* w;
+  float* part_P;            // optional load-balance partials (see aux_partial_kernel)
+  int32_t* part_cnt;
+  float* part_z;
 };
+
+constexpr int kAuxWarps = 8;
+
+// One token's contribution to the load-balance statistics, identical in every kernel that
+// takes it: P_i gets softmax(g)_i (sigmoid scoring: s_i / sum_j s_j), z gets lse(g)^2.
+template <int V>
+__device__ __forceinline__ void token_stats(const float (&gv)[V], int lane, int E, int score,
+                                            float (&accP)[V], float& zacc) {
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < V; ++i) m = fmaxf(m, gv[i]);
+  m = warp_max(m);
+  float ex[V], se = 0.f;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    ex[i] = (lane * V + i) < E ? expf(gv[i] - m) : 0.f;
+    se += ex[i];
+  }
+  se = warp_sum(se);
+  const float lse = m + logf(se);
+  if (score == MOE_SCORE_SOFTMAX) {
+#pragma unroll
+    for (int i = 0; i < V; ++i) accP[i] += ex[i] / se;
+  } else {
+    float sv[V], ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      sv[i] = (lane * V + i) < E ? 1.0f / (1.0f + expf(-gv[i])) : 0.f;
+      ss += sv[i];
+    }
+    ss = warp_sum(ss);
+#pragma unroll
+    for (int i = 0; i < V; ++i) accP[i] += sv[i] / ss;
+  }
+  if (lane == 0) zacc += lse * lse;
+}
+
+// The CTA's warps add their partials in a fixed order and write one row per CTA.
+template <int V>
+__device__ __forceinline__ void write_block_stats(const float (&accP)[V], const int (&cnt)[V],
+                                                  float zacc, int E, float* part_P,
+                                                  int32_t* part_cnt, float* part_z,
+                                                  unsigned char* smem) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float* sP = reinterpret_cast<float*>(smem);                       // [warps][E]
+  int* sC = reinterpret_cast<int*>(sP + kAuxWarps * E);              // [warps][E]
+  float* sZ = reinterpret_cast<float*>(sC + kAuxWarps * E);
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int e = lane * V + i;
+    if (e < E) {
+      sP[warp * E + e] = accP[i];
+      sC[warp * E + e] = cnt[i];
+    }
+  }
+  if (lane == 0) sZ[warp] = zacc;
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    float pv = 0.f;
+    int c = 0;
+    for (int w = 0; w < kAuxWarps; ++w) { pv += sP[w * E + e]; c += sC[w * E + e]; }
+    part_P[(size_t)blockIdx.x * E + e] = pv;
+    part_cnt[(size_t)blockIdx.x * E + e] = c;
+  }
+  if (threadIdx.x == 0) {
+    float z = 0.f;
+    for (int w = 0; w < kAuxWarps; ++w) z += sZ[w];
+    part_z[blockIdx.x] = z;
+  }
+}
 
 template <int V>
 __global__ void __launch_bounds__(256) route_topk_kernel(RouteArgs a) {
@@ -187,12 +330,19 @@ __global__ void __launch_bounds__(256) route_topk_kernel(RouteArgs a) {
   const bool grouped = a.score == MOE_SCORE_SIGMOID && a.n_groups > 1 && a.topk_groups < a.n_groups;
   float* row = route_smem + warp * (E + 32);
   float* gsc = row + E;
+  const bool stats = a.part_P != nullptr;
+  float accP[V];
+  int cnt[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) { accP[i] = 0.f; cnt[i] = 0; }
+  float zacc = 0.f;
   for (int t = blockIdx.x * wpb + warp; t < a.T; t += gridDim.x * wpb) {
-    float key[V], val[V];
+    float key[V], val[V], graw[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) {
       const int e = lane * V + i;
       const float gv = e < E ? a.g[(size_t)t * E + e] : -INFINITY;
+      graw[i] = gv;
       if (a.score == MOE_SCORE_SOFTMAX) {
         key[i] = gv;
         val[i] = gv;
@@ -203,6 +353,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(RouteArgs a) {
         key[i] = e < E ? sv + b : -INFINITY;
       }
     }
+    if (stats) token_stats<V>(graw, lane, E, a.score, accP, zacc);
     if (grouped) {
       const int per = E / a.n_groups;
 #pragma unroll
@@ -261,7 +412,10 @@ __global__ void __launch_bounds__(256) route_topk_kernel(RouteArgs a) {
       if (lane == owner) {
 #pragma unroll
         for (int i = 0; i < V; ++i)
-          if (lane * V + i == bi) taken |= 1u << i;
+          if (lane * V + i == bi) {
+            taken |= 1u << i;
+            cnt[i] += 1;
+          }
       }
       const float v = __shfl_sync(0xffffffffu, bv, owner);
       (void)mine;
@@ -295,16 +449,23 @@ __global__ void __launch_bounds__(256) route_topk_kernel(RouteArgs a) {
       a.w[(size_t)t * k + lane] = (num / den) * a.scale;
     }
   }
+  if (stats)
+    write_block_stats<V>(accP, cnt, zacc, E, a.part_P, a.part_cnt, a.part_z,
+                         reinterpret_cast<unsigned char*>(route_smem));
 }
 
 cudaError_t launch_route_topk(const moe_config& c, const float* logits, const float* bias,
-                              int32_t* idx, float* w, DevStatus* st, cudaStream_t s) {
+                              int32_t* idx, float* w, DevStatus* st, cudaStream_t s,
+                              float* part_P, int32_t* part_cnt, float* part_z) {
   (void)st;
   RouteArgs a{logits, bias, c.T, c.E, c.k, c.score, c.n_groups, c.topk_groups, c.renormalize,
-              c.route_scale, idx, w};
-  const int wpb = 8;
-  const int blocks = ceil_div(c.T, wpb);
-  const size_t smem = (size_t)wpb * (c.E + 32) * sizeof(float);
+              c.route_scale, idx, w, part_P, part_cnt, part_z};
+  const int wpb = kAuxWarps;
+  // with the statistics, the grid is the statistics' fixed block count (fixed token sets)
+  const int blocks = part_P ? aux_blocks(c) : ceil_div(c.T, wpb);
+  const size_t route_bytes = (size_t)wpb * (c.E + 32) * sizeof(float);
+  const size_t stats_bytes = (size_t)kAuxWarps * c.E * 8 + kAuxWarps * 4 + 16;
+  const size_t smem = route_bytes > stats_bytes ? route_bytes : stats_bytes;
   if (c.E <= 32) route_topk_kernel<1><<<blocks, wpb * 32, smem, s>>>(a);
   else if (c.E <= 64) route_topk_kernel<2><<<blocks, wpb * 32, smem, s>>>(a);
   else if (c.E <= 128) route_topk_kernel<4><<<blocks, wpb * 32, smem, s>>>(a);
@@ -328,8 +489,6 @@ struct AuxArgs {
   float* part_z;            // [nblk]
 };
 
-constexpr int kAuxWarps = 8;
-
 template <int V>
 __global__ void __launch_bounds__(kAuxWarps * 32) aux_partial_kernel(AuxArgs a) {
   extern __shared__ unsigned char aux_smem[];
@@ -342,36 +501,12 @@ __global__ void __launch_bounds__(kAuxWarps * 32) aux_partial_kernel(AuxArgs a) 
   float zacc = 0.f;
   for (int t = blockIdx.x * kAuxWarps + warp; t < a.T; t += gridDim.x * kAuxWarps) {
     float gv[V];
-    float m = -INFINITY;
 #pragma unroll
     for (int i = 0; i < V; ++i) {
       const int e = lane * V + i;
       gv[i] = e < E ? a.g[(size_t)t * E + e] : -INFINITY;
-      m = fmaxf(m, gv[i]);
     }
-    m = warp_max(m);
-    float ex[V], se = 0.f;
-#pragma unroll
-    for (int i = 0; i < V; ++i) {
-      ex[i] = (lane * V + i) < E ? expf(gv[i] - m) : 0.f;
-      se += ex[i];
-    }
-    se = warp_sum(se);
-    const float lse = m + logf(se);
-    if (a.score == MOE_SCORE_SOFTMAX) {
-#pragma unroll
-      for (int i = 0; i < V; ++i) accP[i] += ex[i] / se;
-    } else {
-      float sv[V], ss = 0.f;
-#pragma unroll
-      for (int i = 0; i < V; ++i) {
-        sv[i] = (lane * V + i) < E ? 1.0f / (1.0f + expf(-gv[i])) : 0.f;
-        ss += sv[i];
-      }
-      ss = warp_sum(ss);
-#pragma unroll
-      for (int i = 0; i < V; ++i) accP[i] += sv[i] / ss;
-    }
+    token_stats<V>(gv, lane, E, a.score, accP, zacc);
     if (a.ec_C <= 0) {
       for (int j = 0; j < a.k; ++j) {
         const int e = a.idx[(size_t)t * a.k + j];
@@ -382,78 +517,50 @@ __global__ void __launch_bounds__(kAuxWarps * 32) aux_partial_kernel(AuxArgs a) 
         }
       }
     }
-    if (lane == 0) zacc += lse * lse;
   }
-  // fixed-order reduction over the CTA's warps
-  double* sP = reinterpret_cast<double*>(aux_smem);                 // [warps][E]
-  int* sC = reinterpret_cast<int*>(sP + kAuxWarps * E);              // [warps][E]
-  double* sZ = reinterpret_cast<double*>(sC + kAuxWarps * E + (kAuxWarps * E & 1));
-#pragma unroll
-  for (int i = 0; i < V; ++i) {
-    const int e = lane * V + i;
-    if (e < E) {
-      sP[warp * E + e] = accP[i];
-      sC[warp * E + e] = cnt[i];
-    }
-  }
-  if (lane == 0) sZ[warp] = zacc;
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    double p = 0.0;
-    int c = 0;
-    for (int w = 0; w < kAuxWarps; ++w) { p += sP[w * E + e]; c += sC[w * E + e]; }
-    a.part_P[(size_t)blockIdx.x * E + e] = (float)p;
-    a.part_cnt[(size_t)blockIdx.x * E + e] = c;
-  }
-  if (threadIdx.x == 0) {
-    double z = 0.0;
-    for (int w = 0; w < kAuxWarps; ++w) z += sZ[w];
-    a.part_z[blockIdx.x] = (float)z;
-  }
+  write_block_stats<V>(accP, cnt, zacc, E, a.part_P, a.part_cnt, a.part_z, aux_smem);
 }
 
-// One warp per expert: lanes sum blocks lane, lane+32, ... in float64, then a butterfly in a
-// fixed order; warp 0 also sums the z partials.  Deterministic for a given block count.
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
+// One warp per expert: lanes sum blocks lane, lane+32, ... (float32 for P and z, integers for
+// counts), then a butterfly in a fixed order; warp 0 also sums the z partials.  Deterministic
+// for a given block count.  (No float64: its throughput on this part is a tiny fraction.)
 __global__ void __launch_bounds__(1024) aux_final_kernel(const float* part_P,
                                                         const int32_t* part_cnt,
                                                         const float* part_z, int nblk, int T,
                                                         int E, int ec_C, float* f, float* P,
                                                         float* l_balance, float* z_loss) {
-  __shared__ double prod[256];
+  __shared__ float prod[256];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const float invT = 1.0f / (float)T;
   for (int e = warp; e < E; e += nw) {
-    double p = 0.0, c = 0.0;
+    float p = 0.f;
+    int c = 0;
     for (int b = lane; b < nblk; b += 32) {
       p += part_P[(size_t)b * E + e];
       c += part_cnt[(size_t)b * E + e];
     }
-    p = warp_sum_d(p);
-    c = warp_sum_d(c);
+    p = warp_sum(p);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
     if (ec_C > 0) c = ec_C;
-    const double fe = c / T, Pe = p / T;
+    const float fe = (float)c * invT, Pe = p * invT;
     if (lane == 0) {
-      if (f) f[e] = (float)fe;
-      if (P) P[e] = (float)Pe;
+      if (f) f[e] = fe;
+      if (P) P[e] = Pe;
       prod[e] = fe * Pe;
     }
   }
   __syncthreads();
   if (warp == 0) {
-    double acc = 0.0;
+    float acc = 0.f;
     for (int e = lane; e < E; e += 32) acc += prod[e];
-    acc = warp_sum_d(acc);
-    double z = 0.0;
+    acc = warp_sum(acc);
+    float z = 0.f;
     for (int b = lane; b < nblk; b += 32) z += part_z[b];
-    z = warp_sum_d(z);
+    z = warp_sum(z);
     if (lane == 0) {
-      if (l_balance) *l_balance = (float)(E * acc);
-      if (z_loss) *z_loss = (float)(z / T);
+      if (l_balance) *l_balance = (float)E * acc;
+      if (z_loss) *z_loss = z * invT;
     }
   }
 }
@@ -470,14 +577,20 @@ cudaError_t launch_aux_stats(const moe_config& c, const float* logits, const int
   (void)st;
   const int ecC = c.routing == MOE_ROUTE_EXPERT_CHOICE ? (int)((long long)c.T * c.k / c.E) : 0;
   AuxArgs a{logits, idx, c.T, c.E, c.k, c.score, ecC, part_P, part_cnt, part_z};
-  const size_t smem = (size_t)kAuxWarps * c.E * (sizeof(double) + sizeof(int)) + 8 +
-                      kAuxWarps * sizeof(double) + 16;
+  const size_t smem = (size_t)kAuxWarps * c.E * 8 + kAuxWarps * 4 + 16;
   if (c.E <= 32) aux_partial_kernel<1><<<nblocks, kAuxWarps * 32, smem, s>>>(a);
   else if (c.E <= 64) aux_partial_kernel<2><<<nblocks, kAuxWarps * 32, smem, s>>>(a);
   else if (c.E <= 128) aux_partial_kernel<4><<<nblocks, kAuxWarps * 32, smem, s>>>(a);
   else aux_partial_kernel<8><<<nblocks, kAuxWarps * 32, smem, s>>>(a);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
+  return launch_aux_final(c, part_P, part_cnt, part_z, nblocks, f, P, l_balance, z_loss, s);
+}
+
+cudaError_t launch_aux_final(const moe_config& c, const float* part_P, const int32_t* part_cnt,
+                             const float* part_z, int nblocks, float* f, float* P,
+                             float* l_balance, float* z_loss, cudaStream_t s) {
+  const int ecC = c.routing == MOE_ROUTE_EXPERT_CHOICE ? (int)((long long)c.T * c.k / c.E) : 0;
   aux_final_kernel<<<1, 1024, 0, s>>>(part_P, part_cnt, part_z, nblocks, c.T, c.E, ecC, f, P,
                                       l_balance, z_loss);
   return cudaGetLastError();

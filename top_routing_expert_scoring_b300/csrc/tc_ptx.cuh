@@ -125,6 +125,9 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 // 2-D bf16 tensor [rows, cols] (cols contiguous) read in boxes of 64 columns x 128 rows with
 // the 128-byte swizzle.  Host side; false when the driver entry point or the encode fails.
 bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols);
+// Same with a box of 64 columns x box_rows rows (box_rows a multiple of 8, <= 256).
+bool make_map_box(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                  uint32_t box_rows);
 
 }  // namespace tc
 }  // namespace moe
