@@ -152,6 +152,28 @@ class ClockSampler:
                 "samples": len(self.samples)}
 
 
+def max_over_ranks(ms: float, device) -> float:
+    """The slowest rank's time (every rank processes its own token batch; the job is done when
+    the last one is).  Single process: returns ms."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(ms)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_rank: int, steps: int, ms_max: float) -> float:
+    """Whole-job throughput: the tokens all ranks processed over the slowest rank's time."""
+    return world * tokens_per_rank * steps / (ms_max / 1e3)
+
+
+def runs_reference_arm(rank: int) -> bool:
+    """Under torchrun only rank 0 times the oracle; the other ranks exit without work."""
+    return rank == 0
+
+
 def cpu_cores():
     try:
         from threadpoolctl import threadpool_info
@@ -336,7 +358,7 @@ def main():
               "parallelism": "replicas" if world == 1 else f"replicas x{world} (token shards)"}
 
     if args.impl == "reference":
-        if rank != 0:
+        if not runs_reference_arm(rank):
             return
         torch.manual_seed(0)
         inp = moe_inputs.make_inputs(wl, device="cpu")
@@ -425,14 +447,10 @@ def main():
             step(gemm_pairs[i])
         t_end.record(stream)
         barrier()
-    ms_total = t_start.elapsed_time(t_end)
+    ms_total = max_over_ranks(t_start.elapsed_time(t_end), dev)
     gemm_ms = [a.elapsed_time(b) for a, b in gemm_pairs]
-    if world > 1:
-        tt = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(tt.item())
     ms_step = ms_total / args.steps
-    value = world * T * args.steps / (ms_total / 1e3)
+    value = job_tokens_per_s(world, T, args.steps, ms_total)
 
     # end to end through the public call with host buffers (pinned), copies inside the region
     x_host = inp["x"].cpu().pin_memory()
@@ -459,7 +477,7 @@ def main():
         e2e_step()
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev) / args.steps
     st = m.sync_status(ws)
     if st != 0:
         raise RuntimeError(f"device status {st}: {m.status_string(st)}")

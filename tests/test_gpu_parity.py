@@ -73,6 +73,9 @@ SMALL = {
     "softmax_cap": dict(name="mixtral", T=700, d=256, F=384, capacity_factor=1.25),
     "softmax_collapsed_cap": dict(name="mixtral_collapsed", T=600, d=256, F=256,
                                   capacity_factor=1.0),
+    # Switch routing: k = 1, the weight is the probability itself (no renormalisation)
+    "switch_k1": dict(name="mixtral", T=500, d=256, F=256, k=1, renormalize=False,
+                      capacity_factor=1.0),
     # bf16 DeepSeek-V3-like gate: sigmoid + bias, 8 groups keep 4, top-8, scale 2.5, shared
     "v3_like": dict(name="v3", T=333, d=256, E=64, F=256, F_shared=256),
     # bf16 DeepSeekMoE-like: 2 shared experts, d not a multiple of 256 (N=128 down tiles)

@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(256) router_logits_simt(const T* __restrict__ 
 // lane; a butterfly reduction (fixed order) finishes them.  HBM-bound on reading x.
 // ------------------------------------------------------------------------------------------
 template <int EP>
-__global__ void __launch_bounds__(256) router_logits_stream(const uint4* __restrict__ x,
+__global__ void __launch_bounds__(512) router_logits_stream(const uint4* __restrict__ x,
                                                            const uint4* __restrict__ w,
                                                            float* __restrict__ g, int Tn,
                                                            int d8, int E) {
@@ -135,10 +135,11 @@ static cudaError_t launch_stream(const moe_config& c, const void* x, const void*
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const int per_sm = smem <= 64 * 1024 ? 3 : (smem <= 100 * 1024 ? 2 : 1);
-  int blocks = ceil_div(c.T, 8);
-  if (blocks > num_sms() * per_sm) blocks = num_sms() * per_sm;
-  router_logits_stream<EP><<<blocks, 256, smem, s>>>((const uint4*)x, (const uint4*)w_gate, logits,
+  // one CTA of 16 warps per SM: the router weights are staged once per SM, and each warp
+  // then streams its share of the token rows
+  int blocks = ceil_div(c.T, 16);
+  if (blocks > num_sms()) blocks = num_sms();
+  router_logits_stream<EP><<<blocks, 512, smem, s>>>((const uint4*)x, (const uint4*)w_gate, logits,
                                                      c.T, d8, c.E);
   return cudaGetLastError();
 }
@@ -566,7 +567,7 @@ __global__ void __launch_bounds__(1024) aux_final_kernel(const float* part_P,
 }
 
 int aux_blocks(const moe_config& c) {
-  int b = ceil_div(c.T, kAuxWarps * 8);
+  int b = ceil_div(c.T, kAuxWarps * 2);
   return b < 1 ? 1 : (b > 512 ? 512 : b);
 }
 
