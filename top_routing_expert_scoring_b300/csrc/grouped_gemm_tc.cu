@@ -15,7 +15,8 @@
 //     accumulators (2 x 256 columns) let the epilogue of one tile overlap the MMAs of the next;
 //   * GEMM 1 puts 128 gate rows and the matching 128 up rows of W13 in one B tile, so one
 //     N=256 MMA yields both halves and the epilogue forms SiLU(gate) * up directly;
-//   * rows of an M tile past its expert's end are computed and never stored;
+//   * rows of an M tile past its expert's end are computed and never stored; an expert's last
+//     tile with <= 64 rows runs as an M = 64 MMA, halving its wasted tensor work;
 //   * every mbarrier wait is bounded (about 2 s); on expiry the CTA records MOE_ERR_TIMEOUT in
 //     the status word, stops its loops, waits (bounded) for its own copies and MMAs in flight,
 //     frees TMEM and returns.
@@ -195,11 +196,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------- MMA issuer ---------------------------------------------
-    const uint32_t idesc = idesc_bf16_f32(BM, p.bn);
+    const uint32_t idesc_full = idesc_bf16_f32(BM, p.bn);
+    const uint32_t idesc_half = idesc_bf16_f32(64, p.bn);
     int stage = 0, acc = 0;
     uint32_t ph = 0, aph = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      // an expert's last tile with <= 64 rows runs as an M = 64 MMA (half the tensor work)
+      const uint32_t idesc = decode_tile(tile, p).rows <= 64 ? idesc_half : idesc_full;
       if (!wait_bounded(tempty0 + 8 * acc, aph ^ 1u, abort_flag, p.st, 2, true)) {
         ok = false;
         break;
@@ -247,10 +251,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * 256) +
                           (static_cast<uint32_t>(q * 32) << 16);
-      const bool live = r < ti.rows;
+      // M = 128: row r = 32q + lane sits in TMEM lane r.  M = 64: rows 16q .. 16q+15 sit in the
+      // first 16 lanes of the warp's 32-lane quarter.
+      const bool half = ti.rows <= 64;
+      const int row = half ? q * 16 + lane : r;
+      const bool live = half ? (lane < 16 && row < ti.rows) : (r < ti.rows);
       if (p.swiglu) {
         __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
-                              static_cast<size_t>(ti.row0 + r) * p.ldo + ti.nt * 128;
+                              static_cast<size_t>(ti.row0 + row) * p.ldo + ti.nt * 128;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t gr[32], ur[32];
@@ -275,7 +283,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       } else if (p.out_f32) {
-        float* orow = static_cast<float*>(p.out) + static_cast<size_t>(ti.row0 + r) * p.ldo +
+        float* orow = static_cast<float*>(p.out) + static_cast<size_t>(ti.row0 + row) * p.ldo +
                       ti.nt * p.bn;
         const int nchunks = p.bn / 32;
 #pragma unroll 1
@@ -291,7 +299,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       } else {
         __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
-                              static_cast<size_t>(ti.row0 + r) * p.ldo + ti.nt * p.bn;
+                              static_cast<size_t>(ti.row0 + row) * p.ldo + ti.nt * p.bn;
         const int nchunks = p.bn / 32;
 #pragma unroll 1
         for (int c = 0; c < nchunks; ++c) {

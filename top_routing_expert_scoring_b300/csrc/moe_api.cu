@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 
 #include "common.cuh"
@@ -43,9 +44,15 @@ int rows_max(const moe_config& c) { return c.T * c.k; }
 
 // Decode regime: bf16 with few rows per expert (<= 64 on average); the swap-AB kernel streams
 // each touched expert's weights once with the tokens on the MMA's N side.
+// The environment variable MOE_B300_PATH=prefill|decode|auto overrides the choice (decode
+// still needs bf16, token choice and d % 256 == 0).
 bool decode_regime(const moe_config& c) {
-  return c.dtype == MOE_DTYPE_BF16 && c.routing == MOE_ROUTE_TOKEN_CHOICE &&
-         (long long)c.T * c.k <= 64ll * c.E && c.d_model % 256 == 0;
+  if (c.dtype != MOE_DTYPE_BF16 || c.routing != MOE_ROUTE_TOKEN_CHOICE || c.d_model % 256 != 0)
+    return false;
+  const char* env = getenv("MOE_B300_PATH");
+  if (env && strcmp(env, "decode") == 0) return true;
+  if (env && strcmp(env, "prefill") == 0) return false;
+  return (long long)c.T * c.k <= 64ll * c.E;
 }
 
 bool decode_split_possible(const moe_config& c) {
