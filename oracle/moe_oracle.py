@@ -31,7 +31,13 @@ design notes of the repository):
   * expert-choice: C = T*k/E tokens per expert, selected by the raw logit column
     ([G] §2.2 ExpertChoiceRouter code block), weight = softmax probability p[t, e]
     (parity of the weights unpinned: the page returns raw logits);
-  * expert FFN = SwiGLU (SiLU(x W1) * (x W3)) W2 without biases ([L17] §5.2).
+  * expert FFN = SwiGLU (SiLU(x W1) * (x W3)) W2 without biases ([L17] §5.2);
+  * router backward: the loss is alpha * L_balance + beta * z + <d_w, w> with f and the
+    selection held fixed ([R] §3.4: f is not differentiable); the z-loss gradient uses the
+    softmax of the logits in both scoring modes;
+  * bias update: the load of an expert is its number of selections before capacity drops, the
+    target is the mean load T*k/E, and a load equal to it leaves the bias unchanged ([A]
+    update_bias code block; [L17] §3.4).
 """
 from __future__ import annotations
 
@@ -325,6 +331,89 @@ def aux_stats_from_counts(g32: np.ndarray, counts: np.ndarray, E: int, score: st
     k = counts.sum() / T
     return {"f": f, "P": P, "l_balance": L, "l_balance_per_k": L / k if k else 0.0, "z_loss": z,
             "counts": counts.astype(np.int64)}
+
+
+# ----------------------------------------------------------------------------------------------
+# Router-side backward and the selection-bias update ([R] §3.4; [L17] §3.2 and §3.4;
+# [A] load_balancing_loss, router_z_loss, loss_free_balancing_routing and update_bias code blocks)
+# ----------------------------------------------------------------------------------------------
+def router_backward(g32: np.ndarray, idx: np.ndarray, d_w, f, alpha: float, beta: float,
+                    score: str = "softmax", renormalize: bool = True, route_scale: float = 1.0):
+    """Gradient dL/dg [T, E] (float64) of the router-side loss
+
+        L = alpha * E * sum_i f_i P_i  +  beta * z  +  sum_{t,j} d_w[t, j] * w[t, j]
+
+    with respect to the logits g, the selection idx [T, k] and the frequencies f [E] held fixed:
+    f_i is a count and Top-k a selection, so the balance term reaches g only through P_i
+    ([R] §3.4; [L17] §3.2), and the sigmoid route's bias only enters the selection ([L17] §3.4).
+
+      P_i = (1/T) sum_t prob[t, i], prob = softmax(g) or s / sum(s) with s = sigmoid(g)
+      z   = (1/T) sum_t lse_t^2, lse_t = logsumexp(g_t)      (both scoring modes)
+      w   = route_scale * v_S / sum_S v  (renormalize) or route_scale * v_S, v = p or s
+      d_w = upstream gradient of the routing weights (None: that term is absent)
+
+    Chain rule, step by step: the balance term gives dL/dprob[t, i] = alpha * E * f_i / T; the
+    weights give dL/dv on the selected entries; softmax maps a gradient G on p to
+    p * (G - <G, p>), the normalisation q = s / sum(s) maps c to (c - <c, q>) / sum(s), the
+    sigmoid multiplies by s (1 - s); the z-loss adds beta * (2/T) * lse_t * p.
+    """
+    g = np.asarray(g32, F64)
+    T, E = g.shape
+    idx64 = np.asarray(idx).astype(np.int64)
+    p = softmax(g)
+    m = g.max(axis=1, keepdims=True)
+    lse = m[:, 0] + np.log(np.exp(g - m).sum(axis=1))
+    v = p if score == "softmax" else sigmoid(g)
+
+    dv = np.zeros((T, E), F64)                          # dL/dv from the routing weights
+    if d_w is not None:
+        dW = np.asarray(d_w, F64)
+        vS = np.take_along_axis(v, idx64, axis=1)
+        if renormalize:
+            sumS = vS.sum(axis=1, keepdims=True)
+            wS = route_scale * vS / sumS
+            dvS = (route_scale * dW - (dW * wS).sum(axis=1, keepdims=True)) / sumS
+        else:
+            dvS = route_scale * dW
+        np.put_along_axis(dv, idx64, dvS, axis=1)        # a token's k experts are distinct
+
+    c = np.zeros(E, F64) if f is None else alpha * E * np.asarray(f, F64) / T
+    if score == "softmax":
+        G = dv + c[None, :]                              # dL/dp
+        dg = p * (G - (G * p).sum(axis=1, keepdims=True))
+    else:
+        s = v
+        ssum = s.sum(axis=1, keepdims=True)
+        q = s / ssum
+        ds = dv + (c[None, :] - (c[None, :] * q).sum(axis=1, keepdims=True)) / ssum
+        dg = ds * s * (1.0 - s)
+    dg = dg + beta * (2.0 / T) * lse[:, None] * p
+    return dg
+
+
+def router_param_grads(x: np.ndarray, w_gate: np.ndarray, dg: np.ndarray):
+    """With g = x W_gate^T: dL/dW_gate = dg^T x  [E, d] and dL/dx = dg W_gate  [T, d]
+    (float64)."""
+    dg = np.asarray(dg, F64)
+    return dg.T @ np.asarray(x, F64), dg @ np.asarray(w_gate, F64)
+
+
+def bias_update(bias: np.ndarray, counts: np.ndarray, T: int, k: int, gamma: float):
+    """One step of the loss-free balancing bias rule ([L17] §3.4; [A] update_bias code block):
+    an expert whose load is above the mean load T*k/E gets b -= gamma, one below gets
+    b += gamma, one exactly at the mean keeps b.  The load is the number of (token, choice)
+    selections before any capacity drop, compared exactly as integers (counts * E vs T * k).
+    The bias is float32 state and the update is one float32 addition.
+    """
+    b = np.asarray(bias, F32).copy()
+    counts = np.asarray(counts, np.int64)
+    E = len(b)
+    over = counts * E > T * k
+    under = counts * E < T * k
+    g32 = F32(gamma)
+    b[over] = (b[over] - g32).astype(F32)
+    b[under] = (b[under] + g32).astype(F32)
+    return b
 
 
 def expected_distinct_experts(E: int, k: int, B: int) -> float:
