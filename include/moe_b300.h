@@ -224,6 +224,61 @@ int moe_workspace_views(const moe_config* cfg, void* ws, float** logits, int32_t
  * moe_sync_status().  Exists so tests can exercise the timeout path without a fault. */
 int moe_selftest_timeout(void* ws, int32_t limit_us, void* stream);
 
+/* ---------------------------------------------------------------------------------------------
+ * Router-side backward.
+ *
+ * Differentiates  L = alpha * L_balance + beta * z + sum_{t,j} d_topk_w[t,j] * topk_w[t,j]
+ * with respect to the router logits, the gate weights and the input, holding the selection
+ * and the frequencies f fixed:
+ *   - L_balance = E * sum_i f_i P_i.  f_i is a count, so the gradient reaches the router only
+ *     through P_i ("MoE 路由数学" §3.4; "Systems for Mixture-of-Experts Models" §3.2).
+ *     P_i is the token mean of softmax(g) (softmax scoring) or of s_i / sum_j s_j with
+ *     s = sigmoid(g) (sigmoid scoring).
+ *   - z = mean over tokens of logsumexp(g_t)^2 (router_z_loss code block of "Mixture of
+ *     Experts 架构"), in both scoring modes.
+ *   - topk_w are the routing weights as moe_forward computes them (renormalised, times
+ *     route_scale); the sigmoid route's bias only enters the selection and gets no gradient
+ *     ("Systems for Mixture-of-Experts Models" §3.4).
+ *
+ * Arguments (device pointers, caller-owned, row-major):
+ *   x         [T, d_model] bf16 or fp32 (cfg->dtype), the router input of the forward
+ *   w_gate    [E, d_model] same type, the router weight
+ *   logits    [T, E] fp32, the forward's logits (moe_router_topk, or moe_workspace_views)
+ *   topk_idx  [T, k] int32, the forward's selection.  May be NULL when d_topk_w is NULL.
+ *   d_topk_w  [T, k] fp32 upstream gradient of topk_w, or NULL (that term is absent)
+ *   f         [E] fp32 frequencies as moe_forward / moe_aux_stats return them (count / T, or
+ *             any other normalisation the caller's loss uses).  May be NULL when alpha == 0.
+ *   alpha, beta  loss coefficients (finite)
+ *   d_logits  [T, E] fp32 out: dL/dg, or NULL
+ *   d_w_gate  [E, d_model] fp32 out: dL/dW_gate (required)
+ *   d_x       [T, d_model] fp32 out: dL/dx through the router, or NULL
+ *   ws        workspace of moe_router_backward_workspace_size bytes, 256-byte aligned.  Its
+ *             first bytes hold the device status word that moe_sync_status reads.
+ * Precision: dL/dg in fp32; with bf16 activations the two gradient GEMMs take dL/dg rounded
+ * once to bf16 as their tensor-core operand (fp32 accumulate), so each product carries a
+ * relative error <= 2^-8.  With fp32 activations they run in fp32.  Results are
+ * deterministic (fixed summation order).
+ * Errors: MOE_ERR_ARG for NULL required pointers, a NULL f with alpha != 0, non-finite
+ * coefficients; MOE_ERR_UNSUPPORTED for expert-choice configurations; MOE_ERR_WORKSPACE for
+ * a missing or misaligned workspace.  An expert index outside [0, E) in topk_idx is skipped
+ * and recorded in the status word as MOE_ERR_ARG (detail = token). */
+int moe_router_backward_workspace_size(const moe_config* cfg, size_t* bytes);
+int moe_router_backward(const moe_config* cfg, const void* x, const void* w_gate,
+                        const float* logits, const int32_t* topk_idx, const float* d_topk_w,
+                        const float* f, float alpha, float beta, float* d_logits,
+                        float* d_w_gate, float* d_x, void* ws, void* stream);
+
+/* One step of the loss-free balancing bias rule ("Systems for Mixture-of-Experts Models"
+ * §3.4; update_bias code block of "Mixture of Experts 架构"): for each expert i, with
+ * load_i = f_i * T recovered exactly (f as moe_forward returns it, count / T rounded once to
+ * fp32) and the mean load T*k/E,
+ *   load_i > mean: bias[i] -= gamma;   load_i < mean: bias[i] += gamma;   equal: unchanged.
+ * The load counts selections before capacity drops.  f [E] fp32 and bias [E] fp32 (in/out)
+ * are device pointers.  Errors: MOE_ERR_ARG for NULL pointers or a non-finite gamma;
+ * MOE_ERR_SHAPE when T*k >= 2^23 (the exact recovery of the load needs T*k < 2^23). */
+int moe_bias_update(const moe_config* cfg, const float* f, float* bias, float gamma,
+                    void* stream);
+
 #ifdef __cplusplus
 }
 #endif

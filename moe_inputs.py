@@ -13,6 +13,7 @@ or trained weights are involved: every tensor is i.i.d. random,
   W_gate ~ N(0, 1/d)                    [E, d]   (row e = expert e's router vector)
   W1, W3 ~ N(0, 1/d), W2 ~ N(0, 1/F)    per expert, SwiGLU
   bias   ~ U(-0.1, 0.1)                 [E]      (selection-only bias, sigmoid scoring)
+  d_topk_w ~ N(0, 1)                    [T, k]   (upstream gradient of the routing weights)
 
 Each tensor is drawn from its own torch.Generator, seeded from (workload, tensor name, seed), so
 the draws do not depend on the order in which tensors are made.  Large weight sets may be drawn
@@ -167,6 +168,17 @@ def make_inputs(wl: Workload, seed: int = 0, device: str = "cpu", T: int | None 
     d = make_router_inputs(wl, seed, device, T)
     d.update(make_expert_weights(wl, seed, device))
     return d
+
+
+def make_grad_inputs(wl: Workload, seed: int = 0, device: str = "cpu", T: int | None = None):
+    """Inputs of the router-side backward and the bias update: an upstream gradient of the
+    routing weights d_topk_w ~ N(0, 1) [T, k] float32 and a bias state ~ U(-0.1, 0.1) [E]
+    float32."""
+    T = wl.T if T is None else T
+    d_w = _normal((T, wl.k), 1.0, _gen(wl.name, "d_topk_w", seed, device), device, torch.float32)
+    g = _gen(wl.name, "bias_state", seed, device)
+    b = (torch.rand((wl.E,), generator=g, device=device, dtype=torch.float32) * 2 - 1) * 0.1
+    return {"d_topk_w": d_w.contiguous(), "bias_state": b}
 
 
 def to_f64(t: torch.Tensor | None):

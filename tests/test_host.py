@@ -109,3 +109,41 @@ def test_workspace_grows_with_tokens():
     m = _lib()
     wl = moe_inputs.workload("mixtral")
     assert m.workspace_size(config_of(wl, T=8192)) > m.workspace_size(config_of(wl, T=4096))
+
+
+def test_router_backward_rejections_before_any_launch():
+    m = _lib()
+    P = ctypes.c_void_p
+    fake, ws = P(0x1000), P(0x100000)
+    f = ctypes.c_float
+    cfg = config_of(moe_inputs.workload("mixtral"), T=64)
+    bw = m.lib.moe_router_backward
+    args = lambda **kw: [kw.get(n, fake) for n in ("x", "w", "g", "idx", "dw", "f")] + [
+        f(kw.get("alpha", 0.01)), f(kw.get("beta", 0.001))] + [
+        kw.get(n, fake) for n in ("dlog", "dW", "dx", "ws")] + [None]
+    assert bw(ctypes.byref(cfg), *args(x=None, ws=ws)) == -1
+    assert bw(ctypes.byref(cfg), *args(dW=None, ws=ws)) == -1
+    assert bw(ctypes.byref(cfg), *args(f=None, ws=ws)) == -1           # alpha != 0 needs f
+    assert bw(ctypes.byref(cfg), *args(idx=None, ws=ws)) == -1         # d_topk_w needs idx
+    assert bw(ctypes.byref(cfg), *args(alpha=float("nan"), ws=ws)) == -1
+    assert bw(ctypes.byref(cfg), *args(ws=None)) == -4
+    assert bw(ctypes.byref(cfg), *args(ws=P(0x100001))) == -4
+    ec = config_of(moe_inputs.workload("dsmoe16b_ec"), T=64)
+    assert bw(ctypes.byref(ec), *args(ws=ws)) == -3
+    ub = m.lib.moe_bias_update
+    assert ub(ctypes.byref(cfg), None, fake, f(0.001), None) == -1
+    assert ub(ctypes.byref(cfg), fake, fake, f(float("inf")), None) == -1
+    big = config_of(moe_inputs.workload("mixtral"), T=1 << 20)
+    big.k = 8
+    assert ub(ctypes.byref(big), fake, fake, f(0.001), None) == -2
+
+
+def test_router_backward_workspace_sizes():
+    m = _lib()
+    wl = moe_inputs.workload("v3")
+    small = m.router_backward_workspace_size(config_of(wl, T=1024))
+    large = m.router_backward_workspace_size(config_of(wl, T=8192))
+    # at least the two bf16 copies of dL/dg ([T, E64] and [E64, T64])
+    assert large >= 2 * 8192 * 256 * 2 and large > small
+    tiny = moe_inputs.workload("tiny")
+    assert m.router_backward_workspace_size(config_of(tiny)) >= tiny.T * tiny.E * 4

@@ -77,6 +77,10 @@ _SIGS = {
     "moe_forward_timed": ([_CFG] + [_P] * 19, ctypes.c_int),
     "moe_workspace_views": ([_CFG, _P] + [ctypes.POINTER(_P)] * 5, ctypes.c_int),
     "moe_selftest_timeout": ([_P, ctypes.c_int32, _P], ctypes.c_int),
+    "moe_router_backward_workspace_size": ([_CFG, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
+    "moe_router_backward": ([_CFG] + [_P] * 6 + [ctypes.c_float, ctypes.c_float] + [_P] * 5,
+                            ctypes.c_int),
+    "moe_bias_update": ([_CFG, _P, _P, ctypes.c_float, _P], ctypes.c_int),
 }
 EXPORTED = tuple(_SIGS)
 
@@ -242,3 +246,29 @@ def moe_workspace_views(cfg, ws):
 def moe_selftest_timeout(ws, limit_us, stream=None):
     _check("moe_selftest_timeout", lib.moe_selftest_timeout(_ptr(ws), int(limit_us),
                                                             _stream(stream)))
+
+
+def router_backward_workspace_size(cfg: MoeConfig) -> int:
+    n = ctypes.c_size_t()
+    _check("moe_router_backward_workspace_size",
+           lib.moe_router_backward_workspace_size(ctypes.byref(cfg), ctypes.byref(n)))
+    return n.value
+
+
+def router_backward_workspace(cfg: MoeConfig, device="cuda"):
+    """A zeroed device workspace for moe_router_backward (torch allocation)."""
+    import torch
+    return torch.zeros(router_backward_workspace_size(cfg), dtype=torch.uint8, device=device)
+
+
+def moe_router_backward(cfg, x, w_gate, logits, topk_idx, d_topk_w, f, alpha, beta, d_logits,
+                        d_w_gate, d_x, ws, stream=None):
+    _check("moe_router_backward", lib.moe_router_backward(
+        ctypes.byref(cfg), _ptr(x), _ptr(w_gate), _ptr(logits), _ptr(topk_idx), _ptr(d_topk_w),
+        _ptr(f), float(alpha), float(beta), _ptr(d_logits), _ptr(d_w_gate), _ptr(d_x), _ptr(ws),
+        _stream(stream)))
+
+
+def moe_bias_update(cfg, f, bias, gamma, stream=None):
+    _check("moe_bias_update", lib.moe_bias_update(ctypes.byref(cfg), _ptr(f), _ptr(bias),
+                                                  float(gamma), _stream(stream)))

@@ -369,17 +369,22 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-bool make_map_box(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
-                  uint32_t box_rows) {
+bool make_map_strided(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                      uint64_t row_stride, uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
+  cuuint64_t strides[1] = {row_stride * 2};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_map_box(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                  uint32_t box_rows) {
+  return make_map_strided(m, base, rows, cols, cols, box_rows);
 }
 
 // 2-D bf16 tensor [rows, cols] (cols contiguous) read in boxes of 64 columns x 128 rows.

@@ -128,6 +128,9 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols);
 // Same with a box of 64 columns x box_rows rows (box_rows a multiple of 8, <= 256).
 bool make_map_box(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                   uint32_t box_rows);
+// Same for rows that lie row_stride elements apart (row_stride * 2 a multiple of 16 bytes).
+bool make_map_strided(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                      uint64_t row_stride, uint32_t box_rows);
 
 }  // namespace tc
 }  // namespace moe
