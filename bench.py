@@ -314,6 +314,93 @@ def decode_sweep(args):
         torch.cuda.empty_cache()
 
 
+def router_backward_bytes_flops(wl):
+    """Algorithmic bytes and FLOPs of one router-side backward (moe_router_backward with every
+    output): reads logits, selection, d_topk_w, f, x and W_gate; writes dL/dg, dW_gate and dx
+    (float32).  FLOPs: the two gradient products, 2 T d E each."""
+    T, d, E, k = wl.T, wl.d, wl.E, wl.k
+    rd = T * E * 4 + T * k * 8 + E * 4 + T * d * 2 + E * d * 2
+    wr = T * E * 4 + E * d * 4 + T * d * 4
+    return {"bytes": rd + wr, "flops": 4 * T * d * E}
+
+
+def router_backward_sweep(args):
+    """Router-side backward (dL/dg, dW_gate, dx) per workload: CUDA events around each call, L2
+    flushed (256 MB write) between calls outside the events.  The routing inputs come from the
+    forward's own router call."""
+    import torch
+    import moe_inputs
+    import top_routing_expert_scoring_b300 as m
+    torch.cuda.set_device(0)
+    peaks, peak_kind = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    tflops = float(peaks["bf16_tflops"])
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for name in args.backward_workloads.split(","):
+        wl = moe_inputs.workload(name)
+        T, E, k, d = wl.T, wl.E, wl.k, wl.d
+        cfg = m.make_config(T, d, E, k, wl.F, wl.F_sh, wl.score, wl.routing, wl.n_groups,
+                            wl.topk_groups, wl.renormalize, wl.route_scale, wl.capacity_factor,
+                            wl.dtype)
+        inp = moe_inputs.make_router_inputs(wl, device="cuda")
+        gi = moe_inputs.make_grad_inputs(wl, device="cuda")
+        ws_f = m.workspace(cfg)
+        logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+        idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        f = torch.empty(E, dtype=torch.float32, device="cuda")
+        P = torch.empty(E, dtype=torch.float32, device="cuda")
+        lb = torch.empty(1, dtype=torch.float32, device="cuda")
+        z = torch.empty(1, dtype=torch.float32, device="cuda")
+        m.moe_router_topk(cfg, inp["x"], inp["w_gate"], inp["bias"], logits, idx, w, ws_f)
+        m.moe_aux_stats(cfg, logits, idx, f, P, lb, z, ws_f)
+        del ws_f
+        ws = m.router_backward_workspace(cfg)
+        d_logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+        dW = torch.empty((E, d), dtype=torch.float32, device="cuda")
+        dx = torch.empty((T, d), dtype=torch.float32, device="cuda")
+
+        def call():
+            m.moe_router_backward(cfg, inp["x"], inp["w_gate"], logits, idx, gi["d_topk_w"], f,
+                                  0.01, 0.001, d_logits, dW, dx, ws)
+        for _ in range(max(3, args.warmup)):
+            call()
+        torch.cuda.synchronize()
+        reps = args.backward_steps
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        with ClockSampler(torch.cuda.current_device()) as clk:
+            clk.start()
+            for a, b in ev:
+                flush.fill_(1)
+                a.record()
+                call()
+                b.record()
+            torch.cuda.synchronize()
+        st = m.sync_status(ws)
+        if st != 0:
+            raise RuntimeError(f"device status {st}: {m.status_string(st)}")
+        ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+        bf = router_backward_bytes_flops(wl)
+        gbs = bf["bytes"] / (ms / 1e3) / 1e9
+        tfs = bf["flops"] / (ms / 1e3) / 1e12
+        hbm_ms = bf["bytes"] / (hbm * 1e9) * 1e3
+        tc_ms = 4 * T * d * ((E + 63) // 64 * 64) / (tflops * 1e12) * 1e3
+        print(json.dumps({
+            "metric": "router-side backward (dL/dg, dW_gate, dx) tokens/s; % of HBM roofline",
+            "mode": "router_backward", "workload": name, "value": T / (ms / 1e3),
+            "unit": "tokens/s", "ms_per_call_median": ms, "steps": reps, "dtype": wl.dtype,
+            "data": "synthetic",
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                         "frac": gbs / hbm, "peak_kind": f"{peak_kind} copy bandwidth",
+                         "algorithmic_bytes": bf["bytes"]},
+            "floors_ms": {"hbm": hbm_ms, "tensor_padded_E64": tc_ms},
+            "tflops_algorithmic": tfs,
+            "clocks": clk.summary(), "l2": "256 MB buffer written between calls"}))
+        del inp, gi, ws, logits, idx, w, d_logits, dW, dx
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -329,12 +416,20 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=100)
     ap.add_argument("--no-graphs", action="store_true",
                     help="decode sweep: launch each forward directly instead of a CUDA graph")
+    ap.add_argument("--router-backward", action="store_true",
+                    help="time the router-side backward instead of the forward (one line per "
+                         "workload)")
+    ap.add_argument("--backward-workloads", default="mixtral,dsmoe16b,v3")
+    ap.add_argument("--backward-steps", type=int, default=50)
     ap.add_argument("--tokens", type=int, default=0,
                     help="override T (smaller cases for profiler captures; not a bench line)")
     args = ap.parse_args()
 
     if args.decode_sweep:
         decode_sweep(args)
+        return
+    if args.router_backward:
+        router_backward_sweep(args)
         return
 
     import torch

@@ -522,39 +522,54 @@ __global__ void __launch_bounds__(kAuxWarps * 32) aux_partial_kernel(AuxArgs a) 
   write_block_stats<V>(accP, cnt, zacc, E, a.part_P, a.part_cnt, a.part_z, aux_smem);
 }
 
-// One warp per expert: lanes sum blocks lane, lane+32, ... (float32 for P and z, integers for
-// counts), then a butterfly in a fixed order; warp 0 also sums the z partials.  Deterministic
-// for a given block count.  (No float64: its throughput on this part is a tiny fraction.)
+// Lanes own consecutive experts (coalesced reads of a partial row); the 32 warps split into
+// G = 32-expert groups x W = 32/G block strides.  Each thread sums blocks sub, sub+W, ... of its
+// expert (float32 for P, integers for counts), then thread (sub 0) adds the W sums in order;
+// warp 0 also sums the z partials.  Deterministic for a given block count.  (No float64: its
+// throughput on this part is a tiny fraction.)
 __global__ void __launch_bounds__(1024) aux_final_kernel(const float* part_P,
                                                         const int32_t* part_cnt,
                                                         const float* part_z, int nblk, int T,
                                                         int E, int ec_C, float* f, float* P,
                                                         float* l_balance, float* z_loss) {
+  __shared__ float sp[1024];
+  __shared__ int sc[1024];
   __shared__ float prod[256];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const float invT = 1.0f / (float)T;
-  for (int e = warp; e < E; e += nw) {
-    float p = 0.f;
-    int c = 0;
-    for (int b = lane; b < nblk; b += 32) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int G = 1;
+  while (G * 32 < E) G <<= 1;                  // expert groups of 32 (E <= 256: G <= 8)
+  const int W = 32 / G;                        // warps per group = block stride
+  const int g = warp % G, sub = warp / G;
+  const int e = g * 32 + lane;
+  float p = 0.f;
+  int c = 0;
+  if (e < E) {
+    for (int b = sub; b < nblk; b += W) {
       p += part_P[(size_t)b * E + e];
       c += part_cnt[(size_t)b * E + e];
     }
-    p = warp_sum(p);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-    if (ec_C > 0) c = ec_C;
-    const float fe = (float)c * invT, Pe = p * invT;
-    if (lane == 0) {
-      if (f) f[e] = fe;
-      if (P) P[e] = Pe;
-      prod[e] = fe * Pe;
+  }
+  sp[sub * 32 * G + e] = p;
+  sc[sub * 32 * G + e] = c;
+  __syncthreads();
+  const float invT = 1.0f / (float)T;
+  if (sub == 0 && e < E) {
+    float ps = 0.f;
+    int cs = 0;
+    for (int w = 0; w < W; ++w) {
+      ps += sp[w * 32 * G + e];
+      cs += sc[w * 32 * G + e];
     }
+    if (ec_C > 0) cs = ec_C;
+    const float fe = (float)cs * invT, Pe = ps * invT;
+    if (f) f[e] = fe;
+    if (P) P[e] = Pe;
+    prod[e] = fe * Pe;
   }
   __syncthreads();
   if (warp == 0) {
     float acc = 0.f;
-    for (int e = lane; e < E; e += 32) acc += prod[e];
+    for (int x = lane; x < E; x += 32) acc += prod[x];
     acc = warp_sum(acc);
     float z = 0.f;
     for (int b = lane; b < nblk; b += 32) z += part_z[b];

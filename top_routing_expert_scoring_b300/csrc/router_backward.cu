@@ -35,12 +35,14 @@
 namespace moe {
 namespace {
 
-constexpr int kBwTokens = 64;     // tokens per CTA of the scores kernel
+constexpr int kBwTokens = 16;     // tokens per CTA of the scores kernel (2 per warp)
 constexpr int kBwWarps = 8;
-constexpr int kTPad = kBwTokens + 2;   // shared row of the transposed tile (conflict-free)
+// shared row of the transposed tile: 18 bf16 = 9 words, odd, so the 32 lanes writing 32
+// experts of one token hit 32 different banks
+constexpr int kTPad = kBwTokens + 2;
 
 int e64_of(int E) { return (E + 63) / 64 * 64; }
-long long t64_of(int T) { return ((long long)T + 63) / 64 * 64; }
+long long t64_of(int T) { return ((long long)T + 63) / 64 * 64; }   // >= every CTA's tokens
 
 struct ScoresArgs {
   int T, E, E64, k, score, renorm;
@@ -198,10 +200,12 @@ __global__ void __launch_bounds__(kBwWarps * 32) router_bw_scores_kernel(const S
   }
   if (a.dgT) {
     __syncthreads();
-    // row e of the transposed block: 64 tokens = 32 words, one per lane
-    for (int e = warp; e < a.E64; e += kBwWarps) {
-      const uint32_t wv = *reinterpret_cast<const uint32_t*>(&sT[e][2 * lane]);
-      *reinterpret_cast<uint32_t*>(a.dgT + static_cast<size_t>(e) * a.T64 + t_base + 2 * lane) =
+    // row e of the transposed block: 16 tokens = 8 words = one 32-byte sector; a warp writes
+    // 4 rows per instruction, 8 lanes per row
+    const int sub = lane >> 3, wd = lane & 7;
+    for (int e = warp * 4 + sub; e < a.E64; e += kBwWarps * 4) {
+      const uint32_t wv = *reinterpret_cast<const uint32_t*>(&sT[e][2 * wd]);
+      *reinterpret_cast<uint32_t*>(a.dgT + static_cast<size_t>(e) * a.T64 + t_base + 2 * wd) =
           wv;
     }
   }
@@ -224,7 +228,8 @@ constexpr int MN_ATOM = 64 * BK * 2;          // one 64-column MN-major box: 8 K
 constexpr int TMEM_COLS = 512;
 constexpr int THREADS = 192;
 constexpr int NBARS = 2 * STAGES + 5;
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * (A_STAGE + B_STAGE) + 256;
+constexpr int STAGE_OUT = 32 * 32 * 4;       // per epilogue warp: 32 rows x 32 fp32 columns
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * (A_STAGE + B_STAGE) + 256 + 4 * STAGE_OUT;
 
 struct Params {
   int M, N, KB;           // rows of D, MMA N, K blocks of 64
@@ -399,6 +404,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------- epilogue -----------------------------------------------
     const int q = warp & 3;
     const int r = q * 32 + lane;
+    float* stage_out = reinterpret_cast<float*>(sB + STAGES * B_STAGE + 256) +
+                       (warp - 2) * (STAGE_OUT / 4);
     int acc = 0;
     uint32_t aph = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -417,14 +424,28 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int c = 0; c < p.N / 32; ++c) {
         uint32_t vr[32];
         tmem_ld32(tb + c * 32, vr);
-        if (!live) continue;
         if (p.out_mode == 0) {
-          float* orow = p.out + static_cast<size_t>(m) * p.ldo + n0 + c * 32;
-          uint4* dst = reinterpret_cast<uint4*>(orow);
+          // Through this warp's shared buffer so that each store instruction writes 4 rows x
+          // 128 contiguous bytes (full lines) instead of 32 rows x 16 bytes.  16-byte chunk j of
+          // row i sits at chunk j ^ (i & 7): conflict-free both ways.
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[v] = make_uint4(vr[4 * v], vr[4 * v + 1], vr[4 * v + 2], vr[4 * v + 3]);
-        } else {
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(stage_out + lane * 32 + ((j ^ (lane & 7)) << 2)) =
+                make_uint4(vr[4 * j], vr[4 * j + 1], vr[4 * j + 2], vr[4 * j + 3]);
+          __syncwarp();
+          const int jj = lane & 7;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int row = 4 * i + (lane >> 3);
+            const uint4 v =
+                *reinterpret_cast<const uint4*>(stage_out + row * 32 + ((jj ^ (row & 7)) << 2));
+            const int mr = ti.mt * BM + q * 32 + row;
+            if (mr < p.M)
+              *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(mr) * p.ldo + n0 + c * 32 +
+                                        jj * 4) = v;
+          }
+          __syncwarp();
+        } else if (live) {
           // column n of this row goes to row n of the transposed partial: lanes hold
           // consecutive m, so each store instruction writes 128 contiguous bytes
 #pragma unroll
