@@ -416,6 +416,98 @@ def bias_update(bias: np.ndarray, counts: np.ndarray, T: int, k: int, gamma: flo
     return b
 
 
+# ----------------------------------------------------------------------------------------------
+# FP8 (E4M3) expert weights and activations for decode ("Systems for Mixture-of-Experts Models"
+# §1.4: DeepSeek-V3 keeps its weights in FP8; "MoE 推理优化深入" §4.2: per-expert quantisation)
+# ----------------------------------------------------------------------------------------------
+E4M3_MAX = 448.0
+
+
+def e4m3_round(v) -> np.ndarray:
+    """Nearest E4M3 value (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no infinities;
+    largest finite 448 = 1.75 * 2^8, smallest subnormal 2^-9), ties to the even mantissa, values
+    beyond 448 saturated to +-448.  Input float32 values, output float64 values on the grid."""
+    v = np.asarray(v, F32).astype(F64)
+    a = np.abs(v)
+    # spacing of the grid around a: 2^(e-3) in the binade [2^e, 2^(e+1)), e >= -6; 2^-9 below
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))          # a = m * 2^ex, m in [0.5, 1)
+    e = np.maximum(ex - 1, -6)
+    quantum = np.ldexp(1.0, e - 3)
+    r = np.rint(a / quantum) * quantum                   # np.rint: ties to even
+    r = np.minimum(r, E4M3_MAX)
+    return np.copysign(r, v)
+
+
+def quantize_rows_fp8(V: np.ndarray):
+    """Per-row E4M3 quantisation with the decisions in float32: amax = max |v| over the row,
+    inv = float32(448 / amax), code = e4m3(float32(v * inv)), scale = float32(amax / 448);
+    a row of zeros gets codes 0 and scale 0.  Returns (codes as float64 values [rows, cols],
+    scales float64 [rows]); the row is represented by codes * scale."""
+    V32 = np.asarray(V, F32)
+    amax = np.abs(V32).max(axis=1).astype(F32)
+    nz = amax > 0
+    inv = np.zeros_like(amax)
+    inv[nz] = (F32(E4M3_MAX) / amax[nz]).astype(F32)
+    scaled = (V32 * inv[:, None]).astype(F32)
+    codes = e4m3_round(scaled)
+    scale = np.zeros_like(amax)
+    scale[nz] = (amax[nz] / F32(E4M3_MAX)).astype(F32)
+    return codes, scale.astype(F64)
+
+
+def fp8_expert_weights(w13, w2, ws13=None, ws2=None):
+    """Quantised expert weights: every weight row (output channel) of W13 [E, 2F, d],
+    W2 [E, d, F] and of the shared expert gets its own scale.  Returns a dict of dequantised
+    float64 arrays with the same shapes (codes * scale)."""
+    def deq(W):
+        W = np.asarray(W, F64)
+        flat = W.reshape(-1, W.shape[-1])
+        c, s = quantize_rows_fp8(flat)
+        return (c * s[:, None]).reshape(W.shape)
+    out = {"w13": deq(w13), "w2": deq(w2), "ws13": None, "ws2": None}
+    if ws13 is not None:
+        out["ws13"] = deq(ws13)
+        out["ws2"] = deq(ws2)
+    return out
+
+
+def moe_forward_fp8(wl, x, w_gate, bias, wq, tokens=None):
+    """The layer with FP8 expert weights (dequantised, from fp8_expert_weights) and FP8
+    activations: every row that enters an expert GEMM (the token's x for the gate/up
+    projection, its h for the down projection) is quantised per row as in quantize_rows_fp8,
+    the products are exact in float64.  Routing, weights and statistics are those of the bf16
+    layer (the router runs in bf16).  h is formed in float64 and rounded to float32 before its
+    quantisation decision (the precision of the kernels).  tokens: evaluate only these tokens'
+    outputs (routing still over all T).  Returns (out rows [len(tokens) or T, d], route dict)."""
+    r = route(wl, x, w_gate, bias)
+    T = r["g32"].shape[0]
+    E = r["g32"].shape[1]
+    C = capacity(wl.capacity_factor, wl.k, T, E)
+    disp = dispatch(r["idx"], E, C)
+    toks = np.arange(T) if tokens is None else np.asarray(tokens)
+    xq, xs = quantize_rows_fp8(np.asarray(x, F64)[toks])
+    xd = xq * xs[:, None]                                  # dequantised token rows
+
+    def ffn(xrow, W13, W2):
+        F = W13.shape[0] // 2
+        gu = xrow @ W13.T
+        h = silu(gu[:, :F]) * gu[:, F:]
+        hq, hs = quantize_rows_fp8(h.astype(F32))
+        return (hq * hs[:, None]) @ W2.T
+
+    d = xd.shape[1]
+    out = np.zeros((len(toks), d), F64)
+    if wq["ws13"] is not None:
+        out += ffn(xd, wq["ws13"], wq["ws2"])
+    for e in range(E):
+        sel_t, sel_j = np.nonzero((r["idx"][toks] == e) & (disp["row_of"][toks] >= 0))
+        if len(sel_t) == 0:
+            continue
+        y = ffn(xd[sel_t], wq["w13"][e], wq["w2"][e])
+        out[sel_t] += r["w"][toks][sel_t, sel_j][:, None] * y
+    return out, r
+
+
 def expected_distinct_experts(E: int, k: int, B: int) -> float:
     """E * (1 - (1 - k/E)^B): experts touched by a batch of B tokens under uniform, independent
     routing ([L17] §1.4)."""
