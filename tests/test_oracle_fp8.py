@@ -94,16 +94,17 @@ def test_fp8_layer_with_identity_quantisation_is_the_bf16_layer(monkeypatch, cas
 @pytest.mark.parametrize("case", [dict(name="v3", T=24, d=256, E=16, F=256, F_shared=256),
                                   dict(name="mixtral", T=20, d=256, E=8, F=512)])
 def test_fp8_layer_error_against_bf16_layer(case):
-    """E4M3 keeps 4 significant bits: each quantised operand carries a relative error of up to
-    2^-4 (RMS about 2^-4/sqrt(3) x 0.7 for normal values), so the layer output moves by a few
-    percent of its RMS — clearly nonzero and well below the size of any structural mistake."""
+    """E4M3 keeps 4 significant bits: a value with significand m in [1, 2) is rounded by up to
+    2^-4/m relative, an RMS of about 2^-4 sqrt(E[1/m^2]/3) ~ 2.5% per operand.  Four operands
+    (x, W1|W3, h, W2) give ~5-6% of the output RMS: clearly nonzero and far below the size of
+    any structural mistake."""
     wl, h = _small(**case)
     want = O.moe_forward(wl, h["x"], h["w_gate"], h["bias"], h["w13"], h["w2"], h["ws13"],
                          h["ws2"])["out"]
     wq = O.fp8_expert_weights(h["w13"], h["w2"], h["ws13"], h["ws2"])
     got, _ = O.moe_forward_fp8(wl, h["x"], h["w_gate"], h["bias"], wq)
     rel = np.sqrt(np.mean((got - want) ** 2)) / np.sqrt(np.mean(want ** 2))
-    assert 0.005 < rel < 0.08, rel
+    assert 0.01 < rel < 0.10, rel
 
 
 def test_fp8_layer_token_subset_matches_full():
