@@ -279,6 +279,43 @@ int moe_router_backward(const moe_config* cfg, const void* x, const void* w_gate
 int moe_bias_update(const moe_config* cfg, const float* f, float* bias, float gamma,
                     void* stream);
 
+/* ---------------------------------------------------------------------------------------------
+ * FP8 (E4M3) expert weights for decode.
+ *
+ * A decode step is bound by reading the touched experts' weights ("Systems for
+ * Mixture-of-Experts Models" §1.4, which also notes that DeepSeek-V3 keeps its weights in FP8;
+ * "MoE 推理优化深入" §4.2 on quantised experts).  One-byte E4M3 weights halve those bytes.  The
+ * tensor cores multiply E4M3 by E4M3, so the activations entering each expert GEMM (the token's
+ * x, then its h) are quantised per row the same way on the fly.
+ *
+ * Quantisation of one row v (float32 decisions):
+ *   amax = max |v|;  inv = 448 / amax;  code = e4m3(v * inv);  scale = amax / 448
+ * with round to nearest even and saturation at +-448 (the largest finite E4M3 value); a row of
+ * zeros gets codes 0 and scale 0.  The row is represented by code * scale.
+ *
+ * moe_quantize_fp8: rows x cols bf16 (device, row-major, cols a multiple of 16) -> dst
+ * [rows, cols] E4M3 codes (one byte each) and scale [rows] fp32.  Use it once per weight
+ * tensor: W13 [E*2F, d], W2 [E*d, F], shared WS13 [2Fs, d], WS2 [d, Fs].  Errors: MOE_ERR_ARG
+ * (NULL pointer), MOE_ERR_SHAPE (rows < 1, cols < 16 or not a multiple of 16).
+ *
+ * moe_forward_fp8: the layer of moe_forward with the quantised expert weights (codes and
+ * scales as moe_quantize_fp8 writes them, in the layouts of moe_forward's w13/w2/ws13/ws2).
+ * Routing, statistics and combine are those of moe_forward (bf16 router); the expert GEMMs
+ * run on the decode kernels (weights on the MMA's M side, tokens on N) for every batch size,
+ * so the call is meant for decode-sized batches.  Requires cfg->dtype bf16 (activations),
+ * token choice and d_model % 256 == 0 (MOE_ERR_UNSUPPORTED / MOE_ERR_SHAPE otherwise).  The
+ * workspace is moe_fp8_workspace_size bytes, 256-byte aligned; its status word is read by
+ * moe_sync_status.  Other arguments and outputs as in moe_forward. */
+int moe_quantize_fp8(int64_t rows, int64_t cols, const void* src, uint8_t* dst, float* scale,
+                     void* stream);
+int moe_fp8_workspace_size(const moe_config* cfg, size_t* bytes);
+int moe_forward_fp8(const moe_config* cfg, const void* x, const void* w_gate, const float* bias,
+                    const uint8_t* w13_q, const float* w13_scale, const uint8_t* w2_q,
+                    const float* w2_scale, const uint8_t* ws13_q, const float* ws13_scale,
+                    const uint8_t* ws2_q, const float* ws2_scale, void* out, int32_t* topk_idx,
+                    float* topk_w, float* f, float* P, float* l_balance, float* z_loss,
+                    int32_t* n_dropped, void* ws, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

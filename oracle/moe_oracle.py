@@ -459,15 +459,10 @@ def fp8_expert_weights(w13, w2, ws13=None, ws2=None):
     """Quantised expert weights: every weight row (output channel) of W13 [E, 2F, d],
     W2 [E, d, F] and of the shared expert gets its own scale.  Returns a dict of dequantised
     float64 arrays with the same shapes (codes * scale)."""
-    def deq(W):
-        W = np.asarray(W, F64)
-        flat = W.reshape(-1, W.shape[-1])
-        c, s = quantize_rows_fp8(flat)
-        return (c * s[:, None]).reshape(W.shape)
-    out = {"w13": deq(w13), "w2": deq(w2), "ws13": None, "ws2": None}
+    out = {"w13": dequantized_fp8(w13), "w2": dequantized_fp8(w2), "ws13": None, "ws2": None}
     if ws13 is not None:
-        out["ws13"] = deq(ws13)
-        out["ws2"] = deq(ws2)
+        out["ws13"] = dequantized_fp8(ws13)
+        out["ws2"] = dequantized_fp8(ws2)
     return out
 
 
@@ -487,25 +482,58 @@ def moe_forward_fp8(wl, x, w_gate, bias, wq, tokens=None):
     toks = np.arange(T) if tokens is None else np.asarray(tokens)
     xq, xs = quantize_rows_fp8(np.asarray(x, F64)[toks])
     xd = xq * xs[:, None]                                  # dequantised token rows
-
-    def ffn(xrow, W13, W2):
-        F = W13.shape[0] // 2
-        gu = xrow @ W13.T
-        h = silu(gu[:, :F]) * gu[:, F:]
-        hq, hs = quantize_rows_fp8(h.astype(F32))
-        return (hq * hs[:, None]) @ W2.T
-
     d = xd.shape[1]
     out = np.zeros((len(toks), d), F64)
     if wq["ws13"] is not None:
-        out += ffn(xd, wq["ws13"], wq["ws2"])
+        out += fp8_ffn(xd, wq["ws13"], wq["ws2"])
     for e in range(E):
         sel_t, sel_j = np.nonzero((r["idx"][toks] == e) & (disp["row_of"][toks] >= 0))
         if len(sel_t) == 0:
             continue
-        y = ffn(xd[sel_t], wq["w13"][e], wq["w2"][e])
+        y = fp8_ffn(xd[sel_t], wq["w13"][e], wq["w2"][e])
         out[sel_t] += r["w"][toks][sel_t, sel_j][:, None] * y
     return out, r
+
+
+def fp8_ffn(xd, W13, W2):
+    """One SwiGLU expert on dequantised E4M3 token rows xd with dequantised weights W13 [2F, d]
+    and W2 [d, F]: h = SiLU(x W1) * (x W3) in float64, rounded to float32, quantised per row,
+    then y = h_q W2."""
+    F = W13.shape[0] // 2
+    gu = xd @ W13.T
+    h = silu(gu[:, :F]) * gu[:, F:]
+    hq, hs = quantize_rows_fp8(h.astype(F32))
+    return (hq * hs[:, None]) @ W2.T
+
+
+def dequantized_fp8(W):
+    """codes * scale of the per-row quantisation of a weight tensor (last axis = row)."""
+    W = np.asarray(W, F64)
+    c, s = quantize_rows_fp8(W.reshape(-1, W.shape[-1]))
+    return (c * s[:, None]).reshape(W.shape)
+
+
+def moe_forward_fp8_sampled(x, idx, w, row_of, expert_weights, shared_weights=None, tokens=None):
+    """moe_forward_fp8 for the sampled tokens only, from a given selection, with the bf16 expert
+    weights fetched one expert at a time (expert_weights(e) -> (w13 [2F,d], w2 [d,F]) float64,
+    shared_weights() -> (ws13, ws2) or None) and quantised here, so that full-size layers can
+    be checked without quantising every expert."""
+    tokens = np.asarray(tokens)
+    xq, xs = quantize_rows_fp8(np.asarray(x[tokens], F64))
+    xd = xq * xs[:, None]
+    out = np.zeros_like(xd)
+    if shared_weights is not None:
+        sw = shared_weights()
+        if sw is not None:
+            out += fp8_ffn(xd, dequantized_fp8(sw[0]), dequantized_fp8(sw[1]))
+    sel = idx[tokens]
+    keep = row_of[tokens] >= 0
+    for e in np.unique(sel[keep]):
+        w13, w2 = expert_weights(int(e))
+        rows, slots = np.nonzero((sel == e) & keep)
+        y = fp8_ffn(xd[rows], dequantized_fp8(w13), dequantized_fp8(w2))
+        out[rows] += w[tokens][rows, slots][:, None] * y
+    return out
 
 
 def expected_distinct_experts(E: int, k: int, B: int) -> float:

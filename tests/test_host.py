@@ -147,3 +147,26 @@ def test_router_backward_workspace_sizes():
     assert large >= 2 * 8192 * 256 * 2 and large > small
     tiny = moe_inputs.workload("tiny")
     assert m.router_backward_workspace_size(config_of(tiny)) >= tiny.T * tiny.E * 4
+
+
+def test_fp8_rejections_before_any_launch():
+    m = _lib()
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    assert m.lib.moe_quantize_fp8(4, 64, None, fake, fake, None) == -1
+    assert m.lib.moe_quantize_fp8(4, 40, fake, fake, fake, None) == -2    # cols % 16
+    assert m.lib.moe_quantize_fp8(0, 64, fake, fake, fake, None) == -2
+    n = ctypes.c_size_t()
+    tiny = config_of(moe_inputs.workload("tiny"))                         # float32 activations
+    assert m.lib.moe_fp8_workspace_size(ctypes.byref(tiny), ctypes.byref(n)) == -3
+    d384 = config_of(moe_inputs.workload("mixtral", d=384), T=8)          # d % 256 != 0
+    assert m.lib.moe_fp8_workspace_size(ctypes.byref(d384), ctypes.byref(n)) == -2
+    ec = config_of(moe_inputs.workload("dsmoe16b_ec"), T=64)
+    assert m.lib.moe_fp8_workspace_size(ctypes.byref(ec), ctypes.byref(n)) == -3
+    v3 = config_of(moe_inputs.workload("v3"), T=64)
+    assert m.lib.moe_forward_fp8(ctypes.byref(v3), *([None] * 21)) == -1
+    # the shared expert's codes are required when the layer has one
+    args = [fake] * 21
+    args[7] = None
+    assert m.lib.moe_forward_fp8(ctypes.byref(v3), *args) == -1
+    assert m.fp8_workspace_size(v3) > m.workspace_size(v3)

@@ -113,3 +113,15 @@ def test_fp8_layer_token_subset_matches_full():
     full, _ = O.moe_forward_fp8(wl, h["x"], h["w_gate"], h["bias"], wq)
     part, _ = O.moe_forward_fp8(wl, h["x"], h["w_gate"], h["bias"], wq, tokens=[3, 17, 0])
     assert np.allclose(part, full[[3, 17, 0]], rtol=0, atol=1e-12)
+
+
+def test_fp8_sampled_matches_full():
+    wl, h = _small("v3", T=24, d=128, E=16, F=128, F_shared=128)
+    wq = O.fp8_expert_weights(h["w13"], h["w2"], h["ws13"], h["ws2"])
+    full, r = O.moe_forward_fp8(wl, h["x"], h["w_gate"], h["bias"], wq)
+    disp = O.dispatch(r["idx"], wl.E, O.capacity(wl.capacity_factor, wl.k, wl.T, wl.E))
+    toks = [5, 0, 23]
+    part = O.moe_forward_fp8_sampled(h["x"], r["idx"], r["w"], disp["row_of"],
+                                     lambda e: (h["w13"][e], h["w2"][e]),
+                                     lambda: (h["ws13"], h["ws2"]), toks)
+    assert np.allclose(part, full[toks], rtol=0, atol=1e-12)

@@ -81,6 +81,9 @@ _SIGS = {
     "moe_router_backward": ([_CFG] + [_P] * 6 + [ctypes.c_float, ctypes.c_float] + [_P] * 5,
                             ctypes.c_int),
     "moe_bias_update": ([_CFG, _P, _P, ctypes.c_float, _P], ctypes.c_int),
+    "moe_quantize_fp8": ([ctypes.c_int64, ctypes.c_int64, _P, _P, _P, _P], ctypes.c_int),
+    "moe_fp8_workspace_size": ([_CFG, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
+    "moe_forward_fp8": ([_CFG] + [_P] * 21, ctypes.c_int),
 }
 EXPORTED = tuple(_SIGS)
 
@@ -272,3 +275,44 @@ def moe_router_backward(cfg, x, w_gate, logits, topk_idx, d_topk_w, f, alpha, be
 def moe_bias_update(cfg, f, bias, gamma, stream=None):
     _check("moe_bias_update", lib.moe_bias_update(ctypes.byref(cfg), _ptr(f), _ptr(bias),
                                                   float(gamma), _stream(stream)))
+
+
+def moe_quantize_fp8(src, dst, scale, stream=None):
+    """Per-row E4M3 quantisation of a bf16 tensor (leading dimensions flattened into rows):
+    dst uint8 of the same shape receives the codes, scale float32 [rows] the row scales."""
+    cols = src.shape[-1]
+    rows = src.numel() // cols
+    _check("moe_quantize_fp8", lib.moe_quantize_fp8(rows, cols, _ptr(src), _ptr(dst), _ptr(scale),
+                                                    _stream(stream)))
+
+
+def quantize_fp8(src, stream=None):
+    """Codes (uint8, shape of src) and row scales (float32 [rows]) of a bf16 device tensor."""
+    import torch
+    dst = torch.empty(src.shape, dtype=torch.uint8, device=src.device)
+    scale = torch.empty(src.numel() // src.shape[-1], dtype=torch.float32, device=src.device)
+    moe_quantize_fp8(src, dst, scale, stream)
+    return dst, scale
+
+
+def fp8_workspace_size(cfg: MoeConfig) -> int:
+    n = ctypes.c_size_t()
+    _check("moe_fp8_workspace_size",
+           lib.moe_fp8_workspace_size(ctypes.byref(cfg), ctypes.byref(n)))
+    return n.value
+
+
+def fp8_workspace(cfg: MoeConfig, device="cuda"):
+    """A zeroed device workspace for moe_forward_fp8 (torch allocation)."""
+    import torch
+    return torch.zeros(fp8_workspace_size(cfg), dtype=torch.uint8, device=device)
+
+
+def moe_forward_fp8(cfg, x, w_gate, bias, w13_q, w13_s, w2_q, w2_s, ws13_q, ws13_s, ws2_q, ws2_s,
+                    out, topk_idx=None, topk_w=None, f=None, P=None, l_balance=None, z_loss=None,
+                    n_dropped=None, ws=None, stream=None):
+    _check("moe_forward_fp8", lib.moe_forward_fp8(
+        ctypes.byref(cfg), _ptr(x), _ptr(w_gate), _ptr(bias), _ptr(w13_q), _ptr(w13_s),
+        _ptr(w2_q), _ptr(w2_s), _ptr(ws13_q), _ptr(ws13_s), _ptr(ws2_q), _ptr(ws2_s), _ptr(out),
+        _ptr(topk_idx), _ptr(topk_w), _ptr(f), _ptr(P), _ptr(l_balance), _ptr(z_loss),
+        _ptr(n_dropped), _ptr(ws), _stream(stream)))

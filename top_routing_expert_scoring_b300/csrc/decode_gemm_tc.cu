@@ -17,6 +17,7 @@
 // prefill kernels.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -67,6 +68,11 @@ struct Params {
   size_t shared_stride;     // GEMM 2: elements between K-slice partials of out_shared
   int stages;               // ring depth
   int stage;                // bytes per ring stage
+  int fp8;                  // operands are E4M3 codes (kind::f8f6f4) instead of bf16
+  int bk;                   // K elements per ring stage: 64 (bf16) or 128 (E4M3), 128 bytes
+  const float* sa;          // E4M3: scale of each routed weight row (row index of A)
+  const float* sa_shared;   // E4M3: scale of each shared weight row
+  const float* sb;          // E4M3: scale of each token row (row index of B)
   DevStatus* st;
 };
 
@@ -182,7 +188,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         a0 = (sh ? 0 : t.j * p.a_rows_routed) + t.wb * 256;
         a1 = a0 + 128;
       }
-      const int KB = (sh ? p.K_shared : p.K_routed) / BK;
+      const int KB = (sh ? p.K_shared : p.K_routed) / p.bk;
       const int kb0 = t.ks * KB / p.ksplit, kb1 = (t.ks + 1) * KB / p.ksplit;
       for (int kb = kb0; kb < kb1; ++kb) {
         if (!wait_bounded(empty0 + 8 * stage, ph ^ 1u, abort_flag, p.st, 21, true)) {
@@ -192,9 +198,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t fb = full0 + 8 * stage;
         const uint32_t sa = smem_u32(smem + stage * STAGE);
         mbar_expect_tx(fb, A_STAGE + b_bytes);
-        tma_load_2d(sa, am, fb, kb * BK, a0);
-        tma_load_2d(sa + A_BOX, am, fb, kb * BK, a1);
-        tma_load_2d(sa + A_STAGE, bm, fb, kb * BK, t.row0);
+        tma_load_2d(sa, am, fb, kb * p.bk, a0);
+        tma_load_2d(sa + A_BOX, am, fb, kb * p.bk, a1);
+        tma_load_2d(sa + A_STAGE, bm, fb, kb * p.bk, t.row0);
         issued |= 1u << stage;
         last_par = (last_par & ~(1u << stage)) | (ph << stage);
         if (++stage == STAGES) {
@@ -216,8 +222,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
       const DTile t = decode_dtile(tile, p, prefix, J);
       const int n16 = (t.n + 15) & ~15;
-      const uint32_t idesc = idesc_bf16_f32(128, n16);
-      const int KB = (t.j >= p.E ? p.K_shared : p.K_routed) / BK;
+      const uint32_t idesc = p.fp8 ? idesc_e4m3_f32(128, n16) : idesc_bf16_f32(128, n16);
+      const int KB = (t.j >= p.E ? p.K_shared : p.K_routed) / p.bk;
       const int kb0 = t.ks * KB / p.ksplit, kb1 = (t.ks + 1) * KB / p.ksplit;
       if (!wait_bounded(tempty0 + 8 * acc, aph ^ 1u, abort_flag, p.st, 22, true)) {
         ok = false;
@@ -233,12 +239,23 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const uint32_t sa = smem_u32(smem + stage * STAGE);
         const uint32_t sb = sa + A_STAGE;
+        // four MMAs per 128-byte stage row: K = 16 bf16 or K = 32 E4M3 each, 32 bytes apart
+        if (p.fp8) {
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint64_t bdesc = sw128_desc(sb + kk * 32);
-          const uint32_t accum = (kb != kb0 || kk != 0) ? 1u : 0u;
-          tc_mma(d0, sw128_desc(sa + kk * 32), bdesc, idesc, accum);
-          tc_mma(d0 + 128, sw128_desc(sa + A_BOX + kk * 32), bdesc, idesc, accum);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bdesc = sw128_desc(sb + kk * 32);
+            const uint32_t accum = (kb != kb0 || kk != 0) ? 1u : 0u;
+            tc_mma_f8(d0, sw128_desc(sa + kk * 32), bdesc, idesc, accum);
+            tc_mma_f8(d0 + 128, sw128_desc(sa + A_BOX + kk * 32), bdesc, idesc, accum);
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bdesc = sw128_desc(sb + kk * 32);
+            const uint32_t accum = (kb != kb0 || kk != 0) ? 1u : 0u;
+            tc_mma(d0, sw128_desc(sa + kk * 32), bdesc, idesc, accum);
+            tc_mma(d0 + 128, sw128_desc(sa + A_BOX + kk * 32), bdesc, idesc, accum);
+          }
         }
         tc_commit(empty0 + 8 * stage);
         if (++stage == STAGES) {
@@ -271,13 +288,38 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * 256) +
                           (static_cast<uint32_t>(q * 32) << 16);
       const bool sh = t.j >= p.E;
+      // E4M3: this thread's two weight rows carry scales s_lo, s_hi; token rows carry sb[row]
+      float s_lo = 1.0f, s_hi = 1.0f;
+      if (p.fp8) {
+        const float* sa = sh ? p.sa_shared : p.sa;
+        int a0;
+        if (p.gemm == 1) {
+          a0 = (sh ? 0 : t.j * p.a_rows_routed) + t.wb * 128 + f;
+          s_lo = sa[a0];
+          s_hi = sa[a0 + (sh ? p.up_shared : p.up_routed)];
+        } else {
+          a0 = (sh ? 0 : t.j * p.a_rows_routed) + t.wb * 256 + f;
+          s_lo = sa[a0];
+          s_hi = sa[a0 + 128];
+        }
+      }
 #pragma unroll 1
       for (int c0 = 0; c0 < t.n; c0 += 32) {
         uint32_t lo[32], hi[32];
         tmem_ld32(tb + c0, lo);
         tmem_ld32(tb + 128 + c0, hi);
         const int m = min(32, t.n - c0);
-        if (p.gemm == 1 && p.ksplit == 1) {
+        if (p.fp8) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (i < m) {
+              const float sr = p.sb[t.row0 + c0 + i];
+              lo[i] = __float_as_uint(__uint_as_float(lo[i]) * s_lo * sr);
+              hi[i] = __float_as_uint(__uint_as_float(hi[i]) * s_hi * sr);
+            }
+          }
+        }
+        if (p.gemm == 1 && p.gu == nullptr) {
           __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
@@ -355,6 +397,49 @@ __global__ void __launch_bounds__(256) swiglu_finalize_kernel(const float* __res
   }
 }
 
+// E4M3 path: h[r][:] = SiLU(sum_s gate_s[r][:]) * sum_s up_s[r][:] (slices in order), then the
+// row is quantised as every E4M3 operand: amax = max |h|, inv = 448 / amax, code = e4m3(h * inv)
+// (round to nearest even, saturating), scale = amax / 448; a zero row gets codes 0, scale 0.
+// One CTA per row; the row's h stays in shared memory between the two passes.
+__global__ void __launch_bounds__(256) swiglu_quant_kernel(const float* __restrict__ gu,
+                                                          size_t part_stride, int S,
+                                                          const int32_t* __restrict__ offsets,
+                                                          int E, int n_shared_rows, int F, int Fs,
+                                                          int ldo, uint8_t* __restrict__ h8,
+                                                          float* __restrict__ hs) {
+  extern __shared__ float hrow[];
+  __shared__ float red[8];
+  const int nk = offsets[E];
+  const int r = blockIdx.x;
+  if (r >= nk + n_shared_rows) return;
+  const int Fr = r < nk ? F : Fs;
+  const float* src = gu + static_cast<size_t>(r) * (2 * ldo);
+  float amax = 0.f;
+  for (int f = threadIdx.x; f < Fr; f += blockDim.x) {
+    float g = 0.f, u = 0.f;
+    for (int sl = 0; sl < S; ++sl) {
+      g += src[sl * part_stride + f];
+      u += src[sl * part_stride + ldo + f];
+    }
+    const float hv = (g / (1.0f + expf(-g))) * u;
+    hrow[f] = hv;
+    amax = fmaxf(amax, fabsf(hv));
+  }
+  amax = warp_max(amax);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) amax = fmaxf(amax, red[w]);
+  const float inv = amax > 0.f ? 448.0f / amax : 0.f;
+  uint8_t* dst = h8 + static_cast<size_t>(r) * ldo;
+  for (int f2 = 2 * threadIdx.x; f2 < Fr; f2 += 2 * blockDim.x) {
+    const __nv_fp8x2_storage_t q = __nv_cvt_float2_to_fp8x2(
+        make_float2(hrow[f2] * inv, hrow[f2 + 1] * inv), __NV_SATFINITE, __NV_E4M3);
+    *reinterpret_cast<__nv_fp8x2_storage_t*>(dst + f2) = q;
+  }
+  if (threadIdx.x == 0) hs[r] = amax > 0.f ? amax / 448.0f : 0.f;
+}
+
 static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& as, const CUtensorMap& b,
                           const CUtensorMap& bs, Params p, int upper_tiles, cudaStream_t s) {
   static bool attr_set = false;
@@ -382,17 +467,22 @@ cudaError_t launch_ffn_decode(const DecodeFFN& g, DevStatus* st, cudaStream_t s)
   using namespace dec;
   const bool sh = g.F_shared > 0;
   const int Fmax = g.F > g.F_shared ? g.F : g.F_shared;
+  // bf16: boxes of 64 elements; E4M3: boxes of 128 one-byte codes (the same 128-byte rows)
+  auto map = [&](CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box) {
+    return g.fp8 ? tc::make_map_u8(m, base, rows, cols, box)
+                 : tc::make_map_box(m, base, rows, cols, box);
+  };
   CUtensorMap ma1, mas1, mb1, mbs1, ma2, mas2, mb2, mbs2;
-  if (!tc::make_map_box(&ma1, g.w13, (uint64_t)g.E * 2 * g.F, (uint64_t)g.d, 128) ||
-      !tc::make_map_box(&ma2, g.w2, (uint64_t)g.E * g.d, (uint64_t)g.F, 128) ||
-      !tc::make_map_box(&mb1, g.x, (uint64_t)g.max_rows, (uint64_t)g.d, g.np) ||
-      !tc::make_map_box(&mb2, g.h, (uint64_t)g.max_rows, (uint64_t)Fmax, g.np) ||
-      !tc::make_map_box(&mbs1, g.x, (uint64_t)g.max_rows, (uint64_t)g.d, g.np_shared) ||
-      !tc::make_map_box(&mbs2, g.h, (uint64_t)g.max_rows, (uint64_t)Fmax, g.np_shared))
+  if (!map(&ma1, g.w13, (uint64_t)g.E * 2 * g.F, (uint64_t)g.d, 128) ||
+      !map(&ma2, g.w2, (uint64_t)g.E * g.d, (uint64_t)g.F, 128) ||
+      !map(&mb1, g.x, (uint64_t)g.max_rows, (uint64_t)g.d, g.np) ||
+      !map(&mb2, g.h, (uint64_t)g.max_rows, (uint64_t)Fmax, g.np) ||
+      !map(&mbs1, g.x, (uint64_t)g.max_rows, (uint64_t)g.d, g.np_shared) ||
+      !map(&mbs2, g.h, (uint64_t)g.max_rows, (uint64_t)Fmax, g.np_shared))
     return cudaErrorInvalidValue;
   if (sh) {
-    if (!tc::make_map_box(&mas1, g.ws13, (uint64_t)2 * g.F_shared, (uint64_t)g.d, 128) ||
-        !tc::make_map_box(&mas2, g.ws2, (uint64_t)g.d, (uint64_t)g.F_shared, 128))
+    if (!map(&mas1, g.ws13, (uint64_t)2 * g.F_shared, (uint64_t)g.d, 128) ||
+        !map(&mas2, g.ws2, (uint64_t)g.d, (uint64_t)g.F_shared, 128))
       return cudaErrorInvalidValue;
   } else {
     mas1 = ma1;
@@ -420,13 +510,30 @@ cudaError_t launch_ffn_decode(const DecodeFFN& g, DevStatus* st, cudaStream_t s)
   p1.gu = g.gu;
   p1.part_stride = static_cast<size_t>(g.max_rows) * 2 * Fmax;
   p1.shared_stride = 0;
+  p1.fp8 = g.fp8;
+  p1.bk = g.fp8 ? 128 : 64;
+  p1.sa = g.s13;
+  p1.sa_shared = g.ss13;
+  p1.sb = g.sx;
   p1.st = st;
   // upper bound of the tile count: every routed row in its own chunk is impossible to exceed
   const int chunks_upper = ceil_div(g.max_rows, g.np) + g.E + ceil_div(g.T, g.np_shared) + 1;
   const int wbmax1 = p1.wb_routed > p1.wb_shared ? p1.wb_routed : p1.wb_shared;
   cudaError_t err = launch(ma1, mas1, mb1, mbs1, p1, chunks_upper * wbmax1 * g.ksplit1, s);
   if (err != cudaSuccess) return err;
-  if (g.ksplit1 > 1) {
+  if (g.fp8) {
+    static bool attr = false;
+    if (!attr) {
+      err = cudaFuncSetAttribute(swiglu_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 200 * 1024);
+      if (err != cudaSuccess) return err;
+      attr = true;
+    }
+    swiglu_quant_kernel<<<g.max_rows, 256, static_cast<size_t>(Fmax) * 4, s>>>(
+        g.gu, p1.part_stride, g.ksplit1, g.offsets, g.E, sh ? g.T : 0, g.F,
+        sh ? g.F_shared : 0, Fmax, static_cast<uint8_t*>(g.h), g.hs);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  } else if (g.ksplit1 > 1) {
     const long long work = static_cast<long long>(g.max_rows) * Fmax;
     int blocks = static_cast<int>((work + 255) / 256);
     if (blocks > num_sms() * 8) blocks = num_sms() * 8;
@@ -451,6 +558,9 @@ cudaError_t launch_ffn_decode(const DecodeFFN& g, DevStatus* st, cudaStream_t s)
   p2.gu = nullptr;
   p2.part_stride = g.y_part_stride;
   p2.shared_stride = g.shared_part_stride;
+  p2.sa = g.s2;
+  p2.sa_shared = g.ss2;
+  p2.sb = g.hs;
   return launch(ma2, mas2, mb2, mbs2, p2, chunks_upper * p2.wb_routed * g.ksplit2, s);
 }
 

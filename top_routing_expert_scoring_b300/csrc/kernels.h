@@ -96,8 +96,23 @@ struct DecodeFFN {
   float* gu;                // [ksplit1][max_rows, 2 max(F, F_shared)] f32 when ksplit1 > 1
   size_t y_part_stride;     // elements between y partials (max_rows * d)
   size_t shared_part_stride;// elements between shared partials (T * d)
+  // E4M3 operands: x, h, w13, w2, ws13, ws2 hold one-byte codes and these hold the per-row
+  // scales; gu must be set (gate/up always go through the float32 partials, then h is
+  // quantised per row into h / hs)
+  int fp8;
+  const float* s13;         // [E * 2F]
+  const float* s2;          // [E * d]
+  const float* ss13;        // [2 Fs]
+  const float* ss2;         // [d]
+  const float* sx;          // [max_rows] token-row scales of x
+  float* hs;                // [max_rows] token-row scales of h (written)
 };
 cudaError_t launch_ffn_decode(const DecodeFFN& g, DevStatus* st, cudaStream_t s);
+// Per-row E4M3 quantisation of bf16 rows (see moe_quantize_fp8); rows read from *nrows_base +
+// nrows_extra when nrows_base is set (device-side count), else nrows_max.
+cudaError_t launch_quantize_rows(const void* src, long long nrows_max, int cols,
+                                 const int32_t* nrows_base, int nrows_extra, uint8_t* dst,
+                                 float* scale, cudaStream_t s);
 
 // ---- combine ---------------------------------------------------------------------------------
 // y_perm and shared_out (or NULL) are float32 [*, d]; out follows c.out_dtype.  With nsplit > 1

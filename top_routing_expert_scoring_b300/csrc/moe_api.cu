@@ -602,3 +602,159 @@ int moe_selftest_timeout(void* ws, int32_t limit_us, void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------------
+// FP8 (E4M3) expert weights: the decode kernels on one-byte codes with per-row scales
+// ---------------------------------------------------------------------------------------------
+namespace moe {
+namespace {
+
+// K slices of an FP8 decode GEMM: the same rule as the bf16 decode path (about two waves of
+// tiles from the expected touched experts), without the regime switch.
+int fp8_split(const moe_config& c, int tiles_per_entry, int kblocks) {
+  const double touched = c.E * (1.0 - std::pow(1.0 - (double)c.k / c.E, (double)c.T));
+  const double entries = touched + (c.d_ff_shared > 0 ? 1.0 : 0.0);
+  const double tiles = entries * tiles_per_entry;
+  int sp = (int)std::ceil(2.0 * num_sms() / (tiles > 1 ? tiles : 1));
+  if (sp > kMaxSplit) sp = kMaxSplit;
+  if (sp > kblocks) sp = kblocks;
+  return sp < 1 ? 1 : sp;
+}
+
+struct Fp8Layout {
+  Layout base;
+  size_t x8, sx, h8, hs, gu, y, sh, total;
+  int ks1, ks2;
+};
+
+Fp8Layout fp8_layout(const moe_config& c) {
+  Fp8Layout L{};
+  L.base = layout(c);
+  size_t o = L.base.total;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align_up(o + (bytes ? bytes : 1));
+    return at;
+  };
+  const size_t R = rows_max(c), T = c.T, d = c.d_model, F = c.d_ff, Fs = c.d_ff_shared;
+  const size_t rows = R + T, Fmax = F > Fs ? F : Fs;
+  L.ks1 = fp8_split(c, c.d_ff / 128, c.d_model / 128);
+  const int kf = (int)((Fs > 0 && Fs < F ? Fs : F) / 128);
+  L.ks2 = fp8_split(c, c.d_model / 256, kf);
+  L.x8 = take(rows * d);
+  L.sx = take(rows * 4);
+  L.h8 = take(rows * Fmax);
+  L.hs = take(rows * 4);
+  L.gu = take((size_t)L.ks1 * rows * 2 * Fmax * 4);
+  L.y = take((size_t)L.ks2 * R * d * 4);
+  L.sh = take(Fs ? (size_t)L.ks2 * T * d * 4 : 0);
+  L.total = o;
+  return L;
+}
+
+int check_fp8_config(const moe_config* c) {
+  int st = moe_check_config(c);
+  if (st) return st;
+  if (c->dtype != MOE_DTYPE_BF16 || c->routing != MOE_ROUTE_TOKEN_CHOICE)
+    return MOE_ERR_UNSUPPORTED;
+  if (c->d_model % 256) return MOE_ERR_SHAPE;
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" {
+
+int moe_fp8_workspace_size(const moe_config* c, size_t* bytes) {
+  int st = check_fp8_config(c);
+  if (st) return st;
+  if (!bytes) return MOE_ERR_ARG;
+  *bytes = fp8_layout(*c).total;
+  return MOE_OK;
+}
+
+int moe_forward_fp8(const moe_config* c, const void* x, const void* w_gate, const float* bias,
+                    const uint8_t* w13_q, const float* w13_scale, const uint8_t* w2_q,
+                    const float* w2_scale, const uint8_t* ws13_q, const float* ws13_scale,
+                    const uint8_t* ws2_q, const float* ws2_scale, void* out, int32_t* topk_idx,
+                    float* topk_w, float* f, float* P, float* l_balance, float* z_loss,
+                    int32_t* n_dropped, void* ws, void* stream) {
+  int st = check_fp8_config(c);
+  if (st) return st;
+  if (!x || !w_gate || !w13_q || !w13_scale || !w2_q || !w2_scale || !out) return MOE_ERR_ARG;
+  const bool has_sh = c->d_ff_shared > 0;
+  if (has_sh && (!ws13_q || !ws13_scale || !ws2_q || !ws2_scale)) return MOE_ERR_ARG;
+  if ((st = check_ws(ws))) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Fp8Layout F8 = fp8_layout(*c);
+  const Layout& L = F8.base;
+  DevStatus* dst = at<DevStatus>(ws, L.status);
+  float* g = at<float>(ws, L.logits);
+  f = f ? f : at<float>(ws, L.f);
+  P = P ? P : at<float>(ws, L.P);
+  l_balance = l_balance ? l_balance : at<float>(ws, L.lb);
+  z_loss = z_loss ? z_loss : at<float>(ws, L.z);
+  int32_t* idx = topk_idx ? topk_idx : at<int32_t>(ws, L.idx);
+  float* w = topk_w ? topk_w : at<float>(ws, L.w);
+  float* part_P = at<float>(ws, L.part_P);
+  int32_t* part_cnt = at<int32_t>(ws, L.part_cnt);
+  float* part_z = at<float>(ws, L.part_z);
+
+  if (launch_router_logits(*c, x, w_gate, g, s) != cudaSuccess ||
+      launch_route_topk(*c, g, bias, idx, w, dst, s, part_P, part_cnt, part_z) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  DispatchBufs b{at<uint32_t>(ws, L.bitmap), at<int32_t>(ws, L.blk_base),
+                 at<int32_t>(ws, L.counts), at<int32_t>(ws, L.kept), at<int32_t>(ws, L.offsets),
+                 at<int32_t>(ws, L.mtp), n_dropped ? n_dropped : at<int32_t>(ws, L.n_dropped),
+                 at<int32_t>(ws, L.pos), at<int32_t>(ws, L.row_of), at<int32_t>(ws, L.perm)};
+  // routed rows in expert order, then (with shared experts) the T token rows
+  if (launch_dispatch(*c, capacity_of(*c), idx, b, x, at<void>(ws, L.x_perm), dst, s, has_sh) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  const int R = rows_max(*c);
+  uint8_t* x8 = at<uint8_t>(ws, F8.x8);
+  float* sx = at<float>(ws, F8.sx);
+  if (launch_quantize_rows(at<void>(ws, L.x_perm), (long long)R + c->T, c->d_model,
+                           b.offsets + c->E, has_sh ? c->T : 0, x8, sx, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  DecodeFFN gd{};
+  gd.x = x8;
+  gd.offsets = b.offsets;
+  gd.E = c->E;
+  gd.T = c->T;
+  gd.d = c->d_model;
+  gd.F = c->d_ff;
+  gd.F_shared = c->d_ff_shared;
+  gd.max_rows = R + c->T;
+  gd.np = pow2_clamp(2ll * c->T * c->k / c->E, 16, 128);
+  gd.np_shared = pow2_clamp(c->T, 16, 128);
+  gd.w13 = w13_q;
+  gd.w2 = w2_q;
+  gd.ws13 = ws13_q;
+  gd.ws2 = ws2_q;
+  gd.h = at<void>(ws, F8.h8);
+  gd.ksplit1 = F8.ks1;
+  gd.ksplit2 = F8.ks2;
+  gd.gu = at<float>(ws, F8.gu);
+  gd.y = at<float>(ws, F8.y);
+  gd.shared_out = has_sh ? at<float>(ws, F8.sh) : nullptr;
+  gd.y_part_stride = (size_t)R * c->d_model;
+  gd.shared_part_stride = (size_t)c->T * c->d_model;
+  gd.fp8 = 1;
+  gd.s13 = w13_scale;
+  gd.s2 = w2_scale;
+  gd.ss13 = ws13_scale;
+  gd.ss2 = ws2_scale;
+  gd.sx = sx;
+  gd.hs = at<float>(ws, F8.hs);
+  if (launch_ffn_decode(gd, dst, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_combine(*c, gd.y, b.row_of, w, gd.shared_out, out, s, F8.ks2, gd.y_part_stride,
+                     gd.shared_part_stride) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return cuda_status(launch_aux_final(*c, part_P, part_cnt, part_z, aux_blocks(*c), f, P,
+                                      l_balance, z_loss, s));
+}
+
+}  // extern "C"
+

@@ -99,6 +99,22 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
       : "memory");
 }
+// Instruction descriptor, kind::f8f6f4: D = f32, A = B = E4M3 (format 0), both K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// One MMA on 8-bit operands: K = 32 elements (32 bytes) per instruction, the same byte step
+// along a 128-byte swizzled row as K = 16 in bf16.
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+      : "memory");
+}
+
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -128,6 +144,10 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols);
 // Same with a box of 64 columns x box_rows rows (box_rows a multiple of 8, <= 256).
 bool make_map_box(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                   uint32_t box_rows);
+// 2-D byte tensor [rows, cols] (E4M3 codes) read in boxes of 128 columns (bytes) x box_rows
+// rows with the 128-byte swizzle: the same shared-memory layout as a 64-column bf16 box.
+bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                 uint32_t box_rows);
 // Same for rows that lie row_stride elements apart (row_stride * 2 a multiple of 16 bytes).
 bool make_map_strided(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                       uint64_t row_stride, uint32_t box_rows);
