@@ -229,11 +229,22 @@ def decode_sweep(args):
     torch.cuda.set_device(0)
     peaks, peak_kind = load_peaks()
     hbm = float(peaks["hbm_gbs"])
+    fp8 = args.fp8
     for name in args.decode_workloads.split(","):
         wl0 = moe_inputs.workload(name)
         weights = moe_inputs.make_expert_weights(wl0, device="cuda")
-        per_expert = 3 * wl0.d * wl0.F * 2
-        shared_bytes = 3 * wl0.d * wl0.F_sh * 2
+        if fp8:
+            # one-byte E4M3 codes plus one fp32 scale per weight row, quantised once up front
+            q = {key: (m.quantize_fp8(weights[key]) if weights[key] is not None else (None, None))
+                 for key in ("w13", "w2", "ws13", "ws2")}
+            torch.cuda.synchronize()
+            del weights
+            torch.cuda.empty_cache()
+            per_expert = 3 * wl0.d * wl0.F + (2 * wl0.F + wl0.d) * 4
+            shared_bytes = 3 * wl0.d * wl0.F_sh + ((2 * wl0.F_sh + wl0.d) * 4 if wl0.F_sh else 0)
+        else:
+            per_expert = 3 * wl0.d * wl0.F * 2
+            shared_bytes = 3 * wl0.d * wl0.F_sh * 2
         for B in [int(b) for b in args.decode_batches.split(",")]:
             wl = wl0.replace(T=B)
             cfg = m.make_config(B, wl.d, wl.E, wl.k, wl.F, wl.F_sh, wl.score, wl.routing,
@@ -242,14 +253,19 @@ def decode_sweep(args):
             steps = args.decode_steps
             routers = [moe_inputs.make_router_inputs(wl, seed=1000 + i, device="cuda")
                        for i in range(steps)]
-            ws = m.workspace(cfg)
+            ws = m.fp8_workspace(cfg) if fp8 else m.workspace(cfg)
             out = torch.empty((B, wl.d), dtype=torch.float32, device="cuda")
             idx_all = torch.empty((steps, B, wl.k), dtype=torch.int32, device="cuda")
 
             def fwd(i):
                 r = routers[i]
-                m.moe_forward(cfg, r["x"], r["w_gate"], r["bias"], weights["w13"], weights["w2"],
-                              weights["ws13"], weights["ws2"], out, topk_idx=idx_all[i], ws=ws)
+                if fp8:
+                    m.moe_forward_fp8(cfg, r["x"], r["w_gate"], r["bias"], *q["w13"], *q["w2"],
+                                      *q["ws13"], *q["ws2"], out, topk_idx=idx_all[i], ws=ws)
+                else:
+                    m.moe_forward(cfg, r["x"], r["w_gate"], r["bias"], weights["w13"],
+                                  weights["w2"], weights["ws13"], weights["ws2"], out,
+                                  topk_idx=idx_all[i], ws=ws)
             for i in range(min(5, steps)):
                 fwd(i)
             torch.cuda.synchronize()
@@ -297,9 +313,12 @@ def decode_sweep(args):
             se_z = (sum((v - mean_z) ** 2 for v in dz) / max(len(dz) - 1, 1)) ** 0.5 / math.sqrt(len(dz))
             print(json.dumps({
                 "metric": "MoE layer fwd tokens/s, decode batch; % of HBM BW on touched expert "
-                          "weights", "mode": "decode", "workload": f"{name} B={B}",
+                          "weights", "mode": "decode_fp8" if fp8 else "decode",
+                "workload": f"{name} B={B}",
                 "value": B * steps / total_s, "unit": "tokens/s", "steps": steps,
-                "ms_per_step": sum(ms) / steps, "dtype": "bf16", "data": "synthetic",
+                "ms_per_step": sum(ms) / steps,
+                "dtype": "e4m3 expert weights and activations, bf16 router" if fp8 else "bf16",
+                "data": "synthetic",
                 "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
                              "frac": gbs / hbm, "peak_kind": f"{peak_kind} copy bandwidth"},
                 "bytes_per_step_mean": sum(step_bytes) / steps,
@@ -310,7 +329,10 @@ def decode_sweep(args):
                 "l2": "each step reads >= 0.35 GB of expert weights (> 126 MB L2)"}))
             del routers, ws, graphs
             torch.cuda.empty_cache()
-        del weights
+        if fp8:
+            del q
+        else:
+            del weights
         torch.cuda.empty_cache()
 
 
@@ -414,6 +436,8 @@ def main():
     ap.add_argument("--decode-workloads", default="v3,mixtral")
     ap.add_argument("--decode-batches", default="1,8,64,256")
     ap.add_argument("--decode-steps", type=int, default=100)
+    ap.add_argument("--fp8", action="store_true",
+                    help="decode sweep: E4M3 expert weights (moe_forward_fp8)")
     ap.add_argument("--no-graphs", action="store_true",
                     help="decode sweep: launch each forward directly instead of a CUDA graph")
     ap.add_argument("--router-backward", action="store_true",
