@@ -400,42 +400,54 @@ __global__ void __launch_bounds__(256) swiglu_finalize_kernel(const float* __res
 // E4M3 path: h[r][:] = SiLU(sum_s gate_s[r][:]) * sum_s up_s[r][:] (slices in order), then the
 // row is quantised as every E4M3 operand: amax = max |h|, inv = 448 / amax, code = e4m3(h * inv)
 // (round to nearest even, saturating), scale = amax / 448; a zero row gets codes 0, scale 0.
-// One CTA per row; the row's h stays in shared memory between the two passes.
-__global__ void __launch_bounds__(256) swiglu_quant_kernel(const float* __restrict__ gu,
-                                                          size_t part_stride, int S,
-                                                          const int32_t* __restrict__ offsets,
-                                                          int E, int n_shared_rows, int F, int Fs,
-                                                          int ldo, uint8_t* __restrict__ h8,
-                                                          float* __restrict__ hs) {
-  extern __shared__ float hrow[];
-  __shared__ float red[8];
+// One CTA per row (up to 1024 threads, four columns per thread and step); the row's h stays in
+// shared memory between the two passes.
+__global__ void __launch_bounds__(1024) swiglu_quant_kernel(const float* __restrict__ gu,
+                                                           size_t part_stride, int S,
+                                                           const int32_t* __restrict__ offsets,
+                                                           int E, int n_shared_rows, int F,
+                                                           int Fs, int ldo,
+                                                           uint8_t* __restrict__ h8,
+                                                           float* __restrict__ hs) {
+  extern __shared__ float4 hrow4[];
+  __shared__ float red[32];
   const int nk = offsets[E];
   const int r = blockIdx.x;
   if (r >= nk + n_shared_rows) return;
-  const int Fr = r < nk ? F : Fs;
-  const float* src = gu + static_cast<size_t>(r) * (2 * ldo);
+  const int F4 = (r < nk ? F : Fs) / 4;
+  const float4* src = reinterpret_cast<const float4*>(gu + static_cast<size_t>(r) * (2 * ldo));
+  const size_t ps4 = part_stride / 4, up4 = static_cast<size_t>(ldo) / 4;
   float amax = 0.f;
-  for (int f = threadIdx.x; f < Fr; f += blockDim.x) {
-    float g = 0.f, u = 0.f;
-    for (int sl = 0; sl < S; ++sl) {
-      g += src[sl * part_stride + f];
-      u += src[sl * part_stride + ldo + f];
+  for (int f = threadIdx.x; f < F4; f += blockDim.x) {
+    float4 g = src[f], u = src[up4 + f];
+    for (int sl = 1; sl < S; ++sl) {
+      const float4 g2 = src[sl * ps4 + f], u2 = src[sl * ps4 + up4 + f];
+      g.x += g2.x; g.y += g2.y; g.z += g2.z; g.w += g2.w;
+      u.x += u2.x; u.y += u2.y; u.z += u2.z; u.w += u2.w;
     }
-    const float hv = (g / (1.0f + expf(-g))) * u;
-    hrow[f] = hv;
-    amax = fmaxf(amax, fabsf(hv));
+    float4 hv;
+    hv.x = (g.x / (1.0f + expf(-g.x))) * u.x;
+    hv.y = (g.y / (1.0f + expf(-g.y))) * u.y;
+    hv.z = (g.z / (1.0f + expf(-g.z))) * u.z;
+    hv.w = (g.w / (1.0f + expf(-g.w))) * u.w;
+    hrow4[f] = hv;
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(hv.x), fabsf(hv.y)), fmaxf(fabsf(hv.z), fabsf(hv.w))));
   }
   amax = warp_max(amax);
+  const int nw = blockDim.x >> 5;
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
   __syncthreads();
   amax = red[0];
-  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) amax = fmaxf(amax, red[w]);
+  for (int w = 1; w < nw; ++w) amax = fmaxf(amax, red[w]);
   const float inv = amax > 0.f ? 448.0f / amax : 0.f;
-  uint8_t* dst = h8 + static_cast<size_t>(r) * ldo;
-  for (int f2 = 2 * threadIdx.x; f2 < Fr; f2 += 2 * blockDim.x) {
-    const __nv_fp8x2_storage_t q = __nv_cvt_float2_to_fp8x2(
-        make_float2(hrow[f2] * inv, hrow[f2 + 1] * inv), __NV_SATFINITE, __NV_E4M3);
-    *reinterpret_cast<__nv_fp8x2_storage_t*>(dst + f2) = q;
+  uint32_t* dst = reinterpret_cast<uint32_t*>(h8 + static_cast<size_t>(r) * ldo);
+  for (int f = threadIdx.x; f < F4; f += blockDim.x) {
+    const float4 hv = hrow4[f];
+    const uint32_t q0 = __nv_cvt_float2_to_fp8x2(make_float2(hv.x * inv, hv.y * inv),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    const uint32_t q1 = __nv_cvt_float2_to_fp8x2(make_float2(hv.z * inv, hv.w * inv),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    dst[f] = (q0 & 0xFFFFu) | (q1 << 16);
   }
   if (threadIdx.x == 0) hs[r] = amax > 0.f ? amax / 448.0f : 0.f;
 }
@@ -529,7 +541,9 @@ cudaError_t launch_ffn_decode(const DecodeFFN& g, DevStatus* st, cudaStream_t s)
       if (err != cudaSuccess) return err;
       attr = true;
     }
-    swiglu_quant_kernel<<<g.max_rows, 256, static_cast<size_t>(Fmax) * 4, s>>>(
+    int threads = Fmax / 4;
+    threads = threads > 1024 ? 1024 : (threads + 31) / 32 * 32;
+    swiglu_quant_kernel<<<g.max_rows, threads, static_cast<size_t>(Fmax) * 4, s>>>(
         g.gu, p1.part_stride, g.ksplit1, g.offsets, g.E, sh ? g.T : 0, g.F,
         sh ? g.F_shared : 0, Fmax, static_cast<uint8_t*>(g.h), g.hs);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;

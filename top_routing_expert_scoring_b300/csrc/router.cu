@@ -145,10 +145,11 @@ static cudaError_t launch_stream(const moe_config& c, const void* x, const void*
 }
 
 // ------------------------------------------------------------------------------------------
-// Logits for a handful of tokens (T <= 16, bf16): one CTA per expert streams that expert's
-// router row once (16-byte loads; its 8 warps take one eighth of d each) and forms the T dot
-// products against the token rows, which stay in L1/L2; the 8 partial sums are added in a
-// fixed order.  Spreads the router weights over every SM instead of one tile.
+// Logits for decode-sized batches (bf16): one CTA per (expert, group of TP tokens) streams
+// that expert's router row once (16-byte loads; its 8 warps take one eighth of d each) and
+// forms the group's dot products against the token rows, which stay in L1/L2; the 8 partial
+// sums are added in a fixed order.  Spreads the router weights over every SM instead of one
+// tile; x is re-read from L2 once per expert, so this is for small E or very small T.
 // ------------------------------------------------------------------------------------------
 template <int TP>
 __global__ void __launch_bounds__(256) router_logits_few(const uint4* __restrict__ x,
@@ -158,6 +159,9 @@ __global__ void __launch_bounds__(256) router_logits_few(const uint4* __restrict
   __shared__ float part[8][TP];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int e = blockIdx.x;
+  const int t_base = blockIdx.y * TP;
+  x += (size_t)t_base * d8;
+  Tn -= t_base;
   float acc[TP];
 #pragma unroll
   for (int t = 0; t < TP; ++t) acc[t] = 0.f;
@@ -200,19 +204,19 @@ __global__ void __launch_bounds__(256) router_logits_few(const uint4* __restrict
     float v = 0.f;
 #pragma unroll
     for (int q = 0; q < 8; ++q) v += part[q][threadIdx.x];
-    g[(size_t)threadIdx.x * E + e] = v;
+    g[(size_t)(t_base + threadIdx.x) * E + e] = v;
   }
 }
 
 cudaError_t launch_router_logits(const moe_config& c, const void* x, const void* w_gate,
                                  float* logits, cudaStream_t s) {
-  if (c.dtype == MOE_DTYPE_BF16 && c.T <= 16) {
+  if (c.dtype == MOE_DTYPE_BF16 && (c.T <= 16 || (c.E <= 32 && c.T <= 512))) {
     if (c.T <= 4)
       router_logits_few<4><<<c.E, 256, 0, s>>>((const uint4*)x, (const uint4*)w_gate, logits, c.T,
                                                c.d_model / 8, c.E);
     else
-      router_logits_few<16><<<c.E, 256, 0, s>>>((const uint4*)x, (const uint4*)w_gate, logits,
-                                                c.T, c.d_model / 8, c.E);
+      router_logits_few<16><<<dim3(c.E, ceil_div(c.T, 16)), 256, 0, s>>>(
+          (const uint4*)x, (const uint4*)w_gate, logits, c.T, c.d_model / 8, c.E);
     return cudaGetLastError();
   }
   if (c.dtype == MOE_DTYPE_BF16) {
