@@ -59,8 +59,33 @@ struct Params {
   void* out;                // bf16 rows, or float32 rows when out_f32
   int out_f32;
   int ldo;
+  // A gathered from the token rows (GEMM 1 only): row r of the expert-ordered space is token
+  // perm[r] / gk of gx [T, K]; NULL: A is read by TMA from the materialised rows
+  const int32_t* gperm;
+  int gk;
+  const __nv_bfloat16* gx;
   DevStatus* st;
 };
+
+// Rows of the gather producer's lag: a lane signals stage n - kGatherLag once its copies for
+// that stage have landed (cp.async groups complete in order).
+constexpr int kGatherLag = 2;
+static_assert(kGatherLag < STAGES, "the producer must not wait on a stage it has to refill");
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 // ---------------------------------------------------------------------------------------------
 // Tile list
@@ -106,6 +131,10 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const Params& p) {
 // ---------------------------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------------------------
+// GATHER: the gate/up GEMM's A rows come from the token rows through the whole producer warp
+// (cp.async) instead of one TMA box over the materialised rows; a separate instantiation so the
+// default kernel's code is unchanged.
+template <bool GATHER>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, const Params p) {
@@ -127,7 +156,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full0 + 8 * s, 1);
+      // gather mode: 32 producer lanes arrive once their copies land, plus the B expect_tx
+      mbar_init(full0 + 8 * s, GATHER ? 33 : 1);
       mbar_init(empty0 + 8 * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -152,7 +182,90 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int total = total_tiles(p);
   const int KB = p.K / BK;
 
-  if (warp == 0 && lane == 0) {
+  if (GATHER && warp == 0) {
+    // ------------------------ gathering producer (whole warp) -------------------------------
+    // A: 128 rows of 64 bf16 per stage, copied straight from the token rows with cp.async in
+    // the 128-byte swizzled layout TMA would write (16-byte chunk j of row r at j ^ (r & 7)).
+    // Lanes 8q..8q+7 copy one row's 128 bytes (full lines); rows past the tile are zero-filled.
+    // B: lane 0's TMA, as in the TMA producer.  Each lane waits for its own copies kGatherLag
+    // stages later, fences them for the tensor core (async proxy) and arrives.
+    int stage = 0;
+    uint32_t ph = 0;
+    uint32_t issued = 0, last_par = 0;
+    const int nbox = (p.swiglu || p.bn > 128) ? 2 : 1;
+    const uint32_t bbytes = nbox * B_BOX;
+    const int chunk = lane & 7, rsub = lane >> 3;
+    int hist[kGatherLag];                 // stages of the copy groups still to be signalled
+    int npend = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+      const TileInfo ti = decode_tile(tile, p);
+      int tok[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int r = rsub + 4 * i;
+        tok[i] = r < ti.rows ? p.gperm[ti.row0 + r] / p.gk : -1;
+      }
+      int b0, b1;
+      if (p.swiglu) {
+        b0 = ti.e * p.b_rows + ti.nt * 128;
+        b1 = b0 + p.up_off;
+      } else {
+        b0 = ti.e * p.b_rows + ti.nt * p.bn;
+        b1 = b0 + 128;
+      }
+      for (int kb = 0; kb < KB; ++kb) {
+        int okw = 1;
+        if (lane == 0)
+          okw = wait_bounded(empty0 + 8 * stage, ph ^ 1u, abort_flag, p.st, 1, true) ? 1 : 0;
+        okw = __shfl_sync(0xffffffffu, okw, 0);
+        if (!okw) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = full0 + 8 * stage;
+        if (lane == 0) {
+          mbar_expect_tx(fb, bbytes);
+          tma_load_2d(smem_u32(sB + stage * B_STAGE), &tmB, fb, kb * BK, b0);
+          if (nbox == 2) tma_load_2d(smem_u32(sB + stage * B_STAGE + B_BOX), &tmB, fb, kb * BK, b1);
+        }
+        const uint32_t sa = smem_u32(sA + stage * A_STAGE);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int r = rsub + 4 * i;
+          const int t = tok[i];
+          const __nv_bfloat16* src =
+              p.gx + static_cast<size_t>(t < 0 ? 0 : t) * p.K + kb * BK + chunk * 8;
+          cp_async16(sa + r * 128 + ((chunk ^ (r & 7)) << 4), src, t < 0 ? 0u : 16u);
+        }
+        cp_async_commit();
+        issued |= 1u << stage;
+        last_par = (last_par & ~(1u << stage)) | (ph << stage);
+        if (npend == kGatherLag) {
+          cp_async_wait<kGatherLag>();
+          fence_proxy_async_smem();
+          mbar_arrive(full0 + 8 * hist[0]);
+#pragma unroll
+          for (int j = 0; j + 1 < kGatherLag; ++j) hist[j] = hist[j + 1];
+          --npend;
+        }
+        hist[npend++] = stage;
+        if (++stage == STAGES) {
+          stage = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+    // the copies still in flight: land, fence, signal
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    for (int j = 0; j < npend; ++j) mbar_arrive(full0 + 8 * hist[j]);
+    if (!ok && lane == 0) {
+      for (int s = 0; s < STAGES; ++s)
+        if ((issued >> s) & 1u)
+          wait_bounded(full0 + 8 * s, (last_par >> s) & 1u, abort_flag, p.st, 5, false);
+    }
+  } else if (warp == 0 && lane == 0) {
     // ------------------------------- TMA producer -------------------------------------------
     int stage = 0;
     uint32_t ph = 0;
@@ -409,16 +522,23 @@ static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const 
                               int upper_tiles, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel,
+    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(SMEM_BYTES));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(SMEM_BYTES));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   int grid = num_sms();
   if (upper_tiles < grid) grid = upper_tiles;
   if (grid < 1) grid = 1;
-  grouped_gemm_tc_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(a, b, p);
+  if (p.gperm)
+    grouped_gemm_tc_kernel<true><<<grid, THREADS, SMEM_BYTES, s>>>(a, b, p);
+  else
+    grouped_gemm_tc_kernel<false><<<grid, THREADS, SMEM_BYTES, s>>>(a, b, p);
   return cudaGetLastError();
 }
 
@@ -436,14 +556,21 @@ static bool use_pair_kernel(const GroupedFFN& g) {
   return (long long)g.max_rows / g.E >= 2048;
 }
 
+bool ffn_uses_pair(const GroupedFFN& g) { return use_pair_kernel(g); }
+
 cudaError_t launch_ffn_tc(const GroupedFFN& g, DevStatus* st, cudaStream_t s) {
   using namespace tc;
-  if (use_pair_kernel(g)) return launch_ffn_tc2(g, st, s);
+  if (use_pair_kernel(g)) {
+    if (g.gather_perm) return cudaErrorInvalidValue;   // the pair kernel reads materialised rows
+    return launch_ffn_tc2(g, st, s);
+  }
   CUtensorMap mx, mw13, mh, mw2;
-  if (!make_map(&mx, g.x, (uint64_t)g.max_rows, (uint64_t)g.d) ||
-      !make_map(&mw13, g.w13, (uint64_t)g.E * 2 * g.F, (uint64_t)g.d) ||
+  if (!make_map(&mw13, g.w13, (uint64_t)g.E * 2 * g.F, (uint64_t)g.d) ||
       !make_map(&mh, g.h, (uint64_t)g.max_rows, (uint64_t)g.F) ||
       !make_map(&mw2, g.w2, (uint64_t)g.E * g.d, (uint64_t)g.F))
+    return cudaErrorInvalidValue;
+  if (g.gather_perm) mx = mw13;   // not read: A is gathered from the token rows
+  else if (!make_map(&mx, g.x, (uint64_t)g.max_rows, (uint64_t)g.d))
     return cudaErrorInvalidValue;
   const int mt_upper = g.uniform_rows >= 0 ? ceil_div(g.uniform_rows, BM)
                                            : ceil_div(g.max_rows, BM) + g.E;
@@ -461,6 +588,9 @@ cudaError_t launch_ffn_tc(const GroupedFFN& g, DevStatus* st, cudaStream_t s) {
   p1.out = g.h;
   p1.out_f32 = 0;
   p1.ldo = g.F;
+  p1.gperm = g.gather_perm;
+  p1.gk = g.gather_k;
+  p1.gx = static_cast<const __nv_bfloat16*>(g.gather_x);
   p1.st = st;
   cudaError_t err = launch_one(mx, mw13, p1, mt_upper * p1.n_tiles, s);
   if (err != cudaSuccess) return err;
@@ -474,6 +604,7 @@ cudaError_t launch_ffn_tc(const GroupedFFN& g, DevStatus* st, cudaStream_t s) {
   p2.out = g.y;
   p2.out_f32 = 1;
   p2.ldo = g.d;
+  p2.gperm = nullptr;
   return launch_one(mh, mw2, p2, mt_upper * p2.n_tiles, s);
 }
 

@@ -67,7 +67,14 @@ struct GroupedFFN {
   const void* w2;           // [E, d, F]
   void* h;                  // [max_rows, F] scratch
   float* y;                 // [max_rows, d] float32
+  // Optional (single-CTA kernel only): gather the gate/up GEMM's A rows straight from the
+  // token rows, row r = token gather_perm[r] / gather_k of gather_x [T, d]; x is then unused.
+  const int32_t* gather_perm;
+  int gather_k;
+  const void* gather_x;
 };
+// true when launch_ffn_tc would run the CTA-pair kernel for g (which needs materialised rows)
+bool ffn_uses_pair(const GroupedFFN& g);
 // Tensor-core path.  Picks the CTA-pair kernel (cta_group::2, 256-row tiles) for one group of
 // >= 512 rows or for experts averaging >= 2048 rows (d % 256 == 0), else the single-CTA
 // kernel; the environment variable MOE_B300_GEMM=single|pair|auto overrides the choice (pair

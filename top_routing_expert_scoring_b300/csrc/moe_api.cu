@@ -55,6 +55,23 @@ bool decode_regime(const moe_config& c) {
   return (long long)c.T * c.k <= 64ll * c.E;
 }
 
+// Prefill gate/up GEMM reading its A rows straight from x (no materialised x_perm), on the
+// single-CTA kernel.  Off by default: the warp-wide cp.async gather costs the GEMM more than
+// the separate row copy it saves (measured on Mixtral-, DeepSeekMoE- and V3-shaped layers).
+// MOE_B300_GATHER=fused turns it on.
+bool gather_fused(const moe_config& c, bool dec) {
+  if (dec || c.dtype != MOE_DTYPE_BF16 || c.routing != MOE_ROUTE_TOKEN_CHOICE) return false;
+  const char* env0 = getenv("MOE_B300_GATHER");
+  if (!env0 || strcmp(env0, "fused") != 0) return false;
+  GroupedFFN probe{};
+  probe.uniform_rows = -1;
+  probe.E = c.E;
+  probe.d = c.d_model;
+  probe.F = c.d_ff;
+  probe.max_rows = rows_max(c);
+  return !ffn_uses_pair(probe);
+}
+
 bool decode_split_possible(const moe_config& c) {
   return decode_regime(c) && (long long)c.T * c.k <= kSplitRows;
 }
@@ -305,8 +322,12 @@ namespace {
 
 int run_ffn(const moe_config& c, const void* xin, const int32_t* offsets, const int32_t* mtp,
             int uniform_rows, int E, int F, int max_rows, const void* w13, const void* w2,
-            float* y, void* ws, const Layout& L, cudaStream_t s) {
+            float* y, void* ws, const Layout& L, cudaStream_t s,
+            const int32_t* gather_perm = nullptr, const void* gather_x = nullptr) {
   GroupedFFN g{};
+  g.gather_perm = gather_perm;
+  g.gather_k = c.k;
+  g.gather_x = gather_x;
   g.x = xin;
   g.offsets = offsets;
   g.mtile_prefix = mtp;
@@ -467,12 +488,14 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
         cudaSuccess)
       return MOE_ERR_CUDA;
     const bool dec = decode_regime(*c);
+    const bool fuse = gather_fused(*c, dec);
     DispatchBufs b{at<uint32_t>(ws, L.bitmap), at<int32_t>(ws, L.blk_base),
                    at<int32_t>(ws, L.counts), at<int32_t>(ws, L.kept),
                    at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.mtp),
                    n_dropped ? n_dropped : at<int32_t>(ws, L.n_dropped), at<int32_t>(ws, L.pos),
                    at<int32_t>(ws, L.row_of), at<int32_t>(ws, L.perm)};
-    if ((e = launch_dispatch(*c, capacity_of(*c), idx, b, x, at<void>(ws, L.x_perm), dst, s,
+    if ((e = launch_dispatch(*c, capacity_of(*c), idx, b, fuse ? nullptr : x,
+                             fuse ? nullptr : at<void>(ws, L.x_perm), dst, s,
                              dec && shared != nullptr)) != cudaSuccess)
       return MOE_ERR_CUDA;
     if (dec) {
@@ -511,7 +534,8 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
     } else {
       if (mark(ev_begin) != cudaSuccess) return MOE_ERR_CUDA;
       if ((st = run_ffn(*c, at<void>(ws, L.x_perm), b.offsets, b.mtile_prefix, -1, c->E,
-                        c->d_ff, rows_max(*c), w13, w2, at<float>(ws, L.y_perm), ws, L, s)))
+                        c->d_ff, rows_max(*c), w13, w2, at<float>(ws, L.y_perm), ws, L, s,
+                        fuse ? b.perm : nullptr, fuse ? x : nullptr)))
         return st;
       if (mark(ev_end) != cudaSuccess) return MOE_ERR_CUDA;
       if (shared && (st = run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13,
