@@ -12,9 +12,15 @@
 
 namespace moe {
 
-// Columns per warp: a token's row is split over ceil(d / 512) warps so that small batches still
-// spread over the GPU (each lane handles 4 columns per 128-column step).
+// Columns per warp: a token's row is split over ceil(d / slice) warps, slice = 512 while that
+// still gives >= 2048 warps, else 256 or 128, so that decode batches still spread over the GPU
+// (each lane handles 4 columns per 128-column step).
 constexpr int kCombineSlice = 512;
+inline int combine_slice(const moe_config& c) {
+  for (int sl = kCombineSlice; sl > 128; sl >>= 1)
+    if ((long long)c.T * ceil_div(c.d_model, sl) >= 2048) return sl;
+  return 128;
+}
 
 // float4 of y / shared in, 4 output values out (bf16: 8 bytes, float32: 16 bytes).
 template <typename TOut>
@@ -66,14 +72,14 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                      const float* __restrict__ shared,
                                                      TOut* __restrict__ out, int Tn, int d,
                                                      int k, int nsplit, size_t y_stride,
-                                                     size_t shared_stride) {
+                                                     size_t shared_stride, int slice) {
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int slices = ceil_div(d, kCombineSlice);
+  const int slices = ceil_div(d, slice);
   const int t = gw / slices;
   if (t >= Tn) return;
-  const int v0 = (gw - t * slices) * kCombineSlice;
-  const int v1 = min(d, v0 + kCombineSlice);
+  const int v0 = (gw - t * slices) * slice;
+  const int v1 = min(d, v0 + slice);
   int rows[8];
   float ws[8];
 #pragma unroll
@@ -107,15 +113,17 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 cudaError_t launch_combine(const moe_config& c, const float* y_perm, const int32_t* row_of,
                            const float* w, const float* shared_out, void* out, cudaStream_t s,
                            int nsplit, size_t y_stride, size_t shared_stride) {
-  const int blocks = ceil_div(c.T * ceil_div(c.d_model, kCombineSlice) * 32, 256);
+  const int slice = combine_slice(c);
+  const int blocks = ceil_div(c.T * ceil_div(c.d_model, slice) * 32, 256);
   if (c.out_dtype == MOE_DTYPE_F32)
     combine_kernel<float><<<blocks, 256, 0, s>>>(y_perm, row_of, w, shared_out, (float*)out,
                                                  c.T, c.d_model, c.k, nsplit, y_stride,
-                                                 shared_stride);
+                                                 shared_stride, slice);
   else
     combine_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(y_perm, row_of, w, shared_out,
                                                          (__nv_bfloat16*)out, c.T, c.d_model,
-                                                         c.k, nsplit, y_stride, shared_stride);
+                                                         c.k, nsplit, y_stride, shared_stride,
+                                                         slice);
   return cudaGetLastError();
 }
 

@@ -137,6 +137,9 @@ __global__ void __launch_bounds__(kDispatchBlock) dispatch_scatter_kernel(
 
 // T <= 256 (one token block): count, scan, scatter and the row gather in one launch.  Every
 // CTA recomputes the (small) dispatch in shared memory with the same counting scheme as the
+// 16-byte vectors per row segment copied by one warp in the small dispatch (2 KB)
+constexpr int kSmallCopySeg = 128;
+
 // three-kernel path (bitmap of the tokens per expert, scans, popcount ranks), so the results
 // are identical; CTA 0 publishes it, and all CTAs copy their share of the rows: routed rows
 // [0, nkept), then (append_shared) the T token rows after them for the shared experts.
@@ -238,15 +241,30 @@ __global__ void __launch_bounds__(kDispatchBlock) dispatch_small_kernel(
   if (lead)
     for (int r = tid; r < T * k; r += blockDim.x) perm[r] = r < nkept ? s_perm[r] : -1;
   if (x == nullptr) return;
-  // row copies: warp-granular, grid-strided over routed rows then appended rows
+  // row copies: one warp per 2 KB segment of a row (routed rows, then appended rows), four
+  // 16-byte loads in flight per lane
   const int lane = tid & 31;
   const int nrows = nkept + (append_shared ? T : 0);
+  const int n16 = row_bytes / 16;
+  const int segs = ceil_div(n16, kSmallCopySeg);
   const int warps = (gridDim.x * blockDim.x) >> 5;
-  for (int r = (blockIdx.x * blockDim.x + tid) >> 5; r < nrows; r += warps) {
+  for (int item = (blockIdx.x * blockDim.x + tid) >> 5; item < nrows * segs; item += warps) {
+    const int r = item / segs, sg = item - r * segs;
     const int src_t = r < nkept ? s_perm[r] / k : r - nkept;
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)src_t * row_bytes);
     uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)r * row_bytes);
-    for (int i = lane; i < row_bytes / 16; i += 32) dst[i] = __ldg(src + i);
+    const int i0 = sg * kSmallCopySeg, i1 = min(n16, i0 + kSmallCopySeg);
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + lane + 32 * u;
+      if (i < i1) v[u] = __ldg(src + i);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + lane + 32 * u;
+      if (i < i1) dst[i] = v[u];
+    }
   }
 }
 
@@ -309,7 +327,8 @@ cudaError_t launch_dispatch(const moe_config& c, int capacity, const int32_t* id
   const int row_bytes = c.d_model * esz;
   if (nblk == 1) {
     const int rows = c.T * c.k + (append_shared ? c.T : 0);
-    int blocks = x ? ceil_div(rows, 8) : 1;
+    const int items = rows * ceil_div(row_bytes / 16, kSmallCopySeg);
+    int blocks = x ? ceil_div(items, 8) : 1;
     if (blocks > num_sms()) blocks = num_sms();
     dispatch_small_kernel<<<blocks, kDispatchBlock, 0, s>>>(
         idx, c.T, c.E, c.k, capacity, b.counts, b.kept, b.offsets, b.mtile_prefix, b.n_dropped,

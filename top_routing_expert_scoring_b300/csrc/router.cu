@@ -91,28 +91,37 @@ __global__ void __launch_bounds__(512) router_logits_stream(const uint4* __restr
 #pragma unroll
     for (int e = 0; e < EP; ++e) acc[e] = 0.f;
     const uint4* xr = x + (size_t)t * d8;
-    for (int c = lane; c < d8; c += 32) {
-      const uint4 xv = __ldg(xr + c);
-      const __nv_bfloat162* xh = reinterpret_cast<const __nv_bfloat162*>(&xv);
-      float xf[8];
+    // four independent 16-byte loads in flight per lane, then their products in order
+    for (int c0 = lane; c0 < d8; c0 += 128) {
+      uint4 xv[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(xh[i]);
-        xf[2 * i] = f.x;
-        xf[2 * i + 1] = f.y;
-      }
+      for (int u = 0; u < 4; ++u)
+        xv[u] = c0 + 32 * u < d8 ? __ldg(xr + c0 + 32 * u) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-      for (int e = 0; e < EP; ++e) {
-        const uint4 wv = wsm[e * d8 + c];
-        const __nv_bfloat162* wh = reinterpret_cast<const __nv_bfloat162*>(&wv);
-        float a = acc[e];
+      for (int u = 0; u < 4; ++u) {
+        const int c = c0 + 32 * u;
+        if (c >= d8) break;
+        const __nv_bfloat162* xh = reinterpret_cast<const __nv_bfloat162*>(&xv[u]);
+        float xf[8];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float2 f = __bfloat1622float2(wh[i]);
-          a = fmaf(xf[2 * i], f.x, a);
-          a = fmaf(xf[2 * i + 1], f.y, a);
+          const float2 f = __bfloat1622float2(xh[i]);
+          xf[2 * i] = f.x;
+          xf[2 * i + 1] = f.y;
         }
-        acc[e] = a;
+#pragma unroll
+        for (int e = 0; e < EP; ++e) {
+          const uint4 wv = wsm[e * d8 + c];
+          const __nv_bfloat162* wh = reinterpret_cast<const __nv_bfloat162*>(&wv);
+          float a = acc[e];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(wh[i]);
+            a = fmaf(xf[2 * i], f.x, a);
+            a = fmaf(xf[2 * i + 1], f.y, a);
+          }
+          acc[e] = a;
+        }
       }
     }
 #pragma unroll
