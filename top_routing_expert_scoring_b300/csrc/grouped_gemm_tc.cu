@@ -500,6 +500,18 @@ bool make_map_box(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols
   return make_map_strided(m, base, rows, cols, cols, box_rows);
 }
 
+bool make_map_f32_store(CUtensorMap* m, void* base, uint64_t rows, uint64_t cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 4};
+  cuuint32_t box[2] = {32u, 32u};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                  uint32_t box_rows) {
   auto fn = encode_fn();

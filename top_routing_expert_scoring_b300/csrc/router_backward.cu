@@ -228,8 +228,10 @@ constexpr int MN_ATOM = 64 * BK * 2;          // one 64-column MN-major box: 8 K
 constexpr int TMEM_COLS = 512;
 constexpr int THREADS = 192;
 constexpr int NBARS = 2 * STAGES + 5;
-constexpr int STAGE_OUT = 32 * 32 * 4;       // per epilogue warp: 32 rows x 32 fp32 columns
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * (A_STAGE + B_STAGE) + 256 + 4 * STAGE_OUT;
+constexpr int STAGE_OUT = 32 * 32 * 4;       // one 32-row x 32-column fp32 chunk, 4 KB
+// ring | per epilogue warp two chunk buffers (1024-byte aligned, 128-byte swizzle) | barriers
+constexpr size_t SMEM_BYTES =
+    1024 + (size_t)STAGES * (A_STAGE + B_STAGE) + 4 * 2 * STAGE_OUT + 256;
 
 struct Params {
   int M, N, KB;           // rows of D, MMA N, K blocks of 64
@@ -270,13 +272,15 @@ __device__ __forceinline__ Tile tile_of(int tile, const Params& p) {
 
 __global__ void __launch_bounds__(THREADS, 1)
     router_grad_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                            const __grid_constant__ CUtensorMap tmB, const Params p) {
+                            const __grid_constant__ CUtensorMap tmB,
+                            const __grid_constant__ CUtensorMap tmO, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_STAGE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_STAGE);
+  uint8_t* sOut = sB + STAGES * B_STAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + 4 * 2 * STAGE_OUT);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -404,8 +408,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------- epilogue -----------------------------------------------
     const int q = warp & 3;
     const int r = q * 32 + lane;
-    float* stage_out = reinterpret_cast<float*>(sB + STAGES * B_STAGE + 256) +
-                       (warp - 2) * (STAGE_OUT / 4);
+    const uint32_t out_buf0 = smem_u32(sOut) + (warp - 2) * 2 * STAGE_OUT;
+    int ob = 0;
     int acc = 0;
     uint32_t aph = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -425,26 +429,26 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t vr[32];
         tmem_ld32(tb + c * 32, vr);
         if (p.out_mode == 0) {
-          // Through this warp's shared buffer so that each store instruction writes 4 rows x
-          // 128 contiguous bytes (full lines) instead of 32 rows x 16 bytes.  16-byte chunk j of
-          // row i sits at chunk j ^ (i & 7): conflict-free both ways.
+          // The warp's 32 rows x 32 columns go to one of its two shared buffers in the
+          // 128-byte-swizzled layout (16-byte chunk j of row i at chunk j ^ (i & 7):
+          // conflict-free), then leave as one TMA store; rows past M are clipped by the TMA.
+          const uint32_t buf = out_buf0 + ob * STAGE_OUT;
+          if (lane == 0) bulk_wait_read<1>();     // the store that used this buffer has read it
+          __syncwarp();
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<uint4*>(stage_out + lane * 32 + ((j ^ (lane & 7)) << 2)) =
-                make_uint4(vr[4 * j], vr[4 * j + 1], vr[4 * j + 2], vr[4 * j + 3]);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             buf + lane * 128 + ((j ^ (lane & 7)) << 4)),
+                         "r"(vr[4 * j]), "r"(vr[4 * j + 1]), "r"(vr[4 * j + 2]),
+                         "r"(vr[4 * j + 3])
+                         : "memory");
+          fence_async_smem();
           __syncwarp();
-          const int jj = lane & 7;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int row = 4 * i + (lane >> 3);
-            const uint4 v =
-                *reinterpret_cast<const uint4*>(stage_out + row * 32 + ((jj ^ (row & 7)) << 2));
-            const int mr = ti.mt * BM + q * 32 + row;
-            if (mr < p.M)
-              *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(mr) * p.ldo + n0 + c * 32 +
-                                        jj * 4) = v;
+          if (lane == 0) {
+            tma_store_2d(&tmO, buf, n0 + c * 32, ti.mt * BM + q * 32);
+            bulk_commit();
           }
-          __syncwarp();
+          ob ^= 1;
         } else if (live) {
           // column n of this row goes to row n of the transposed partial: lanes hold
           // consecutive m, so each store instruction writes 128 contiguous bytes
@@ -463,6 +467,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       acc ^= 1;
       if (acc == 0) aph ^= 1u;
     }
+    if (lane == 0) bulk_wait_all();              // this warp's TMA stores are complete
   }
 
   __syncthreads();
@@ -475,7 +480,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const Params& p, cudaStream_t s) {
+cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
+                   const Params& p, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(router_grad_gemm_kernel,
@@ -487,7 +493,7 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const Params& p, 
   const int total = p.m_tiles * p.n_tiles * p.splits;
   int grid = num_sms();
   if (total < grid) grid = total;
-  router_grad_gemm_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(a, b, p);
+  router_grad_gemm_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(a, b, o, p);
   return cudaGetLastError();
 }
 
@@ -709,7 +715,7 @@ int moe_router_backward(const moe_config* c, const void* x, const void* w_gate,
   p.n_valid = E;
   p.st = dst;
   p.out = L.splits > 1 ? at_bw<float>(ws, L.part) : d_w_gate;
-  e = rg::launch(ma, mb, p, s);
+  e = rg::launch(ma, mb, mb, p, s);   // transposed-partial mode: no store map
   if (e == cudaSuccess && L.splits > 1) {
     const long long n4 = (long long)E * d / 4;
     splitk_reduce_kernel<<<num_sms() * 4, 256, 0, s>>>(at_bw<const float4>(ws, L.part),
@@ -726,6 +732,8 @@ int moe_router_backward(const moe_config* c, const void* x, const void* w_gate,
     if (!tc::make_map_box(&mx2, a.dg16, (uint64_t)T, (uint64_t)E64, 128) ||
         !tc::make_map_box(&mw2, w_gate, (uint64_t)E, (uint64_t)d, 64))
       return MOE_ERR_CUDA;
+    CUtensorMap mo;
+    if (!tc::make_map_f32_store(&mo, d_x, (uint64_t)T, (uint64_t)d)) return MOE_ERR_CUDA;
     rg::Params q{};
     q.M = T;
     q.N = bn;
@@ -740,7 +748,7 @@ int moe_router_backward(const moe_config* c, const void* x, const void* w_gate,
     q.ldo = d;
     q.n_valid = d;
     q.st = dst;
-    e = rg::launch(mx2, mw2, q, s);
+    e = rg::launch(mx2, mw2, mo, q, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   return MOE_OK;

@@ -65,6 +65,31 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// TMA store of one box from shared memory, tracked in the issuing thread's bulk group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// wait until at most N of this thread's bulk groups still read their shared-memory source
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// wait until all of this thread's bulk groups have completed
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// order this thread's generic shared-memory writes before later async-proxy (TMA) reads
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -148,6 +173,9 @@ bool make_map_box(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols
 // rows with the 128-byte swizzle: the same shared-memory layout as a 64-column bf16 box.
 bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                  uint32_t box_rows);
+// 2-D float32 tensor [rows, cols] written by TMA stores of 32 x 32 boxes from shared memory laid
+// out with the 128-byte swizzle (16-byte chunk j of row r at chunk j ^ (r & 7)).
+bool make_map_f32_store(CUtensorMap* m, void* base, uint64_t rows, uint64_t cols);
 // Same for rows that lie row_stride elements apart (row_stride * 2 a multiple of 16 bytes).
 bool make_map_strided(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                       uint64_t row_stride, uint32_t box_rows);
