@@ -454,14 +454,9 @@ __global__ void __launch_bounds__(1024) swiglu_quant_kernel(const float* __restr
 
 static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& as, const CUtensorMap& b,
                           const CUtensorMap& bs, Params p, int upper_tiles, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_gemm_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(SMEM_LIMIT));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(decode_gemm_kernel),
+                                 static_cast<int>(SMEM_LIMIT));
+  if (e != cudaSuccess) return e;
   const int np_max = p.NP > p.NPs ? p.NP : p.NPs;
   p.stage = stage_bytes(np_max);
   p.stages = num_stages(np_max);
@@ -534,13 +529,8 @@ cudaError_t launch_ffn_decode(const DecodeFFN& g, DevStatus* st, cudaStream_t s)
   cudaError_t err = launch(ma1, mas1, mb1, mbs1, p1, chunks_upper * wbmax1 * g.ksplit1, s);
   if (err != cudaSuccess) return err;
   if (g.fp8) {
-    static bool attr = false;
-    if (!attr) {
-      err = cudaFuncSetAttribute(swiglu_quant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 200 * 1024);
-      if (err != cudaSuccess) return err;
-      attr = true;
-    }
+    err = smem_attr_once(reinterpret_cast<const void*>(swiglu_quant_kernel), 200 * 1024);
+    if (err != cudaSuccess) return err;
     int threads = Fmax / 4;
     threads = threads > 1024 ? 1024 : (threads + 31) / 32 * 32;
     swiglu_quant_kernel<<<g.max_rows, threads, static_cast<size_t>(Fmax) * 4, s>>>(

@@ -532,18 +532,10 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
 
 static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const Params& p,
                               int upper_tiles, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(SMEM_BYTES));
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(SMEM_BYTES));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  const void* fn = p.gperm ? reinterpret_cast<const void*>(grouped_gemm_tc_kernel<true>)
+                           : reinterpret_cast<const void*>(grouped_gemm_tc_kernel<false>);
+  cudaError_t e = smem_attr_once(fn, static_cast<int>(SMEM_BYTES));
+  if (e != cudaSuccess) return e;
   int grid = num_sms();
   if (upper_tiles < grid) grid = upper_tiles;
   if (grid < 1) grid = 1;

@@ -435,14 +435,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 cudaError_t launch_tc2(const CUtensorMap& a, const CUtensorMap& b, const tc2::Params& p,
                        int upper_pair_tiles, cudaStream_t s) {
   using namespace tc2;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc2_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(SMEM_BYTES));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e0 = smem_attr_once(reinterpret_cast<const void*>(grouped_gemm_tc2_kernel),
+                                  static_cast<int>(SMEM_BYTES));
+  if (e0 != cudaSuccess) return e0;
   int clusters = num_sms() / 2;
   if (upper_pair_tiles < clusters) clusters = upper_pair_tiles;
   if (clusters < 1) clusters = 1;

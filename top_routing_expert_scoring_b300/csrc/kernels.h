@@ -1,6 +1,10 @@
 // Host-side launchers of the MoE layer kernels.  Each returns cudaSuccess or the launch error.
 #pragma once
 
+#include <mutex>
+#include <set>
+#include <utility>
+
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -145,5 +149,20 @@ cudaError_t launch_gather_ec(const moe_config& c, const int32_t* ec_tokens, cons
 cudaError_t launch_timeout_probe(DevStatus* st, int limit_us, cudaStream_t s);
 
 int num_sms();
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (device, kernel): a process that
+// drives several GPUs gets the attribute on each of them.
+inline cudaError_t smem_attr_once(const void* func, int bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<int, const void*>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({dev, func})) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert({dev, func});
+  return e;
+}
 
 }  // namespace moe

@@ -137,13 +137,9 @@ static cudaError_t launch_stream(const moe_config& c, const void* x, const void*
                                  float* logits, cudaStream_t s) {
   const int d8 = c.d_model / 8;
   const size_t smem = (size_t)EP * d8 * sizeof(uint4);
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(router_logits_stream<EP>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(router_logits_stream<EP>),
+                                 200 * 1024);
+  if (e != cudaSuccess) return e;
   // one CTA of 16 warps per SM: the router weights are staged once per SM, and each warp
   // then streams its share of the token rows
   int blocks = ceil_div(c.T, 16);

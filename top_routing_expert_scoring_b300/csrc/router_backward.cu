@@ -482,14 +482,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
                    const Params& p, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(router_grad_gemm_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(SMEM_BYTES));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(router_grad_gemm_kernel),
+                                 static_cast<int>(SMEM_BYTES));
+  if (e != cudaSuccess) return e;
   const int total = p.m_tiles * p.n_tiles * p.splits;
   int grid = num_sms();
   if (total < grid) grid = total;
