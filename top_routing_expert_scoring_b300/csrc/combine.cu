@@ -73,6 +73,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                      TOut* __restrict__ out, int Tn, int d,
                                                      int k, int nsplit, size_t y_stride,
                                                      size_t shared_stride, int slice) {
+  pdl_prologue();
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int slices = ceil_div(d, slice);
@@ -116,11 +117,11 @@ cudaError_t launch_combine(const moe_config& c, const float* y_perm, const int32
   const int slice = combine_slice(c);
   const int blocks = ceil_div(c.T * ceil_div(c.d_model, slice) * 32, 256);
   if (c.out_dtype == MOE_DTYPE_F32)
-    combine_kernel<float><<<blocks, 256, 0, s>>>(y_perm, row_of, w, shared_out, (float*)out,
+    launch_pdl(combine_kernel<float>, blocks, 256, 0, s, y_perm, row_of, w, shared_out, (float*)out,
                                                  c.T, c.d_model, c.k, nsplit, y_stride,
                                                  shared_stride, slice);
   else
-    combine_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(y_perm, row_of, w, shared_out,
+    launch_pdl(combine_kernel<__nv_bfloat16>, blocks, 256, 0, s, y_perm, row_of, w, shared_out,
                                                          (__nv_bfloat16*)out, c.T, c.d_model,
                                                          c.k, nsplit, y_stride, shared_stride,
                                                          slice);
@@ -136,6 +137,7 @@ __global__ void __launch_bounds__(256) combine_ec_kernel(const float* __restrict
                                                         const float* __restrict__ w_flat,
                                                         const float* __restrict__ shared,
                                                         TOut* __restrict__ out, int Tn, int d) {
+  pdl_prologue();
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int slices = ceil_div(d, kCombineSlice);
@@ -160,10 +162,10 @@ cudaError_t launch_combine_ec(const moe_config& c, const float* y_perm, const in
                               const float* shared_out, void* out, cudaStream_t s) {
   const int blocks = ceil_div(c.T * ceil_div(c.d_model, kCombineSlice) * 32, 256);
   if (c.out_dtype == MOE_DTYPE_F32)
-    combine_ec_kernel<float><<<blocks, 256, 0, s>>>(y_perm, tok_ptr, tok_rows, ec_w_flat,
+    launch_pdl(combine_ec_kernel<float>, blocks, 256, 0, s, y_perm, tok_ptr, tok_rows, ec_w_flat,
                                                     shared_out, (float*)out, c.T, c.d_model);
   else
-    combine_ec_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(
+    launch_pdl(combine_ec_kernel<__nv_bfloat16>, blocks, 256, 0, s, 
         y_perm, tok_ptr, tok_rows, ec_w_flat, shared_out, (__nv_bfloat16*)out, c.T, c.d_model);
   return cudaGetLastError();
 }

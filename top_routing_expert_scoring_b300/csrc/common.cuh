@@ -65,6 +65,16 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Programmatic dependent launch.  Every kernel of the layer starts with this: it waits until the
+// grids it depends on have completed and their writes are visible (a no-op when the kernel was
+// launched without the programmatic-serialization attribute), then lets the next kernel's CTAs
+// be scheduled, so its launch overlaps this kernel's run.  No global memory is touched before
+// the wait, so neither read-after-write nor write-after-read across kernels can race.
+__device__ __forceinline__ void pdl_prologue() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Rows of one M tile of the expert GEMMs.
 constexpr int kTileM = 128;
 // Tokens per dispatch block (one thread per token).

@@ -118,6 +118,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                        const __grid_constant__ CUtensorMap tmAs,
                        const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmBs, const Params p) {
+  pdl_prologue();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -380,6 +381,7 @@ __global__ void __launch_bounds__(256) swiglu_finalize_kernel(const float* __res
                                                              const int32_t* __restrict__ offsets,
                                                              int E, int T, int F, int Fs, int ldo,
                                                              __nv_bfloat16* __restrict__ h) {
+  pdl_prologue();
   const int nk = offsets[E];
   const int rows = nk + T;
   const size_t total = static_cast<size_t>(rows) * ldo;
@@ -409,6 +411,7 @@ __global__ void __launch_bounds__(1024) swiglu_quant_kernel(const float* __restr
                                                            int Fs, int ldo,
                                                            uint8_t* __restrict__ h8,
                                                            float* __restrict__ hs) {
+  pdl_prologue();
   extern __shared__ float4 hrow4[];
   __shared__ float red[32];
   const int nk = offsets[E];
@@ -464,7 +467,7 @@ static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& as, const CUt
   int grid = num_sms();
   if (upper_tiles < grid) grid = upper_tiles;
   if (grid < 1) grid = 1;
-  decode_gemm_kernel<<<grid, THREADS, smem, s>>>(a, as, b, bs, p);
+  launch_pdl(decode_gemm_kernel, grid, THREADS, smem, s, a, as, b, bs, p);
   return cudaGetLastError();
 }
 
@@ -472,6 +475,7 @@ static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& as, const CUt
 
 cudaError_t launch_ffn_decode(const DecodeFFN& g, DevStatus* st, cudaStream_t s) {
   using namespace dec;
+  if (g.np > NP_MAX || g.np_shared > NP_MAX) return cudaErrorInvalidValue;
   const bool sh = g.F_shared > 0;
   const int Fmax = g.F > g.F_shared ? g.F : g.F_shared;
   // bf16: boxes of 64 elements; E4M3: boxes of 128 one-byte codes (the same 128-byte rows)
@@ -533,7 +537,7 @@ cudaError_t launch_ffn_decode(const DecodeFFN& g, DevStatus* st, cudaStream_t s)
     if (err != cudaSuccess) return err;
     int threads = Fmax / 4;
     threads = threads > 1024 ? 1024 : (threads + 31) / 32 * 32;
-    swiglu_quant_kernel<<<g.max_rows, threads, static_cast<size_t>(Fmax) * 4, s>>>(
+    launch_pdl(swiglu_quant_kernel, g.max_rows, threads, static_cast<size_t>(Fmax) * 4, s, 
         g.gu, p1.part_stride, g.ksplit1, g.offsets, g.E, sh ? g.T : 0, g.F,
         sh ? g.F_shared : 0, Fmax, static_cast<uint8_t*>(g.h), g.hs);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
@@ -541,7 +545,7 @@ cudaError_t launch_ffn_decode(const DecodeFFN& g, DevStatus* st, cudaStream_t s)
     const long long work = static_cast<long long>(g.max_rows) * Fmax;
     int blocks = static_cast<int>((work + 255) / 256);
     if (blocks > num_sms() * 8) blocks = num_sms() * 8;
-    swiglu_finalize_kernel<<<blocks, 256, 0, s>>>(g.gu, p1.part_stride, g.ksplit1, g.offsets, g.E,
+    launch_pdl(swiglu_finalize_kernel, blocks, 256, 0, s, g.gu, p1.part_stride, g.ksplit1, g.offsets, g.E,
                                                   g.T, g.F, sh ? g.F_shared : 0, Fmax,
                                                   static_cast<__nv_bfloat16*>(g.h));
     if ((err = cudaGetLastError()) != cudaSuccess) return err;

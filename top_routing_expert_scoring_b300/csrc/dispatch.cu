@@ -22,6 +22,7 @@ constexpr int kWords = kDispatchBlock / 32;   // bitmap words per expert per blo
 __global__ void __launch_bounds__(kDispatchBlock) dispatch_count_kernel(
     const int32_t* __restrict__ idx, int T, int E, int k, uint32_t* __restrict__ bitmap,
     int32_t* __restrict__ blk_cnt, DevStatus* st) {
+  pdl_prologue();
   __shared__ uint32_t bm[256 * kWords];
   const int tid = threadIdx.x;
   for (int i = tid; i < E * kWords; i += blockDim.x) bm[i] = 0u;
@@ -61,6 +62,7 @@ __global__ void __launch_bounds__(256) dispatch_scan_kernel(int32_t* __restrict_
                                                            int32_t* __restrict__ offsets,
                                                            int32_t* __restrict__ mtile_prefix,
                                                            int32_t* __restrict__ n_dropped) {
+  pdl_prologue();
   __shared__ int s_kept[256];
   __shared__ int s_mt[256];
   __shared__ int s_drop[256];
@@ -109,6 +111,7 @@ __global__ void __launch_bounds__(kDispatchBlock) dispatch_scatter_kernel(
     const uint32_t* __restrict__ bitmap, const int32_t* __restrict__ blk_base,
     const int32_t* __restrict__ offsets, int32_t* __restrict__ pos, int32_t* __restrict__ row_of,
     int32_t* __restrict__ perm) {
+  pdl_prologue();
   __shared__ uint32_t bm[256 * kWords];
   const int tid = threadIdx.x;
   const uint32_t* gbm = bitmap + (size_t)blockIdx.x * E * kWords;
@@ -150,6 +153,7 @@ __global__ void __launch_bounds__(kDispatchBlock) dispatch_small_kernel(
     int32_t* __restrict__ pos, int32_t* __restrict__ row_of, int32_t* __restrict__ perm,
     DevStatus* st, const unsigned char* __restrict__ x, unsigned char* __restrict__ x_perm,
     int row_bytes, int append_shared) {
+  pdl_prologue();
   __shared__ uint32_t bm[256 * kWords];
   __shared__ int s_kept[256];
   __shared__ int s_mt[256];
@@ -276,6 +280,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const int32_t* __restr
                                                          int32_t* __restrict__ perm,
                                                          const unsigned char* __restrict__ x,
                                                          unsigned char* __restrict__ x_perm) {
+  pdl_prologue();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int nkept = offsets[E];
@@ -298,6 +303,7 @@ __global__ void __launch_bounds__(256) append_rows_kernel(const int32_t* __restr
                                                          int E, int T, int row_bytes,
                                                          const unsigned char* __restrict__ x,
                                                          unsigned char* __restrict__ x_perm) {
+  pdl_prologue();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const size_t base = (size_t)offsets[E];
@@ -313,7 +319,7 @@ cudaError_t launch_append_rows(const moe_config& c, const int32_t* offsets, cons
   const int row_bytes = c.d_model * (c.dtype == MOE_DTYPE_F32 ? 4 : 2);
   int blocks = ceil_div(c.T, 8);
   if (blocks > num_sms() * 4) blocks = num_sms() * 4;
-  append_rows_kernel<<<blocks, 256, 0, s>>>(offsets, c.E, c.T, row_bytes,
+  launch_pdl(append_rows_kernel, blocks, 256, 0, s, offsets, c.E, c.T, row_bytes,
                                             (const unsigned char*)x, (unsigned char*)x_perm);
   return cudaGetLastError();
 }
@@ -330,19 +336,19 @@ cudaError_t launch_dispatch(const moe_config& c, int capacity, const int32_t* id
     const int items = rows * ceil_div(row_bytes / 16, kSmallCopySeg);
     int blocks = x ? ceil_div(items, 8) : 1;
     if (blocks > num_sms()) blocks = num_sms();
-    dispatch_small_kernel<<<blocks, kDispatchBlock, 0, s>>>(
+    launch_pdl(dispatch_small_kernel, blocks, kDispatchBlock, 0, s, 
         idx, c.T, c.E, c.k, capacity, b.counts, b.kept, b.offsets, b.mtile_prefix, b.n_dropped,
         b.pos, b.row_of, b.perm, st, (const unsigned char*)x, (unsigned char*)x_perm, row_bytes,
         append_shared ? 1 : 0);
     return cudaGetLastError();
   } else {
-    dispatch_count_kernel<<<nblk, kDispatchBlock, 0, s>>>(idx, c.T, c.E, c.k, b.bitmap,
+    launch_pdl(dispatch_count_kernel, nblk, kDispatchBlock, 0, s, idx, c.T, c.E, c.k, b.bitmap,
                                                           b.blk_base, st);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    dispatch_scan_kernel<<<1, 256, 0, s>>>(b.blk_base, nblk, c.E, capacity, b.counts, b.kept,
+    launch_pdl(dispatch_scan_kernel, 1, 256, 0, s, b.blk_base, nblk, c.E, capacity, b.counts, b.kept,
                                            b.offsets, b.mtile_prefix, b.n_dropped);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    dispatch_scatter_kernel<<<nblk, kDispatchBlock, 0, s>>>(idx, c.T, c.E, c.k, capacity,
+    launch_pdl(dispatch_scatter_kernel, nblk, kDispatchBlock, 0, s, idx, c.T, c.E, c.k, capacity,
                                                             b.bitmap, b.blk_base, b.offsets,
                                                             b.pos, b.row_of, b.perm);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
@@ -351,7 +357,7 @@ cudaError_t launch_dispatch(const moe_config& c, int capacity, const int32_t* id
   int blocks = ceil_div(total_rows, 8);
   const int cap_blocks = num_sms() * 8;
   if (blocks > cap_blocks) blocks = cap_blocks;
-  gather_rows_kernel<16><<<blocks, 256, 0, s>>>(b.offsets, c.E, c.k, total_rows, row_bytes,
+  launch_pdl(gather_rows_kernel<16>, blocks, 256, 0, s, b.offsets, c.E, c.k, total_rows, row_bytes,
                                                 b.perm, (const unsigned char*)x,
                                                 (unsigned char*)x_perm);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;

@@ -50,6 +50,7 @@ __device__ int block_exclusive_scan(int v, int* s_warp, int& total) {
 // Per-token softmax normaliser (max, sum of exp) used for the weights.
 __global__ void __launch_bounds__(256) token_softmax_stats(const float* __restrict__ g, int T,
                                                           int E, float2* __restrict__ ms) {
+  pdl_prologue();
   const int lane = threadIdx.x & 31;
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (t >= T) return;
@@ -68,6 +69,7 @@ __global__ void __launch_bounds__(kEcThreads) ec_select_kernel(const float* __re
                                                               int32_t* __restrict__ ec_tokens,
                                                               float* __restrict__ ec_w,
                                                               int32_t* __restrict__ posmap) {
+  pdl_prologue();
   __shared__ int hist[256];
   __shared__ int s_warp[64];
   __shared__ int s_sel[2];
@@ -125,6 +127,7 @@ __global__ void __launch_bounds__(kEcThreads) ec_select_kernel(const float* __re
 
 __global__ void __launch_bounds__(256) ec_count_kernel(const int32_t* __restrict__ posmap, int T,
                                                       int E, int32_t* __restrict__ cnt) {
+  pdl_prologue();
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= T) return;
   int c = 0;
@@ -134,6 +137,7 @@ __global__ void __launch_bounds__(256) ec_count_kernel(const int32_t* __restrict
 
 __global__ void __launch_bounds__(kEcThreads) ec_scan_kernel(const int32_t* __restrict__ cnt,
                                                             int T, int32_t* __restrict__ ptr) {
+  pdl_prologue();
   __shared__ int s_warp[64];
   int run = 0;
   for (int base = 0; base < T; base += kEcThreads) {
@@ -151,6 +155,7 @@ __global__ void __launch_bounds__(256) ec_fill_kernel(const int32_t* __restrict_
                                                      int E, int C,
                                                      const int32_t* __restrict__ ptr,
                                                      int32_t* __restrict__ rows) {
+  pdl_prologue();
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= T) return;
   int o = ptr[t];
@@ -166,15 +171,16 @@ cudaError_t launch_expert_choice(const moe_config& c, const float* logits, int32
                                  cudaStream_t s) {
   (void)st;
   const int C = (int)((long long)c.T * c.k / c.E);
-  token_softmax_stats<<<ceil_div(c.T * 32, 256), 256, 0, s>>>(logits, c.T, c.E, ms);
-  ec_select_kernel<<<c.E, kEcThreads, 0, s>>>(logits, c.T, c.E, C, ms, ec_tokens, ec_w, posmap);
-  ec_count_kernel<<<ceil_div(c.T, 256), 256, 0, s>>>(posmap, c.T, c.E, tok_cnt);
-  ec_scan_kernel<<<1, kEcThreads, 0, s>>>(tok_cnt, c.T, tok_ptr);
-  ec_fill_kernel<<<ceil_div(c.T, 256), 256, 0, s>>>(posmap, c.T, c.E, C, tok_ptr, tok_rows);
+  launch_pdl(token_softmax_stats, ceil_div(c.T * 32, 256), 256, 0, s, logits, c.T, c.E, ms);
+  launch_pdl(ec_select_kernel, c.E, kEcThreads, 0, s, logits, c.T, c.E, C, ms, ec_tokens, ec_w, posmap);
+  launch_pdl(ec_count_kernel, ceil_div(c.T, 256), 256, 0, s, posmap, c.T, c.E, tok_cnt);
+  launch_pdl(ec_scan_kernel, 1, kEcThreads, 0, s, tok_cnt, c.T, tok_ptr);
+  launch_pdl(ec_fill_kernel, ceil_div(c.T, 256), 256, 0, s, posmap, c.T, c.E, C, tok_ptr, tok_rows);
   return cudaGetLastError();
 }
 
 __global__ void ec_offsets_kernel(int E, int C, int32_t* offsets, int32_t* mtp) {
+  pdl_prologue();
   for (int e = threadIdx.x; e <= E; e += blockDim.x) {
     offsets[e] = e * C;
     mtp[e] = e * ceil_div(C, kTileM);
@@ -185,6 +191,7 @@ __global__ void __launch_bounds__(256) gather_by_token_kernel(const int32_t* __r
                                                              int rows, int row_bytes,
                                                              const unsigned char* __restrict__ x,
                                                              unsigned char* __restrict__ xp) {
+  pdl_prologue();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
@@ -199,12 +206,12 @@ cudaError_t launch_gather_ec(const moe_config& c, const int32_t* ec_tokens, cons
                              void* x_perm, int32_t* offsets, int32_t* mtile_prefix,
                              cudaStream_t s) {
   const int C = (int)((long long)c.T * c.k / c.E);
-  ec_offsets_kernel<<<1, 256, 0, s>>>(c.E, C, offsets, mtile_prefix);
+  launch_pdl(ec_offsets_kernel, 1, 256, 0, s, c.E, C, offsets, mtile_prefix);
   const int rows = c.E * C;
   const int esz = c.dtype == MOE_DTYPE_F32 ? 4 : 2;
   int blocks = ceil_div(rows, 8);
   if (blocks > num_sms() * 8) blocks = num_sms() * 8;
-  gather_by_token_kernel<<<blocks, 256, 0, s>>>(ec_tokens, rows, c.d_model * esz,
+  launch_pdl(gather_by_token_kernel, blocks, 256, 0, s, ec_tokens, rows, c.d_model * esz,
                                                 (const unsigned char*)x, (unsigned char*)x_perm);
   return cudaGetLastError();
 }

@@ -51,6 +51,7 @@ __device__ __forceinline__ void locate_tile(int tile, const int32_t* mtp, const 
 
 template <typename T, bool SWIGLU>
 __global__ void __launch_bounds__(256) ffn_simt_kernel(SimtArgs a) {
+  pdl_prologue();
   using TO = typename std::conditional<SWIGLU, T, float>::type;   // h in T, y in float32
   constexpr int TM = kTileM, TN = 64, TK = 16;
   __shared__ float As[TK][TM + 4];
@@ -125,11 +126,11 @@ cudaError_t launch_ffn_simt(const GroupedFFN& g, bool f32, DevStatus* st, cudaSt
                 g.uniform_rows};
   dim3 g1(mtiles, ceil_div(g.F, 64)), g2(mtiles, ceil_div(g.d, 64));
   if (f32) {
-    ffn_simt_kernel<float, true><<<g1, 256, 0, s>>>(up);
-    ffn_simt_kernel<float, false><<<g2, 256, 0, s>>>(down);
+    launch_pdl(ffn_simt_kernel<float, true>, g1, 256, 0, s, up);
+    launch_pdl(ffn_simt_kernel<float, false>, g2, 256, 0, s, down);
   } else {
-    ffn_simt_kernel<__nv_bfloat16, true><<<g1, 256, 0, s>>>(up);
-    ffn_simt_kernel<__nv_bfloat16, false><<<g2, 256, 0, s>>>(down);
+    launch_pdl(ffn_simt_kernel<__nv_bfloat16, true>, g1, 256, 0, s, up);
+    launch_pdl(ffn_simt_kernel<__nv_bfloat16, false>, g2, 256, 0, s, down);
   }
   return cudaGetLastError();
 }

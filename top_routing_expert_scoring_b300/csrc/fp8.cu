@@ -24,6 +24,7 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const __nv_bfloat16*
                                                            int nrows_extra,
                                                            uint8_t* __restrict__ dst,
                                                            float* __restrict__ scale) {
+  pdl_prologue();
   long long nrows = nrows_max;
   if (nrows_base) {
     const long long n = static_cast<long long>(*nrows_base) + nrows_extra;
@@ -77,7 +78,7 @@ cudaError_t launch_quantize_rows(const void* src, long long nrows_max, int cols,
   const long long cap = static_cast<long long>(num_sms()) * 16;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  quantize_rows_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(
+  launch_pdl(quantize_rows_kernel, static_cast<int>(blocks), 256, 0, s, 
       static_cast<const __nv_bfloat16*>(src), nrows_max, cols, nrows_base, nrows_extra, dst,
       scale);
   return cudaGetLastError();

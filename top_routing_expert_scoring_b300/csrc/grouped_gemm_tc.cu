@@ -138,6 +138,7 @@ template <bool GATHER>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, const Params p) {
+  pdl_prologue();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -540,9 +541,9 @@ static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const 
   if (upper_tiles < grid) grid = upper_tiles;
   if (grid < 1) grid = 1;
   if (p.gperm)
-    grouped_gemm_tc_kernel<true><<<grid, THREADS, SMEM_BYTES, s>>>(a, b, p);
+    launch_pdl(grouped_gemm_tc_kernel<true>, grid, THREADS, SMEM_BYTES, s, a, b, p);
   else
-    grouped_gemm_tc_kernel<false><<<grid, THREADS, SMEM_BYTES, s>>>(a, b, p);
+    launch_pdl(grouped_gemm_tc_kernel<false>, grid, THREADS, SMEM_BYTES, s, a, b, p);
   return cudaGetLastError();
 }
 

@@ -41,6 +41,7 @@ constexpr int MAX_E = 256;
 constexpr int NBARS = 2 * STAGES + 5;        // full, empty, tmem full x2, tmem empty x2, drain
 // stages | barriers | tmem slot, abort flag, issued counts | pair-tile prefix
 constexpr size_t CTRL_BYTES = 8 * NBARS + 16 + 4 * STAGES;
+static_assert(CTRL_BYTES <= 256, "the control block must fit its 256-byte slot");
 constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE + 256 + (MAX_E + 1) * 4;
 
 struct Params {
@@ -187,6 +188,7 @@ __device__ __forceinline__ PairTile decode_pair(int tile, const Params& p, const
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB, const Params p) {
+  pdl_prologue();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -446,13 +448,15 @@ cudaError_t launch_tc2(const CUtensorMap& a, const CUtensorMap& b, const tc2::Pa
   cfg.blockDim = dim3(THREADS, 1, 1);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_prologue
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, grouped_gemm_tc2_kernel, a, b, p);
 }
 

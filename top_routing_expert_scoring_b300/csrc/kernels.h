@@ -150,6 +150,25 @@ cudaError_t launch_timeout_probe(DevStatus* st, int limit_us, cudaStream_t s);
 
 int num_sms();
 
+// Launch with the programmatic-serialization attribute: the kernel may be scheduled while the
+// previous kernel in the stream still runs; it waits for it in pdl_prologue() before touching
+// global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (device, kernel): a process that
 // drives several GPUs gets the attribute on each of them.
 inline cudaError_t smem_attr_once(const void* func, int bytes) {

@@ -348,6 +348,7 @@ int run_ffn(const moe_config& c, const void* xin, const int32_t* offsets, const 
 // offsets [E+1] given by the caller: the M-tile prefix the GEMM scheduler needs is rebuilt
 // on the device from them.
 __global__ void mtp_from_offsets(const int32_t* offsets, int E, int32_t* mtp) {
+  pdl_prologue();
   __shared__ int s[256];
   const int e = threadIdx.x;
   int v = 0;
@@ -402,7 +403,7 @@ int moe_expert_ffn(const moe_config* c, const void* x_perm, const int32_t* offse
                                                                              : MOE_ERR_CUDA;
   }
   int32_t* mtp = at<int32_t>(ws, L.mtp);
-  mtp_from_offsets<<<1, 256, 0, s>>>(offsets, c->E, mtp);
+  launch_pdl(mtp_from_offsets, 1, 256, 0, s, offsets, c->E, mtp);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   return run_ffn(*c, x_perm, offsets, mtp, -1, c->E, c->d_ff, rows_max(*c), w13, w2, y_perm, ws,
                  L, s);

@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(256) router_logits_simt(const T* __restrict__ 
                                                          const T* __restrict__ w,
                                                          float* __restrict__ g, int Tn, int d,
                                                          int E) {
+  pdl_prologue();
   constexpr int TT = 32, TE = 64, TK = 32;
   __shared__ float xs[TK][TT + 1];
   __shared__ float wsm[TK][TE + 1];
@@ -78,6 +79,7 @@ __global__ void __launch_bounds__(512) router_logits_stream(const uint4* __restr
                                                            const uint4* __restrict__ w,
                                                            float* __restrict__ g, int Tn,
                                                            int d8, int E) {
+  pdl_prologue();
   extern __shared__ uint4 wsm[];                  // [EP][d8]: 8 bf16 per uint4
   for (int i = threadIdx.x; i < EP * d8; i += blockDim.x) {
     const int e = i / d8;
@@ -144,7 +146,7 @@ static cudaError_t launch_stream(const moe_config& c, const void* x, const void*
   // then streams its share of the token rows
   int blocks = ceil_div(c.T, 16);
   if (blocks > num_sms()) blocks = num_sms();
-  router_logits_stream<EP><<<blocks, 512, smem, s>>>((const uint4*)x, (const uint4*)w_gate, logits,
+  launch_pdl(router_logits_stream<EP>, blocks, 512, smem, s, (const uint4*)x, (const uint4*)w_gate, logits,
                                                      c.T, d8, c.E);
   return cudaGetLastError();
 }
@@ -161,6 +163,7 @@ __global__ void __launch_bounds__(256) router_logits_few(const uint4* __restrict
                                                         const uint4* __restrict__ w,
                                                         float* __restrict__ g, int Tn, int d8,
                                                         int E) {
+  pdl_prologue();
   __shared__ float part[8][TP];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int e = blockIdx.x;
@@ -217,10 +220,10 @@ cudaError_t launch_router_logits(const moe_config& c, const void* x, const void*
                                  float* logits, cudaStream_t s) {
   if (c.dtype == MOE_DTYPE_BF16 && (c.T <= 16 || (c.E <= 32 && c.T <= 512))) {
     if (c.T <= 4)
-      router_logits_few<4><<<c.E, 256, 0, s>>>((const uint4*)x, (const uint4*)w_gate, logits, c.T,
+      launch_pdl(router_logits_few<4>, c.E, 256, 0, s, (const uint4*)x, (const uint4*)w_gate, logits, c.T,
                                                c.d_model / 8, c.E);
     else
-      router_logits_few<16><<<dim3(c.E, ceil_div(c.T, 16)), 256, 0, s>>>(
+      launch_pdl(router_logits_few<16>, dim3(c.E, ceil_div(c.T, 16)), 256, 0, s, 
           (const uint4*)x, (const uint4*)w_gate, logits, c.T, c.d_model / 8, c.E);
     return cudaGetLastError();
   }
@@ -235,10 +238,10 @@ cudaError_t launch_router_logits(const moe_config& c, const void* x, const void*
   }
   dim3 grid(ceil_div(c.T, 32), ceil_div(c.E, 64));
   if (c.dtype == MOE_DTYPE_F32)
-    router_logits_simt<float><<<grid, 256, 0, s>>>((const float*)x, (const float*)w_gate, logits,
+    launch_pdl(router_logits_simt<float>, grid, 256, 0, s, (const float*)x, (const float*)w_gate, logits,
                                                    c.T, c.d_model, c.E);
   else
-    router_logits_simt<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16*)x,
+    launch_pdl(router_logits_simt<__nv_bfloat16>, grid, 256, 0, s, (const __nv_bfloat16*)x,
                                                            (const __nv_bfloat16*)w_gate, logits,
                                                            c.T, c.d_model, c.E);
   return cudaGetLastError();
@@ -334,6 +337,7 @@ __device__ __forceinline__ void write_block_stats(const float (&accP)[V], const 
 
 template <int V>
 __global__ void __launch_bounds__(256) route_topk_kernel(RouteArgs a) {
+  pdl_prologue();
   extern __shared__ float route_smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, wpb = blockDim.x >> 5;
   const int E = a.E, k = a.k;
@@ -476,10 +480,10 @@ cudaError_t launch_route_topk(const moe_config& c, const float* logits, const fl
   const size_t route_bytes = (size_t)wpb * (c.E + 32) * sizeof(float);
   const size_t stats_bytes = (size_t)kAuxWarps * c.E * 8 + kAuxWarps * 4 + 16;
   const size_t smem = route_bytes > stats_bytes ? route_bytes : stats_bytes;
-  if (c.E <= 32) route_topk_kernel<1><<<blocks, wpb * 32, smem, s>>>(a);
-  else if (c.E <= 64) route_topk_kernel<2><<<blocks, wpb * 32, smem, s>>>(a);
-  else if (c.E <= 128) route_topk_kernel<4><<<blocks, wpb * 32, smem, s>>>(a);
-  else route_topk_kernel<8><<<blocks, wpb * 32, smem, s>>>(a);
+  if (c.E <= 32) launch_pdl(route_topk_kernel<1>, blocks, wpb * 32, smem, s, a);
+  else if (c.E <= 64) launch_pdl(route_topk_kernel<2>, blocks, wpb * 32, smem, s, a);
+  else if (c.E <= 128) launch_pdl(route_topk_kernel<4>, blocks, wpb * 32, smem, s, a);
+  else launch_pdl(route_topk_kernel<8>, blocks, wpb * 32, smem, s, a);
   return cudaGetLastError();
 }
 
@@ -501,6 +505,7 @@ struct AuxArgs {
 
 template <int V>
 __global__ void __launch_bounds__(kAuxWarps * 32) aux_partial_kernel(AuxArgs a) {
+  pdl_prologue();
   extern __shared__ unsigned char aux_smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int E = a.E;
@@ -541,6 +546,7 @@ __global__ void __launch_bounds__(1024) aux_final_kernel(const float* part_P,
                                                         const float* part_z, int nblk, int T,
                                                         int E, int ec_C, float* f, float* P,
                                                         float* l_balance, float* z_loss) {
+  pdl_prologue();
   __shared__ float sp[1024];
   __shared__ int sc[1024];
   __shared__ float prod[256];
@@ -603,10 +609,10 @@ cudaError_t launch_aux_stats(const moe_config& c, const float* logits, const int
   const int ecC = c.routing == MOE_ROUTE_EXPERT_CHOICE ? (int)((long long)c.T * c.k / c.E) : 0;
   AuxArgs a{logits, idx, c.T, c.E, c.k, c.score, ecC, part_P, part_cnt, part_z};
   const size_t smem = (size_t)kAuxWarps * c.E * 8 + kAuxWarps * 4 + 16;
-  if (c.E <= 32) aux_partial_kernel<1><<<nblocks, kAuxWarps * 32, smem, s>>>(a);
-  else if (c.E <= 64) aux_partial_kernel<2><<<nblocks, kAuxWarps * 32, smem, s>>>(a);
-  else if (c.E <= 128) aux_partial_kernel<4><<<nblocks, kAuxWarps * 32, smem, s>>>(a);
-  else aux_partial_kernel<8><<<nblocks, kAuxWarps * 32, smem, s>>>(a);
+  if (c.E <= 32) launch_pdl(aux_partial_kernel<1>, nblocks, kAuxWarps * 32, smem, s, a);
+  else if (c.E <= 64) launch_pdl(aux_partial_kernel<2>, nblocks, kAuxWarps * 32, smem, s, a);
+  else if (c.E <= 128) launch_pdl(aux_partial_kernel<4>, nblocks, kAuxWarps * 32, smem, s, a);
+  else launch_pdl(aux_partial_kernel<8>, nblocks, kAuxWarps * 32, smem, s, a);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   return launch_aux_final(c, part_P, part_cnt, part_z, nblocks, f, P, l_balance, z_loss, s);
@@ -616,7 +622,7 @@ cudaError_t launch_aux_final(const moe_config& c, const float* part_P, const int
                              const float* part_z, int nblocks, float* f, float* P,
                              float* l_balance, float* z_loss, cudaStream_t s) {
   const int ecC = c.routing == MOE_ROUTE_EXPERT_CHOICE ? (int)((long long)c.T * c.k / c.E) : 0;
-  aux_final_kernel<<<1, 1024, 0, s>>>(part_P, part_cnt, part_z, nblocks, c.T, c.E, ecC, f, P,
+  launch_pdl(aux_final_kernel, 1, 1024, 0, s, part_P, part_cnt, part_z, nblocks, c.T, c.E, ecC, f, P,
                                       l_balance, z_loss);
   return cudaGetLastError();
 }

@@ -60,6 +60,7 @@ struct ScoresArgs {
 
 template <int V>
 __global__ void __launch_bounds__(kBwWarps * 32) router_bw_scores_kernel(const ScoresArgs a) {
+  pdl_prologue();
   __shared__ __nv_bfloat16 sT[256][kTPad];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t_base = blockIdx.x * kBwTokens;
@@ -274,6 +275,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     router_grad_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmO, const Params p) {
+  pdl_prologue();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -488,7 +490,7 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap
   const int total = p.m_tiles * p.n_tiles * p.splits;
   int grid = num_sms();
   if (total < grid) grid = total;
-  router_grad_gemm_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(a, b, o, p);
+  launch_pdl(router_grad_gemm_kernel, grid, THREADS, SMEM_BYTES, s, a, b, o, p);
   return cudaGetLastError();
 }
 
@@ -497,6 +499,7 @@ cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap
 // dW[e, c] = sum over slices s (in order) of part[s, e, c]
 __global__ void splitk_reduce_kernel(const float4* __restrict__ part, float4* __restrict__ out,
                                      long long n4, int splits) {
+  pdl_prologue();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
        i += (long long)gridDim.x * blockDim.x) {
     float4 a = part[i];
@@ -511,6 +514,7 @@ __global__ void splitk_reduce_kernel(const float4* __restrict__ part, float4* __
 // float32 configuration: dW[e, c] = sum_t dg[t, e] x[t, c]; dx[t, c] = sum_e dg[t, e] W[e, c]
 __global__ void dw_simt_kernel(const float* __restrict__ dg, const float* __restrict__ x,
                                float* __restrict__ dw, int T, int E, int d) {
+  pdl_prologue();
   const long long n = (long long)E * d;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
@@ -522,6 +526,7 @@ __global__ void dw_simt_kernel(const float* __restrict__ dg, const float* __rest
 }
 __global__ void dx_simt_kernel(const float* __restrict__ dg, const float* __restrict__ w,
                                float* __restrict__ dx, int T, int E, int d) {
+  pdl_prologue();
   const long long n = (long long)T * d;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
@@ -534,6 +539,7 @@ __global__ void dx_simt_kernel(const float* __restrict__ dg, const float* __rest
 
 __global__ void bias_update_kernel(const float* __restrict__ f, float* __restrict__ bias, int T,
                                    int k, int E, float gamma) {
+  pdl_prologue();
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= E) return;
   // f = load / T rounded once to float32; load < 2^23, so rint(f * T) is the load exactly
@@ -610,7 +616,7 @@ cudaError_t launch_scores(const ScoresArgs& a, cudaStream_t s) {
   const int V = ceil_div(a.E, 32);
   switch (V) {
 #define MOE_BW_CASE(n) \
-  case n: router_bw_scores_kernel<n><<<grid, kBwWarps * 32, 0, s>>>(a); break;
+  case n: launch_pdl(router_bw_scores_kernel<n>, grid, kBwWarps * 32, 0, s, a); break;
     MOE_BW_CASE(1) MOE_BW_CASE(2) MOE_BW_CASE(3) MOE_BW_CASE(4)
     MOE_BW_CASE(5) MOE_BW_CASE(6) MOE_BW_CASE(7) MOE_BW_CASE(8)
 #undef MOE_BW_CASE
@@ -683,10 +689,10 @@ int moe_router_backward(const moe_config* c, const void* x, const void* w_gate,
 
   const int T = c->T, E = c->E, d = c->d_model;
   if (!tc) {
-    dw_simt_kernel<<<num_sms() * 4, 256, 0, s>>>(dg32, static_cast<const float*>(x), d_w_gate,
+    launch_pdl(dw_simt_kernel, num_sms() * 4, 256, 0, s, dg32, static_cast<const float*>(x), d_w_gate,
                                                  T, E, d);
     if (d_x)
-      dx_simt_kernel<<<num_sms() * 4, 256, 0, s>>>(dg32, static_cast<const float*>(w_gate), d_x,
+      launch_pdl(dx_simt_kernel, num_sms() * 4, 256, 0, s, dg32, static_cast<const float*>(w_gate), d_x,
                                                    T, E, d);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
   }
@@ -713,7 +719,7 @@ int moe_router_backward(const moe_config* c, const void* x, const void* w_gate,
   e = rg::launch(ma, mb, mb, p, s);   // transposed-partial mode: no store map
   if (e == cudaSuccess && L.splits > 1) {
     const long long n4 = (long long)E * d / 4;
-    splitk_reduce_kernel<<<num_sms() * 4, 256, 0, s>>>(at_bw<const float4>(ws, L.part),
+    launch_pdl(splitk_reduce_kernel, num_sms() * 4, 256, 0, s, at_bw<const float4>(ws, L.part),
                                                         reinterpret_cast<float4*>(d_w_gate), n4,
                                                         L.splits);
     e = cudaGetLastError();
@@ -755,7 +761,8 @@ int moe_bias_update(const moe_config* c, const float* f, float* bias, float gamm
   if (!f || !bias) return MOE_ERR_ARG;
   if (!std::isfinite(gamma)) return MOE_ERR_ARG;
   if ((long long)c->T * c->k >= (1ll << 23)) return MOE_ERR_SHAPE;
-  bias_update_kernel<<<ceil_div(c->E, 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+  launch_pdl(bias_update_kernel, ceil_div(c->E, 256), 256, 0, static_cast<cudaStream_t>(stream),
+      
       f, bias, c->T, c->k, c->E, gamma);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
