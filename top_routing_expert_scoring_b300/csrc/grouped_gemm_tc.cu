@@ -64,6 +64,9 @@ struct Params {
   const int32_t* gperm;
   int gk;
   const __nv_bfloat16* gx;
+  // N = 256 only: the last tiles of the list may each run as two N = 128 halves, to even out
+  // the final wave over the CTAs (see choose_tail_split)
+  int tail_split;
   DevStatus* st;
 };
 
@@ -92,6 +95,7 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // ---------------------------------------------------------------------------------------------
 struct TileInfo {
   int e, row0, rows, nt;
+  int col0, bn;             // first output column and MMA N of this tile
 };
 
 __device__ __forceinline__ int total_tiles(const Params& p) {
@@ -125,7 +129,30 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const Params& p) {
   const int mt = tt - ti.nt * mt_e;
   ti.row0 = row_base + mt * BM;
   ti.rows = min(BM, row_end - ti.row0);
+  ti.col0 = ti.nt * p.bn;
+  ti.bn = p.bn;
   return ti;
+}
+
+// With `split` tail halves, the list is total - split whole tiles followed by 2 * split half
+// tiles: half tile h is the left (h even) or right half of whole tile total - split + h / 2.
+__device__ __forceinline__ TileInfo decode_tile(int tile, const Params& p, int total, int split) {
+  const int whole = total - split;
+  if (tile < whole) return decode_tile(tile, p);
+  const int h = tile - whole;
+  TileInfo ti = decode_tile(whole + (h >> 1), p);
+  ti.bn = p.bn >> 1;
+  ti.col0 += (h & 1) * ti.bn;
+  return ti;
+}
+
+// Number of trailing whole tiles to run as halves.  Tile t goes to CTA t mod G (persistent
+// round-robin); a whole tile costs 2, a half tile 1.  With total = qG + r, the unsplit list
+// costs 2(q+1) on its busiest CTA.  Splitting the r tiles of the last partial wave gives 2r
+// halves after q full waves: 2q + 1 when 2r <= G.  For r > G/2, no split beats 2(q+1).
+__device__ __forceinline__ int choose_tail_split(int total, int G) {
+  const int r = total % G;
+  return (r > 0 && 2 * r <= G) ? r : 0;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -182,6 +209,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   const int total = total_tiles(p);
   const int KB = p.K / BK;
+  const int split = p.tail_split ? choose_tail_split(total, gridDim.x) : 0;
+  const int ntiles = total + split;
 
   if (GATHER && warp == 0) {
     // ------------------------ gathering producer (whole warp) -------------------------------
@@ -199,8 +228,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     int hist[kGatherLag];                 // stages of the copy groups still to be signalled
     int npend = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-      const TileInfo ti = decode_tile(tile, p);
+    for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+      const TileInfo ti = decode_tile(tile, p, total, split);
       int tok[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
@@ -212,7 +241,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         b0 = ti.e * p.b_rows + ti.nt * 128;
         b1 = b0 + p.up_off;
       } else {
-        b0 = ti.e * p.b_rows + ti.nt * p.bn;
+        b0 = ti.e * p.b_rows + ti.col0;
         b1 = b0 + 128;
       }
       for (int kb = 0; kb < KB; ++kb) {
@@ -271,17 +300,18 @@ __global__ void __launch_bounds__(THREADS, 1)
     int stage = 0;
     uint32_t ph = 0;
     uint32_t issued = 0, last_par = 0;   // per-stage bit masks for the drain
-    const int nbox = (p.swiglu || p.bn > 128) ? 2 : 1;
-    const uint32_t bytes = A_STAGE + nbox * B_BOX;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-      const TileInfo ti = decode_tile(tile, p);
+    for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+      const TileInfo ti = decode_tile(tile, p, total, split);
+      // B: two 128-row boxes (SwiGLU gate + up, or N = 256), else one
+      const int nbox = (p.swiglu || ti.bn > 128) ? 2 : 1;
+      const uint32_t bytes = A_STAGE + nbox * B_BOX;
       int b0, b1;
       if (p.swiglu) {
         b0 = ti.e * p.b_rows + ti.nt * 128;
         b1 = b0 + p.up_off;
       } else {
-        b0 = ti.e * p.b_rows + ti.nt * p.bn;
+        b0 = ti.e * p.b_rows + ti.col0;
         b1 = b0 + 128;
       }
       for (int kb = 0; kb < KB; ++kb) {
@@ -310,14 +340,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------- MMA issuer ---------------------------------------------
-    const uint32_t idesc_full = idesc_bf16_f32(BM, p.bn);
-    const uint32_t idesc_half = idesc_bf16_f32(64, p.bn);
     int stage = 0, acc = 0;
     uint32_t ph = 0, aph = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
+    for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
       // an expert's last tile with <= 64 rows runs as an M = 64 MMA (half the tensor work)
-      const uint32_t idesc = decode_tile(tile, p).rows <= 64 ? idesc_half : idesc_full;
+      const TileInfo tm = decode_tile(tile, p, total, split);
+      const uint32_t idesc = idesc_bf16_f32(tm.rows <= 64 ? 64 : BM, tm.bn);
       if (!wait_bounded(tempty0 + 8 * acc, aph ^ 1u, abort_flag, p.st, 2, true)) {
         ok = false;
         break;
@@ -356,8 +385,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int r = q * 32 + lane;            // row of the tile held by this thread
     int acc = 0;
     uint32_t aph = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const TileInfo ti = decode_tile(tile, p);
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+      const TileInfo ti = decode_tile(tile, p, total, split);
       int ok = 1;
       if (lane == 0) ok = wait_bounded(tfull0 + 8 * acc, aph, abort_flag, p.st, 4, true) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -398,8 +427,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       } else if (p.out_f32) {
         float* orow = static_cast<float*>(p.out) + static_cast<size_t>(ti.row0 + row) * p.ldo +
-                      ti.nt * p.bn;
-        const int nchunks = p.bn / 32;
+                      ti.col0;
+        const int nchunks = ti.bn / 32;
 #pragma unroll 1
         for (int c = 0; c < nchunks; ++c) {
           uint32_t vr[32];
@@ -413,8 +442,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       } else {
         __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
-                              static_cast<size_t>(ti.row0 + row) * p.ldo + ti.nt * p.bn;
-        const int nchunks = p.bn / 32;
+                              static_cast<size_t>(ti.row0 + row) * p.ldo + ti.col0;
+        const int nchunks = ti.bn / 32;
 #pragma unroll 1
         for (int c = 0; c < nchunks; ++c) {
           uint32_t vr[32];
@@ -610,6 +639,7 @@ cudaError_t launch_ffn_tc(const GroupedFFN& g, DevStatus* st, cudaStream_t s) {
   p2.out_f32 = 1;
   p2.ldo = g.d;
   p2.gperm = nullptr;
+  p2.tail_split = p2.bn == 256 ? 1 : 0;
   return launch_one(mh, mw2, p2, mt_upper * p2.n_tiles, s);
 }
 
