@@ -55,7 +55,7 @@ enum {
   MOE_OK = 0,
   MOE_ERR_ARG = -1,          /* NULL pointer or bad enum value */
   MOE_ERR_SHAPE = -2,        /* sizes out of range or not aligned as required */
-  MOE_ERR_UNSUPPORTED = -3,  /* a valid request this build does not implement */
+  MOE_ERR_UNSUPPORTED = -3,  /* a valid request this library does not implement */
   MOE_ERR_WORKSPACE = -4,    /* workspace NULL, too small or misaligned */
   MOE_ERR_CUDA = -5,         /* a CUDA runtime call failed */
   MOE_ERR_TIMEOUT = -6       /* a bounded device-side wait ran out */
@@ -97,8 +97,9 @@ int moe_check_config(const moe_config* cfg);
  * ["Systems for MoE Models" §2.4]; T*k when cf <= 0 (no limit).  Host only. */
 int moe_capacity(const moe_config* cfg, int32_t* capacity);
 
-/* Bytes of device workspace that every call below needs for cfg (host only).  The same
- * workspace size serves every entry point. */
+/* Bytes of device workspace that the forward-path calls below need for cfg (host only).  The
+ * router backward and the FP8 forward have their own queries
+ * (moe_router_backward_workspace_size, moe_fp8_workspace_size). */
 int moe_workspace_size(const moe_config* cfg, size_t* bytes);
 
 /* Reads and clears the device status word at the start of `ws` (copies 4 bytes to the host
@@ -122,8 +123,8 @@ int moe_router_topk(const moe_config* cfg, const void* x, const void* w_gate, co
  * P_i = mean_t softmax(g_t)_i (sigmoid scoring: mean_t s_ti / sum_j s_tj);
  * z = mean_t (logsumexp_i g_ti)^2.
  *   logits [T,E] f32, topk_idx [T,k] int32 -> f [E], P [E], l_balance [1], z_loss [1] (f32).
- * Reductions run in a fixed order (fp32 per token block, fp64 across blocks): results are
- * bit-identical from run to run. */
+ * Reductions run in float32 in a fixed order (per token block, then across blocks): results
+ * are bit-identical from run to run. */
 int moe_aux_stats(const moe_config* cfg, const float* logits, const int32_t* topk_idx, float* f,
                   float* P, float* l_balance, float* z_loss, void* ws, void* stream);
 

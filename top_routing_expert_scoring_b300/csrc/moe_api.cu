@@ -191,7 +191,7 @@ const char* moe_status_string(int status) {
     case MOE_OK: return "ok";
     case MOE_ERR_ARG: return "invalid argument (NULL pointer, bad enum or bad index)";
     case MOE_ERR_SHAPE: return "unsupported or inconsistent sizes";
-    case MOE_ERR_UNSUPPORTED: return "request not implemented by this build";
+    case MOE_ERR_UNSUPPORTED: return "request not implemented by this library";
     case MOE_ERR_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
     case MOE_ERR_CUDA: return "CUDA runtime error";
     case MOE_ERR_TIMEOUT: return "a bounded device-side wait ran out";

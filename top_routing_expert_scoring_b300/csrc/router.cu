@@ -490,8 +490,8 @@ cudaError_t launch_route_topk(const moe_config& c, const float* logits, const fl
 // ------------------------------------------------------------------------------------------
 // Statistics.  Each CTA owns a fixed set of tokens (warp w of CTA b takes tokens
 // b*8 + w + i*gridDim*8), accumulates per-expert sums in registers, reduces its warps in a
-// fixed order and writes one partial row; a single CTA then sums the rows in float64 in
-// block order.  No floating-point atomics, so the results are reproducible bit for bit.
+// fixed order and writes one partial row; a single CTA then sums the rows in float32 in a
+// fixed order.  No floating-point atomics, so the results are reproducible bit for bit.
 // ------------------------------------------------------------------------------------------
 struct AuxArgs {
   const float* g;
