@@ -108,8 +108,11 @@ def test_small_layer_parity(case):
 
 
 @pytest.mark.parametrize("case", ["v3_like", "softmax_cap"])
-def test_bf16_output(case):
-    # the layer output rounded once to bf16: the bound adds that rounding (2^-8 |out|)
+def test_bf16_output(case, monkeypatch):
+    # the layer output rounded once to bf16: the bound adds that rounding (2^-8 |out|).  The
+    # bf16 mode rounds the combine pass's float32 sum, so the float32 reference run below uses
+    # that pass too (a k <= 2 float32 layer would otherwise add its terms in the down GEMM)
+    monkeypatch.setenv("MOE_B300_COMBINE", "separate")
     spec = dict(SMALL[case])
     wl = moe_inputs.workload(spec.pop("name"), **spec)
     inp = _inputs(wl)
@@ -513,3 +516,27 @@ def test_fused_gather_matches_materialised_rows(monkeypatch, spec):
     b = U.run_forward(wl, inp)
     assert torch.equal(a["out"], b["out"])
     assert (a["idx"] == b["idx"]).all()
+
+
+@pytest.mark.parametrize("spec", [
+    dict(name="mixtral", T=700, d=256, F=384, capacity_factor=1.25),
+    dict(name="mixtral", T=513, d=256, E=16, k=1, F=256, renormalize=False),
+])
+def test_fused_combine_is_deterministic_and_matches_the_combine_pass(monkeypatch, spec):
+    """With k <= 2 and no shared experts the down GEMM adds w * y into the zeroed output itself:
+    a token gets at most two addends, so the result is the same whatever order they land in.
+    It differs from the separate combine pass (which forms w2 y2 + w1 y1 with fused
+    multiply-adds) by a few float32 roundings of the two terms."""
+    wl = moe_inputs.workload(**spec)
+    inp = _inputs(wl)
+    monkeypatch.setenv("MOE_B300_PATH", "prefill")
+    monkeypatch.setenv("MOE_B300_GEMM", "single")
+    monkeypatch.delenv("MOE_B300_COMBINE", raising=False)
+    a = U.run_forward(wl, inp)
+    b = U.run_forward(wl, inp)
+    assert torch.equal(a["out"], b["out"])
+    monkeypatch.setenv("MOE_B300_COMBINE", "separate")
+    c = U.run_forward(wl, inp)
+    fa, fc = a["out"].double().cpu().numpy(), c["out"].double().cpu().numpy()
+    rms = np.sqrt(np.mean(fc ** 2))
+    assert np.max(np.abs(fa - fc)) <= 1e-5 * rms

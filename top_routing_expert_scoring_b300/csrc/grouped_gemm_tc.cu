@@ -67,6 +67,12 @@ struct Params {
   // N = 256 only: the last tiles of the list may each run as two N = 128 halves, to even out
   // the final wave over the CTAs (see choose_tail_split)
   int tail_split;
+  // float32 epilogue only: instead of storing row r, add w[perm[r]] * row into token
+  // perm[r] / scat_k of scat_out [T, ldo] (float32 vector reductions); rows with perm < 0 skip
+  float* scat_out;
+  const int32_t* scat_perm;
+  const float* scat_w;
+  int scat_k;
   DevStatus* st;
 };
 
@@ -425,6 +431,34 @@ __global__ void __launch_bounds__(THREADS, 1)
                                   packed[4 * v + 3]);
           }
         }
+      } else if (p.out_f32 && p.scat_out) {
+        // gate weight applied here and the expert's row added into its token's output
+        float* orow = nullptr;
+        float wt = 0.f;
+        if (live) {
+          const int pair = p.scat_perm[ti.row0 + row];
+          if (pair >= 0) {
+            wt = p.scat_w[pair];
+            orow = p.scat_out + static_cast<size_t>(pair / p.scat_k) * p.ldo + ti.col0;
+          }
+        }
+        const int nchunks = ti.bn / 32;
+#pragma unroll 1
+        for (int c = 0; c < nchunks; ++c) {
+          uint32_t vr[32];
+          tmem_ld32(tb + c * 32, vr);
+          if (orow) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(
+                               orow + c * 32 + 4 * v),
+                           "f"(wt * __uint_as_float(vr[4 * v])),
+                           "f"(wt * __uint_as_float(vr[4 * v + 1])),
+                           "f"(wt * __uint_as_float(vr[4 * v + 2])),
+                           "f"(wt * __uint_as_float(vr[4 * v + 3]))
+                           : "memory");
+          }
+        }
       } else if (p.out_f32) {
         float* orow = static_cast<float*>(p.out) + static_cast<size_t>(ti.row0 + row) * p.ldo +
                       ti.col0;
@@ -640,6 +674,10 @@ cudaError_t launch_ffn_tc(const GroupedFFN& g, DevStatus* st, cudaStream_t s) {
   p2.ldo = g.d;
   p2.gperm = nullptr;
   p2.tail_split = p2.bn == 256 ? 1 : 0;
+  p2.scat_out = g.scatter_out;
+  p2.scat_perm = g.scatter_perm;
+  p2.scat_w = g.scatter_w;
+  p2.scat_k = g.gather_k;
   return launch_one(mh, mw2, p2, mt_upper * p2.n_tiles, s);
 }
 

@@ -74,8 +74,14 @@ struct GroupedFFN {
   // Optional (single-CTA kernel only): gather the gate/up GEMM's A rows straight from the
   // token rows, row r = token gather_perm[r] / gather_k of gather_x [T, d]; x is then unused.
   const int32_t* gather_perm;
-  int gather_k;
+  int gather_k;             // k of the layer (pair index / k = token)
   const void* gather_x;
+  // Optional (single-CTA kernel only): the down GEMM adds w[perm[r]] * y_r into the float32
+  // output row of token perm[r] / k instead of storing y (y is then unused); the output must be
+  // zeroed first.  Deterministic only with at most two addends per output element.
+  float* scatter_out;
+  const int32_t* scatter_perm;
+  const float* scatter_w;
 };
 // true when launch_ffn_tc would run the CTA-pair kernel for g (which needs materialised rows)
 bool ffn_uses_pair(const GroupedFFN& g);

@@ -72,6 +72,24 @@ bool gather_fused(const moe_config& c, bool dec) {
   return !ffn_uses_pair(probe);
 }
 
+// Prefill down GEMM adding w * y straight into the float32 layer output (no y rows, no combine
+// pass).  Deterministic because a token receives at most two addends (0 + a = a and a + b =
+// b + a exactly), so only for k <= 2 without shared experts; single-CTA kernel only.  The
+// environment variable MOE_B300_COMBINE=separate turns it off.
+bool combine_fused(const moe_config& c, bool dec) {
+  if (dec || c.dtype != MOE_DTYPE_BF16 || c.routing != MOE_ROUTE_TOKEN_CHOICE) return false;
+  if (c.k > 2 || c.d_ff_shared > 0 || c.out_dtype != MOE_DTYPE_F32) return false;
+  GroupedFFN probe{};
+  probe.uniform_rows = -1;
+  probe.E = c.E;
+  probe.d = c.d_model;
+  probe.F = c.d_ff;
+  probe.max_rows = rows_max(c);
+  if (ffn_uses_pair(probe)) return false;
+  const char* env = getenv("MOE_B300_COMBINE");
+  return !(env && strcmp(env, "separate") == 0);
+}
+
 bool decode_split_possible(const moe_config& c) {
   return decode_regime(c) && (long long)c.T * c.k <= kSplitRows;
 }
@@ -323,11 +341,16 @@ namespace {
 int run_ffn(const moe_config& c, const void* xin, const int32_t* offsets, const int32_t* mtp,
             int uniform_rows, int E, int F, int max_rows, const void* w13, const void* w2,
             float* y, void* ws, const Layout& L, cudaStream_t s,
-            const int32_t* gather_perm = nullptr, const void* gather_x = nullptr) {
+            const int32_t* gather_perm = nullptr, const void* gather_x = nullptr,
+            float* scatter_out = nullptr, const int32_t* scatter_perm = nullptr,
+            const float* scatter_w = nullptr) {
   GroupedFFN g{};
   g.gather_perm = gather_perm;
   g.gather_k = c.k;
   g.gather_x = gather_x;
+  g.scatter_out = scatter_out;
+  g.scatter_perm = scatter_perm;
+  g.scatter_w = scatter_w;
   g.x = xin;
   g.offsets = offsets;
   g.mtile_prefix = mtp;
@@ -533,17 +556,22 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
                               g.ksplit2, g.y_part_stride, g.shared_part_stride)) != cudaSuccess)
         return MOE_ERR_CUDA;
     } else {
+      const bool scat = combine_fused(*c, dec);
+      if (scat && cudaMemsetAsync(out, 0, (size_t)c->T * c->d_model * 4, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
       if (mark(ev_begin) != cudaSuccess) return MOE_ERR_CUDA;
       if ((st = run_ffn(*c, at<void>(ws, L.x_perm), b.offsets, b.mtile_prefix, -1, c->E,
                         c->d_ff, rows_max(*c), w13, w2, at<float>(ws, L.y_perm), ws, L, s,
-                        fuse ? b.perm : nullptr, fuse ? x : nullptr)))
+                        fuse ? b.perm : nullptr, fuse ? x : nullptr,
+                        scat ? static_cast<float*>(out) : nullptr, scat ? b.perm : nullptr,
+                        scat ? w : nullptr)))
         return st;
       if (mark(ev_end) != cudaSuccess) return MOE_ERR_CUDA;
       if (shared && (st = run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13,
                                   ws2, shared, ws, L, s)))
         return st;
-      if ((e = launch_combine(*c, at<float>(ws, L.y_perm), b.row_of, w, shared, out, s)) !=
-          cudaSuccess)
+      if (!scat && (e = launch_combine(*c, at<float>(ws, L.y_perm), b.row_of, w, shared, out,
+                                       s)) != cudaSuccess)
         return MOE_ERR_CUDA;
     }
     return cuda_status(launch_aux_final(*c, part_P, part_cnt, part_z, aux_blocks(*c), f, P,
