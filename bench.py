@@ -542,8 +542,13 @@ def main():
                             gemm_events[0], gemm_events[1])
 
     # our kernels per forward: router logits, Top-k (+statistics partials), dispatch (1 kernel
-    # for T <= 256, else 4), 2 expert GEMMs, 2 shared-expert GEMMs, combine, statistics final
-    launches_per_step = 1 + 1 + (1 if T <= 256 else 4) + 2 + (2 if shared else 0) + 1 + 1
+    # for T <= 256, else 4), 2 expert GEMMs, 2 shared-expert GEMMs, combine, statistics final.
+    # A k <= 2 bf16 layer without shared experts and with a float32 output has no combine
+    # kernel: the down GEMM adds the weighted rows into the output itself.
+    combine_in_gemm = (wl.k <= 2 and not shared and wl.dtype == "bf16"
+                       and os.environ.get("MOE_B300_COMBINE") != "separate")
+    launches_per_step = (1 + 1 + (1 if T <= 256 else 4) + 2 + (2 if shared else 0)
+                         + (0 if combine_in_gemm else 1) + 1)
     if wl.routing == "expert_choice":
         launches_per_step = 1 + 5 + 2 + 2 + (2 if shared else 0) + 1 + 2
 
