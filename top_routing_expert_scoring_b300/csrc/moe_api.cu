@@ -94,18 +94,39 @@ bool decode_split_possible(const moe_config& c) {
   return decode_regime(c) && (long long)c.T * c.k <= kSplitRows;
 }
 
-// Expected experts touched by T tokens, E(1 - (1 - k/E)^T) ("Systems for MoE Models" §1.4),
-// plus the shared experts, sets how many tiles a decode GEMM has; K is split until there are
-// about two waves of tiles.
-int decode_split(const moe_config& c, int tiles_per_entry, int kblocks) {
-  if (!decode_split_possible(c)) return 1;
+// K slices of a decode GEMM.  The expected experts touched by T tokens, E(1 - (1 - k/E)^T)
+// ("Systems for MoE Models" §1.4), plus the shared experts, give the tile count; each slice
+// count ks is costed in units of one K block streamed by every SM:
+//   ceil(tiles * ks / SMs) * (ceil(kblocks / ks) + 1)          waves x (blocks per tile + fill)
+//   + (ks - 1) * 2 * partial_bytes / (SMs * 32 KB)             extra partials written and read
+// and the cheapest (fewest slices on ties) is taken, at most kMaxSplit.  With 8 or more waves
+// unsplit the tail wave is a small share of a weight stream that runs at full bandwidth
+// anyway, and slicing only adds partials and a finalize pass: one slice (measured on
+// DeepSeek-V3- and Mixtral-shaped decode batches).
+int split_by_waves(const moe_config& c, int tiles_per_entry, int kblocks, double partial_bytes) {
   const double touched = c.E * (1.0 - std::pow(1.0 - (double)c.k / c.E, (double)c.T));
   const double entries = touched + (c.d_ff_shared > 0 ? 1.0 : 0.0);
-  const double tiles = entries * tiles_per_entry;
-  int sp = (int)std::ceil(2.0 * num_sms() / (tiles > 1 ? tiles : 1));
-  if (sp > kMaxSplit) sp = kMaxSplit;
-  if (sp > kblocks) sp = kblocks;
-  return sp < 1 ? 1 : sp;
+  const long long tiles = (long long)std::ceil(entries * tiles_per_entry);
+  const int sms = num_sms();
+  if (tiles >= 8ll * sms) return 1;
+  const double unit = (double)sms * 32768.0;     // one 256-row weight K block on every SM
+  int best = 1;
+  double best_cost = 1e300;
+  for (int ks = 1; ks <= kMaxSplit && ks <= kblocks; ++ks) {
+    const double waves = (double)((tiles * ks + sms - 1) / sms);
+    const double cost = waves * (double)((kblocks + ks - 1) / ks + 1) +
+                        (ks - 1) * 2.0 * partial_bytes / unit;
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = ks;
+    }
+  }
+  return best;
+}
+
+int decode_split(const moe_config& c, int tiles_per_entry, int kblocks, double partial_bytes) {
+  if (!decode_split_possible(c)) return 1;
+  return split_by_waves(c, tiles_per_entry, kblocks, partial_bytes);
 }
 
 int pow2_clamp(long long v, int lo, int hi) {
@@ -417,7 +438,8 @@ int moe_expert_ffn(const moe_config* c, const void* x_perm, const int32_t* offse
     g.w2 = w2;
     g.h = at<void>(ws, L.h);
     g.y = y_perm;
-    g.ksplit1 = decode_split(*c, c->d_ff / 128, c->d_model / 64);
+    g.ksplit1 = decode_split(*c, c->d_ff / 128, c->d_model / 64,
+                             (double)g.max_rows * 2 * c->d_ff * 4);
     g.ksplit2 = 1;                          // the caller's y_perm holds one slice
     g.gu = g.ksplit1 > 1 ? at<float>(ws, L.dec_gu) : nullptr;
     g.y_part_stride = (size_t)rows_max(*c) * c->d_model;
@@ -539,11 +561,14 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
       g.ws13 = ws13;
       g.ws2 = ws2;
       g.h = at<void>(ws, L.h);
-      g.ksplit1 = decode_split(*c, c->d_ff / 128, c->d_model / 64);
+      const int Fmx = c->d_ff > c->d_ff_shared ? c->d_ff : c->d_ff_shared;
+      g.ksplit1 = decode_split(*c, c->d_ff / 128, c->d_model / 64,
+                               (double)g.max_rows * 2 * Fmx * 4);
       // every K slice must hold at least one 64-wide block of both the routed and shared K
       const int kb2 = (c->d_ff_shared > 0 && c->d_ff_shared < c->d_ff ? c->d_ff_shared
                                                                       : c->d_ff) / 64;
-      g.ksplit2 = decode_split(*c, c->d_model / 256, kb2);
+      g.ksplit2 = decode_split(*c, c->d_model / 256, kb2,
+                               (double)(rows_max(*c) + (shared ? c->T : 0)) * c->d_model * 4);
       g.gu = g.ksplit1 > 1 ? at<float>(ws, L.dec_gu) : nullptr;
       g.y = g.ksplit2 > 1 ? at<float>(ws, L.dec_y) : at<float>(ws, L.y_perm);
       g.shared_out = g.ksplit2 > 1 ? at<float>(ws, L.dec_sh) : shared;
@@ -662,17 +687,7 @@ int moe_selftest_timeout(void* ws, int32_t limit_us, void* stream) {
 namespace moe {
 namespace {
 
-// K slices of an FP8 decode GEMM: the same rule as the bf16 decode path (about two waves of
-// tiles from the expected touched experts), without the regime switch.
-int fp8_split(const moe_config& c, int tiles_per_entry, int kblocks) {
-  const double touched = c.E * (1.0 - std::pow(1.0 - (double)c.k / c.E, (double)c.T));
-  const double entries = touched + (c.d_ff_shared > 0 ? 1.0 : 0.0);
-  const double tiles = entries * tiles_per_entry;
-  int sp = (int)std::ceil(2.0 * num_sms() / (tiles > 1 ? tiles : 1));
-  if (sp > kMaxSplit) sp = kMaxSplit;
-  if (sp > kblocks) sp = kblocks;
-  return sp < 1 ? 1 : sp;
-}
+
 
 struct Fp8Layout {
   Layout base;
@@ -691,9 +706,10 @@ Fp8Layout fp8_layout(const moe_config& c) {
   };
   const size_t R = rows_max(c), T = c.T, d = c.d_model, F = c.d_ff, Fs = c.d_ff_shared;
   const size_t rows = R + T, Fmax = F > Fs ? F : Fs;
-  L.ks1 = fp8_split(c, c.d_ff / 128, c.d_model / 128);
+  // K slices as on the bf16 decode path (split_by_waves), on 128-element E4M3 K blocks
+  L.ks1 = split_by_waves(c, c.d_ff / 128, c.d_model / 128, (double)rows * 2 * Fmax * 4);
   const int kf = (int)((Fs > 0 && Fs < F ? Fs : F) / 128);
-  L.ks2 = fp8_split(c, c.d_model / 256, kf);
+  L.ks2 = split_by_waves(c, c.d_model / 256, kf, (double)(R + (Fs ? T : 0)) * d * 4);
   L.x8 = take(rows * d);
   L.sx = take(rows * 4);
   L.h8 = take(rows * Fmax);
