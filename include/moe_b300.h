@@ -75,7 +75,8 @@ typedef struct moe_config {
   int32_t score;        /* MOE_SCORE_* */
   int32_t routing;      /* MOE_ROUTE_* */
   int32_t n_groups;     /* expert groups (sigmoid scoring); 1 = no group limit */
-  int32_t topk_groups;  /* groups kept per token; == n_groups = no limit */
+  int32_t topk_groups;  /* groups kept per token; == n_groups = no limit; a limit needs
+                           >= 2 experts per group (group score = sum of its top two) */
   int32_t renormalize;  /* 1: w = p_S / sum_S p (default); 0: w = p_S (Switch, k = 1) */
   float route_scale;    /* weights are multiplied by it (1.0; DeepSeek-V3: 2.5) */
   float capacity_factor;/* C = ceil(cf*k*T/E); <= 0: no capacity limit */

@@ -130,6 +130,9 @@ def sigmoid_group_route(g32: np.ndarray, bias: np.ndarray, k: int, n_groups: int
     sb = (s32 + np.asarray(bias, F32)[None, :]).astype(F32)              # float32 add
     if n_groups > 1 and topk_groups < n_groups:
         per = E // n_groups
+        if per < 2:
+            raise ValueError("a group score is the sum of the group's two largest scores: "
+                             "a group needs at least two experts")
         grouped = sb.reshape(T, n_groups, per)
         top2 = -np.sort(-grouped, axis=-1, kind="stable")[..., :2]         # two largest, desc
         gscore = (top2[..., 0] + top2[..., 1]).astype(F32)                 # float32 add

@@ -170,3 +170,11 @@ def test_fp8_rejections_before_any_launch():
     args[7] = None
     assert m.lib.moe_forward_fp8(ctypes.byref(v3), *args) == -1
     assert m.fp8_workspace_size(v3) > m.workspace_size(v3)
+
+
+def test_group_limit_needs_two_experts_per_group():
+    m = _lib()
+    wl = moe_inputs.workload("v3", T=16, d=256, E=8, n_groups=8, topk_groups=5, k=2)
+    assert m.check_config(config_of(wl)) == -2
+    ok = moe_inputs.workload("v3", T=16, d=256, E=8, n_groups=4, topk_groups=2, k=2)
+    assert m.check_config(config_of(ok)) == 0

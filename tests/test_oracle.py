@@ -420,3 +420,9 @@ def test_pins_catch_planted_mistakes(monkeypatch):
         return (key.shape[-1] - 1 - order[..., :k]).astype(np.int32)
     keys = np.array([[1, 1, 0, 2]], np.float32)
     assert list(bad_topk(keys, 2)[0]) != _brute_topk(keys[0].tolist(), 2)
+
+
+def test_group_limit_with_one_expert_per_group_is_refused():
+    g = np.zeros((2, 8), np.float32)
+    with pytest.raises(ValueError):
+        O.sigmoid_group_route(g, np.zeros(8), 2, 8, 5, 1.0)

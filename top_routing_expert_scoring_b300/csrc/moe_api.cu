@@ -259,6 +259,7 @@ int moe_check_config(const moe_config* c) {
   if (c->topk_groups < 1 || c->topk_groups > c->n_groups) return MOE_ERR_SHAPE;
   if (c->topk_groups < c->n_groups) {
     if (c->score != MOE_SCORE_SIGMOID) return MOE_ERR_UNSUPPORTED;
+    if (c->E / c->n_groups < 2) return MOE_ERR_SHAPE;   // group score = sum of the top two
     if (c->topk_groups * (c->E / c->n_groups) < c->k) return MOE_ERR_SHAPE;
   }
   if (c->dtype == MOE_DTYPE_BF16) {
