@@ -2,9 +2,13 @@
 // (y and shared in float32; out rounded once to bf16, or kept in float32)
 //   ["MoE 路由数学" §2.1 Output = sum_{i in S} p~_i Expert_i(x), §2.2 shared experts;
 //    "Systems for Mixture-of-Experts Models" §2.2 step 4 (add back in place)]
-// One warp per 512-column slice of a token, 16-byte vector loads, fp32 accumulation in the fixed order
-// j = 0..k-1 after the shared term; each token's row is written once (no atomics).  A dropped
-// pair (row -1) adds nothing and the other weights keep their values.
+// fp32 accumulation in the fixed order j = 0..k-1 after the shared term; each token's row is
+// written once (no atomics).  A dropped pair (row -1) adds nothing and the other weights keep
+// their values.  Two kernels compute the same sums in the same order:
+//   - combine_kernel (prefill): one warp per 512-column slice of a token, 16-byte loads;
+//   - combine_rows_kernel (decode batches, or y in K-slice partials): one CTA per 128-column
+//     chunk of a token with one warp per addend row, so that every load of the chunk is in
+//     flight at once; warp 0 then adds the rows in the fixed order.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -12,9 +16,9 @@
 
 namespace moe {
 
-// Columns per warp: a token's row is split over ceil(d / slice) warps, slice = 512 while that
-// still gives >= 2048 warps, else 256 or 128, so that decode batches still spread over the GPU
-// (each lane handles 4 columns per 128-column step).
+// Columns per warp of the prefill kernel: a token's row is split over ceil(d / slice) warps,
+// slice = 512 while that still gives >= 2048 warps, else 256 or 128, so that narrow rows still
+// spread over the GPU (each lane handles 4 columns per 128-column step).
 constexpr int kCombineSlice = 512;
 inline int combine_slice(const moe_config& c) {
   for (int sl = kCombineSlice; sl > 128; sl >>= 1)
@@ -46,14 +50,27 @@ __device__ __forceinline__ void load_shared4(const float* shared, size_t off, fl
   }
 }
 
-// Sum of nsplit partials (stride apart), in order, of 4 consecutive values.
-__device__ __forceinline__ void sum_parts4(const float* p, int nsplit, size_t stride, float* v) {
-  float4 q = __ldg(reinterpret_cast<const float4*>(p));
-  v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
-  for (int sl = 1; sl < nsplit; ++sl) {
-    q = __ldg(reinterpret_cast<const float4*>(p + sl * stride));
-    v[0] += q.x; v[1] += q.y; v[2] += q.z; v[3] += q.w;
+// Sum of nsplit partials (stride apart), in slice order, of 4 consecutive values; the loads of
+// up to eight slices are issued before the first add.
+constexpr int kPartGroup = 8;
+__device__ __forceinline__ float4 sum_parts4(const float* p, int nsplit, size_t stride) {
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < nsplit; s0 += kPartGroup) {
+    float4 q[kPartGroup];
+#pragma unroll
+    for (int i = 0; i < kPartGroup; ++i)
+      if (s0 + i < nsplit) q[i] = __ldg(reinterpret_cast<const float4*>(p + (s0 + i) * stride));
+#pragma unroll
+    for (int i = 0; i < kPartGroup; ++i) {
+      if (s0 + i >= nsplit) break;
+      if (s0 + i == 0) {
+        v = q[0];
+      } else {
+        v.x += q[i].x; v.y += q[i].y; v.z += q[i].z; v.w += q[i].w;
+      }
+    }
   }
+  return v;
 }
 
 __device__ __forceinline__ void fma4(float wt, const float* y, float* acc) {
@@ -64,15 +81,14 @@ __device__ __forceinline__ void fma4(float wt, const float* y, float* acc) {
   acc[3] = fmaf(wt, q.w, acc[3]);
 }
 
-// Token-choice combine (y float32, shared float32, out bf16 or float32).
+// Token-choice combine, prefill: y and shared hold one slice (float32), out bf16 or float32.
 template <typename TOut>
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y,
                                                      const int32_t* __restrict__ row_of,
                                                      const float* __restrict__ w,
                                                      const float* __restrict__ shared,
                                                      TOut* __restrict__ out, int Tn, int d,
-                                                     int k, int nsplit, size_t y_stride,
-                                                     size_t shared_stride, int slice) {
+                                                     int k, int slice) {
   pdl_prologue();
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -90,42 +106,96 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   }
   for (int v = v0 + lane * 4; v < v1; v += 128) {
     float acc[4];
-    if (nsplit == 1) {
-      load_shared4(shared, (size_t)t * d + v, acc);
+    load_shared4(shared, (size_t)t * d + v, acc);
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (rows[j] >= 0) fma4(ws[j], y + (size_t)rows[j] * d + v, acc);
-    } else {
-      if (shared) sum_parts4(shared + (size_t)t * d + v, nsplit, shared_stride, acc);
-      else acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (rows[j] < 0) continue;
-        float yv[4];
-        sum_parts4(y + (size_t)rows[j] * d + v, nsplit, y_stride, yv);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[i] = fmaf(ws[j], yv[i], acc[i]);
-      }
-    }
+    for (int j = 0; j < 8; ++j)
+      if (rows[j] >= 0) fma4(ws[j], y + (size_t)rows[j] * d + v, acc);
     store4<TOut>(out + (size_t)t * d + v, acc);
   }
+}
+
+// Token-choice combine, decode: CTA (t, chunk) has k + 1 warps; warp j < k sums the nsplit
+// slices of y[row_of[t, j]] over the chunk's 128 columns, warp k those of shared[t] (when
+// given), and warp 0 adds them: acc = shared (or 0), then acc = fma(w[t, j], row_j, acc) for
+// j = 0..k-1, skipping dropped pairs.
+template <typename TOut>
+__global__ void __launch_bounds__(288) combine_rows_kernel(const float* __restrict__ y,
+                                                          const int32_t* __restrict__ row_of,
+                                                          const float* __restrict__ w,
+                                                          const float* __restrict__ shared,
+                                                          TOut* __restrict__ out, int d, int k,
+                                                          int nsplit, size_t y_stride,
+                                                          size_t shared_stride) {
+  pdl_prologue();
+  __shared__ float4 part[9][32];
+  __shared__ float s_w[8];
+  __shared__ int s_live[8];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int chunks = ceil_div(d, 128);
+  const int t = blockIdx.x / chunks;
+  const int v = (blockIdx.x - t * chunks) * 128 + lane * 4;
+  const float* src = nullptr;
+  size_t stride = y_stride;
+  if (warp < k) {
+    const int r = row_of[(size_t)t * k + warp];
+    if (lane == 0) {
+      s_live[warp] = r >= 0;
+      s_w[warp] = w[(size_t)t * k + warp];
+    }
+    if (r >= 0) src = y + (size_t)r * d;
+  } else if (shared) {
+    src = shared + (size_t)t * d;
+    stride = shared_stride;
+  }
+  if (src && v < d) part[warp][lane] = sum_parts4(src + v, nsplit, stride);
+  __syncthreads();
+  if (warp != 0 || v >= d) return;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  if (shared) {
+    const float4 q = part[k][lane];
+    acc[0] = q.x; acc[1] = q.y; acc[2] = q.z; acc[3] = q.w;
+  }
+  for (int j = 0; j < k; ++j) {
+    if (!s_live[j]) continue;
+    const float wt = s_w[j];
+    const float4 q = part[j][lane];
+    acc[0] = fmaf(wt, q.x, acc[0]);
+    acc[1] = fmaf(wt, q.y, acc[1]);
+    acc[2] = fmaf(wt, q.z, acc[2]);
+    acc[3] = fmaf(wt, q.w, acc[3]);
+  }
+  store4<TOut>(out + (size_t)t * d + v, acc);
+}
+
+// y in K-slice partials, or too few (token, 128-column) slices for the prefill kernel to fill
+// the GPU with warps, takes the row-parallel kernel.
+constexpr int kCombineMinWarps = 2048;
+
+template <typename TOut>
+cudaError_t launch_combine_t(const moe_config& c, const float* y_perm, const int32_t* row_of,
+                             const float* w, const float* shared_out, TOut* out, cudaStream_t s,
+                             int nsplit, size_t y_stride, size_t shared_stride) {
+  if (nsplit > 1 || (long long)c.T * ceil_div(c.d_model, 128) < kCombineMinWarps) {
+    const int blocks = c.T * ceil_div(c.d_model, 128);
+    launch_pdl(combine_rows_kernel<TOut>, blocks, 32 * (c.k + 1), 0, s, y_perm, row_of, w,
+               shared_out, out, c.d_model, c.k, nsplit, y_stride, shared_stride);
+  } else {
+    const int slice = combine_slice(c);
+    const int blocks = ceil_div(c.T * ceil_div(c.d_model, slice) * 32, 256);
+    launch_pdl(combine_kernel<TOut>, blocks, 256, 0, s, y_perm, row_of, w, shared_out, out, c.T,
+               c.d_model, c.k, slice);
+  }
+  return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const moe_config& c, const float* y_perm, const int32_t* row_of,
                            const float* w, const float* shared_out, void* out, cudaStream_t s,
                            int nsplit, size_t y_stride, size_t shared_stride) {
-  const int slice = combine_slice(c);
-  const int blocks = ceil_div(c.T * ceil_div(c.d_model, slice) * 32, 256);
   if (c.out_dtype == MOE_DTYPE_F32)
-    launch_pdl(combine_kernel<float>, blocks, 256, 0, s, y_perm, row_of, w, shared_out, (float*)out,
-                                                 c.T, c.d_model, c.k, nsplit, y_stride,
-                                                 shared_stride, slice);
-  else
-    launch_pdl(combine_kernel<__nv_bfloat16>, blocks, 256, 0, s, y_perm, row_of, w, shared_out,
-                                                         (__nv_bfloat16*)out, c.T, c.d_model,
-                                                         c.k, nsplit, y_stride, shared_stride,
-                                                         slice);
-  return cudaGetLastError();
+    return launch_combine_t(c, y_perm, row_of, w, shared_out, static_cast<float*>(out), s,
+                            nsplit, y_stride, shared_stride);
+  return launch_combine_t(c, y_perm, row_of, w, shared_out, static_cast<__nv_bfloat16*>(out), s,
+                          nsplit, y_stride, shared_stride);
 }
 
 // Expert-choice combine: token t sums the rows tok_rows[tok_ptr[t] .. tok_ptr[t+1]) (ascending

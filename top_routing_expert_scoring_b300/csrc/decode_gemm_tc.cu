@@ -391,20 +391,88 @@ __global__ void __launch_bounds__(256) swiglu_finalize_kernel(const float* __res
     if (f >= (r < nk ? F : Fs)) continue;
     float g = 0.f, u = 0.f;
     const float* src = gu + static_cast<size_t>(r) * (2 * ldo) + f;
-    for (int sl = 0; sl < S; ++sl) {
-      g += src[sl * part_stride];
-      u += src[sl * part_stride + ldo];
+    for (int s0 = 0; s0 < S; s0 += 8) {            // eight slices' loads in flight, then adds
+      float qg[8], qu[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (s0 + i < S) {
+          qg[i] = src[(s0 + i) * part_stride];
+          qu[i] = src[(s0 + i) * part_stride + ldo];
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (s0 + i >= S) break;
+        g += qg[i];
+        u += qu[i];
+      }
     }
     h[i] = __float2bfloat16_rn((g / (1.0f + expf(-g))) * u);
   }
 }
 
+// Gate and up sums over S K slices (part_stride apart), in slice order, of two groups of four
+// consecutive columns (pa, and pb when two): the loads of two slices of both groups are in
+// flight together.
+__device__ __forceinline__ void add4(float4& a, const float4& b) {
+  a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+}
+__device__ __forceinline__ void sum_slices4x2(const float4* pa, const float4* pb, bool two,
+                                              size_t ps4, size_t up4, int S, float4 (&g)[2],
+                                              float4 (&u)[2]) {
+  g[0] = pa[0];
+  u[0] = pa[up4];
+  if (two) {
+    g[1] = pb[0];
+    u[1] = pb[up4];
+  }
+  for (int sl = 1; sl < S; sl += 2) {
+    const bool more = sl + 1 < S;
+    const float4 ga = pa[sl * ps4], ua = pa[sl * ps4 + up4];
+    float4 gb = ga, ub = ua, gc = ga, uc = ua, gd = ga, ud = ua;
+    if (more) { gb = pa[(sl + 1) * ps4]; ub = pa[(sl + 1) * ps4 + up4]; }
+    if (two) {
+      gc = pb[sl * ps4];
+      uc = pb[sl * ps4 + up4];
+      if (more) { gd = pb[(sl + 1) * ps4]; ud = pb[(sl + 1) * ps4 + up4]; }
+    }
+    add4(g[0], ga); add4(u[0], ua);
+    if (more) { add4(g[0], gb); add4(u[0], ub); }
+    if (two) {
+      add4(g[1], gc); add4(u[1], uc);
+      if (more) { add4(g[1], gd); add4(u[1], ud); }
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(remote)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(local))), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
 // E4M3 path: h[r][:] = SiLU(sum_s gate_s[r][:]) * sum_s up_s[r][:] (slices in order), then the
 // row is quantised as every E4M3 operand: amax = max |h|, inv = 448 / amax, code = e4m3(h * inv)
 // (round to nearest even, saturating), scale = amax / 448; a zero row gets codes 0, scale 0.
-// One CTA per row (up to 1024 threads, four columns per thread and step); the row's h stays in
-// shared memory between the two passes.
-__global__ void __launch_bounds__(1024) swiglu_quant_kernel(const float* __restrict__ gu,
+// Row r is split over the CTAs of a cluster (a cluster of one CTA when rows are many), one
+// column range each; h stays in shared memory between the two passes, and the row's amax is
+// the maximum of the CTAs' maxima, read through distributed shared memory.  A maximum does not
+// depend on how the row is split, so the bytes do not either.
+__global__ void __launch_bounds__(1024, 1) swiglu_quant_kernel(const float* __restrict__ gu,
                                                            size_t part_stride, int S,
                                                            const int32_t* __restrict__ offsets,
                                                            int E, int n_shared_rows, int F,
@@ -414,45 +482,78 @@ __global__ void __launch_bounds__(1024) swiglu_quant_kernel(const float* __restr
   pdl_prologue();
   extern __shared__ float4 hrow4[];
   __shared__ float red[32];
+  __shared__ float cta_amax, row_amax;
+  const uint32_t crank = cluster_ctarank(), csize = cluster_nctarank();
   const int nk = offsets[E];
-  const int r = blockIdx.x;
-  if (r >= nk + n_shared_rows) return;
+  const int r = blockIdx.x / csize;
+  if (r >= nk + n_shared_rows) return;        // the whole cluster shares r
   const int F4 = (r < nk ? F : Fs) / 4;
+  const int chunk = ceil_div(F4, static_cast<int>(csize));
+  const int f0 = static_cast<int>(crank) * chunk;
+  const int f1 = min(F4, f0 + chunk);
   const float4* src = reinterpret_cast<const float4*>(gu + static_cast<size_t>(r) * (2 * ldo));
   const size_t ps4 = part_stride / 4, up4 = static_cast<size_t>(ldo) / 4;
   float amax = 0.f;
-  for (int f = threadIdx.x; f < F4; f += blockDim.x) {
-    float4 g = src[f], u = src[up4 + f];
-    for (int sl = 1; sl < S; ++sl) {
-      const float4 g2 = src[sl * ps4 + f], u2 = src[sl * ps4 + up4 + f];
-      g.x += g2.x; g.y += g2.y; g.z += g2.z; g.w += g2.w;
-      u.x += u2.x; u.y += u2.y; u.z += u2.z; u.w += u2.w;
+  for (int f = f0 + threadIdx.x; f < f1; f += 2 * blockDim.x) {
+    const int fb = f + blockDim.x;
+    const bool two = fb < f1;
+    float4 g[2], u[2];
+    sum_slices4x2(src + f, src + (two ? fb : f), two, ps4, up4, S, g, u);
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      if (c == 1 && !two) break;
+      float4 hv;
+      hv.x = (g[c].x / (1.0f + expf(-g[c].x))) * u[c].x;
+      hv.y = (g[c].y / (1.0f + expf(-g[c].y))) * u[c].y;
+      hv.z = (g[c].z / (1.0f + expf(-g[c].z))) * u[c].z;
+      hv.w = (g[c].w / (1.0f + expf(-g[c].w))) * u[c].w;
+      hrow4[(c ? fb : f) - f0] = hv;
+      amax = fmaxf(amax,
+                   fmaxf(fmaxf(fabsf(hv.x), fabsf(hv.y)), fmaxf(fabsf(hv.z), fabsf(hv.w))));
     }
-    float4 hv;
-    hv.x = (g.x / (1.0f + expf(-g.x))) * u.x;
-    hv.y = (g.y / (1.0f + expf(-g.y))) * u.y;
-    hv.z = (g.z / (1.0f + expf(-g.z))) * u.z;
-    hv.w = (g.w / (1.0f + expf(-g.w))) * u.w;
-    hrow4[f] = hv;
-    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(hv.x), fabsf(hv.y)), fmaxf(fabsf(hv.z), fabsf(hv.w))));
   }
   amax = warp_max(amax);
   const int nw = blockDim.x >> 5;
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
   __syncthreads();
-  amax = red[0];
-  for (int w = 1; w < nw; ++w) amax = fmaxf(amax, red[w]);
+  if (threadIdx.x == 0) {
+    float m = red[0];
+    for (int w = 1; w < nw; ++w) m = fmaxf(m, red[w]);
+    cta_amax = m;
+  }
+  // every CTA's maximum is visible cluster-wide after this barrier
+  asm volatile("barrier.cluster.arrive.release.aligned;\n"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  if (threadIdx.x < 32) {                     // lane q reads CTA q's maximum (csize <= 8)
+    float m = threadIdx.x < csize ? ld_cluster_f32(&cta_amax, threadIdx.x) : 0.f;
+    m = warp_max(m);
+    if (threadIdx.x == 0) row_amax = m;
+  }
+  __syncthreads();
+  // done reading the other CTAs' shared memory; no CTA leaves before all have arrived here
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  amax = row_amax;
   const float inv = amax > 0.f ? 448.0f / amax : 0.f;
   uint32_t* dst = reinterpret_cast<uint32_t*>(h8 + static_cast<size_t>(r) * ldo);
-  for (int f = threadIdx.x; f < F4; f += blockDim.x) {
-    const float4 hv = hrow4[f];
+  for (int f = f0 + threadIdx.x; f < f1; f += blockDim.x) {
+    const float4 hv = hrow4[f - f0];
     const uint32_t q0 = __nv_cvt_float2_to_fp8x2(make_float2(hv.x * inv, hv.y * inv),
                                                  __NV_SATFINITE, __NV_E4M3);
     const uint32_t q1 = __nv_cvt_float2_to_fp8x2(make_float2(hv.z * inv, hv.w * inv),
                                                  __NV_SATFINITE, __NV_E4M3);
     dst[f] = (q0 & 0xFFFFu) | (q1 << 16);
   }
-  if (threadIdx.x == 0) hs[r] = amax > 0.f ? amax / 448.0f : 0.f;
+  if (crank == 0 && threadIdx.x == 0) hs[r] = amax > 0.f ? amax / 448.0f : 0.f;
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Cluster size for the quantising finalize: split each row over up to 8 CTAs while the rows
+// alone give fewer than two CTAs per SM and every CTA keeps at least 32 four-column groups.
+static int swiglu_quant_cluster(int rows, int F4) {
+  int cn = 1;
+  while (cn < 8 && static_cast<long long>(rows) * cn < 2ll * num_sms() && F4 / (2 * cn) >= 32)
+    cn *= 2;
+  return cn;
 }
 
 static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& as, const CUtensorMap& b,
@@ -535,12 +636,28 @@ cudaError_t launch_ffn_decode(const DecodeFFN& g, DevStatus* st, cudaStream_t s)
   if (g.fp8) {
     err = smem_attr_once(reinterpret_cast<const void*>(swiglu_quant_kernel), 200 * 1024);
     if (err != cudaSuccess) return err;
-    int threads = Fmax / 4;
-    threads = threads > 1024 ? 1024 : (threads + 31) / 32 * 32;
-    launch_pdl(swiglu_quant_kernel, g.max_rows, threads, static_cast<size_t>(Fmax) * 4, s, 
-        g.gu, p1.part_stride, g.ksplit1, g.offsets, g.E, sh ? g.T : 0, g.F,
-        sh ? g.F_shared : 0, Fmax, static_cast<uint8_t*>(g.h), g.hs);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    const int cn = swiglu_quant_cluster(g.max_rows, Fmax / 4);
+    const int chunk = ceil_div(Fmax / 4, cn);
+    int threads = ((chunk + 1) / 2 + 31) / 32 * 32;     // two column groups per thread
+    if (threads > 1024) threads = 1024;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(g.max_rows * cn);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(chunk) * 16;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cn;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_prologue
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    err = cudaLaunchKernelEx(&cfg, swiglu_quant_kernel, static_cast<const float*>(g.gu),
+                             p1.part_stride, g.ksplit1, g.offsets, g.E, sh ? g.T : 0, g.F,
+                             sh ? g.F_shared : 0, Fmax, static_cast<uint8_t*>(g.h), g.hs);
+    if (err != cudaSuccess) return err;
   } else if (g.ksplit1 > 1) {
     const long long work = static_cast<long long>(g.max_rows) * Fmax;
     int blocks = static_cast<int>((work + 255) / 256);

@@ -160,6 +160,7 @@ __global__ void __launch_bounds__(kDispatchBlock) dispatch_small_kernel(
   __shared__ int s_drop[256];
   __shared__ int s_off[257];
   __shared__ int s_perm[256 * 8];
+  __shared__ int s_wsum[3][kDispatchBlock / 32];
   const bool lead = blockIdx.x == 0;
   const int tid = threadIdx.x;
   for (int i = tid; i < E * kWords; i += blockDim.x) bm[i] = 0u;
@@ -194,17 +195,26 @@ __global__ void __launch_bounds__(kDispatchBlock) dispatch_small_kernel(
     counts[e] = total;
     kept[e] = kp;
   }
-  __syncthreads();
-  for (int sft = 1; sft < 256; sft <<= 1) {
-    const int a = e >= sft ? s_kept[e - sft] : 0;
-    const int b = e >= sft ? s_mt[e - sft] : 0;
-    const int c = e >= sft ? s_drop[e - sft] : 0;
+  // inclusive scans over the 256 expert slots: within each warp by shuffles, then each warp
+  // adds the totals of the warps before it
+  {
+    const int lane = tid & 31, wi = tid >> 5;
+    int a = s_kept[e], b = s_mt[e], c = s_drop[e];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a2 = __shfl_up_sync(0xffffffffu, a, o);
+      const int b2 = __shfl_up_sync(0xffffffffu, b, o);
+      const int c2 = __shfl_up_sync(0xffffffffu, c, o);
+      if (lane >= o) { a += a2; b += b2; c += c2; }
+    }
+    if (lane == 31) { s_wsum[0][wi] = a; s_wsum[1][wi] = b; s_wsum[2][wi] = c; }
     __syncthreads();
-    s_kept[e] += a;
-    s_mt[e] += b;
-    s_drop[e] += c;
-    __syncthreads();
+    for (int q = 0; q < wi; ++q) { a += s_wsum[0][q]; b += s_wsum[1][q]; c += s_wsum[2][q]; }
+    s_kept[e] = a;
+    s_mt[e] = b;
+    s_drop[e] = c;
   }
+  __syncthreads();
   if (e < E) s_off[e + 1] = s_kept[e];
   if (e == 0) s_off[0] = 0;
   if (lead) {

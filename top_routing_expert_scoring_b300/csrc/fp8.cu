@@ -69,16 +69,91 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const __nv_bfloat16*
   }
 }
 
+// One CTA per row, for short lists of rows (the token rows of a decode batch): each thread keeps
+// up to kRowVecs 16-byte vectors of the row in registers, so the row is read once and all its
+// loads are in flight together; the amax is reduced over the CTA.  Per element the arithmetic
+// is the warp kernel's, and a maximum does not depend on its order, so both give the same bytes.
+constexpr int kRowVecs = 4;
+__global__ void __launch_bounds__(1024) quantize_row_cta_kernel(
+    const __nv_bfloat16* __restrict__ src, long long nrows_max, int cols,
+    const int32_t* nrows_base, int nrows_extra, uint8_t* __restrict__ dst,
+    float* __restrict__ scale) {
+  pdl_prologue();
+  __shared__ float red[32];
+  long long nrows = nrows_max;
+  if (nrows_base) {
+    const long long n = static_cast<long long>(*nrows_base) + nrows_extra;
+    nrows = n < nrows_max ? n : nrows_max;
+  }
+  const long long row = blockIdx.x;
+  if (row >= nrows) return;
+  const int vecs = cols / 8;
+  const uint4* s = reinterpret_cast<const uint4*>(src + row * cols);
+  uint4 v[kRowVecs];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRowVecs; ++i) {
+    const int c = threadIdx.x + i * blockDim.x;
+    if (c < vecs) v[i] = s[c];
+  }
+#pragma unroll
+  for (int i = 0; i < kRowVecs; ++i) {
+    if (threadIdx.x + i * blockDim.x >= vecs) break;
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __bfloat1622float2(b[j]);
+      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+  amax = warp_max(amax);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+  for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) amax = fmaxf(amax, red[w]);
+  const float inv = amax > 0.f ? 448.0f / amax : 0.f;
+  uint2* d = reinterpret_cast<uint2*>(dst + row * cols);
+#pragma unroll
+  for (int i = 0; i < kRowVecs; ++i) {
+    const int c = threadIdx.x + i * blockDim.x;
+    if (c >= vecs) break;
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
+    uint32_t packed[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float2 f0 = __bfloat1622float2(b[2 * j]);
+      const float2 f1 = __bfloat1622float2(b[2 * j + 1]);
+      const uint32_t q0 = __nv_cvt_float2_to_fp8x2(make_float2(f0.x * inv, f0.y * inv),
+                                                   __NV_SATFINITE, __NV_E4M3);
+      const uint32_t q1 = __nv_cvt_float2_to_fp8x2(make_float2(f1.x * inv, f1.y * inv),
+                                                   __NV_SATFINITE, __NV_E4M3);
+      packed[j] = (q0 & 0xFFFFu) | (q1 << 16);
+    }
+    d[c] = make_uint2(packed[0], packed[1]);
+  }
+  if (threadIdx.x == 0) scale[row] = amax > 0.f ? amax / 448.0f : 0.f;
+}
+
 }  // namespace
 
 cudaError_t launch_quantize_rows(const void* src, long long nrows_max, int cols,
                                  const int32_t* nrows_base, int nrows_extra, uint8_t* dst,
                                  float* scale, cudaStream_t s) {
+  const int vecs = cols / 8;
+  if (nrows_max <= 8ll * num_sms() && vecs <= kRowVecs * 1024) {
+    int threads = (vecs + 1) / 2;
+    threads = (threads + 31) / 32 * 32;
+    if (threads > 1024) threads = 1024;
+    launch_pdl(quantize_row_cta_kernel, static_cast<int>(nrows_max), threads, 0, s,
+               static_cast<const __nv_bfloat16*>(src), nrows_max, cols, nrows_base, nrows_extra,
+               dst, scale);
+    return cudaGetLastError();
+  }
   long long blocks = (nrows_max + 7) / 8;
   const long long cap = static_cast<long long>(num_sms()) * 16;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  launch_pdl(quantize_rows_kernel, static_cast<int>(blocks), 256, 0, s, 
+  launch_pdl(quantize_rows_kernel, static_cast<int>(blocks), 256, 0, s,
       static_cast<const __nv_bfloat16*>(src), nrows_max, cols, nrows_base, nrows_extra, dst,
       scale);
   return cudaGetLastError();

@@ -19,9 +19,9 @@ cudaError_t launch_router_logits(const moe_config& c, const void* x, const void*
 // Router logits on the tensor cores (bf16, E a multiple of 32): g = x W_gate^T in fp32.
 cudaError_t launch_router_tc(const moe_config& c, const void* x, const void* w_gate,
                              float* logits, cudaStream_t s);
-// With part_P/part_cnt/part_z the kernel also writes the load-balance partials of
-// aux_blocks(c) fixed token sets (the same values launch_aux_stats' first kernel produces);
-// launch_aux_final then reduces them.
+// With part_P/part_cnt/part_z the kernel also writes the load-balance partials, aux_rows(c)
+// rows: one per fixed token set, or one per token for decode batches with E > 32 (route_cta);
+// launch_aux_stats' first kernel writes the same values, and launch_aux_final reduces them.
 cudaError_t launch_route_topk(const moe_config& c, const float* logits, const float* bias,
                               int32_t* idx, float* w, DevStatus* st, cudaStream_t s,
                               float* part_P = nullptr, int32_t* part_cnt = nullptr,
@@ -34,6 +34,8 @@ cudaError_t launch_aux_stats(const moe_config& c, const float* logits, const int
                              float* part_z, int nblocks, float* f, float* P, float* l_balance,
                              float* z_loss, DevStatus* st, cudaStream_t s);
 int aux_blocks(const moe_config& c);
+bool route_cta(const moe_config& c);
+int aux_rows(const moe_config& c);
 
 // ---- dispatch --------------------------------------------------------------------------------
 struct DispatchBufs {

@@ -146,7 +146,7 @@ Layout layout(const moe_config& c) {
   const size_t T = c.T, E = c.E, k = c.k, d = c.d_model, F = c.d_ff, Fs = c.d_ff_shared;
   const size_t esz = c.dtype == MOE_DTYPE_F32 ? 4 : 2;
   const size_t nblk = (T + kDispatchBlock - 1) / kDispatchBlock;
-  const size_t naux = aux_blocks(c);
+  const size_t naux = aux_rows(c);
   const size_t R = rows_max(c);
   L.status = take(sizeof(DevStatus));
   L.logits = take(T * E * 4);
@@ -333,7 +333,7 @@ int moe_aux_stats(const moe_config* c, const float* logits, const int32_t* topk_
   const Layout L = layout(*c);
   return cuda_status(launch_aux_stats(
       *c, logits, topk_idx, nullptr, at<float>(ws, L.part_P), at<int32_t>(ws, L.part_cnt),
-      at<float>(ws, L.part_z), aux_blocks(*c), f, P, l_balance, z_loss,
+      at<float>(ws, L.part_z), aux_rows(*c), f, P, l_balance, z_loss,
       at<DevStatus>(ws, L.status), s));
 }
 
@@ -600,7 +600,7 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
                                        s)) != cudaSuccess)
         return MOE_ERR_CUDA;
     }
-    return cuda_status(launch_aux_final(*c, part_P, part_cnt, part_z, aux_blocks(*c), f, P,
+    return cuda_status(launch_aux_final(*c, part_P, part_cnt, part_z, aux_rows(*c), f, P,
                                         l_balance, z_loss, s));
   }
 
@@ -629,7 +629,7 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
                              at<int32_t>(ws, L.tok_rows), ec_w, shared, out, s)) != cudaSuccess)
     return MOE_ERR_CUDA;
   return cuda_status(launch_aux_stats(*c, g, nullptr, nullptr, part_P, part_cnt, part_z,
-                                      aux_blocks(*c), f, P, l_balance, z_loss, dst, s));
+                                      aux_rows(*c), f, P, l_balance, z_loss, dst, s));
 }
 
 }  // namespace
@@ -822,7 +822,7 @@ int moe_forward_fp8(const moe_config* c, const void* x, const void* w_gate, cons
   if (launch_combine(*c, gd.y, b.row_of, w, gd.shared_out, out, s, F8.ks2, gd.y_part_stride,
                      gd.shared_part_stride) != cudaSuccess)
     return MOE_ERR_CUDA;
-  return cuda_status(launch_aux_final(*c, part_P, part_cnt, part_z, aux_blocks(*c), f, P,
+  return cuda_status(launch_aux_final(*c, part_P, part_cnt, part_z, aux_rows(*c), f, P,
                                       l_balance, z_loss, s));
 }
 

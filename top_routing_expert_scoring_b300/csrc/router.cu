@@ -153,10 +153,11 @@ static cudaError_t launch_stream(const moe_config& c, const void* x, const void*
 
 // ------------------------------------------------------------------------------------------
 // Logits for decode-sized batches (bf16): one CTA per (expert, group of TP tokens) streams
-// that expert's router row once (16-byte loads; its 8 warps take one eighth of d each) and
-// forms the group's dot products against the token rows, which stay in L1/L2; the 8 partial
-// sums are added in a fixed order.  Spreads the router weights over every SM instead of one
-// tile; x is re-read from L2 once per expert, so this is for small E or very small T.
+// that expert's router row (16-byte loads; its 8 warps take one eighth of d each) and forms
+// the group's dot products against the token rows, which stay in L1/L2; the 8 partial sums are
+// added in a fixed order.  Spreads the work over many SMs instead of one tile; the router row
+// is re-read from L2 once per token group and x once per expert, so this is for small E or
+// very small T.
 // ------------------------------------------------------------------------------------------
 template <int TP>
 __global__ void __launch_bounds__(256) router_logits_few(const uint4* __restrict__ x,
@@ -219,12 +220,9 @@ __global__ void __launch_bounds__(256) router_logits_few(const uint4* __restrict
 cudaError_t launch_router_logits(const moe_config& c, const void* x, const void* w_gate,
                                  float* logits, cudaStream_t s) {
   if (c.dtype == MOE_DTYPE_BF16 && (c.T <= 16 || (c.E <= 32 && c.T <= 512))) {
-    if (c.T <= 4)
-      launch_pdl(router_logits_few<4>, c.E, 256, 0, s, (const uint4*)x, (const uint4*)w_gate, logits, c.T,
-                                               c.d_model / 8, c.E);
-    else
-      launch_pdl(router_logits_few<16>, dim3(c.E, ceil_div(c.T, 16)), 256, 0, s, 
-          (const uint4*)x, (const uint4*)w_gate, logits, c.T, c.d_model / 8, c.E);
+    // four tokens per CTA: a lane keeps the four token loads of a step in flight together
+    launch_pdl(router_logits_few<4>, dim3(c.E, ceil_div(c.T, 4)), 256, 0, s,
+               (const uint4*)x, (const uint4*)w_gate, logits, c.T, c.d_model / 8, c.E);
     return cudaGetLastError();
   }
   if (c.dtype == MOE_DTYPE_BF16) {
@@ -468,12 +466,204 @@ __global__ void __launch_bounds__(256) route_topk_kernel(RouteArgs a) {
                          reinterpret_cast<unsigned char*>(route_smem));
 }
 
+// ------------------------------------------------------------------------------------------
+// Decode batches with E > 32: one CTA per token, thread e <-> expert e (E <= 256).  The warp
+// kernel above gives each lane E/32 experts and then walks k rounds of a warp-wide arg-max,
+// a long serial chain when a step has only a few tokens.  Here every step is a parallel count:
+//   1. each expert's rank within its segment (its group under a group limit, else its warp's
+//      32 experts) = the number of segment members that rank before it;
+//   2. group limit: a group's score is its rank-0 plus rank-1 key (its two largest), a group is
+//      kept when fewer than topk_groups groups rank before it (ties: lower group);
+//   3. candidates = kept experts of segment rank < k (the k best of the kept experts are among
+//      them); a candidate's rank among the candidates is its rank among all kept experts, and
+//      ranks 0..k-1 are the selection in rank order.
+// The order is the same strict (key descending, index ascending) order as everywhere, so the
+// selection is the same set in the same order; renormalised weights are formed as in the warp
+// kernel (lanes 0..k-1 of warp 0 in rank order).  With the statistics, each token writes its
+// own partial row (p_t, the selection indicator and lse_t^2); aux_token_kernel writes the same
+// rows for the separate statistics call, so both reduce to the same bits.
+// ------------------------------------------------------------------------------------------
+constexpr int kRouteCtaMaxT = 64;
+
+bool route_cta(const moe_config& c) {
+  return c.routing == MOE_ROUTE_TOKEN_CHOICE && c.E > 32 && c.T <= kRouteCtaMaxT;
+}
+
+int aux_rows(const moe_config& c) { return route_cta(c) ? c.T : aux_blocks(c); }
+
+// Block-wide reductions over blockDim/32 warps (every thread gets the result); red holds one
+// value per warp and is free again on return.
+__device__ __forceinline__ float block_max(float v, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_max(v);
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float m = red[0];
+  for (int w = 1; w < nw; ++w) m = fmaxf(m, red[w]);
+  __syncthreads();
+  return m;
+}
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_sum(v);
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = red[0];
+  for (int w = 1; w < nw; ++w) t += red[w];
+  __syncthreads();
+  return t;
+}
+
+// One token's statistics in the CTA layout (thread e holds g_e; invalid threads hold nothing):
+// P contribution softmax(g)_e (sigmoid scoring: s_e / sum_j s_j) and lse(g).
+__device__ __forceinline__ void token_stats_cta(float gv, bool valid, int score, float* red,
+                                                float& pc, float& lse) {
+  const float m = block_max(valid ? gv : -INFINITY, red);
+  const float ex = valid ? expf(gv - m) : 0.f;
+  const float se = block_sum(ex, red);
+  lse = m + logf(se);
+  if (score == MOE_SCORE_SOFTMAX) {
+    pc = ex / se;
+  } else {
+    const float sv = valid ? 1.0f / (1.0f + expf(-gv)) : 0.f;
+    const float ss = block_sum(sv, red);
+    pc = sv / ss;
+  }
+}
+
+__global__ void __launch_bounds__(256) route_topk_cta_kernel(RouteArgs a) {
+  pdl_prologue();
+  __shared__ float skey[256];
+  __shared__ float sval[256];
+  __shared__ float slot_key[256];
+  __shared__ int slot_idx[256];
+  __shared__ float gtop[2][32];
+  __shared__ int sel_idx[8];
+  __shared__ float sel_val[8];
+  __shared__ float red[8];
+  const int t = blockIdx.x, e = threadIdx.x, lane = e & 31, warp = e >> 5;
+  const int E = a.E, k = a.k;
+  const bool valid = e < E;
+  const float gv = valid ? a.g[(size_t)t * E + e] : -INFINITY;
+  float key, val;
+  if (a.score == MOE_SCORE_SOFTMAX) {
+    key = gv;
+    val = gv;
+  } else {
+    const float sv = valid ? 1.0f / (1.0f + expf(-gv)) : 0.f;
+    const float b = (valid && a.bias) ? a.bias[e] : 0.f;
+    val = sv;
+    key = valid ? sv + b : -INFINITY;
+  }
+  skey[e] = key;
+  sval[e] = val;
+  slot_idx[e] = -1;
+  float pc = 0.f, lse = 0.f;
+  const bool stats = a.part_P != nullptr;
+  if (stats) token_stats_cta(gv, valid, a.score, red, pc, lse);
+  __syncthreads();
+  const bool grouped =
+      a.score == MOE_SCORE_SIGMOID && a.n_groups > 1 && a.topk_groups < a.n_groups;
+  const int seg_len = grouped ? E / a.n_groups : 32;
+  const int seg = e / seg_len;
+  const int s0 = seg * seg_len, s1 = min(E, s0 + seg_len);
+  int r_seg = 0;
+  if (valid)
+    for (int q = s0; q < s1; ++q) r_seg += ranks_before(skey[q], q, key, e) ? 1 : 0;
+  bool kept = true;
+  if (grouped) {
+    if (valid && r_seg < 2) gtop[r_seg][seg] = key;
+    __syncthreads();
+    if (valid) {
+      const float gs = gtop[0][seg] + gtop[1][seg];
+      int grank = 0;
+      for (int q = 0; q < a.n_groups; ++q)
+        grank += ranks_before(gtop[0][q] + gtop[1][q], q, gs, seg) ? 1 : 0;
+      kept = grank < a.topk_groups;
+    }
+  }
+  const int kk = min(seg_len, k);
+  const bool cand = valid && kept && r_seg < kk;
+  if (cand) {
+    slot_key[seg * kk + r_seg] = key;
+    slot_idx[seg * kk + r_seg] = e;
+  }
+  __syncthreads();
+  const int nslots = ceil_div(E, seg_len) * kk;
+  bool selected = false;
+  if (cand) {
+    int rank = 0;
+    for (int q = 0; q < nslots; ++q) {
+      const int qi = slot_idx[q];
+      if (qi >= 0 && ranks_before(slot_key[q], qi, key, e)) ++rank;
+    }
+    if (rank < k) {
+      sel_idx[rank] = e;
+      sel_val[rank] = val;
+      selected = true;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int my_sel = lane < k ? sel_idx[lane] : -1;
+    const float my_val = lane < k ? sel_val[lane] : 0.f;
+    const float first_val = sel_val[0];
+    float num;
+    if (a.score == MOE_SCORE_SOFTMAX) num = lane < k ? expf(my_val - first_val) : 0.f;
+    else num = lane < k ? my_val : 0.f;
+    float den;
+    if (a.renorm) {
+      den = warp_sum(num);
+    } else if (a.score == MOE_SCORE_SOFTMAX) {
+      float part = 0.f;
+      for (int q = lane; q < E; q += 32) part += expf(sval[q] - first_val);
+      den = warp_sum(part);
+    } else {
+      den = 1.f;
+    }
+    if (lane < k) {
+      a.idx[(size_t)t * k + lane] = my_sel;
+      a.w[(size_t)t * k + lane] = (num / den) * a.scale;
+    }
+  }
+  if (stats && valid) {
+    a.part_P[(size_t)t * E + e] = pc;
+    a.part_cnt[(size_t)t * E + e] = selected ? 1 : 0;
+    if (e == 0) a.part_z[t] = lse * lse;
+  }
+}
+
+// The statistics rows of route_topk_cta_kernel for a given selection (moe_aux_stats).
+__global__ void __launch_bounds__(256) aux_token_kernel(const float* __restrict__ g,
+                                                       const int32_t* __restrict__ idx, int E,
+                                                       int k, int score, float* part_P,
+                                                       int32_t* part_cnt, float* part_z) {
+  pdl_prologue();
+  __shared__ float red[8];
+  const int t = blockIdx.x, e = threadIdx.x;
+  const bool valid = e < E;
+  const float gv = valid ? g[(size_t)t * E + e] : -INFINITY;
+  float pc, lse;
+  token_stats_cta(gv, valid, score, red, pc, lse);
+  if (!valid) return;
+  int c = 0;
+  for (int j = 0; j < k; ++j) c |= idx[(size_t)t * k + j] == e ? 1 : 0;
+  part_P[(size_t)t * E + e] = pc;
+  part_cnt[(size_t)t * E + e] = c;
+  if (e == 0) part_z[t] = lse * lse;
+}
+
 cudaError_t launch_route_topk(const moe_config& c, const float* logits, const float* bias,
                               int32_t* idx, float* w, DevStatus* st, cudaStream_t s,
                               float* part_P, int32_t* part_cnt, float* part_z) {
   (void)st;
   RouteArgs a{logits, bias, c.T, c.E, c.k, c.score, c.n_groups, c.topk_groups, c.renormalize,
               c.route_scale, idx, w, part_P, part_cnt, part_z};
+  if (route_cta(c)) {
+    launch_pdl(route_topk_cta_kernel, c.T, 32 * ceil_div(c.E, 32), 0, s, a);
+    return cudaGetLastError();
+  }
   const int wpb = kAuxWarps;
   // with the statistics, the grid is the statistics' fixed block count (fixed token sets)
   const int blocks = part_P ? aux_blocks(c) : ceil_div(c.T, wpb);
@@ -559,9 +749,24 @@ __global__ void __launch_bounds__(1024) aux_final_kernel(const float* part_P,
   float p = 0.f;
   int c = 0;
   if (e < E) {
-    for (int b = sub; b < nblk; b += W) {
-      p += part_P[(size_t)b * E + e];
-      c += part_cnt[(size_t)b * E + e];
+    // eight rows' loads in flight, then added in row order
+    for (int b0 = sub; b0 < nblk; b0 += 8 * W) {
+      float qp[8];
+      int qc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int b = b0 + i * W;
+        if (b < nblk) {
+          qp[i] = part_P[(size_t)b * E + e];
+          qc[i] = part_cnt[(size_t)b * E + e];
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (b0 + i * W >= nblk) break;
+        p += qp[i];
+        c += qc[i];
+      }
     }
   }
   sp[sub * 32 * G + e] = p;
@@ -606,6 +811,13 @@ cudaError_t launch_aux_stats(const moe_config& c, const float* logits, const int
                              float* part_z, int nblocks, float* f, float* P, float* l_balance,
                              float* z_loss, DevStatus* st, cudaStream_t s) {
   (void)st;
+  if (route_cta(c)) {                 // per-token rows, as the fused Top-k pass writes them
+    launch_pdl(aux_token_kernel, c.T, 32 * ceil_div(c.E, 32), 0, s, logits, idx, c.E, c.k,
+               c.score, part_P, part_cnt, part_z);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    return launch_aux_final(c, part_P, part_cnt, part_z, c.T, f, P, l_balance, z_loss, s);
+  }
   const int ecC = c.routing == MOE_ROUTE_EXPERT_CHOICE ? (int)((long long)c.T * c.k / c.E) : 0;
   AuxArgs a{logits, idx, c.T, c.E, c.k, c.score, ecC, part_P, part_cnt, part_z};
   const size_t smem = (size_t)kAuxWarps * c.E * 8 + kAuxWarps * 4 + 16;
