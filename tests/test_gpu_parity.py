@@ -90,6 +90,10 @@ SMALL = {
     "decode_mixtral_b32": dict(name="mixtral", T=32, d=512, F=384),
     "decode_collapsed_b256": dict(name="mixtral_collapsed", T=256, d=256, F=256),
     "decode_dsmoe_b100": dict(name="dsmoe16b", T=100, d=256, E=64, F=128, F_shared=128),
+    # E = 256: router logits from the K-sliced decode kernel (4 and 2 slices); Top-k one CTA
+    # per token (T <= 64) or one warp per token
+    "decode_e256_b40": dict(name="v3", T=40, d=512, E=256, F=128, F_shared=128),
+    "decode_e256_b100": dict(name="v3", T=100, d=1024, E=256, F=128, F_shared=128),
     "one_expert": dict(name="mixtral", T=130, d=128, E=1, k=1, F=128),
     # prefill path with E = 1, k = 1 and d = 256 (decode regime needs <= 64 rows per expert)
     "one_expert_d256": dict(name="mixtral", T=300, d=256, E=1, k=1, F=128),
@@ -285,6 +289,8 @@ FULL = {
     "dsmoe16b": dict(name="dsmoe16b"),
     "dsmoe16b_ec": dict(name="dsmoe16b_ec"),
     "v3": dict(name="v3"),
+    "v3_b64": dict(name="v3", T=64),
+    "v3_b256": dict(name="v3", T=256),
 }
 
 

@@ -83,8 +83,13 @@ struct DTile {
 __device__ __forceinline__ int entry_rows(const Params& p, int j) {
   return j < p.E ? p.offsets[j + 1] - p.offsets[j] : p.T;
 }
+// First row of an entry; with no routed entries (E = 0, the router logits) the shared entry's
+// rows start at 0 and offsets may be null.
+__device__ __forceinline__ int shared_row0(const Params& p) {
+  return p.E > 0 ? p.offsets[p.E] : 0;
+}
 __device__ __forceinline__ int entry_row0(const Params& p, int j) {
-  return j < p.E ? p.offsets[j] : p.offsets[p.E];
+  return j < p.E ? p.offsets[j] : shared_row0(p);
 }
 
 __device__ __forceinline__ int entry_np(const Params& p, int j) {
@@ -345,7 +350,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         } else {
           float* out = sh ? p.out_shared + static_cast<size_t>(t.ks) * p.shared_stride
                           : static_cast<float*>(p.out) + static_cast<size_t>(t.ks) * p.part_stride;
-          const int rbase = sh ? t.row0 - p.offsets[p.E] : t.row0;
+          const int rbase = sh ? t.row0 - shared_row0(p) : t.row0;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             if (i < m) {
@@ -572,7 +577,102 @@ static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& as, const CUt
   return cudaGetLastError();
 }
 
+// logits[t][e] = sum over K slices of part[s][t][e] in a fixed order: the slices are cut into
+// 8 consecutive groups, each group summed in slice order by its own thread (its loads in flight
+// together), then the group sums added in group order.  A CTA covers 32 four-column outputs.
+constexpr int kReduceGroups = 8;
+__global__ void __launch_bounds__(256) router_slices_reduce_kernel(const float4* __restrict__ part,
+                                                                  int S, size_t stride4,
+                                                                  size_t n4,
+                                                                  float4* __restrict__ logits) {
+  pdl_prologue();
+  __shared__ float4 gsum[kReduceGroups][32];
+  const int o = threadIdx.x & 31, grp = threadIdx.x >> 5;
+  const size_t i = blockIdx.x * (size_t)32 + o;
+  const int per = (S + kReduceGroups - 1) / kReduceGroups;
+  const int s0 = grp * per, s1 = min(S, s0 + per);
+  if (i < n4 && s0 < s1) {
+    float4 q[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (s0 + j < s1) q[j] = part[(s0 + j) * stride4 + i];
+    float4 v = q[0];
+#pragma unroll
+    for (int j = 1; j < 8; ++j)
+      if (s0 + j < s1) add4(v, q[j]);
+    for (int s = s0 + 8; s < s1; ++s) add4(v, part[s * stride4 + i]);
+    gsum[grp][o] = v;
+  }
+  __syncthreads();
+  if (grp != 0 || i >= n4) return;
+  float4 v = gsum[0][o];
+  for (int g = 1; g < kReduceGroups && g * per < S; ++g) add4(v, gsum[g][o]);
+  logits[i] = v;
+}
+
 }  // namespace dec
+
+// Router logits of a decode-sized batch with E a multiple of 256: g^T = W_gate x^T on the
+// decode kernel (W_gate's rows fill the MMA's M as one shared entry of E / 256 weight blocks,
+// the tokens fill N), with K = d cut into slices so that W_gate's stream spreads over many
+// SMs; a second pass sums the slices in order.
+int router_split(const moe_config& c) {
+  if (c.dtype != MOE_DTYPE_BF16 || c.E % 256 != 0 || c.d_model % 256 != 0) return 0;
+  if (c.T <= 16 || c.T > kRouterSplitMaxT) return 0;
+  const int chunks = ceil_div(c.T, 128);
+  const int kb = c.d_model / dec::BK;
+  int S = num_sms() / (chunks * (c.E / 256));
+  if (S > kb / 4) S = kb / 4;                       // at least four K blocks per slice
+  return S < 1 ? 1 : S;
+}
+
+size_t router_split_bytes(const moe_config& c) {
+  const int S = router_split(c);
+  return S ? (size_t)S * c.T * c.E * 4 : 0;
+}
+
+cudaError_t launch_router_split(const moe_config& c, const void* x, const void* w_gate,
+                                float* part, float* logits, DevStatus* st, cudaStream_t s) {
+  using namespace dec;
+  const int S = router_split(c);
+  if (S < 1 || !part) return cudaErrorInvalidValue;
+  int np = 16;
+  while (np < c.T && np < NP_MAX) np <<= 1;
+  CUtensorMap mw, mx;
+  if (!tc::make_map_box(&mw, w_gate, (uint64_t)c.E, (uint64_t)c.d_model, 128) ||
+      !tc::make_map_box(&mx, x, (uint64_t)c.T, (uint64_t)c.d_model, np))
+    return cudaErrorInvalidValue;
+  Params p{};
+  p.offsets = nullptr;
+  p.E = 0;
+  p.has_shared = 1;
+  p.T = c.T;
+  p.NP = np;
+  p.NPs = np;
+  p.gemm = 2;
+  p.K_routed = c.d_model;
+  p.K_shared = c.d_model;
+  p.wb_routed = 0;
+  p.wb_shared = c.E / 256;
+  p.a_rows_routed = 0;
+  p.out = nullptr;
+  p.out_shared = part;
+  p.ldo = c.E;
+  p.ksplit = S;
+  p.gu = nullptr;
+  p.part_stride = 0;
+  p.shared_stride = (size_t)c.T * c.E;
+  p.fp8 = 0;
+  p.bk = BK;
+  p.st = st;
+  cudaError_t e = launch(mw, mw, mx, mx, p, ceil_div(c.T, np) * p.wb_shared * S, s);
+  if (e != cudaSuccess) return e;
+  const size_t n4 = (size_t)c.T * c.E / 4;
+  launch_pdl(router_slices_reduce_kernel, static_cast<int>((n4 + 31) / 32), 256, 0, s,
+             reinterpret_cast<const float4*>(part), S, (size_t)c.T * c.E / 4, n4,
+             reinterpret_cast<float4*>(logits));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_ffn_decode(const DecodeFFN& g, DevStatus* st, cudaStream_t s) {
   using namespace dec;

@@ -14,8 +14,16 @@
 namespace moe {
 
 // ---- router ----------------------------------------------------------------------------------
+// part (nullable): router_split_bytes(c) of workspace for the K-sliced decode router.
 cudaError_t launch_router_logits(const moe_config& c, const void* x, const void* w_gate,
-                                 float* logits, cudaStream_t s);
+                                 float* logits, cudaStream_t s, float* part = nullptr,
+                                 DevStatus* st = nullptr);
+// K-sliced router for decode batches of a wide router (E % 256 == 0, 16 < T <= 512); 0 = off.
+constexpr int kRouterSplitMaxT = 512;
+int router_split(const moe_config& c);
+size_t router_split_bytes(const moe_config& c);
+cudaError_t launch_router_split(const moe_config& c, const void* x, const void* w_gate,
+                                float* part, float* logits, DevStatus* st, cudaStream_t s);
 // Router logits on the tensor cores (bf16, E a multiple of 32): g = x W_gate^T in fp32.
 cudaError_t launch_router_tc(const moe_config& c, const void* x, const void* w_gate,
                              float* logits, cudaStream_t s);

@@ -33,7 +33,8 @@ size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 struct Layout {
   size_t status, logits, idx, w, bitmap, blk_base, counts, kept, offsets, mtp, n_dropped, pos,
       row_of, perm, part_P, part_cnt, part_z, f, P, lb, z, x_perm, h, y_perm, shared_out,
-      ec_tokens, ec_w, tok_cnt, tok_ptr, tok_rows, posmap, tokstat, dec_gu, dec_y, dec_sh, total;
+      ec_tokens, ec_w, tok_cnt, tok_ptr, tok_rows, posmap, tokstat, dec_gu, dec_y, dec_sh,
+      router_part, total;
 };
 
 // K-split of the decode GEMMs: up to kMaxSplit slices, partial buffers only for small batches.
@@ -192,6 +193,7 @@ Layout layout(const moe_config& c) {
     L.dec_y = take((size_t)kMaxSplit * R * d * 4);
     L.dec_sh = take((size_t)kMaxSplit * T * d * 4);
   }
+  L.router_part = take(router_split_bytes(c));
   L.total = o;
   return L;
 }
@@ -316,7 +318,8 @@ int moe_router_topk(const moe_config* c, const void* x, const void* w_gate, cons
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Layout L = layout(*c);
   float* g = logits ? logits : at<float>(ws, L.logits);
-  cudaError_t e = launch_router_logits(*c, x, w_gate, g, s);
+  cudaError_t e = launch_router_logits(*c, x, w_gate, g, s, at<float>(ws, L.router_part),
+                                       at<DevStatus>(ws, L.status));
   if (e == cudaSuccess)
     e = launch_route_topk(*c, g, bias, topk_idx, topk_w, at<DevStatus>(ws, L.status), s);
   return cuda_status(e);
@@ -523,7 +526,7 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
     return ev ? cudaEventRecord(ev, s) : cudaSuccess;
   };
 
-  cudaError_t e = launch_router_logits(*c, x, w_gate, g, s);
+  cudaError_t e = launch_router_logits(*c, x, w_gate, g, s, at<float>(ws, L.router_part), dst);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   if (c->routing == MOE_ROUTE_TOKEN_CHOICE) {
@@ -771,7 +774,8 @@ int moe_forward_fp8(const moe_config* c, const void* x, const void* w_gate, cons
   int32_t* part_cnt = at<int32_t>(ws, L.part_cnt);
   float* part_z = at<float>(ws, L.part_z);
 
-  if (launch_router_logits(*c, x, w_gate, g, s) != cudaSuccess ||
+  if (launch_router_logits(*c, x, w_gate, g, s, at<float>(ws, L.router_part), dst) !=
+          cudaSuccess ||
       launch_route_topk(*c, g, bias, idx, w, dst, s, part_P, part_cnt, part_z) != cudaSuccess)
     return MOE_ERR_CUDA;
   DispatchBufs b{at<uint32_t>(ws, L.bitmap), at<int32_t>(ws, L.blk_base),

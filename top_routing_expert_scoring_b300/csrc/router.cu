@@ -218,7 +218,8 @@ __global__ void __launch_bounds__(256) router_logits_few(const uint4* __restrict
 }
 
 cudaError_t launch_router_logits(const moe_config& c, const void* x, const void* w_gate,
-                                 float* logits, cudaStream_t s) {
+                                 float* logits, cudaStream_t s, float* part, DevStatus* st) {
+  if (part && router_split(c) > 0) return launch_router_split(c, x, w_gate, part, logits, st, s);
   if (c.dtype == MOE_DTYPE_BF16 && (c.T <= 16 || (c.E <= 32 && c.T <= 512))) {
     // four tokens per CTA: a lane keeps the four token loads of a step in flight together
     launch_pdl(router_logits_few<4>, dim3(c.E, ceil_div(c.T, 4)), 256, 0, s,
