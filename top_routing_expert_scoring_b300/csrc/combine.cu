@@ -41,6 +41,17 @@ __device__ __forceinline__ void store4(TOut* dst, const float* a) {
   }
 }
 
+// Four consecutive values of y as float: 16 bytes of float32 or 8 bytes of bf16.
+__device__ __forceinline__ float4 load4(const float* p) {
+  return __ldg(reinterpret_cast<const float4*>(p));
+}
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
+  const uint2 v = __ldg(reinterpret_cast<const uint2*>(p));
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
 __device__ __forceinline__ void load_shared4(const float* shared, size_t off, float* acc) {
   if (shared) {
     const float4 q = *reinterpret_cast<const float4*>(shared + off);
@@ -53,13 +64,14 @@ __device__ __forceinline__ void load_shared4(const float* shared, size_t off, fl
 // Sum of nsplit partials (stride apart), in slice order, of 4 consecutive values; the loads of
 // up to eight slices are issued before the first add.
 constexpr int kPartGroup = 8;
-__device__ __forceinline__ float4 sum_parts4(const float* p, int nsplit, size_t stride) {
+template <typename TY>
+__device__ __forceinline__ float4 sum_parts4(const TY* p, int nsplit, size_t stride) {
   float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int s0 = 0; s0 < nsplit; s0 += kPartGroup) {
     float4 q[kPartGroup];
 #pragma unroll
     for (int i = 0; i < kPartGroup; ++i)
-      if (s0 + i < nsplit) q[i] = __ldg(reinterpret_cast<const float4*>(p + (s0 + i) * stride));
+      if (s0 + i < nsplit) q[i] = load4(p + (s0 + i) * stride);
 #pragma unroll
     for (int i = 0; i < kPartGroup; ++i) {
       if (s0 + i >= nsplit) break;
@@ -73,17 +85,19 @@ __device__ __forceinline__ float4 sum_parts4(const float* p, int nsplit, size_t 
   return v;
 }
 
-__device__ __forceinline__ void fma4(float wt, const float* y, float* acc) {
-  const float4 q = __ldg(reinterpret_cast<const float4*>(y));
+template <typename TY>
+__device__ __forceinline__ void fma4(float wt, const TY* y, float* acc) {
+  const float4 q = load4(y);
   acc[0] = fmaf(wt, q.x, acc[0]);
   acc[1] = fmaf(wt, q.y, acc[1]);
   acc[2] = fmaf(wt, q.z, acc[2]);
   acc[3] = fmaf(wt, q.w, acc[3]);
 }
 
-// Token-choice combine, prefill: y and shared hold one slice (float32), out bf16 or float32.
-template <typename TOut>
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y,
+// Token-choice combine, prefill: y (float32 or bf16) and shared (float32) hold one slice, out
+// bf16 or float32.
+template <typename TY, typename TOut>
+__global__ void __launch_bounds__(256) combine_kernel(const TY* __restrict__ y,
                                                      const int32_t* __restrict__ row_of,
                                                      const float* __restrict__ w,
                                                      const float* __restrict__ shared,
@@ -118,8 +132,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 // slices of y[row_of[t, j]] over the chunk's 128 columns, warp k those of shared[t] (when
 // given), and warp 0 adds them: acc = shared (or 0), then acc = fma(w[t, j], row_j, acc) for
 // j = 0..k-1, skipping dropped pairs.
-template <typename TOut>
-__global__ void __launch_bounds__(288) combine_rows_kernel(const float* __restrict__ y,
+template <typename TY, typename TOut>
+__global__ void __launch_bounds__(288) combine_rows_kernel(const TY* __restrict__ y,
                                                           const int32_t* __restrict__ row_of,
                                                           const float* __restrict__ w,
                                                           const float* __restrict__ shared,
@@ -134,20 +148,16 @@ __global__ void __launch_bounds__(288) combine_rows_kernel(const float* __restri
   const int chunks = ceil_div(d, 128);
   const int t = blockIdx.x / chunks;
   const int v = (blockIdx.x - t * chunks) * 128 + lane * 4;
-  const float* src = nullptr;
-  size_t stride = y_stride;
   if (warp < k) {
     const int r = row_of[(size_t)t * k + warp];
     if (lane == 0) {
       s_live[warp] = r >= 0;
       s_w[warp] = w[(size_t)t * k + warp];
     }
-    if (r >= 0) src = y + (size_t)r * d;
-  } else if (shared) {
-    src = shared + (size_t)t * d;
-    stride = shared_stride;
+    if (r >= 0 && v < d) part[warp][lane] = sum_parts4(y + (size_t)r * d + v, nsplit, y_stride);
+  } else if (shared && v < d) {
+    part[warp][lane] = sum_parts4(shared + (size_t)t * d + v, nsplit, shared_stride);
   }
-  if (src && v < d) part[warp][lane] = sum_parts4(src + v, nsplit, stride);
   __syncthreads();
   if (warp != 0 || v >= d) return;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -171,26 +181,27 @@ __global__ void __launch_bounds__(288) combine_rows_kernel(const float* __restri
 // the GPU with warps, takes the row-parallel kernel.
 constexpr int kCombineMinWarps = 2048;
 
-template <typename TOut>
-cudaError_t launch_combine_t(const moe_config& c, const float* y_perm, const int32_t* row_of,
+template <typename TY, typename TOut>
+cudaError_t launch_combine_t(const moe_config& c, const TY* y_perm, const int32_t* row_of,
                              const float* w, const float* shared_out, TOut* out, cudaStream_t s,
                              int nsplit, size_t y_stride, size_t shared_stride) {
   if (nsplit > 1 || (long long)c.T * ceil_div(c.d_model, 128) < kCombineMinWarps) {
     const int blocks = c.T * ceil_div(c.d_model, 128);
-    launch_pdl(combine_rows_kernel<TOut>, blocks, 32 * (c.k + 1), 0, s, y_perm, row_of, w,
+    launch_pdl(combine_rows_kernel<TY, TOut>, blocks, 32 * (c.k + 1), 0, s, y_perm, row_of, w,
                shared_out, out, c.d_model, c.k, nsplit, y_stride, shared_stride);
   } else {
     const int slice = combine_slice(c);
     const int blocks = ceil_div(c.T * ceil_div(c.d_model, slice) * 32, 256);
-    launch_pdl(combine_kernel<TOut>, blocks, 256, 0, s, y_perm, row_of, w, shared_out, out, c.T,
-               c.d_model, c.k, slice);
+    launch_pdl(combine_kernel<TY, TOut>, blocks, 256, 0, s, y_perm, row_of, w, shared_out, out,
+               c.T, c.d_model, c.k, slice);
   }
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const moe_config& c, const float* y_perm, const int32_t* row_of,
-                           const float* w, const float* shared_out, void* out, cudaStream_t s,
-                           int nsplit, size_t y_stride, size_t shared_stride) {
+template <typename TY>
+cudaError_t launch_combine_y(const moe_config& c, const TY* y_perm, const int32_t* row_of,
+                             const float* w, const float* shared_out, void* out, cudaStream_t s,
+                             int nsplit, size_t y_stride, size_t shared_stride) {
   if (c.out_dtype == MOE_DTYPE_F32)
     return launch_combine_t(c, y_perm, row_of, w, shared_out, static_cast<float*>(out), s,
                             nsplit, y_stride, shared_stride);
@@ -198,10 +209,24 @@ cudaError_t launch_combine(const moe_config& c, const float* y_perm, const int32
                           nsplit, y_stride, shared_stride);
 }
 
+cudaError_t launch_combine(const moe_config& c, const float* y_perm, const int32_t* row_of,
+                           const float* w, const float* shared_out, void* out, cudaStream_t s,
+                           int nsplit, size_t y_stride, size_t shared_stride) {
+  return launch_combine_y(c, y_perm, row_of, w, shared_out, out, s, nsplit, y_stride,
+                          shared_stride);
+}
+
+cudaError_t launch_combine_bf16y(const moe_config& c, const void* y_perm, const int32_t* row_of,
+                                 const float* w, const float* shared_out, void* out,
+                                 cudaStream_t s) {
+  return launch_combine_y(c, static_cast<const __nv_bfloat16*>(y_perm), row_of, w, shared_out,
+                          out, s, 1, 0, 0);
+}
+
 // Expert-choice combine: token t sums the rows tok_rows[tok_ptr[t] .. tok_ptr[t+1]) (ascending
 // expert order) with weights w_flat[row].
-template <typename TOut>
-__global__ void __launch_bounds__(256) combine_ec_kernel(const float* __restrict__ y,
+template <typename TY, typename TOut>
+__global__ void __launch_bounds__(256) combine_ec_kernel(const TY* __restrict__ y,
                                                         const int32_t* __restrict__ tok_ptr,
                                                         const int32_t* __restrict__ tok_rows,
                                                         const float* __restrict__ w_flat,
@@ -227,17 +252,29 @@ __global__ void __launch_bounds__(256) combine_ec_kernel(const float* __restrict
   }
 }
 
-cudaError_t launch_combine_ec(const moe_config& c, const float* y_perm, const int32_t* tok_ptr,
-                              const int32_t* tok_rows, const float* ec_w_flat,
-                              const float* shared_out, void* out, cudaStream_t s) {
+template <typename TY>
+cudaError_t launch_combine_ec_y(const moe_config& c, const TY* y_perm, const int32_t* tok_ptr,
+                                const int32_t* tok_rows, const float* ec_w_flat,
+                                const float* shared_out, void* out, cudaStream_t s) {
   const int blocks = ceil_div(c.T * ceil_div(c.d_model, kCombineSlice) * 32, 256);
   if (c.out_dtype == MOE_DTYPE_F32)
-    launch_pdl(combine_ec_kernel<float>, blocks, 256, 0, s, y_perm, tok_ptr, tok_rows, ec_w_flat,
-                                                    shared_out, (float*)out, c.T, c.d_model);
+    launch_pdl(combine_ec_kernel<TY, float>, blocks, 256, 0, s, y_perm, tok_ptr, tok_rows,
+               ec_w_flat, shared_out, (float*)out, c.T, c.d_model);
   else
-    launch_pdl(combine_ec_kernel<__nv_bfloat16>, blocks, 256, 0, s, 
-        y_perm, tok_ptr, tok_rows, ec_w_flat, shared_out, (__nv_bfloat16*)out, c.T, c.d_model);
+    launch_pdl(combine_ec_kernel<TY, __nv_bfloat16>, blocks, 256, 0, s, y_perm, tok_ptr,
+               tok_rows, ec_w_flat, shared_out, (__nv_bfloat16*)out, c.T, c.d_model);
   return cudaGetLastError();
+}
+
+cudaError_t launch_combine_ec(const moe_config& c, const void* y_perm, bool y_bf16,
+                              const int32_t* tok_ptr, const int32_t* tok_rows,
+                              const float* ec_w_flat, const float* shared_out, void* out,
+                              cudaStream_t s) {
+  if (y_bf16)
+    return launch_combine_ec_y(c, static_cast<const __nv_bfloat16*>(y_perm), tok_ptr, tok_rows,
+                               ec_w_flat, shared_out, out, s);
+  return launch_combine_ec_y(c, static_cast<const float*>(y_perm), tok_ptr, tok_rows, ec_w_flat,
+                             shared_out, out, s);
 }
 
 }  // namespace moe

@@ -670,7 +670,7 @@ cudaError_t launch_ffn_tc(const GroupedFFN& g, DevStatus* st, cudaStream_t s) {
   p2.b_rows = g.d;
   p2.up_off = 0;
   p2.out = g.y;
-  p2.out_f32 = 1;
+  p2.out_f32 = (g.y_bf16 && !g.scatter_out) ? 0 : 1;
   p2.ldo = g.d;
   p2.gperm = nullptr;
   p2.tail_split = p2.bn == 256 ? 1 : 0;

@@ -493,7 +493,7 @@ cudaError_t launch_ffn_tc2(const GroupedFFN& g, DevStatus* st, cudaStream_t s) {
   p2.b_rows = g.d;
   p2.up_off = 0;
   p2.out = g.y;
-  p2.out_f32 = 1;
+  p2.out_f32 = g.y_bf16 ? 0 : 1;
   p2.ldo = g.d;
   return launch_tc2(mh, mw2, p2, pt_upper * p2.n_tiles, s);
 }

@@ -80,7 +80,8 @@ struct GroupedFFN {
   const void* w13;          // [E, 2F, d]
   const void* w2;           // [E, d, F]
   void* h;                  // [max_rows, F] scratch
-  float* y;                 // [max_rows, d] float32
+  float* y;                 // [max_rows, d] float32, or bf16 when y_bf16
+  int y_bf16;               // the down GEMM rounds y to bf16 (tensor-core kernels only)
   // Optional (single-CTA kernel only): gather the gate/up GEMM's A rows straight from the
   // token rows, row r = token gather_perm[r] / gather_k of gather_x [T, d]; x is then unused.
   const int32_t* gather_perm;
@@ -147,9 +148,15 @@ cudaError_t launch_quantize_rows(const void* src, long long nrows_max, int cols,
 cudaError_t launch_combine(const moe_config& c, const float* y_perm, const int32_t* row_of,
                            const float* w, const float* shared_out, void* out, cudaStream_t s,
                            int nsplit = 1, size_t y_stride = 0, size_t shared_stride = 0);
-cudaError_t launch_combine_ec(const moe_config& c, const float* y_perm, const int32_t* tok_ptr,
-                              const int32_t* tok_rows, const float* ec_w_flat,
-                              const float* shared_out, void* out, cudaStream_t s);
+// The same with y_perm in bf16 (one slice), as the fused forward's down GEMM writes it.
+cudaError_t launch_combine_bf16y(const moe_config& c, const void* y_perm, const int32_t* row_of,
+                                 const float* w, const float* shared_out, void* out,
+                                 cudaStream_t s);
+// y_perm float32, or bf16 when y_bf16.
+cudaError_t launch_combine_ec(const moe_config& c, const void* y_perm, bool y_bf16,
+                              const int32_t* tok_ptr, const int32_t* tok_rows,
+                              const float* ec_w_flat, const float* shared_out, void* out,
+                              cudaStream_t s);
 
 // ---- expert choice ---------------------------------------------------------------------------
 // posmap [E][T]: position of token t in expert e's list or -1; ms [T]: softmax (max, sum).

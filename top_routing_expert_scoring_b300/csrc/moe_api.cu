@@ -368,8 +368,9 @@ int run_ffn(const moe_config& c, const void* xin, const int32_t* offsets, const 
             float* y, void* ws, const Layout& L, cudaStream_t s,
             const int32_t* gather_perm = nullptr, const void* gather_x = nullptr,
             float* scatter_out = nullptr, const int32_t* scatter_perm = nullptr,
-            const float* scatter_w = nullptr) {
+            const float* scatter_w = nullptr, bool y_bf16 = false) {
   GroupedFFN g{};
+  g.y_bf16 = y_bf16 && bf16(c) ? 1 : 0;
   g.gather_perm = gather_perm;
   g.gather_k = c.k;
   g.gather_x = gather_x;
@@ -589,19 +590,23 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
       if (scat && cudaMemsetAsync(out, 0, (size_t)c->T * c->d_model * 4, s) != cudaSuccess)
         return MOE_ERR_CUDA;
       if (mark(ev_begin) != cudaSuccess) return MOE_ERR_CUDA;
+      // y leaves the down GEMM in bf16 when a combine pass reads it back
+      const bool ybf = !scat && bf16(*c);
       if ((st = run_ffn(*c, at<void>(ws, L.x_perm), b.offsets, b.mtile_prefix, -1, c->E,
                         c->d_ff, rows_max(*c), w13, w2, at<float>(ws, L.y_perm), ws, L, s,
                         fuse ? b.perm : nullptr, fuse ? x : nullptr,
                         scat ? static_cast<float*>(out) : nullptr, scat ? b.perm : nullptr,
-                        scat ? w : nullptr)))
+                        scat ? w : nullptr, ybf)))
         return st;
       if (mark(ev_end) != cudaSuccess) return MOE_ERR_CUDA;
       if (shared && (st = run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13,
                                   ws2, shared, ws, L, s)))
         return st;
-      if (!scat && (e = launch_combine(*c, at<float>(ws, L.y_perm), b.row_of, w, shared, out,
-                                       s)) != cudaSuccess)
-        return MOE_ERR_CUDA;
+      if (!scat) {
+        e = ybf ? launch_combine_bf16y(*c, at<void>(ws, L.y_perm), b.row_of, w, shared, out, s)
+                : launch_combine(*c, at<float>(ws, L.y_perm), b.row_of, w, shared, out, s);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+      }
     }
     return cuda_status(launch_aux_final(*c, part_P, part_cnt, part_z, aux_rows(*c), f, P,
                                         l_balance, z_loss, s));
@@ -620,15 +625,17 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
                             at<int32_t>(ws, L.mtp), s)) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (mark(ev_begin) != cudaSuccess) return MOE_ERR_CUDA;
+  const bool ybf = bf16(*c);
   if ((st = run_ffn(*c, at<void>(ws, L.x_perm), at<int32_t>(ws, L.offsets),
                     at<int32_t>(ws, L.mtp), -1, c->E, c->d_ff, c->E * C, w13, w2,
-                    at<float>(ws, L.y_perm), ws, L, s)))
+                    at<float>(ws, L.y_perm), ws, L, s, nullptr, nullptr, nullptr, nullptr,
+                    nullptr, ybf)))
     return st;
   if (mark(ev_end) != cudaSuccess) return MOE_ERR_CUDA;
   if (shared && (st = run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13, ws2,
                               shared, ws, L, s)))
     return st;
-  if ((e = launch_combine_ec(*c, at<float>(ws, L.y_perm), at<int32_t>(ws, L.tok_ptr),
+  if ((e = launch_combine_ec(*c, at<void>(ws, L.y_perm), ybf, at<int32_t>(ws, L.tok_ptr),
                              at<int32_t>(ws, L.tok_rows), ec_w, shared, out, s)) != cudaSuccess)
     return MOE_ERR_CUDA;
   return cuda_status(launch_aux_stats(*c, g, nullptr, nullptr, part_P, part_cnt, part_z,
