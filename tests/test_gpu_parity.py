@@ -93,6 +93,12 @@ SMALL = {
     # E = 256: router logits from the K-sliced decode kernel (4 and 2 slices); Top-k one CTA
     # per token (T <= 64) or one warp per token
     "decode_e256_b40": dict(name="v3", T=40, d=512, E=256, F=128, F_shared=128),
+    # one-CTA-per-token Top-k with E not a multiple of 32 (idle threads in the last warp) and
+    # with groups of 25 and 24 experts that straddle warps
+    "topk_cta_e40": dict(name="mixtral", T=30, d=256, E=40, k=5, F=128),
+    "topk_cta_e200_groups25": dict(name="v3", T=50, d=256, E=200, k=7, F=128, F_shared=128),
+    "topk_cta_e96_groups24": dict(name="v3", T=37, d=256, E=96, k=8, F=128, n_shared=0,
+                                  F_shared=0, n_groups=4, topk_groups=3),
     "decode_e256_b100": dict(name="v3", T=100, d=1024, E=256, F=128, F_shared=128),
     "one_expert": dict(name="mixtral", T=130, d=128, E=1, k=1, F=128),
     # prefill path with E = 1, k = 1 and d = 256 (decode regime needs <= 64 rows per expert)
