@@ -73,6 +73,7 @@ struct Params {
   const float* sa;          // E4M3: scale of each routed weight row (row index of A)
   const float* sa_shared;   // E4M3: scale of each shared weight row
   const float* sb;          // E4M3: scale of each token row (row index of B)
+  float* hf;                // GEMM 1, E4M3, one K slice: h = SiLU(g) * u in float32 [rows, ldo]
   DevStatus* st;
 };
 
@@ -325,7 +326,17 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
           }
         }
-        if (p.gemm == 1 && p.gu == nullptr) {
+        if (p.gemm == 1 && p.hf) {
+          // one K slice: h in float32, formed as the quantising pass would form it
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (i < m) {
+              const float g = __uint_as_float(lo[i]), u = __uint_as_float(hi[i]);
+              p.hf[static_cast<size_t>(t.row0 + c0 + i) * p.ldo + t.wb * 128 + f] =
+                  (g / (1.0f + expf(-g))) * u;
+            }
+          }
+        } else if (p.gemm == 1 && p.gu == nullptr) {
           __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
@@ -473,6 +484,7 @@ __device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t ran
 // E4M3 path: h[r][:] = SiLU(sum_s gate_s[r][:]) * sum_s up_s[r][:] (slices in order), then the
 // row is quantised as every E4M3 operand: amax = max |h|, inv = 448 / amax, code = e4m3(h * inv)
 // (round to nearest even, saturating), scale = amax / 448; a zero row gets codes 0, scale 0.
+// With one K slice the gate/up GEMM has formed h itself (h_ready: gu is one float32 plane).
 // Row r is split over the CTAs of a cluster (a cluster of one CTA when rows are many), one
 // column range each; h stays in shared memory between the two passes, and the row's amax is
 // the maximum of the CTAs' maxima, read through distributed shared memory.  A maximum does not
@@ -481,7 +493,7 @@ __global__ void __launch_bounds__(1024, 1) swiglu_quant_kernel(const float* __re
                                                            size_t part_stride, int S,
                                                            const int32_t* __restrict__ offsets,
                                                            int E, int n_shared_rows, int F,
-                                                           int Fs, int ldo,
+                                                           int Fs, int ldo, int h_ready,
                                                            uint8_t* __restrict__ h8,
                                                            float* __restrict__ hs) {
   pdl_prologue();
@@ -496,22 +508,33 @@ __global__ void __launch_bounds__(1024, 1) swiglu_quant_kernel(const float* __re
   const int chunk = ceil_div(F4, static_cast<int>(csize));
   const int f0 = static_cast<int>(crank) * chunk;
   const int f1 = min(F4, f0 + chunk);
-  const float4* src = reinterpret_cast<const float4*>(gu + static_cast<size_t>(r) * (2 * ldo));
+  // h_ready: gu holds h itself, one float32 plane [rows, ldo] written by the gate/up GEMM
+  const float4* src =
+      reinterpret_cast<const float4*>(gu + static_cast<size_t>(r) * (h_ready ? ldo : 2 * ldo));
   const size_t ps4 = part_stride / 4, up4 = static_cast<size_t>(ldo) / 4;
   float amax = 0.f;
   for (int f = f0 + threadIdx.x; f < f1; f += 2 * blockDim.x) {
     const int fb = f + blockDim.x;
     const bool two = fb < f1;
-    float4 g[2], u[2];
-    sum_slices4x2(src + f, src + (two ? fb : f), two, ps4, up4, S, g, u);
+    float4 hh[2];
+    if (h_ready) {
+      hh[0] = src[f];
+      if (two) hh[1] = src[fb];
+    } else {
+      float4 g[2], u[2];
+      sum_slices4x2(src + f, src + (two ? fb : f), two, ps4, up4, S, g, u);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        hh[c].x = (g[c].x / (1.0f + expf(-g[c].x))) * u[c].x;
+        hh[c].y = (g[c].y / (1.0f + expf(-g[c].y))) * u[c].y;
+        hh[c].z = (g[c].z / (1.0f + expf(-g[c].z))) * u[c].z;
+        hh[c].w = (g[c].w / (1.0f + expf(-g[c].w))) * u[c].w;
+      }
+    }
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       if (c == 1 && !two) break;
-      float4 hv;
-      hv.x = (g[c].x / (1.0f + expf(-g[c].x))) * u[c].x;
-      hv.y = (g[c].y / (1.0f + expf(-g[c].y))) * u[c].y;
-      hv.z = (g[c].z / (1.0f + expf(-g[c].z))) * u[c].z;
-      hv.w = (g[c].w / (1.0f + expf(-g[c].w))) * u[c].w;
+      const float4 hv = hh[c];
       hrow4[(c ? fb : f) - f0] = hv;
       amax = fmaxf(amax,
                    fmaxf(fmaxf(fabsf(hv.x), fabsf(hv.y)), fmaxf(fabsf(hv.z), fabsf(hv.w))));
@@ -727,6 +750,12 @@ cudaError_t launch_ffn_decode(const DecodeFFN& g, DevStatus* st, cudaStream_t s)
   p1.sa = g.s13;
   p1.sa_shared = g.ss13;
   p1.sb = g.sx;
+  // E4M3 with one K slice: the gate/up GEMM writes h itself (half the bytes of gate | up)
+  const bool h_ready = g.fp8 && g.ksplit1 == 1;
+  if (h_ready) {
+    p1.hf = g.gu;
+    p1.gu = nullptr;
+  }
   p1.st = st;
   // upper bound of the tile count: every routed row in its own chunk is impossible to exceed
   const int chunks_upper = ceil_div(g.max_rows, g.np) + g.E + ceil_div(g.T, g.np_shared) + 1;
@@ -756,7 +785,8 @@ cudaError_t launch_ffn_decode(const DecodeFFN& g, DevStatus* st, cudaStream_t s)
     cfg.numAttrs = 2;
     err = cudaLaunchKernelEx(&cfg, swiglu_quant_kernel, static_cast<const float*>(g.gu),
                              p1.part_stride, g.ksplit1, g.offsets, g.E, sh ? g.T : 0, g.F,
-                             sh ? g.F_shared : 0, Fmax, static_cast<uint8_t*>(g.h), g.hs);
+                             sh ? g.F_shared : 0, Fmax, h_ready ? 1 : 0,
+                             static_cast<uint8_t*>(g.h), g.hs);
     if (err != cudaSuccess) return err;
   } else if (g.ksplit1 > 1) {
     const long long work = static_cast<long long>(g.max_rows) * Fmax;

@@ -125,8 +125,9 @@ struct DecodeFFN {
   size_t y_part_stride;     // elements between y partials (max_rows * d)
   size_t shared_part_stride;// elements between shared partials (T * d)
   // E4M3 operands: x, h, w13, w2, ws13, ws2 hold one-byte codes and these hold the per-row
-  // scales; gu must be set (gate/up always go through the float32 partials, then h is
-  // quantised per row into h / hs)
+  // scales; gu must be set: the gate/up GEMM writes its float32 partials there (with one K
+  // slice, h = SiLU(g) * u itself as [max_rows, max(F, F_shared)]), then h is quantised per
+  // row into h / hs
   int fp8;
   const float* s13;         // [E * 2F]
   const float* s2;          // [E * d]
