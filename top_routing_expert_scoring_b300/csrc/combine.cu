@@ -85,6 +85,18 @@ __device__ __forceinline__ float4 sum_parts4(const TY* p, int nsplit, size_t str
   return v;
 }
 
+// Eight consecutive bf16 values of y (16 bytes) into acc[0..7] with fused multiply-adds.
+__device__ __forceinline__ void fma8(float wt, const __nv_bfloat16* y, float* acc) {
+  const uint4 v = __ldg(reinterpret_cast<const uint4*>(y));
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[i]));
+    acc[2 * i] = fmaf(wt, f.x, acc[2 * i]);
+    acc[2 * i + 1] = fmaf(wt, f.y, acc[2 * i + 1]);
+  }
+}
+
 template <typename TY>
 __device__ __forceinline__ void fma4(float wt, const TY* y, float* acc) {
   const float4 q = load4(y);
@@ -118,13 +130,27 @@ __global__ void __launch_bounds__(256) combine_kernel(const TY* __restrict__ y,
     rows[j] = j < k ? row_of[(size_t)t * k + j] : -1;
     ws[j] = j < k ? w[(size_t)t * k + j] : 0.f;
   }
-  for (int v = v0 + lane * 4; v < v1; v += 128) {
-    float acc[4];
-    load_shared4(shared, (size_t)t * d + v, acc);
+  if constexpr (sizeof(TY) == 2) {
+    // bf16 y: eight columns per lane and step, so every y load moves 16 bytes
+    for (int v = v0 + lane * 8; v < v1; v += 256) {
+      float acc[8];
+      load_shared4(shared, (size_t)t * d + v, acc);
+      load_shared4(shared, (size_t)t * d + v + 4, acc + 4);
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (rows[j] >= 0) fma4(ws[j], y + (size_t)rows[j] * d + v, acc);
-    store4<TOut>(out + (size_t)t * d + v, acc);
+      for (int j = 0; j < 8; ++j)
+        if (rows[j] >= 0) fma8(ws[j], y + (size_t)rows[j] * d + v, acc);
+      store4<TOut>(out + (size_t)t * d + v, acc);
+      store4<TOut>(out + (size_t)t * d + v + 4, acc + 4);
+    }
+  } else {
+    for (int v = v0 + lane * 4; v < v1; v += 128) {
+      float acc[4];
+      load_shared4(shared, (size_t)t * d + v, acc);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (rows[j] >= 0) fma4(ws[j], y + (size_t)rows[j] * d + v, acc);
+      store4<TOut>(out + (size_t)t * d + v, acc);
+    }
   }
 }
 
@@ -190,7 +216,8 @@ cudaError_t launch_combine_t(const moe_config& c, const TY* y_perm, const int32_
     launch_pdl(combine_rows_kernel<TY, TOut>, blocks, 32 * (c.k + 1), 0, s, y_perm, row_of, w,
                shared_out, out, c.d_model, c.k, nsplit, y_stride, shared_stride);
   } else {
-    const int slice = combine_slice(c);
+    int slice = combine_slice(c);
+    if (sizeof(TY) == 2 && slice < 256) slice = 256;      // a bf16 warp step covers 256 columns
     const int blocks = ceil_div(c.T * ceil_div(c.d_model, slice) * 32, 256);
     launch_pdl(combine_kernel<TY, TOut>, blocks, 256, 0, s, y_perm, row_of, w, shared_out, out,
                c.T, c.d_model, c.k, slice);
