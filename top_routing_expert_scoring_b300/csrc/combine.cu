@@ -268,14 +268,38 @@ __global__ void __launch_bounds__(256) combine_ec_kernel(const TY* __restrict__ 
   const int v0 = (gw - t * slices) * kCombineSlice;
   const int v1 = min(d, v0 + kCombineSlice);
   const int b = tok_ptr[t], e_ = tok_ptr[t + 1];
-  for (int v = v0 + lane * 4; v < v1; v += 128) {
-    float acc[4];
-    load_shared4(shared, (size_t)t * d + v, acc);
-    for (int q = b; q < e_; ++q) {
-      const int r = tok_rows[q];
-      fma4(w_flat[r], y + (size_t)r * d + v, acc);
+  // the warp's whole slice is accumulated at once (each row's index and weight read once per
+  // row, all of the row's loads in flight); per element: shared first, then the rows in order
+  constexpr int VEC = sizeof(TY) == 2 ? 8 : 4;
+  constexpr int NSTEP = kCombineSlice / (32 * VEC);
+  float acc[NSTEP][VEC];
+#pragma unroll
+  for (int st = 0; st < NSTEP; ++st) {
+    const int v = v0 + st * 32 * VEC + lane * VEC;
+#pragma unroll
+    for (int i = 0; i < VEC; i += 4) {
+      if (v < v1) load_shared4(shared, (size_t)t * d + v + i, &acc[st][i]);
+      else acc[st][i] = acc[st][i + 1] = acc[st][i + 2] = acc[st][i + 3] = 0.f;
     }
-    store4<TOut>(out + (size_t)t * d + v, acc);
+  }
+  for (int q = b; q < e_; ++q) {
+    const int r = tok_rows[q];
+    const float wt = w_flat[r];
+    const TY* yr = y + (size_t)r * d;
+#pragma unroll
+    for (int st = 0; st < NSTEP; ++st) {
+      const int v = v0 + st * 32 * VEC + lane * VEC;
+      if (v >= v1) continue;
+      if constexpr (VEC == 8) fma8(wt, yr + v, acc[st]);
+      else fma4(wt, yr + v, acc[st]);
+    }
+  }
+#pragma unroll
+  for (int st = 0; st < NSTEP; ++st) {
+    const int v = v0 + st * 32 * VEC + lane * VEC;
+    if (v >= v1) continue;
+#pragma unroll
+    for (int i = 0; i < VEC; i += 4) store4<TOut>(out + (size_t)t * d + v + i, &acc[st][i]);
   }
 }
 
