@@ -39,7 +39,7 @@ def load_peaks():
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the grouped GEMM's two launches
 # in one step, from an ncu capture of the bench command on the current kernel build
 # (profiles/launches_mixtral_t4096_bench.md); None for a workload without a capture.
-GEMM_TRAFFIC_BYTES = {("mixtral", 4096): (1946775296 + 224005632) + (1426172160 + 128498688)}
+GEMM_TRAFFIC_BYTES = {("mixtral", 4096): (1946556672 + 224120832) + (1557085440 + 125510656)}
 
 
 def workload_flops_bytes(wl):
