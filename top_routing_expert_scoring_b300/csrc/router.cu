@@ -71,14 +71,17 @@ __global__ void __launch_bounds__(256) router_logits_simt(const T* __restrict__ 
 
 // ------------------------------------------------------------------------------------------
 // Logits for a small expert count (E <= 32, bf16): the router weights stay in shared memory
-// and each warp streams one token row with 16-byte loads, keeping E partial dot products per
-// lane; a butterfly reduction (fixed order) finishes them.  HBM-bound on reading x.
+// and each warp streams TPW token rows at once with 16-byte loads (two for E <= 8: each weight
+// vector read from shared memory then serves both; one for more experts, to stay within the
+// registers), keeping E partial dot products per token and lane; a butterfly reduction (fixed
+// order) finishes them.  HBM-bound on reading x.
 // ------------------------------------------------------------------------------------------
 template <int EP>
-__global__ void __launch_bounds__(512) router_logits_stream(const uint4* __restrict__ x,
+__global__ void __launch_bounds__(512, 1) router_logits_stream(const uint4* __restrict__ x,
                                                            const uint4* __restrict__ w,
                                                            float* __restrict__ g, int Tn,
                                                            int d8, int E) {
+  constexpr int TPW = EP <= 8 ? 2 : 1;
   pdl_prologue();
   extern __shared__ uint4 wsm[];                  // [EP][d8]: 8 bf16 per uint4
   for (int i = threadIdx.x; i < EP * d8; i += blockDim.x) {
@@ -88,49 +91,70 @@ __global__ void __launch_bounds__(512) router_logits_stream(const uint4* __restr
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
-  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tn; t += warps) {
-    float acc[EP];
+  const int groups = (Tn + TPW - 1) / TPW;
+  for (int tg = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; tg < groups; tg += warps) {
+    const int t0 = TPW * tg;
+    const int nt = min(TPW, Tn - t0);
+    float acc[TPW][EP];
 #pragma unroll
-    for (int e = 0; e < EP; ++e) acc[e] = 0.f;
-    const uint4* xr = x + (size_t)t * d8;
-    // four independent 16-byte loads in flight per lane, then their products in order
+    for (int q = 0; q < TPW; ++q)
+#pragma unroll
+      for (int e = 0; e < EP; ++e) acc[q][e] = 0.f;
+    const uint4* xr[TPW];
+#pragma unroll
+    for (int q = 0; q < TPW; ++q) xr[q] = x + (size_t)(t0 + (q < nt ? q : 0)) * d8;
+    // per token four independent 16-byte loads in flight per lane, then their products in order
     for (int c0 = lane; c0 < d8; c0 += 128) {
-      uint4 xv[4];
+      uint4 xv[TPW][4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        xv[u] = c0 + 32 * u < d8 ? __ldg(xr + c0 + 32 * u) : make_uint4(0u, 0u, 0u, 0u);
+      for (int u = 0; u < 4; ++u) {
+        const bool in = c0 + 32 * u < d8;
+#pragma unroll
+        for (int q = 0; q < TPW; ++q)
+          xv[q][u] = in ? __ldg(xr[q] + c0 + 32 * u) : make_uint4(0u, 0u, 0u, 0u);
+      }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int c = c0 + 32 * u;
         if (c >= d8) break;
-        const __nv_bfloat162* xh = reinterpret_cast<const __nv_bfloat162*>(&xv[u]);
-        float xf[8];
+        float xf[TPW][8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __bfloat1622float2(xh[i]);
-          xf[2 * i] = f.x;
-          xf[2 * i + 1] = f.y;
+        for (int q = 0; q < TPW; ++q) {
+          const __nv_bfloat162* xh = reinterpret_cast<const __nv_bfloat162*>(&xv[q][u]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(xh[i]);
+            xf[q][2 * i] = f.x;
+            xf[q][2 * i + 1] = f.y;
+          }
         }
 #pragma unroll
         for (int e = 0; e < EP; ++e) {
           const uint4 wv = wsm[e * d8 + c];
           const __nv_bfloat162* wh = reinterpret_cast<const __nv_bfloat162*>(&wv);
-          float a = acc[e];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 f = __bfloat1622float2(wh[i]);
-            a = fmaf(xf[2 * i], f.x, a);
-            a = fmaf(xf[2 * i + 1], f.y, a);
+          for (int q = 0; q < TPW; ++q) {
+            float a = acc[q][e];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 f = __bfloat1622float2(wh[i]);
+              a = fmaf(xf[q][2 * i], f.x, a);
+              a = fmaf(xf[q][2 * i + 1], f.y, a);
+            }
+            acc[q][e] = a;
           }
-          acc[e] = a;
         }
       }
     }
 #pragma unroll
-    for (int e = 0; e < EP; ++e) acc[e] = warp_sum(acc[e]);
+    for (int q = 0; q < TPW; ++q) {
+      if (q >= nt) break;
 #pragma unroll
-    for (int e = 0; e < EP; ++e)
-      if (lane == e && e < E) g[(size_t)t * E + e] = acc[e];
+      for (int e = 0; e < EP; ++e) acc[q][e] = warp_sum(acc[q][e]);
+#pragma unroll
+      for (int e = 0; e < EP; ++e)
+        if (lane == e && e < E) g[(size_t)(t0 + q) * E + e] = acc[q][e];
+    }
   }
 }
 
