@@ -124,8 +124,9 @@ int moe_router_topk(const moe_config* cfg, const void* x, const void* w_gate, co
  * P_i = mean_t softmax(g_t)_i (sigmoid scoring: mean_t s_ti / sum_j s_tj);
  * z = mean_t (logsumexp_i g_ti)^2.
  *   logits [T,E] f32, topk_idx [T,k] int32 -> f [E], P [E], l_balance [1], z_loss [1] (f32).
- * Reductions run in float32 in a fixed order (per token block, then across blocks): results
- * are bit-identical from run to run. */
+ * Reductions run in float32 in a fixed order (per token block, or per token when E > 32 and
+ * T <= 64, then across blocks): results are bit-identical from run to run, and equal to the
+ * statistics moe_forward returns for the same logits and selection. */
 int moe_aux_stats(const moe_config* cfg, const float* logits, const int32_t* topk_idx, float* f,
                   float* P, float* l_balance, float* z_loss, void* ws, void* stream);
 
@@ -216,7 +217,9 @@ int moe_forward_timed(const moe_config* cfg, const void* x, const void* w_gate, 
                       void* stream, void* ev_expert_begin, void* ev_expert_end);
 
 /* Device addresses of the intermediates moe_forward leaves in `ws` (for inspection and
- * tests): logits [T,E] f32, row_of [T,k] int32, offsets [E+1] int32, x_perm, y_perm (f32). */
+ * tests): logits [T,E] f32, row_of [T,k] int32, offsets [E+1] int32, x_perm, y_perm (f32 from
+ * moe_expert_ffn; after a bf16 prefill moe_forward with a separate combine pass it holds the
+ * rows in bf16). */
 int moe_workspace_views(const moe_config* cfg, void* ws, float** logits, int32_t** row_of,
                         int32_t** offsets, void** x_perm, float** y_perm);
 
