@@ -146,14 +146,81 @@ constexpr int kSmallCopySeg = 128;
 // three-kernel path (bitmap of the tokens per expert, scans, popcount ranks), so the results
 // are identical; CTA 0 publishes it, and all CTAs copy their share of the rows: routed rows
 // [0, nkept), then (append_shared) the T token rows after them for the shared experts.
+// With fin.part_P set, one extra (last) CTA finishes the load-balance statistics instead.
+
+// The statistics' last step with 256 threads, in exactly aux_final_kernel's arithmetic and
+// order: with G = the 32-expert groups (rounded up to a power of two) and W = 32 / G, expert
+// e's sum is the sum over sub = 0..W-1 (in order) of the sums over rows sub, sub + W, ...
+// (in order), each started from 0; f = count / T, P = sum / T; then warp 0 adds f_i P_i over
+// lanes (expert x at lane x mod 32, in order) and the z partials (row b at lane b mod 32),
+// each finished by the same butterfly.
+__device__ void finish_stats_cta(const StatsFinal& fin, int T, int E) {
+  __shared__ float prod[256];
+  const int e = threadIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int G = 1;
+  while (G * 32 < E) G <<= 1;
+  const int W = 32 / G;
+  const float invT = 1.0f / (float)T;
+  if (e < E) {
+    float ps = 0.f;
+    int cs = 0;
+    for (int sub = 0; sub < W; ++sub) {
+      float p = 0.f;
+      int c = 0;
+      for (int b0 = sub; b0 < fin.nrows; b0 += 8 * W) {   // eight rows' loads in flight
+        float qp[8];
+        int qc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int b = b0 + i * W;
+          if (b < fin.nrows) {
+            qp[i] = fin.part_P[(size_t)b * E + e];
+            qc[i] = fin.part_cnt[(size_t)b * E + e];
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (b0 + i * W >= fin.nrows) break;
+          p += qp[i];
+          c += qc[i];
+        }
+      }
+      ps += p;
+      cs += c;
+    }
+    const float fe = (float)cs * invT, Pe = ps * invT;
+    if (fin.f) fin.f[e] = fe;
+    if (fin.P) fin.P[e] = Pe;
+    prod[e] = fe * Pe;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    float acc = 0.f;
+    for (int x = lane; x < E; x += 32) acc += prod[x];
+    acc = warp_sum(acc);
+    float z = 0.f;
+    for (int b = lane; b < fin.nrows; b += 32) z += fin.part_z[b];
+    z = warp_sum(z);
+    if (lane == 0) {
+      if (fin.l_balance) *fin.l_balance = (float)E * acc;
+      if (fin.z_loss) *fin.z_loss = z * invT;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kDispatchBlock) dispatch_small_kernel(
     const int32_t* __restrict__ idx, int T, int E, int k, int capacity,
     int32_t* __restrict__ counts, int32_t* __restrict__ kept, int32_t* __restrict__ offsets,
     int32_t* __restrict__ mtile_prefix, int32_t* __restrict__ n_dropped,
     int32_t* __restrict__ pos, int32_t* __restrict__ row_of, int32_t* __restrict__ perm,
     DevStatus* st, const unsigned char* __restrict__ x, unsigned char* __restrict__ x_perm,
-    int row_bytes, int append_shared) {
+    int row_bytes, int append_shared, const StatsFinal fin) {
   pdl_prologue();
+  const bool with_stats = fin.part_P != nullptr;
+  if (with_stats && blockIdx.x == gridDim.x - 1) {
+    finish_stats_cta(fin, T, E);
+    return;
+  }
   __shared__ uint32_t bm[256 * kWords];
   __shared__ int s_kept[256];
   __shared__ int s_mt[256];
@@ -261,7 +328,7 @@ __global__ void __launch_bounds__(kDispatchBlock) dispatch_small_kernel(
   const int nrows = nkept + (append_shared ? T : 0);
   const int n16 = row_bytes / 16;
   const int segs = ceil_div(n16, kSmallCopySeg);
-  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int warps = ((gridDim.x - (with_stats ? 1 : 0)) * blockDim.x) >> 5;
   for (int item = (blockIdx.x * blockDim.x + tid) >> 5; item < nrows * segs; item += warps) {
     const int r = item / segs, sg = item - r * segs;
     const int src_t = r < nkept ? s_perm[r] / k : r - nkept;
@@ -281,6 +348,8 @@ __global__ void __launch_bounds__(kDispatchBlock) dispatch_small_kernel(
     }
   }
 }
+
+bool dispatch_finalizes_stats(const moe_config& c) { return c.T <= kDispatchBlock; }
 
 // One warp per expert-ordered row; rows past offsets[E] get perm = -1.
 template <int VEC_BYTES>
@@ -336,7 +405,7 @@ cudaError_t launch_append_rows(const moe_config& c, const int32_t* offsets, cons
 
 cudaError_t launch_dispatch(const moe_config& c, int capacity, const int32_t* idx,
                             const DispatchBufs& b, const void* x, void* x_perm, DevStatus* st,
-                            cudaStream_t s, bool append_shared) {
+                            cudaStream_t s, bool append_shared, const StatsFinal* fin) {
   const int nblk = ceil_div(c.T, kDispatchBlock);
   cudaError_t err;
   const int esz = c.dtype == MOE_DTYPE_F32 ? 4 : 2;
@@ -346,10 +415,13 @@ cudaError_t launch_dispatch(const moe_config& c, int capacity, const int32_t* id
     const int items = rows * ceil_div(row_bytes / 16, kSmallCopySeg);
     int blocks = x ? ceil_div(items, 8) : 1;
     if (blocks > num_sms()) blocks = num_sms();
-    launch_pdl(dispatch_small_kernel, blocks, kDispatchBlock, 0, s, 
+    const StatsFinal none{};
+    const StatsFinal& sf = fin ? *fin : none;
+    if (fin) ++blocks;                       // the statistics' CTA
+    launch_pdl(dispatch_small_kernel, blocks, kDispatchBlock, 0, s,
         idx, c.T, c.E, c.k, capacity, b.counts, b.kept, b.offsets, b.mtile_prefix, b.n_dropped,
         b.pos, b.row_of, b.perm, st, (const unsigned char*)x, (unsigned char*)x_perm, row_bytes,
-        append_shared ? 1 : 0);
+        append_shared ? 1 : 0, sf);
     return cudaGetLastError();
   } else {
     launch_pdl(dispatch_count_kernel, nblk, kDispatchBlock, 0, s, idx, c.T, c.E, c.k, b.bitmap,

@@ -58,10 +58,27 @@ struct DispatchBufs {
   int32_t* row_of;      // [T,k]
   int32_t* perm;        // [T*k]
 };
+// The last step of the load-balance statistics (launch_aux_final's arithmetic and order), for
+// the small dispatch to run in one extra CTA: partial rows in, f / P / l_balance / z_loss out
+// (each nullable).
+struct StatsFinal {
+  const float* part_P;
+  const int32_t* part_cnt;
+  const float* part_z;
+  int nrows;
+  float* f;
+  float* P;
+  float* l_balance;
+  float* z_loss;
+};
 // append_shared: also copy the T token rows after the kept rows (decode path's shared rows).
+// fin (nullable): with T <= kDispatchBlock (one launch; dispatch_finalizes_stats) the launch
+// also finishes the statistics, so no launch_aux_final is needed.
 cudaError_t launch_dispatch(const moe_config& c, int capacity, const int32_t* idx,
                             const DispatchBufs& b, const void* x, void* x_perm, DevStatus* st,
-                            cudaStream_t s, bool append_shared = false);
+                            cudaStream_t s, bool append_shared = false,
+                            const StatsFinal* fin = nullptr);
+bool dispatch_finalizes_stats(const moe_config& c);
 
 // x_perm[offsets[E] + t] = x[t] for t < T (rows of the shared experts on the decode path).
 cudaError_t launch_append_rows(const moe_config& c, const int32_t* offsets, const void* x,

@@ -533,8 +533,9 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
   if (c->routing == MOE_ROUTE_TOKEN_CHOICE) {
     int32_t* idx = topk_idx ? topk_idx : at<int32_t>(ws, L.idx);
     float* w = topk_w ? topk_w : at<float>(ws, L.w);
-    // Top-k with the load-balance partials of the same pass; the partials are reduced after
-    // the combine, off the path to the output
+    // Top-k with the load-balance partials of the same pass; the partials are reduced by an
+    // extra CTA of the small dispatch (T <= 256), else after the combine, off the path to the
+    // output
     if ((e = launch_route_topk(*c, g, bias, idx, w, dst, s, part_P, part_cnt, part_z)) !=
         cudaSuccess)
       return MOE_ERR_CUDA;
@@ -545,9 +546,13 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
                    at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.mtp),
                    n_dropped ? n_dropped : at<int32_t>(ws, L.n_dropped), at<int32_t>(ws, L.pos),
                    at<int32_t>(ws, L.row_of), at<int32_t>(ws, L.perm)};
+    // small batches: the dispatch launch also finishes the statistics (one extra CTA)
+    const bool fin_in_dispatch = dispatch_finalizes_stats(*c);
+    const StatsFinal fin{part_P, part_cnt, part_z, aux_rows(*c), f, P, l_balance, z_loss};
     if ((e = launch_dispatch(*c, capacity_of(*c), idx, b, fuse ? nullptr : x,
                              fuse ? nullptr : at<void>(ws, L.x_perm), dst, s,
-                             dec && shared != nullptr)) != cudaSuccess)
+                             dec && shared != nullptr, fin_in_dispatch ? &fin : nullptr)) !=
+        cudaSuccess)
       return MOE_ERR_CUDA;
     if (dec) {
       DecodeFFN g{};
@@ -608,6 +613,7 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
         if (e != cudaSuccess) return MOE_ERR_CUDA;
       }
     }
+    if (fin_in_dispatch) return MOE_OK;
     return cuda_status(launch_aux_final(*c, part_P, part_cnt, part_z, aux_rows(*c), f, P,
                                         l_balance, z_loss, s));
   }
@@ -789,9 +795,12 @@ int moe_forward_fp8(const moe_config* c, const void* x, const void* w_gate, cons
                  at<int32_t>(ws, L.counts), at<int32_t>(ws, L.kept), at<int32_t>(ws, L.offsets),
                  at<int32_t>(ws, L.mtp), n_dropped ? n_dropped : at<int32_t>(ws, L.n_dropped),
                  at<int32_t>(ws, L.pos), at<int32_t>(ws, L.row_of), at<int32_t>(ws, L.perm)};
-  // routed rows in expert order, then (with shared experts) the T token rows
-  if (launch_dispatch(*c, capacity_of(*c), idx, b, x, at<void>(ws, L.x_perm), dst, s, has_sh) !=
-      cudaSuccess)
+  // routed rows in expert order, then (with shared experts) the T token rows; small batches
+  // finish the statistics in the same launch
+  const bool fin_in_dispatch = dispatch_finalizes_stats(*c);
+  const StatsFinal fin{part_P, part_cnt, part_z, aux_rows(*c), f, P, l_balance, z_loss};
+  if (launch_dispatch(*c, capacity_of(*c), idx, b, x, at<void>(ws, L.x_perm), dst, s, has_sh,
+                      fin_in_dispatch ? &fin : nullptr) != cudaSuccess)
     return MOE_ERR_CUDA;
   const int R = rows_max(*c);
   uint8_t* x8 = at<uint8_t>(ws, F8.x8);
@@ -833,6 +842,7 @@ int moe_forward_fp8(const moe_config* c, const void* x, const void* w_gate, cons
   if (launch_combine(*c, gd.y, b.row_of, w, gd.shared_out, out, s, F8.ks2, gd.y_part_stride,
                      gd.shared_part_stride) != cudaSuccess)
     return MOE_ERR_CUDA;
+  if (fin_in_dispatch) return MOE_OK;
   return cuda_status(launch_aux_final(*c, part_P, part_cnt, part_z, aux_rows(*c), f, P,
                                       l_balance, z_loss, s));
 }
