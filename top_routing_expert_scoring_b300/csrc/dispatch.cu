@@ -12,6 +12,9 @@
 //       the expert GEMMs and the drop count;
 //   D3  pos(t,j) = base[block][e] + popcount of bm[e] below t; row, perm;
 //   D4  x_perm[row] = x[t] with 16-byte vector copies, one warp per row.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -142,6 +145,9 @@ __global__ void __launch_bounds__(kDispatchBlock) dispatch_scatter_kernel(
 // CTA recomputes the (small) dispatch in shared memory with the same counting scheme as the
 // 16-byte vectors per row segment copied by one warp in the small dispatch (2 KB)
 constexpr int kSmallCopySeg = 128;
+// E4M3 rows in the small dispatch: up to this many 16-byte vectors per thread (rows of up to
+// kQuantVecs * kDispatchBlock * 8 bf16 values)
+constexpr int kQuantVecs = 4;
 
 // three-kernel path (bitmap of the tokens per expert, scans, popcount ranks), so the results
 // are identical; CTA 0 publishes it, and all CTAs copy their share of the rows: routed rows
@@ -214,7 +220,8 @@ __global__ void __launch_bounds__(kDispatchBlock) dispatch_small_kernel(
     int32_t* __restrict__ mtile_prefix, int32_t* __restrict__ n_dropped,
     int32_t* __restrict__ pos, int32_t* __restrict__ row_of, int32_t* __restrict__ perm,
     DevStatus* st, const unsigned char* __restrict__ x, unsigned char* __restrict__ x_perm,
-    int row_bytes, int append_shared, const StatsFinal fin) {
+    int row_bytes, int append_shared, const StatsFinal fin, uint8_t* __restrict__ x8,
+    float* __restrict__ sx) {
   pdl_prologue();
   const bool with_stats = fin.part_P != nullptr;
   if (with_stats && blockIdx.x == gridDim.x - 1) {
@@ -322,6 +329,62 @@ __global__ void __launch_bounds__(kDispatchBlock) dispatch_small_kernel(
   if (lead)
     for (int r = tid; r < T * k; r += blockDim.x) perm[r] = r < nkept ? s_perm[r] : -1;
   if (x == nullptr) return;
+  if (x8) {
+    // E4M3 rows instead of bf16 copies, one row per CTA at a time, exactly as the row
+    // quantiser makes them: amax = max |v|, inv = 448 / amax, code = e4m3(v * inv) (nearest
+    // even, saturating), scale = amax / 448; the row is read once (registers)
+    __shared__ float red[kDispatchBlock / 32];
+    const int nrows = nkept + (append_shared ? T : 0);
+    const int vecs = row_bytes / 16;
+    const int copy_ctas = gridDim.x - (with_stats ? 1 : 0);
+    for (int r = blockIdx.x; r < nrows; r += copy_ctas) {
+      const int src_t = r < nkept ? s_perm[r] / k : r - nkept;
+      const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)src_t * row_bytes);
+      uint4 v[kQuantVecs];
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < kQuantVecs; ++i) {
+        const int c = tid + i * kDispatchBlock;
+        if (c < vecs) {
+          v[i] = __ldg(src + c);
+          const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(b[j]);
+            amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+          }
+        }
+      }
+      amax = warp_max(amax);
+      if ((tid & 31) == 0) red[tid >> 5] = amax;
+      __syncthreads();
+      amax = red[0];
+      for (int w = 1; w < kDispatchBlock / 32; ++w) amax = fmaxf(amax, red[w]);
+      __syncthreads();                             // red is rewritten for the next row
+      const float inv = amax > 0.f ? 448.0f / amax : 0.f;
+      uint2* d = reinterpret_cast<uint2*>(x8 + (size_t)r * (row_bytes / 2));
+#pragma unroll
+      for (int i = 0; i < kQuantVecs; ++i) {
+        const int c = tid + i * kDispatchBlock;
+        if (c >= vecs) break;
+        const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
+        uint32_t packed[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float2 f0 = __bfloat1622float2(b[2 * j]);
+          const float2 f1 = __bfloat1622float2(b[2 * j + 1]);
+          const uint32_t q0 = __nv_cvt_float2_to_fp8x2(make_float2(f0.x * inv, f0.y * inv),
+                                                       __NV_SATFINITE, __NV_E4M3);
+          const uint32_t q1 = __nv_cvt_float2_to_fp8x2(make_float2(f1.x * inv, f1.y * inv),
+                                                       __NV_SATFINITE, __NV_E4M3);
+          packed[j] = (q0 & 0xFFFFu) | (q1 << 16);
+        }
+        d[c] = make_uint2(packed[0], packed[1]);
+      }
+      if (tid == 0) sx[r] = amax > 0.f ? amax / 448.0f : 0.f;
+    }
+    return;
+  }
   // row copies: one warp per 2 KB segment of a row (routed rows, then appended rows), four
   // 16-byte loads in flight per lane
   const int lane = tid & 31;
@@ -350,6 +413,11 @@ __global__ void __launch_bounds__(kDispatchBlock) dispatch_small_kernel(
 }
 
 bool dispatch_finalizes_stats(const moe_config& c) { return c.T <= kDispatchBlock; }
+
+bool dispatch_quantizes(const moe_config& c) {
+  return c.T <= kDispatchBlock && c.dtype == MOE_DTYPE_BF16 &&
+         c.d_model <= kQuantVecs * kDispatchBlock * 8;
+}
 
 // One warp per expert-ordered row; rows past offsets[E] get perm = -1.
 template <int VEC_BYTES>
@@ -405,7 +473,8 @@ cudaError_t launch_append_rows(const moe_config& c, const int32_t* offsets, cons
 
 cudaError_t launch_dispatch(const moe_config& c, int capacity, const int32_t* idx,
                             const DispatchBufs& b, const void* x, void* x_perm, DevStatus* st,
-                            cudaStream_t s, bool append_shared, const StatsFinal* fin) {
+                            cudaStream_t s, bool append_shared, const StatsFinal* fin,
+                            uint8_t* x8, float* sx) {
   const int nblk = ceil_div(c.T, kDispatchBlock);
   cudaError_t err;
   const int esz = c.dtype == MOE_DTYPE_F32 ? 4 : 2;
@@ -413,7 +482,7 @@ cudaError_t launch_dispatch(const moe_config& c, int capacity, const int32_t* id
   if (nblk == 1) {
     const int rows = c.T * c.k + (append_shared ? c.T : 0);
     const int items = rows * ceil_div(row_bytes / 16, kSmallCopySeg);
-    int blocks = x ? ceil_div(items, 8) : 1;
+    int blocks = x ? (x8 ? rows : ceil_div(items, 8)) : 1;
     if (blocks > num_sms()) blocks = num_sms();
     const StatsFinal none{};
     const StatsFinal& sf = fin ? *fin : none;
@@ -421,7 +490,7 @@ cudaError_t launch_dispatch(const moe_config& c, int capacity, const int32_t* id
     launch_pdl(dispatch_small_kernel, blocks, kDispatchBlock, 0, s,
         idx, c.T, c.E, c.k, capacity, b.counts, b.kept, b.offsets, b.mtile_prefix, b.n_dropped,
         b.pos, b.row_of, b.perm, st, (const unsigned char*)x, (unsigned char*)x_perm, row_bytes,
-        append_shared ? 1 : 0, sf);
+        append_shared ? 1 : 0, sf, x8, sx);
     return cudaGetLastError();
   } else {
     launch_pdl(dispatch_count_kernel, nblk, kDispatchBlock, 0, s, idx, c.T, c.E, c.k, b.bitmap,

@@ -74,11 +74,15 @@ struct StatsFinal {
 // append_shared: also copy the T token rows after the kept rows (decode path's shared rows).
 // fin (nullable): with T <= kDispatchBlock (one launch; dispatch_finalizes_stats) the launch
 // also finishes the statistics, so no launch_aux_final is needed.
+// x8 / sx (nullable, only where dispatch_quantizes): the rows go out as E4M3 codes with their
+// per-row scales (the row quantiser's bytes) instead of bf16 copies into x_perm.
 cudaError_t launch_dispatch(const moe_config& c, int capacity, const int32_t* idx,
                             const DispatchBufs& b, const void* x, void* x_perm, DevStatus* st,
                             cudaStream_t s, bool append_shared = false,
-                            const StatsFinal* fin = nullptr);
+                            const StatsFinal* fin = nullptr, uint8_t* x8 = nullptr,
+                            float* sx = nullptr);
 bool dispatch_finalizes_stats(const moe_config& c);
+bool dispatch_quantizes(const moe_config& c);
 
 // x_perm[offsets[E] + t] = x[t] for t < T (rows of the shared experts on the decode path).
 cudaError_t launch_append_rows(const moe_config& c, const int32_t* offsets, const void* x,

@@ -797,15 +797,19 @@ int moe_forward_fp8(const moe_config* c, const void* x, const void* w_gate, cons
                  at<int32_t>(ws, L.pos), at<int32_t>(ws, L.row_of), at<int32_t>(ws, L.perm)};
   // routed rows in expert order, then (with shared experts) the T token rows; small batches
   // finish the statistics in the same launch
+  // (and, for small batches, write the rows straight as E4M3 codes)
   const bool fin_in_dispatch = dispatch_finalizes_stats(*c);
   const StatsFinal fin{part_P, part_cnt, part_z, aux_rows(*c), f, P, l_balance, z_loss};
-  if (launch_dispatch(*c, capacity_of(*c), idx, b, x, at<void>(ws, L.x_perm), dst, s, has_sh,
-                      fin_in_dispatch ? &fin : nullptr) != cudaSuccess)
-    return MOE_ERR_CUDA;
   const int R = rows_max(*c);
   uint8_t* x8 = at<uint8_t>(ws, F8.x8);
   float* sx = at<float>(ws, F8.sx);
-  if (launch_quantize_rows(at<void>(ws, L.x_perm), (long long)R + c->T, c->d_model,
+  const bool q_in_dispatch = dispatch_quantizes(*c);
+  if (launch_dispatch(*c, capacity_of(*c), idx, b, x, at<void>(ws, L.x_perm), dst, s, has_sh,
+                      fin_in_dispatch ? &fin : nullptr, q_in_dispatch ? x8 : nullptr,
+                      q_in_dispatch ? sx : nullptr) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (!q_in_dispatch &&
+      launch_quantize_rows(at<void>(ws, L.x_perm), (long long)R + c->T, c->d_model,
                            b.offsets + c->E, has_sh ? c->T : 0, x8, sx, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   DecodeFFN gd{};
