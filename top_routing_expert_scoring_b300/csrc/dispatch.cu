@@ -482,8 +482,11 @@ cudaError_t launch_dispatch(const moe_config& c, int capacity, const int32_t* id
   if (nblk == 1) {
     const int rows = c.T * c.k + (append_shared ? c.T : 0);
     const int items = rows * ceil_div(row_bytes / 16, kSmallCopySeg);
+    // row copies: up to one CTA per SM; E4M3 rows (one CTA per row at a time, two barriers
+    // per row): up to four per SM
     int blocks = x ? (x8 ? rows : ceil_div(items, 8)) : 1;
-    if (blocks > num_sms()) blocks = num_sms();
+    const int cap = x8 ? 4 * num_sms() : num_sms();
+    if (blocks > cap) blocks = cap;
     const StatsFinal none{};
     const StatsFinal& sf = fin ? *fin : none;
     if (fin) ++blocks;                       // the statistics' CTA
