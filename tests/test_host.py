@@ -178,3 +178,17 @@ def test_group_limit_needs_two_experts_per_group():
     assert m.check_config(config_of(wl)) == -2
     ok = moe_inputs.workload("v3", T=16, d=256, E=8, n_groups=4, topk_groups=2, k=2)
     assert m.check_config(config_of(ok)) == 0
+
+
+def test_binding_rejects_host_tensors_before_any_call():
+    # the binding hands the library device pointers only: a CPU tensor is refused in Python,
+    # before the C call, so no host address ever reaches a kernel
+    import torch
+    m = _lib()
+    wl = moe_inputs.workload("mixtral", T=8, d=256, F=256)
+    cfg = config_of(wl)
+    x = torch.zeros(8, 256, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        m.moe_forward(cfg, x, x, None, x, x, None, None, x, ws=x)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        m.quantize_fp8(x)
