@@ -35,16 +35,20 @@ def _route(m, wl, cfg, inp):
     return idx, ws
 
 
-def _check_case(m, wl):
+def _check_case(m, wl, gather=True):
+    """Both dispatch entry points on the same routed indices; gather=False passes no x and no
+    x_perm (counts, positions and permutation only)."""
     cfg = U.config_of(wl)
     inp = moe_inputs.make_router_inputs(wl, device=DEV)
     idx, ws = _route(m, wl, cfg, inp)
     a = _outputs(wl.T, wl.E, wl.k, wl.d)
     b = _outputs(wl.T, wl.E, wl.k, wl.d)
     names = ["counts", "kept", "offsets", "pos", "row_of", "perm"]
-    m.moe_dispatch(cfg, idx, inp["x"], *[a[n] for n in names], a["x_perm"], a["n_dropped"], ws)
+    x = inp["x"] if gather else None
+    m.moe_dispatch(cfg, idx, x, *[a[n] for n in names], a["x_perm"] if gather else None,
+                   a["n_dropped"], ws)
     status = torch.full((2,), 123, dtype=torch.int32, device=DEV)
-    m.moe_dispatch_noalloc(cfg, idx, inp["x"], *[b[n] for n in names], b["x_perm"],
+    m.moe_dispatch_noalloc(cfg, idx, x, *[b[n] for n in names], b["x_perm"] if gather else None,
                            b["n_dropped"], status)
     torch.cuda.synchronize()
     assert m.sync_status(ws) == 0
@@ -52,18 +56,25 @@ def _check_case(m, wl):
     for n in names + ["n_dropped"]:
         assert torch.equal(a[n], b[n]), n
     nk = int(a["offsets"][-1].item())
-    assert torch.equal(a["x_perm"][:nk], b["x_perm"][:nk])
+    if gather:
+        assert torch.equal(a["x_perm"][:nk], b["x_perm"][:nk])
+    else:
+        assert not b["x_perm"].any()      # no rows were gathered
     return int(a["n_dropped"].item())
 
 
-def test_noalloc_dispatch_equals_workspace_dispatch_twice():
+def test_noalloc_dispatch_equals_workspace_dispatch_in_a_row():
     m = U.lib()
     first = moe_inputs.workload("v3", T=700, d=256, E=64, F=256, F_shared=256,
                                 capacity_factor=1.25)
     second = moe_inputs.workload("mixtral_collapsed", T=1000, d=256, F=256, capacity_factor=1.0)
+    # T <= 256 runs the one-launch dispatch, which uses only the array's M-tile-prefix words
+    third = moe_inputs.workload("mixtral", T=200, d=256, E=8, k=2, F=256, capacity_factor=1.0)
     d1 = _check_case(m, first)
     d2 = _check_case(m, second)        # same scratch array, different shape, right after
-    assert d1 > 0 and d2 > 0
+    d3 = _check_case(m, third)
+    d4 = _check_case(m, second, gather=False)
+    assert d1 > 0 and d2 > 0 and d3 > 0 and d4 == d2
 
 
 def test_noalloc_dispatch_refuses_more_than_its_scratch_holds():

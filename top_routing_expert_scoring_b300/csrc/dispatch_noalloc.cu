@@ -16,8 +16,11 @@
 // another.  Each call rewrites every scratch word before reading it, and clears the caller's
 // two status words first.
 //
-// The first call on each device looks up the array's device address (cudaGetSymbolAddress,
-// with that device current) and caches it; make that first call before any stream capture.
+// Every call made outside stream capture looks up the array's device address
+// (cudaGetSymbolAddress, with the calling device current) and caches it per device, so the
+// address stays right after a device reset or a context torn down and created again.  A call
+// made while its stream is being captured uses the cached address instead (no lookup during
+// capture): make one call on that device before capturing.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -44,17 +47,22 @@ std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of g_dispatch_scratch on the current device.  In host code the symbol name is
-// only a host-side handle, so the address is looked up once per device (with that device
-// current) and cached.
-int scratch_address(void** out) {
+// only a host-side handle, so the address is looked up with the device current: afresh on
+// every call outside stream capture (a reset device or a re-created context may place the
+// array elsewhere), from the per-device cache while `s` is capturing.
+int scratch_address(cudaStream_t s, void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return MOE_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
     g_scratch_addr[dev] = p;
+  } else if (!g_scratch_addr[dev]) {
+    return MOE_ERR_UNSUPPORTED;       // no uncaptured call on this device yet
   }
   *out = g_scratch_addr[dev];
   return MOE_OK;
@@ -77,9 +85,9 @@ extern "C" int moe_dispatch_noalloc(const moe_config* c, const int32_t* topk_idx
     return MOE_ERR_ARG;
   if ((x == nullptr) != (x_perm == nullptr)) return MOE_ERR_ARG;
   if (c->T > kNoAllocMaxTokens || c->E > kNoAllocMaxExperts) return MOE_ERR_SHAPE;
-  void* base = nullptr;
-  if ((st = scratch_address(&base))) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* base = nullptr;
+  if ((st = scratch_address(s, &base))) return st;
   uint32_t* words = static_cast<uint32_t*>(base);
   DispatchBufs b{words,
                  reinterpret_cast<int32_t*>(words + kBitmapWords),
