@@ -152,12 +152,16 @@ int moe_dispatch(const moe_config* cfg, const int32_t* topk_idx, const void* x, 
  * workspace: its scratch is one fixed array inside the library, about 2.3 MB on every GPU that
  * loads it, held until the process exits.
  *   Same inputs and outputs as moe_dispatch, and bit-identical results, plus
- *   status [2] int32 (device): cleared on entry, then (code, detail) of the first device-side
- *   error (MOE_ERR_ARG for an out-of-range or repeated expert index).
+ *   status [2] int32 (device): a call that passes its host-side checks clears it on the
+ *   stream first, then the kernels write (code, detail) of the first device-side error
+ *   (MOE_ERR_ARG for an out-of-range or repeated expert index).  A call refused on the host
+ *   (its return value is not MOE_OK) enqueues nothing and leaves these words as they were.
  * Limits: T <= 65536 and E <= 256, else MOE_ERR_SHAPE before any launch.  All calls share the
  * one array and it keeps the last call's contents: calls that overlap on the GPU race, so
- * issue them one after another.  The first call on a device looks up the array's device
- * address and caches it; make that first call before any stream capture.  Allocates nothing. */
+ * issue them one after another.  A call outside stream capture looks up the array's device
+ * address (with the calling device current) and caches it; a call on a capturing stream uses
+ * that cached address, so make one uncaptured call on the device before capturing
+ * (MOE_ERR_UNSUPPORTED otherwise).  Allocates nothing. */
 int moe_dispatch_noalloc(const moe_config* cfg, const int32_t* topk_idx, const void* x,
                          int32_t* counts, int32_t* kept, int32_t* offsets, int32_t* pos,
                          int32_t* row_of, int32_t* perm, void* x_perm, int32_t* n_dropped,
@@ -207,9 +211,10 @@ int moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const 
                 float* z_loss, int32_t* n_dropped, void* ws, void* stream);
 
 /* moe_forward that also records two caller-created CUDA events (cudaEvent_t, timing enabled)
- * on `stream` around the expert GEMM launches: the routed experts' grouped GEMMs (prefill),
- * or the routed and shared experts' decode GEMMs.  Same kernels and results as moe_forward;
- * for measuring the GEMM share of a forward.  Both events are required. */
+ * on `stream` around the expert GEMM launches: the routed experts' grouped GEMMs followed by
+ * the shared experts' GEMMs (prefill), or the routed and shared experts' decode GEMMs.  Same
+ * kernels and results as moe_forward; for measuring the GEMM share of a forward.  Both events
+ * are required. */
 int moe_forward_timed(const moe_config* cfg, const void* x, const void* w_gate, const float* bias,
                       const void* w13, const void* w2, const void* ws13, const void* ws2,
                       void* out, int32_t* topk_idx, float* topk_w, float* f, float* P,

@@ -43,7 +43,10 @@ constexpr int B_STAGE = 2 * B_BOX;           // up to 256 rows
 constexpr int TMEM_COLS = 512;               // 2 accumulators x 256 fp32 columns
 constexpr int THREADS = 192;
 constexpr int NBARS = 2 * STAGES + 5;        // full, empty, tmem full x2, tmem empty x2, drain
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * (A_STAGE + B_STAGE) + 256;
+// expert schedule in shared memory: the M-tile prefix in schedule order [257] and the
+// expert at each schedule position [256]
+constexpr int SCHED_BYTES = (257 + 256) * 4;
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * (A_STAGE + B_STAGE) + 256 + SCHED_BYTES;
 
 struct Params {
   const int32_t* offsets;   // [E+1]
@@ -67,6 +70,9 @@ struct Params {
   // N = 256 only: the last tiles of the list may each run as two N = 128 halves, to even out
   // the final wave over the CTAs (see choose_tail_split)
   int tail_split;
+  // expert order of the tile list: 0 = expert index order; 1 = interleaved by row count
+  // (largest, smallest, second largest, second smallest, ...), see build_schedule
+  int order;
   // float32 epilogue only: instead of storing row r, add w[perm[r]] * row into token
   // perm[r] / scat_k of scat_out [T, ldo] (float32 vector reductions); rows with perm < 0 skip
   float* scat_out;
@@ -104,12 +110,19 @@ struct TileInfo {
   int col0, bn;             // first output column and MMA N of this tile
 };
 
-__device__ __forceinline__ int total_tiles(const Params& p) {
-  const int mt = p.uniform_rows >= 0 ? ceil_div(p.uniform_rows, BM) : p.mtp[p.E];
+// The tile list walks the experts in schedule order: position j holds expert ord[j] (ord ==
+// nullptr: expert j) and mtp[j] M tiles precede it.
+struct Sched {
+  const int32_t* mtp;       // [E+1] M-tile prefix in schedule order
+  const int32_t* ord;       // [E] expert at each position, or nullptr for index order
+};
+
+__device__ __forceinline__ int total_tiles(const Params& p, const Sched& sc) {
+  const int mt = p.uniform_rows >= 0 ? ceil_div(p.uniform_rows, BM) : sc.mtp[p.E];
   return mt * p.n_tiles;
 }
 
-__device__ __forceinline__ TileInfo decode_tile(int tile, const Params& p) {
+__device__ __forceinline__ TileInfo decode_tile(int tile, const Params& p, const Sched& sc) {
   TileInfo ti;
   int base_m, mt_e, row_base, row_end;
   if (p.uniform_rows >= 0) {
@@ -119,16 +132,16 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const Params& p) {
     row_base = 0;
     row_end = p.uniform_rows;
   } else {
-    int lo = 0, hi = p.E;   // largest e in [0, E) with mtp[e] * n_tiles <= tile
+    int lo = 0, hi = p.E;   // largest position j in [0, E) with mtp[j] * n_tiles <= tile
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (p.mtp[mid] * p.n_tiles <= tile) lo = mid; else hi = mid;
+      if (sc.mtp[mid] * p.n_tiles <= tile) lo = mid; else hi = mid;
     }
-    ti.e = lo;
-    base_m = p.mtp[lo];
-    mt_e = p.mtp[lo + 1] - base_m;
-    row_base = p.offsets[lo];
-    row_end = p.offsets[lo + 1];
+    ti.e = sc.ord ? sc.ord[lo] : lo;
+    base_m = sc.mtp[lo];
+    mt_e = sc.mtp[lo + 1] - base_m;
+    row_base = p.offsets[ti.e];
+    row_end = p.offsets[ti.e + 1];
   }
   const int tt = tile - base_m * p.n_tiles;
   ti.nt = tt / mt_e;
@@ -140,13 +153,44 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const Params& p) {
   return ti;
 }
 
+// Interleaved expert order, built by every CTA from the offsets (E <= 256, all threads): rank
+// the experts by row count (descending, ties to the lower index) and place rank r at position
+// 2r for the larger half and 2(E-1-r)+1 for the smaller half.  Consecutive tiles, which run at
+// the same time on neighbouring CTAs, then mix experts whose weight stream dominates (few
+// rows: every weight tile read from HBM for one M tile) with experts whose tensor work does
+// (many rows: one weight tile shared by many M tiles), so HBM and the tensor pipes are busy
+// together rather than in turns.  The order only permutes whole experts: every tile computes
+// the same rows as in index order.
+__device__ void build_schedule(const Params& p, int32_t* s_mtp, int32_t* s_ord) {
+  const int E = p.E;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int ce = p.offsets[e + 1] - p.offsets[e];
+    int rank = 0;
+    for (int f = 0; f < E; ++f) {
+      const int cf = p.offsets[f + 1] - p.offsets[f];
+      rank += (cf > ce || (cf == ce && f < e)) ? 1 : 0;
+    }
+    const int half = (E + 1) >> 1;
+    const int pos = rank < half ? 2 * rank : 2 * (E - 1 - rank) + 1;
+    s_ord[pos] = e;
+    s_mtp[pos + 1] = ceil_div(ce, BM);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    s_mtp[0] = 0;
+    for (int j = 0; j < E; ++j) s_mtp[j + 1] += s_mtp[j];
+  }
+  __syncthreads();
+}
+
 // With `split` tail halves, the list is total - split whole tiles followed by 2 * split half
 // tiles: half tile h is the left (h even) or right half of whole tile total - split + h / 2.
-__device__ __forceinline__ TileInfo decode_tile(int tile, const Params& p, int total, int split) {
+__device__ __forceinline__ TileInfo decode_tile(int tile, const Params& p, const Sched& sc,
+                                                int total, int split) {
   const int whole = total - split;
-  if (tile < whole) return decode_tile(tile, p);
+  if (tile < whole) return decode_tile(tile, p, sc);
   const int h = tile - whole;
-  TileInfo ti = decode_tile(whole + (h >> 1), p);
+  TileInfo ti = decode_tile(whole + (h >> 1), p, sc);
   ti.bn = p.bn >> 1;
   ti.col0 += (h & 1) * ti.bn;
   return ti;
@@ -180,6 +224,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_STAGE);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int32_t* s_mtp = reinterpret_cast<int32_t*>(smem + STAGES * (A_STAGE + B_STAGE) + 256);
+  int32_t* s_ord = s_mtp + 257;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t full0 = smem_u32(bars);
@@ -213,7 +259,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int total = total_tiles(p);
+  Sched sc{p.mtp, nullptr};
+  if (p.order == 1 && p.uniform_rows < 0) {
+    build_schedule(p, s_mtp, s_ord);
+    sc = Sched{s_mtp, s_ord};
+  }
+  const int total = total_tiles(p, sc);
   const int KB = p.K / BK;
   const int split = p.tail_split ? choose_tail_split(total, gridDim.x) : 0;
   const int ntiles = total + split;
@@ -235,7 +286,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int npend = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
-      const TileInfo ti = decode_tile(tile, p, total, split);
+      const TileInfo ti = decode_tile(tile, p, sc, total, split);
       int tok[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
@@ -308,7 +359,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t issued = 0, last_par = 0;   // per-stage bit masks for the drain
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
-      const TileInfo ti = decode_tile(tile, p, total, split);
+      const TileInfo ti = decode_tile(tile, p, sc, total, split);
       // B: two 128-row boxes (SwiGLU gate + up, or N = 256), else one
       const int nbox = (p.swiglu || ti.bn > 128) ? 2 : 1;
       const uint32_t bytes = A_STAGE + nbox * B_BOX;
@@ -351,7 +402,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
       // an expert's last tile with <= 64 rows runs as an M = 64 MMA (half the tensor work)
-      const TileInfo tm = decode_tile(tile, p, total, split);
+      const TileInfo tm = decode_tile(tile, p, sc, total, split);
       const uint32_t idesc = idesc_bf16_f32(tm.rows <= 64 ? 64 : BM, tm.bn);
       if (!wait_bounded(tempty0 + 8 * acc, aph ^ 1u, abort_flag, p.st, 2, true)) {
         ok = false;
@@ -392,7 +443,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int acc = 0;
     uint32_t aph = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-      const TileInfo ti = decode_tile(tile, p, total, split);
+      const TileInfo ti = decode_tile(tile, p, sc, total, split);
       int ok = 1;
       if (lane == 0) ok = wait_bounded(tfull0 + 8 * acc, aph, abort_flag, p.st, 4, true) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -612,6 +663,13 @@ static cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const 
 
 }  // namespace tc
 
+// Expert order of the ragged tile lists: interleaved by row count unless the environment
+// variable MOE_B300_ORDER=index asks for expert index order (both compute the same rows).
+static int expert_order() {
+  const char* env = getenv("MOE_B300_ORDER");
+  return (env && strcmp(env, "index") == 0) ? 0 : 1;
+}
+
 static bool use_pair_kernel(const GroupedFFN& g) {
   if (g.d % 256 != 0) return false;
   const char* env = getenv("MOE_B300_GEMM");
@@ -659,6 +717,7 @@ cudaError_t launch_ffn_tc(const GroupedFFN& g, DevStatus* st, cudaStream_t s) {
   p1.gperm = g.gather_perm;
   p1.gk = g.gather_k;
   p1.gx = static_cast<const __nv_bfloat16*>(g.gather_x);
+  p1.order = expert_order();
   p1.st = st;
   cudaError_t err = launch_one(mx, mw13, p1, mt_upper * p1.n_tiles, s);
   if (err != cudaSuccess) return err;

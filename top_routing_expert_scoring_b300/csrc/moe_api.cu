@@ -603,10 +603,10 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
                         scat ? static_cast<float*>(out) : nullptr, scat ? b.perm : nullptr,
                         scat ? w : nullptr, ybf)))
         return st;
-      if (mark(ev_end) != cudaSuccess) return MOE_ERR_CUDA;
       if (shared && (st = run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13,
                                   ws2, shared, ws, L, s)))
         return st;
+      if (mark(ev_end) != cudaSuccess) return MOE_ERR_CUDA;
       if (!scat) {
         e = ybf ? launch_combine_bf16y(*c, at<void>(ws, L.y_perm), b.row_of, w, shared, out, s)
                 : launch_combine(*c, at<float>(ws, L.y_perm), b.row_of, w, shared, out, s);
@@ -637,10 +637,10 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
                     at<float>(ws, L.y_perm), ws, L, s, nullptr, nullptr, nullptr, nullptr,
                     nullptr, ybf)))
     return st;
-  if (mark(ev_end) != cudaSuccess) return MOE_ERR_CUDA;
   if (shared && (st = run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13, ws2,
                               shared, ws, L, s)))
     return st;
+  if (mark(ev_end) != cudaSuccess) return MOE_ERR_CUDA;
   if ((e = launch_combine_ec(*c, at<void>(ws, L.y_perm), ybf, at<int32_t>(ws, L.tok_ptr),
                              at<int32_t>(ws, L.tok_rows), ec_w, shared, out, s)) != cudaSuccess)
     return MOE_ERR_CUDA;
