@@ -16,7 +16,9 @@ or trained weights are involved: every tensor is i.i.d. random,
   d_topk_w ~ N(0, 1)                    [T, k]   (upstream gradient of the routing weights)
 
 Each tensor is drawn from its own torch.Generator, seeded from (workload, tensor name, seed), so
-the draws do not depend on the order in which tensors are made.  Large weight sets may be drawn
+the draws do not depend on the order in which tensors are made; every routed expert's W13 and W2
+have generators of their own (tensor names "w13/e", "w2/e"), so any subset of experts can be
+drawn alone (expert_weights).  Large weight sets may be drawn
 on the GPU (device="cuda") with a CUDA generator; then the oracle receives host copies of them.
 
 Layouts (row-major, contiguous):
@@ -141,13 +143,29 @@ def make_router_inputs(wl: Workload, seed: int = 0, device: str = "cpu", T: int 
     return {"x": x.to(dt).contiguous(), "w_gate": w_gate.to(dt).contiguous(), "bias": bias}
 
 
+def expert_weights(wl: Workload, e: int, seed: int = 0, device: str = "cpu"):
+    """Routed expert e alone: (w13_e [2F, d], w2_e [d, F]), the same values as row e of
+    make_expert_weights."""
+    dt = torch_dtype(wl)
+    d, F = wl.d, wl.F
+    return (_normal((2 * F, d), 1.0 / math.sqrt(d), _gen(wl.name, f"w13/{e}", seed, device),
+                    device, dt),
+            _normal((d, F), 1.0 / math.sqrt(F), _gen(wl.name, f"w2/{e}", seed, device), device,
+                    dt))
+
+
 def make_expert_weights(wl: Workload, seed: int = 0, device: str = "cpu"):
     """Routed expert weights w13 [E,2F,d], w2 [E,d,F] and the shared expert (ws13, ws2)."""
     dt = torch_dtype(wl)
     name = wl.name
     d, F, E = wl.d, wl.F, wl.E
-    w13 = _normal((E, 2 * F, d), 1.0 / math.sqrt(d), _gen(name, "w13", seed, device), device, dt)
-    w2 = _normal((E, d, F), 1.0 / math.sqrt(F), _gen(name, "w2", seed, device), device, dt)
+    w13 = torch.empty((E, 2 * F, d), dtype=dt, device=device)
+    w2 = torch.empty((E, d, F), dtype=dt, device=device)
+    for e in range(E):
+        a, b = expert_weights(wl, e, seed, device)
+        w13[e].copy_(a)
+        w2[e].copy_(b)
+        del a, b
     out = {"w13": w13, "w2": w2, "ws13": None, "ws2": None}
     if wl.n_shared > 0:
         Fs = wl.F_shared
@@ -162,6 +180,14 @@ def make_expert_weights(wl: Workload, seed: int = 0, device: str = "cpu"):
         out["ws13"] = torch.cat(gates + ups, dim=0).contiguous()
         out["ws2"] = torch.cat(downs, dim=1).contiguous()
     return out
+
+
+def shared_weights(wl: Workload, seed: int = 0, device: str = "cpu"):
+    """The shared experts alone, concatenated: (ws13 [2 Fs, d], ws2 [d, Fs]) or (None, None)."""
+    if wl.n_shared == 0:
+        return None, None
+    w = make_expert_weights(wl.replace(E=0), seed, device)
+    return w["ws13"], w["ws2"]
 
 
 def make_inputs(wl: Workload, seed: int = 0, device: str = "cpu", T: int | None = None):

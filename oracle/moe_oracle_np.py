@@ -1,8 +1,10 @@
-"""CPU oracle for the single-GPU MoE layer forward.  TEST INFRASTRUCTURE ONLY.
+"""Independent numpy restatement of the CPU oracle.  TEST INFRASTRUCTURE ONLY.
 
-Only the tests, the smoke check and the benchmark's CPU-baseline leg may import this module.
-The product path (the CUDA library and its Python binding) never imports, links or runs it,
-and this module shares no code with that path.
+The oracle the tests, the smoke check and the benchmark use is the plain C++ one
+(moe_oracle.cpp through moe_oracle.py).  This module computes the same equations separately,
+with numpy's matrix products, and serves only as a cross-check of it (tests that the two agree
+on random layers).  The product path never imports, links or runs it, and it shares no code
+with that path or with the C++ oracle.
 
 Plain, slow, obviously correct: numpy in float64, one step per equation of the pages, no
 blocking or fusion.  Where a step decides an integer (which experts a token selects, which

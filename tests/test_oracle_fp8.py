@@ -78,17 +78,31 @@ def _small(name, **kw):
 
 @pytest.mark.parametrize("case", [dict(name="v3", T=24, d=128, E=16, F=128, F_shared=128),
                                   dict(name="mixtral", T=20, d=128, E=8, F=256)])
-def test_fp8_layer_with_identity_quantisation_is_the_bf16_layer(monkeypatch, case):
+def test_fp8_layer_with_identity_quantisation_is_the_bf16_layer(case):
     wl, h = _small(**case)
     want = O.moe_forward(wl, h["x"], h["w_gate"], h["bias"], h["w13"], h["w2"], h["ws13"],
                          h["ws2"])["out"]
-    monkeypatch.setattr(O, "quantize_rows_fp8",
-                        lambda V: (np.asarray(V, np.float64), np.ones(len(V))))
-    wq = O.fp8_expert_weights(h["w13"], h["w2"], h["ws13"], h["ws2"])
-    got, _ = O.moe_forward_fp8(wl, h["x"], h["w_gate"], h["bias"], wq)
+    with O.fp8_identity_quantisation():
+        wq = O.fp8_expert_weights(h["w13"], h["w2"], h["ws13"], h["ws2"])
+        got, _ = O.moe_forward_fp8(wl, h["x"], h["w_gate"], h["bias"], wq)
+        # the same with the weights quantised inside the sampled path
+        disp = O.dispatch(*_route_disp(wl, h))
+        r = O.route(wl, h["x"], h["w_gate"], h["bias"])
+        part = O.moe_forward_fp8_sampled(h["x"], r["idx"], r["w"], disp["row_of"],
+                                         lambda e: (h["w13"][e], h["w2"][e]),
+                                         lambda: (h["ws13"], h["ws2"]) if h["ws13"] is not None
+                                         else None, [0, 5, wl.T - 1])
     # identical up to float64 rounding (h goes through float32 in the fp8 path)
     scale = np.sqrt(np.mean(want ** 2))
     assert np.max(np.abs(got - want)) <= 1e-6 * scale
+    assert np.max(np.abs(part - want[[0, 5, wl.T - 1]])) <= 1e-6 * scale
+    # outside the context the quantiser is E4M3 again
+    assert np.max(np.abs(O.fp8_expert_weights(h["w13"], h["w2"])["w2"] - h["w2"])) > 0
+
+
+def _route_disp(wl, h):
+    r = O.route(wl, h["x"], h["w_gate"], h["bias"])
+    return r["idx"], wl.E, O.capacity(wl.capacity_factor, wl.k, wl.T, wl.E)
 
 
 @pytest.mark.parametrize("case", [dict(name="v3", T=24, d=256, E=16, F=256, F_shared=256),
