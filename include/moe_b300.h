@@ -228,6 +228,13 @@ int moe_forward_timed(const moe_config* cfg, const void* x, const void* w_gate, 
 int moe_workspace_views(const moe_config* cfg, void* ws, float** logits, int32_t** row_of,
                         int32_t** offsets, void** x_perm, float** y_perm);
 
+/* Device addresses of the expert-choice selection an expert-choice moe_forward leaves in `ws`
+ * ["MoE混合专家模型深度解析" §2.2 Expert Choice]: ec_tokens [E,C] int32, ec_w [E,C] f32,
+ * tok_ptr [T+1] int32, tok_rows [E*C] int32, laid out as moe_expert_choice writes them.
+ * MOE_ERR_ARG for a token-choice configuration.  Any output pointer may be NULL. */
+int moe_workspace_views_ec(const moe_config* cfg, void* ws, int32_t** ec_tokens, float** ec_w,
+                           int32_t** tok_ptr, int32_t** tok_rows);
+
 /* Failure-path self test: launches one tiny kernel whose bounded wait on a flag that nothing
  * sets runs out after about `limit_us` microseconds; it records MOE_ERR_TIMEOUT in the status
  * word of `ws` and returns, leaving the context usable.  Read the result with

@@ -136,10 +136,10 @@ def compare_out(got, ref, tol, report, key="out", bf16_rounded=False):
 
 
 def expert_weight_fetcher(inp):
-    """Per-expert float64 copies of the routed weights (copied from wherever they live)."""
+    """Per-expert host copies of the routed weights in their own dtype (the oracle widens bf16
+    exactly), copied from wherever they live."""
     def fetch(e):
-        return (inp["w13"][e].to("cpu").to(torch.float64).numpy(),
-                inp["w2"][e].to("cpu").to(torch.float64).numpy())
+        return inp["w13"][e].to("cpu"), inp["w2"][e].to("cpu")
     return fetch
 
 
@@ -147,6 +147,20 @@ def shared_fetcher(inp):
     def fetch():
         if inp["ws13"] is None:
             return None
-        return (inp["ws13"].to("cpu").to(torch.float64).numpy(),
-                inp["ws2"].to("cpu").to(torch.float64).numpy())
+        return inp["ws13"].to("cpu"), inp["ws2"].to("cpu")
     return fetch
+
+
+def coverage_tokens(offsets, perm, k, T, rng, n_random):
+    """Tokens whose rows cover every expert's first and last row -- so every expert, its first
+    M tile and its last (ragged) M tile are looked at -- plus n_random tokens drawn at random.
+    offsets [E+1] and perm [T*k] describe the expert-ordered rows."""
+    toks = set()
+    E = len(offsets) - 1
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            toks.add(int(perm[lo]) // k)
+            toks.add(int(perm[hi - 1]) // k)
+    toks |= {int(t) for t in rng.choice(T, size=min(n_random, T), replace=False)}
+    return np.array(sorted(toks), dtype=np.int64)

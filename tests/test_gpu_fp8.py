@@ -128,7 +128,8 @@ def test_fp8_forward_small(case):
     assert 0.01 < rel < 0.10, rel
 
 
-FULL = {"v3_b64": ("v3", 64, 4), "mixtral_b32": ("mixtral", 32, 6)}
+FULL = {"v3_b1": ("v3", 1, 1), "v3_b8": ("v3", 8, 4), "v3_b64": ("v3", 64, 4),
+        "v3_b256": ("v3", 256, 6), "mixtral_b32": ("mixtral", 32, 6)}
 
 
 @pytest.mark.parametrize("case", list(FULL))

@@ -295,9 +295,75 @@ FULL = {
     "dsmoe16b": dict(name="dsmoe16b"),
     "dsmoe16b_ec": dict(name="dsmoe16b_ec"),
     "v3": dict(name="v3"),
+    # decode batches of the full-size layers (the K-split cost model picks the slice counts
+    # these sizes reach, which small cases do not)
+    "v3_b1": dict(name="v3", T=1),
+    "v3_b8": dict(name="v3", T=8),
     "v3_b64": dict(name="v3", T=64),
     "v3_b256": dict(name="v3", T=256),
+    "mixtral_b1": dict(name="mixtral", T=1),
+    "mixtral_b8": dict(name="mixtral", T=8),
+    "mixtral_b64": dict(name="mixtral", T=64),
+    "mixtral_b256": dict(name="mixtral", T=256),
 }
+
+
+def _check_dispatch_of(gpu, wl, idx):
+    """The forward's own dispatch (row_of, offsets, dropped count) against the oracle's
+    dispatch of the very indices the GPU selected -- bit-exact whatever the near ties did."""
+    m = U.lib()
+    _, row_of_p, offsets_p, _, _ = m.moe_workspace_views(gpu["cfg"], gpu["ws"])
+    D = O.dispatch(idx, wl.E, O.capacity(wl.capacity_factor, wl.k, wl.T, wl.E))
+    assert (_read_i32(offsets_p, wl.E + 1) == D["offsets"]).all()
+    assert (_read_i32(row_of_p, wl.T * wl.k).reshape(wl.T, wl.k) == D["row_of"]).all()
+    assert gpu["n_dropped"] == D["n_dropped"]
+    return D
+
+
+def _full_expert_choice(wl, inp, gpu, report):
+    """Expert choice at full size: the forward's logits, its [E, C] token lists, weights and
+    per-token CSR against the oracle, then the output on tokens covering every expert."""
+    m = U.lib()
+    g, g32 = O.router_logits(inp["x"], inp["w_gate"])
+    logits_p, _, _, _, _ = m.moe_workspace_views(gpu["cfg"], gpu["ws"])
+    gl = torch.as_tensor(_DevF32(logits_p, wl.T * wl.E), device=DEV).cpu().numpy()
+    assert np.abs(gl - g).max() <= 1e-5 * np.abs(g).max()
+    tokens, weights, _ = O.expert_choice_route(g32, wl.k)
+    E, C = tokens.shape
+    csr = O.expert_choice_csr(tokens, wl.T)
+    tok_p, w_p, ptr_p, rows_p = m.moe_workspace_views_ec(gpu["cfg"], gpu["ws"])
+    gtok = _read_i32(tok_p, E * C).reshape(E, C)
+    gw = torch.as_tensor(_DevF32(w_p, E * C), device=DEV).cpu().numpy().reshape(E, C)
+    # near ties: an expert whose C-th and (C+1)-th logits (oracle's float32) differ by < 1e-6
+    # relative is reported and left out of the list check
+    col = -np.sort(-g32.astype(np.float64), axis=0)
+    a, b = col[C - 1], col[C]
+    near = (a - b) / np.maximum(np.abs(a), 1e-30) < U.TIE_REL
+    report["near_tie_experts"] = int(near.sum())
+    same = (gtok == tokens).all(axis=1)
+    assert (same | near).all(), np.nonzero(~same & ~near)[0][:10]
+    assert np.abs(gw[same] - weights[same]).max() <= U.WEIGHT_ATOL
+    if same.all():
+        assert (_read_i32(ptr_p, wl.T + 1) == csr["ptr"]).all()
+        assert (_read_i32(rows_p, E * C) == csr["rows"]).all()
+    st = O.aux_stats_from_counts(g32, csr["counts"], wl.E)
+    U.compare_stats(gpu, st, report)
+    # per-token selection as a padded (idx, w, row) table, on tokens covering every expert's
+    # first and last chosen token plus random ones
+    rng = np.random.default_rng(0)
+    pick = set(rng.choice(wl.T, 16, replace=False).tolist())
+    for e in range(E):
+        pick |= {int(tokens[e, 0]), int(tokens[e, -1])}
+    sample = np.array(sorted(pick))
+    kmax = max(int(np.diff(csr["ptr"]).max()), 1)
+    idx = np.zeros((wl.T, kmax), np.int64)
+    w = np.zeros((wl.T, kmax))
+    row_of = -np.ones((wl.T, kmax), np.int64)
+    for t in sample:
+        for n, r in enumerate(csr["rows"][csr["ptr"][t]:csr["ptr"][t + 1]]):
+            e, i = divmod(int(r), C)
+            idx[t, n], w[t, n], row_of[t, n] = e, weights[e, i], r
+    return sample, idx, w, row_of
 
 
 @pytest.mark.parametrize("case", list(FULL))
@@ -307,44 +373,30 @@ def test_full_size_parity(case):
     inp = moe_inputs.make_inputs(wl, device=DEV)
     report = {}
     gpu = U.run_forward(wl, inp)
-    x = moe_inputs.to_f64(inp["x"])
-    wg = moe_inputs.to_f64(inp["w_gate"])
-    bias = moe_inputs.to_f64(inp["bias"])
+    hx = {"x": inp["x"].cpu(), "w_gate": inp["w_gate"].cpu(), "bias": inp["bias"].cpu()}
     rng = np.random.default_rng(0)
-    sample = np.sort(rng.choice(wl.T, size=16 if wl.E > 8 else 32, replace=False))
     if wl.routing == "expert_choice":
-        g, g32 = O.router_logits(x, wg)
-        tokens, weights, p = O.expert_choice_route(g32, wl.k)
-        csr = O.expert_choice_csr(tokens, wl.T)
-        st = O.aux_stats_from_counts(g32, csr["counts"], wl.E)
-        U.compare_stats(gpu, st, report)
-        # per-token selection as a padded (idx, w, row) table for the sampled tokens
-        E, C = tokens.shape
-        kmax = int(np.diff(csr["ptr"]).max())
-        idx = np.zeros((wl.T, max(kmax, 1)), np.int64)
-        w = np.zeros((wl.T, max(kmax, 1)))
-        row_of = -np.ones((wl.T, max(kmax, 1)), np.int64)
-        for t in sample:
-            for n, r in enumerate(csr["rows"][csr["ptr"][t]:csr["ptr"][t + 1]]):
-                e, i = divmod(int(r), C)
-                idx[t, n], w[t, n], row_of[t, n] = e, weights[e, i], r
+        sample, idx, w, row_of = _full_expert_choice(wl, hx, gpu, report)
         ok_tokens = sample
     else:
-        r = O.route(wl, x, wg, bias)
-        ok = U.compare_routing(wl, gpu, r, bias, report)
+        r = O.route(wl, hx["x"], hx["w_gate"], hx["bias"])
+        ok = U.compare_routing(wl, gpu, r, moe_inputs.to_f64(inp["bias"]), report)
+        # dispatch of the GPU's own indices, always (near ties or not)
+        Dg = _check_dispatch_of(gpu, wl, gpu["idx"])
+        # statistics: counts from the GPU's selection, probabilities from the oracle's logits
+        U.compare_stats(gpu, O.aux_stats(r["g32"], gpu["idx"], wl.E, wl.score), report)
         disp = O.dispatch(r["idx"], wl.E, O.capacity(wl.capacity_factor, wl.k, wl.T, wl.E))
         if ok.all():
-            U.compare_stats(gpu, O.aux_stats(r["g32"], r["idx"], wl.E, wl.score), report)
-            assert gpu["n_dropped"] == disp["n_dropped"]
-            m = U.lib()
-            _, row_of_p, offsets_p, _, _ = m.moe_workspace_views(gpu["cfg"], gpu["ws"])
-            assert (_read_i32(offsets_p, wl.E + 1) == disp["offsets"]).all()
-            assert (_read_i32(row_of_p, wl.T * wl.k).reshape(wl.T, wl.k) == disp["row_of"]).all()
+            for key in ("offsets", "row_of", "perm"):
+                assert (Dg[key] == disp[key]).all(), key
         idx, w, row_of = r["idx"], r["w"], disp["row_of"]
+        sample = U.coverage_tokens(disp["offsets"], disp["perm"], wl.k, wl.T, rng,
+                                   16 if wl.E > 8 else 32)
         ok_tokens = sample[ok[sample]]
         report["drop_rate"] = disp["n_dropped"] / (wl.T * wl.k)
         report["f0"] = float(O.aux_stats(r["g32"], r["idx"], wl.E)["f"][0])
-    ref = O.moe_forward_sampled(x, idx, w, row_of, U.expert_weight_fetcher(inp),
+    report["sampled_tokens"] = int(len(ok_tokens))
+    ref = O.moe_forward_sampled(hx["x"], idx, w, row_of, U.expert_weight_fetcher(inp),
                                 U.shared_fetcher(inp), ok_tokens)
     got = gpu["out"][torch.from_numpy(ok_tokens).to(DEV)].float().cpu().numpy()
     U.compare_out(got, ref, U.OUT_TOL_BF16, report)
@@ -517,7 +569,8 @@ class _DevF32:
 ])
 def test_fused_gather_matches_materialised_rows(monkeypatch, spec):
     """The gate/up GEMM reading its rows straight from x (cp.async gather) computes on the very
-    same bf16 operands as the TMA path over the materialised rows: outputs bit-identical."""
+    same bf16 operands as the TMA path over the materialised rows: outputs bit-identical; and
+    the fused path's output against the oracle's layer under the layer bar."""
     wl = moe_inputs.workload(**spec)
     inp = _inputs(wl)
     monkeypatch.setenv("MOE_B300_PATH", "prefill")
@@ -528,6 +581,12 @@ def test_fused_gather_matches_materialised_rows(monkeypatch, spec):
     b = U.run_forward(wl, inp)
     assert torch.equal(a["out"], b["out"])
     assert (a["idx"] == b["idx"]).all()
+    h = U.host(inp)
+    ref = O.moe_forward(wl, h["x"], h["w_gate"], h["bias"], h["w13"], h["w2"], h["ws13"],
+                        h["ws2"])
+    report = {}
+    ok = U.compare_routing(wl, b, ref, h["bias"], report)
+    U.compare_out(b["out"].float().cpu().numpy()[ok], ref["out"][ok], U.OUT_TOL_BF16, report)
 
 
 @pytest.mark.parametrize("spec", [

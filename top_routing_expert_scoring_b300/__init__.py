@@ -16,6 +16,7 @@ __all__ = [
     "workspace_size", "check_config", "sync_status", "status_string", "version",
     "moe_router_topk", "moe_aux_stats", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_shared_ffn",
     "moe_combine", "moe_expert_choice", "moe_forward", "moe_forward_timed", "moe_workspace_views",
+    "moe_workspace_views_ec",
     "moe_selftest_timeout", "EXPORTED", "SCORE", "ROUTING", "DTYPE",
 ]
 
@@ -76,6 +77,7 @@ _SIGS = {
     "moe_forward": ([_CFG] + [_P] * 17, ctypes.c_int),
     "moe_forward_timed": ([_CFG] + [_P] * 19, ctypes.c_int),
     "moe_workspace_views": ([_CFG, _P] + [ctypes.POINTER(_P)] * 5, ctypes.c_int),
+    "moe_workspace_views_ec": ([_CFG, _P] + [ctypes.POINTER(_P)] * 4, ctypes.c_int),
     "moe_selftest_timeout": ([_P, ctypes.c_int32, _P], ctypes.c_int),
     "moe_router_backward_workspace_size": ([_CFG, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
     "moe_router_backward": ([_CFG] + [_P] * 6 + [ctypes.c_float, ctypes.c_float] + [_P] * 5,
@@ -242,6 +244,15 @@ def moe_workspace_views(cfg, ws):
     """Device addresses (ints) of logits, row_of, offsets, x_perm, y_perm inside ws."""
     outs = [ctypes.c_void_p() for _ in range(5)]
     _check("moe_workspace_views", lib.moe_workspace_views(
+        ctypes.byref(cfg), _ptr(ws), *[ctypes.byref(o) for o in outs]))
+    return [o.value for o in outs]
+
+
+def moe_workspace_views_ec(cfg, ws):
+    """Device addresses (ints) of ec_tokens, ec_w, tok_ptr, tok_rows inside ws (expert
+    choice)."""
+    outs = [ctypes.c_void_p() for _ in range(4)]
+    _check("moe_workspace_views_ec", lib.moe_workspace_views_ec(
         ctypes.byref(cfg), _ptr(ws), *[ctypes.byref(o) for o in outs]))
     return [o.value for o in outs]
 

@@ -688,6 +688,20 @@ int moe_workspace_views(const moe_config* c, void* ws, float** logits, int32_t**
   return MOE_OK;
 }
 
+int moe_workspace_views_ec(const moe_config* c, void* ws, int32_t** ec_tokens, float** ec_w,
+                           int32_t** tok_ptr, int32_t** tok_rows) {
+  int st = moe_check_config(c);
+  if (st) return st;
+  if (c->routing != MOE_ROUTE_EXPERT_CHOICE) return MOE_ERR_ARG;
+  if ((st = check_ws(ws))) return st;
+  const Layout L = layout(*c);
+  if (ec_tokens) *ec_tokens = at<int32_t>(ws, L.ec_tokens);
+  if (ec_w) *ec_w = at<float>(ws, L.ec_w);
+  if (tok_ptr) *tok_ptr = at<int32_t>(ws, L.tok_ptr);
+  if (tok_rows) *tok_rows = at<int32_t>(ws, L.tok_rows);
+  return MOE_OK;
+}
+
 int moe_selftest_timeout(void* ws, int32_t limit_us, void* stream) {
   int st = check_ws(ws);
   if (st) return st;
