@@ -100,6 +100,18 @@ SMALL = {
     "topk_cta_e96_groups24": dict(name="v3", T=37, d=256, E=96, k=8, F=128, n_shared=0,
                                   F_shared=0, n_groups=4, topk_groups=3),
     "decode_e256_b100": dict(name="v3", T=100, d=1024, E=256, F=128, F_shared=128),
+    # prefill batches of a wide router (E % 32 == 0, T > 512): scoring, group limit, Top-k and
+    # statistics terms in the router GEMM's epilogue, one thread per token
+    "router_fused_softmax_e64": dict(name="mixtral", T=1000, d=256, E=64, k=6, F=128),
+    "router_fused_v3_e256": dict(name="v3", T=700, d=256, E=256, F=128, F_shared=128),
+    "router_fused_groups_of_64": dict(name="v3", T=600, d=256, E=128, k=6, F=128,
+                                      F_shared=128, n_groups=2, topk_groups=1),
+    # E = 96 (three 32-expert chunks) with a last tile of 20 tokens (M = 64 accumulator layout)
+    "router_fused_e96_tail": dict(name="mixtral", T=1300, d=256, E=96, k=5, F=128),
+    "router_fused_switch_e32": dict(name="mixtral", T=777, d=256, E=32, k=1, F=128,
+                                    renormalize=False),
+    "router_fused_sigmoid_one_group": dict(name="v3", T=900, d=256, E=64, k=6, F=128,
+                                           F_shared=128, n_groups=1, topk_groups=1),
     "one_expert": dict(name="mixtral", T=130, d=128, E=1, k=1, F=128),
     # prefill path with E = 1, k = 1 and d = 256 (decode regime needs <= 64 rows per expert)
     "one_expert_d256": dict(name="mixtral", T=300, d=256, E=1, k=1, F=128),
@@ -326,7 +338,7 @@ def _full_expert_choice(wl, inp, gpu, report):
     m = U.lib()
     g, g32 = O.router_logits(inp["x"], inp["w_gate"])
     logits_p, _, _, _, _ = m.moe_workspace_views(gpu["cfg"], gpu["ws"])
-    gl = torch.as_tensor(_DevF32(logits_p, wl.T * wl.E), device=DEV).cpu().numpy()
+    gl = torch.as_tensor(_DevF32(logits_p, wl.T * wl.E), device=DEV).cpu().numpy().reshape(wl.T, wl.E)
     assert np.abs(gl - g).max() <= 1e-5 * np.abs(g).max()
     tokens, weights, _ = O.expert_choice_route(g32, wl.k)
     E, C = tokens.shape
@@ -520,7 +532,8 @@ def test_forward_replays_in_a_cuda_graph():
     assert torch.equal(out, eager)
 
 
-@pytest.mark.parametrize("case", ["v3_like", "softmax_cap", "decode_b8"])
+@pytest.mark.parametrize("case", ["v3_like", "softmax_cap", "decode_b8", "router_fused_v3_e256",
+                                  "router_fused_e96_tail"])
 def test_forward_timed_and_fused_statistics(case):
     # moe_forward_timed runs moe_forward's kernels (identical output) and brackets the expert
     # GEMMs with the caller's events; the statistics moe_forward fuses into its Top-k pass
@@ -625,3 +638,44 @@ def test_fused_combine_is_deterministic_and_matches_the_combine_pass(monkeypatch
         bound[live] += np.abs(a["w"][live, j])[:, None] * y_abs[rows[live]]
     err = np.abs(fa - fc)[same]
     assert (err <= 2.0 ** -8 * bound[same] + 1e-5 * rms).all()
+
+
+@pytest.mark.parametrize("case", ["router_fused_v3_e256", "router_fused_e96_tail",
+                                  "router_fused_groups_of_64"])
+def test_router_epilogue_matches_separate_passes(case, monkeypatch):
+    """The router GEMM with the routing in its epilogue against the separate logits GEMM and
+    Top-k pass on the same inputs: the same logits (1e-6 relative), the same selection (near
+    ties excepted, as against the oracle) and weights within the weight bar; and the stage entry
+    point moe_router_topk gives the fused forward's selection."""
+    m = U.lib()
+    spec = dict(SMALL[case])
+    wl = moe_inputs.workload(spec.pop("name"), **spec)
+    inp = _inputs(wl)
+    cfg = U.config_of(wl)
+    T, E, k = wl.T, wl.E, wl.k
+    runs = {}
+    for mode in ("fused", "separate"):
+        if mode == "separate":
+            monkeypatch.setenv("MOE_B300_ROUTER", "separate")
+        else:
+            monkeypatch.delenv("MOE_B300_ROUTER", raising=False)
+        ws = m.workspace(cfg)
+        logits = torch.empty((T, E), dtype=torch.float32, device=DEV)
+        idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+        w = torch.empty((T, k), dtype=torch.float32, device=DEV)
+        m.moe_router_topk(cfg, inp["x"], inp["w_gate"], inp["bias"], logits, idx, w, ws)
+        torch.cuda.synchronize()
+        assert m.sync_status(ws) == 0
+        runs[mode] = (logits.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy())
+    gf, i_f, w_f = runs["fused"]
+    gs, i_s, w_s = runs["separate"]
+    assert np.abs(gf - gs).max() <= 1e-6 * np.abs(gs).max()
+    h = U.host(inp)
+    r = O.route(wl, h["x"], h["w_gate"], h["bias"])
+    near = U.deciding_gaps(wl, r, h["bias"]) < U.TIE_REL
+    same = (i_f == i_s).all(axis=1)
+    assert (same | near).all()
+    assert np.abs(w_f[same] - w_s[same]).max() <= U.WEIGHT_ATOL
+    monkeypatch.delenv("MOE_B300_ROUTER", raising=False)
+    fwd = U.run_forward(wl, inp, cfg)
+    assert (fwd["idx"] == i_f).all() and (fwd["w"] == w_f.astype(np.float64)).all()

@@ -29,6 +29,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "route_thread.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -47,6 +48,10 @@ constexpr int NBARS = 2 * STAGES + 5;        // full, empty, tmem full x2, tmem 
 // expert at each schedule position [256]
 constexpr int SCHED_BYTES = (257 + 256) * 4;
 constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * (A_STAGE + B_STAGE) + 256 + SCHED_BYTES;
+// router epilogue (ROUTE instantiation): selection bias [256], per-warp P and count rows
+// [4][256] each, per-warp z terms [4]
+constexpr int ROUTE_BYTES = (256 + 2 * 4 * 256 + 4) * 4;
+constexpr size_t SMEM_BYTES_ROUTE = SMEM_BYTES + ROUTE_BYTES;
 
 struct Params {
   const int32_t* offsets;   // [E+1]
@@ -79,6 +84,19 @@ struct Params {
   const int32_t* scat_perm;
   const float* scat_w;
   int scat_k;
+  // router epilogue (ROUTE instantiation only): with one group of T token rows and B = W_gate
+  // (N = E <= 256 in one tile), each epilogue thread routes its token from the TMEM row of
+  // logits -- scoring, group limit, Top-k, weights -- writes the logits, the selection and the
+  // weights, and the tile's warps add their statistics terms into one partial row per tile
+  const float* r_bias;      // [E] selection bias or NULL
+  float* r_logits;          // [T, E]
+  int32_t* r_idx;           // [T, k]
+  float* r_w;               // [T, k]
+  float* r_part_P;          // [tiles, E]
+  int32_t* r_part_cnt;      // [tiles, E]
+  float* r_part_z;          // [tiles]
+  int r_E, r_k, r_score, r_cpg, r_topk_groups, r_renorm;
+  float r_scale;
   DevStatus* st;
 };
 
@@ -211,7 +229,8 @@ __device__ __forceinline__ int choose_tail_split(int total, int G) {
 // GATHER: the gate/up GEMM's A rows come from the token rows through the whole producer warp
 // (cp.async) instead of one TMA box over the materialised rows; a separate instantiation so the
 // default kernel's code is unchanged.
-template <bool GATHER>
+// ROUTE: the router GEMM with the routing epilogue (see Params::r_*).
+template <bool GATHER, bool ROUTE = false>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, const Params p) {
@@ -358,19 +377,23 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t ph = 0;
     uint32_t issued = 0, last_par = 0;   // per-stage bit masks for the drain
     bool ok = true;
+    // first B rows of a tile's one or two boxes
+    auto b_rows_of = [&](const TileInfo& t, int& r0, int& r1) {
+      if (p.swiglu) {
+        r0 = t.e * p.b_rows + t.nt * 128;
+        r1 = r0 + p.up_off;
+      } else {
+        r0 = t.e * p.b_rows + t.col0;
+        r1 = r0 + 128;
+      }
+    };
     for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
       const TileInfo ti = decode_tile(tile, p, sc, total, split);
       // B: two 128-row boxes (SwiGLU gate + up, or N = 256), else one
       const int nbox = (p.swiglu || ti.bn > 128) ? 2 : 1;
       const uint32_t bytes = A_STAGE + nbox * B_BOX;
       int b0, b1;
-      if (p.swiglu) {
-        b0 = ti.e * p.b_rows + ti.nt * 128;
-        b1 = b0 + p.up_off;
-      } else {
-        b0 = ti.e * p.b_rows + ti.col0;
-        b1 = b0 + 128;
-      }
+      b_rows_of(ti, b0, b1);
       for (int kb = 0; kb < KB; ++kb) {
         if (!wait_bounded(empty0 + 8 * stage, ph ^ 1u, abort_flag, p.st, 1, true)) {
           ok = false;
@@ -436,6 +459,112 @@ __global__ void __launch_bounds__(THREADS, 1)
     // every MMA this thread issued must finish before TMEM is released
     tc_commit(drain);
     wait_bounded(drain, 0u, abort_flag, p.st, 6, false);
+  } else if (ROUTE && warp >= 2) {
+    // ------------------------------- routing epilogue ---------------------------------------
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    const int et = threadIdx.x - 64;        // 0..127 over the four epilogue warps
+    float* s_bias = reinterpret_cast<float*>(smem + STAGES * (A_STAGE + B_STAGE) + 256 +
+                                             SCHED_BYTES);
+    float* s_P = s_bias + 256;              // [4][256]
+    float* s_C = s_P + 4 * 256;             // [4][256] selection counts (exact in float32)
+    float* s_Z = s_C + 4 * 256;             // [4]
+    const int E = p.r_E;
+    for (int e = et; e < E; e += 128) s_bias[e] = p.r_bias ? p.r_bias[e] : 0.f;
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    RouteThreadCfg rc{E / 32, p.r_k, p.r_score, p.r_cpg, p.r_topk_groups, p.r_renorm,
+                      p.r_scale, 1};
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+      const TileInfo ti = decode_tile(tile, p, sc, total, split);
+      int ok = 1;
+      if (lane == 0) ok = wait_bounded(tfull0 + 8 * acc, aph, abort_flag, p.st, 4, true) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        // keep the four warps' named barriers matched (the others may be inside this tile),
+        // then stop; the status word already holds the timeout
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * 256) +
+                          (static_cast<uint32_t>(q * 32) << 16);
+      const bool half = ti.rows <= 64;
+      const int row = half ? q * 16 + lane : r;
+      const bool live = half ? (lane < 16 && row < ti.rows) : (r < ti.rows);
+      const size_t t = static_cast<size_t>(ti.row0 + row);
+      auto load = [&](int c, float (&v)[32]) {
+        uint32_t u[32];
+        tmem_ld32(tb + c * 32, u);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(u[i]);
+      };
+      // the logits, as the statistics and the backward read them
+#pragma unroll 1
+      for (int c = 0; c < E / 32; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tb + c * 32, u);
+        if (live) {
+          uint4* dst = reinterpret_cast<uint4*>(p.r_logits + t * E + c * 32);
+#pragma unroll
+          for (int v4 = 0; v4 < 8; ++v4)
+            dst[v4] = make_uint4(u[4 * v4], u[4 * v4 + 1], u[4 * v4 + 2], u[4 * v4 + 3]);
+        }
+      }
+      RouteThreadOut o;
+      route_thread(rc, s_bias, load, o);
+      if (live) {
+        for (int j = 0; j < p.r_k; ++j) {
+          p.r_idx[t * p.r_k + j] = o.idx[j];
+          p.r_w[t * p.r_k + j] = o.w[j];
+        }
+      }
+      // statistics terms: P contributions and selection counts summed over the warp's tokens
+      // per expert (fixed butterfly order), then over the four warps in order
+#pragma unroll 1
+      for (int c = 0; c < E / 32; ++c) {
+        float v[32], pr[32];
+        load(c, v);
+        token_probs(rc, o, v, pr);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (!live) pr[i] = 0.f;
+          v[i] = 0.f;
+        }
+        if (live) {
+#pragma unroll
+          for (int j = 0; j < kRouteMaxK; ++j) {
+            const int e = o.idx[j] - c * 32;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (j < p.r_k && e == i) v[i] = 1.f;
+          }
+        }
+        const float ps = warp_column_sum(pr);
+        const float cs = warp_column_sum(v);
+        s_P[q * 256 + c * 32 + lane] = ps;
+        s_C[q * 256 + c * 32 + lane] = cs;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      const float lse = o.m + logf(o.se);
+      const float zt = warp_sum(live ? lse * lse : 0.f);
+      if (lane == 0) s_Z[q] = zt;
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      for (int e = et; e < E; e += 128) {
+        p.r_part_P[static_cast<size_t>(tile) * E + e] =
+            ((s_P[e] + s_P[256 + e]) + s_P[512 + e]) + s_P[768 + e];
+        p.r_part_cnt[static_cast<size_t>(tile) * E + e] = static_cast<int32_t>(
+            s_C[e] + s_C[256 + e] + s_C[512 + e] + s_C[768 + e]);
+      }
+      if (et == 0) p.r_part_z[tile] = ((s_Z[0] + s_Z[1]) + s_Z[2]) + s_Z[3];
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      acc ^= 1;
+      if (acc == 0) aph ^= 1u;
+    }
   } else if (warp >= 2) {
     // ------------------------------- epilogue -----------------------------------------------
     const int q = warp & 3;                 // TMEM lanes 32q .. 32q+31 belong to this warp
@@ -766,6 +895,51 @@ cudaError_t launch_router_tc(const moe_config& c, const void* x, const void* w_g
   p.ldo = c.E;
   p.st = nullptr;
   return launch_one(mx, mw, p, ceil_div(c.T, BM) * p.n_tiles, s);
+}
+
+// Router GEMM with the routing epilogue: one group of T rows, B = W_gate [E, d] (E % 32 == 0,
+// E <= 256) in one N = E tile, 128-token tiles; one partial statistics row per tile.
+cudaError_t launch_router_fused(const moe_config& c, const void* x, const void* w_gate,
+                                const float* bias, float* logits, int32_t* idx, float* w,
+                                float* part_P, int32_t* part_cnt, float* part_z, DevStatus* st,
+                                cudaStream_t s) {
+  using namespace tc;
+  CUtensorMap mx, mw;
+  if (!make_map(&mx, x, (uint64_t)c.T, (uint64_t)c.d_model) ||
+      !make_map(&mw, w_gate, (uint64_t)c.E, (uint64_t)c.d_model))
+    return cudaErrorInvalidValue;
+  Params p{};
+  p.E = 1;
+  p.uniform_rows = c.T;
+  p.K = c.d_model;
+  p.bn = c.E;
+  p.n_tiles = 1;
+  p.b_rows = c.E;
+  p.st = st;
+  p.r_bias = c.score == MOE_SCORE_SIGMOID ? bias : nullptr;
+  p.r_logits = logits;
+  p.r_idx = idx;
+  p.r_w = w;
+  p.r_part_P = part_P;
+  p.r_part_cnt = part_cnt;
+  p.r_part_z = part_z;
+  p.r_E = c.E;
+  p.r_k = c.k;
+  p.r_score = c.score;
+  const bool limit = c.score == MOE_SCORE_SIGMOID && c.n_groups > 1 &&
+                     c.topk_groups < c.n_groups;
+  p.r_cpg = limit ? (c.E / c.n_groups) / 32 : 0;
+  p.r_topk_groups = c.topk_groups;
+  p.r_renorm = c.renormalize;
+  p.r_scale = c.route_scale;
+  const void* fn = reinterpret_cast<const void*>(grouped_gemm_tc_kernel<false, true>);
+  cudaError_t e = smem_attr_once(fn, static_cast<int>(SMEM_BYTES_ROUTE));
+  if (e != cudaSuccess) return e;
+  int grid = num_sms();
+  const int tiles = ceil_div(c.T, BM);
+  if (tiles < grid) grid = tiles;
+  launch_pdl(grouped_gemm_tc_kernel<false, true>, grid, THREADS, SMEM_BYTES_ROUTE, s, mx, mw, p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_timeout_probe(DevStatus* st, int limit_us, cudaStream_t s) {

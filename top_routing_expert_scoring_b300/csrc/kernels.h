@@ -44,6 +44,13 @@ cudaError_t launch_aux_stats(const moe_config& c, const float* logits, const int
 int aux_blocks(const moe_config& c);
 bool route_cta(const moe_config& c);
 int aux_rows(const moe_config& c);
+// Prefill router with the routing in the GEMM epilogue (router_fused(c)): writes the logits,
+// the selection, the weights and one statistics partial row per 128-token tile (aux_rows(c)).
+bool router_fused(const moe_config& c);
+cudaError_t launch_router_fused(const moe_config& c, const void* x, const void* w_gate,
+                                const float* bias, float* logits, int32_t* idx, float* w,
+                                float* part_P, int32_t* part_cnt, float* part_z, DevStatus* st,
+                                cudaStream_t s);
 
 // ---- dispatch --------------------------------------------------------------------------------
 struct DispatchBufs {

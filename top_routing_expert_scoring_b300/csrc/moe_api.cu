@@ -318,6 +318,11 @@ int moe_router_topk(const moe_config* c, const void* x, const void* w_gate, cons
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Layout L = layout(*c);
   float* g = logits ? logits : at<float>(ws, L.logits);
+  if (router_fused(*c))
+    return cuda_status(launch_router_fused(*c, x, w_gate, bias, g, topk_idx, topk_w,
+                                           at<float>(ws, L.part_P), at<int32_t>(ws, L.part_cnt),
+                                           at<float>(ws, L.part_z), at<DevStatus>(ws, L.status),
+                                           s));
   cudaError_t e = launch_router_logits(*c, x, w_gate, g, s, at<float>(ws, L.router_part),
                                        at<DevStatus>(ws, L.status));
   if (e == cudaSuccess)
@@ -527,18 +532,23 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
     return ev ? cudaEventRecord(ev, s) : cudaSuccess;
   };
 
-  cudaError_t e = launch_router_logits(*c, x, w_gate, g, s, at<float>(ws, L.router_part), dst);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  cudaError_t e = cudaSuccess;
+  if (!(c->routing == MOE_ROUTE_TOKEN_CHOICE && router_fused(*c))) {
+    e = launch_router_logits(*c, x, w_gate, g, s, at<float>(ws, L.router_part), dst);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
 
   if (c->routing == MOE_ROUTE_TOKEN_CHOICE) {
     int32_t* idx = topk_idx ? topk_idx : at<int32_t>(ws, L.idx);
     float* w = topk_w ? topk_w : at<float>(ws, L.w);
-    // Top-k with the load-balance partials of the same pass; the partials are reduced by an
-    // extra CTA of the small dispatch (T <= 256), else after the combine, off the path to the
-    // output
-    if ((e = launch_route_topk(*c, g, bias, idx, w, dst, s, part_P, part_cnt, part_z)) !=
-        cudaSuccess)
-      return MOE_ERR_CUDA;
+    // Top-k with the load-balance partials of the same pass (in the router GEMM's epilogue for
+    // prefill batches of a wide router); the partials are reduced by an extra CTA of the small
+    // dispatch (T <= 256), else after the combine, off the path to the output
+    if (router_fused(*c))
+      e = launch_router_fused(*c, x, w_gate, bias, g, idx, w, part_P, part_cnt, part_z, dst, s);
+    else
+      e = launch_route_topk(*c, g, bias, idx, w, dst, s, part_P, part_cnt, part_z);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
     const bool dec = decode_regime(*c);
     const bool fuse = gather_fused(*c, dec);
     DispatchBufs b{at<uint32_t>(ws, L.bitmap), at<int32_t>(ws, L.blk_base),
@@ -801,10 +811,16 @@ int moe_forward_fp8(const moe_config* c, const void* x, const void* w_gate, cons
   int32_t* part_cnt = at<int32_t>(ws, L.part_cnt);
   float* part_z = at<float>(ws, L.part_z);
 
-  if (launch_router_logits(*c, x, w_gate, g, s, at<float>(ws, L.router_part), dst) !=
-          cudaSuccess ||
-      launch_route_topk(*c, g, bias, idx, w, dst, s, part_P, part_cnt, part_z) != cudaSuccess)
+  if (router_fused(*c)) {
+    if (launch_router_fused(*c, x, w_gate, bias, g, idx, w, part_P, part_cnt, part_z, dst, s) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+  } else if (launch_router_logits(*c, x, w_gate, g, s, at<float>(ws, L.router_part), dst) !=
+                 cudaSuccess ||
+             launch_route_topk(*c, g, bias, idx, w, dst, s, part_P, part_cnt, part_z) !=
+                 cudaSuccess) {
     return MOE_ERR_CUDA;
+  }
   DispatchBufs b{at<uint32_t>(ws, L.bitmap), at<int32_t>(ws, L.blk_base),
                  at<int32_t>(ws, L.counts), at<int32_t>(ws, L.kept), at<int32_t>(ws, L.offsets),
                  at<int32_t>(ws, L.mtp), n_dropped ? n_dropped : at<int32_t>(ws, L.n_dropped),

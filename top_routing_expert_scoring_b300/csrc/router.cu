@@ -11,8 +11,12 @@
 //                                                   load_balancing_loss / router_z_loss blocks]
 #include <cuda_bf16.h>
 
+#include <cstdlib>
+#include <cstring>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "route_thread.cuh"
 
 namespace moe {
 
@@ -514,7 +518,97 @@ bool route_cta(const moe_config& c) {
   return c.routing == MOE_ROUTE_TOKEN_CHOICE && c.E > 32 && c.T <= kRouteCtaMaxT;
 }
 
-int aux_rows(const moe_config& c) { return route_cta(c) ? c.T : aux_blocks(c); }
+// Prefill batches of a bf16 router with E a multiple of 32 (<= 256) and groups of whole 32-expert
+// chunks: the router GEMM's epilogue does the scoring, the Top-k and the statistics terms
+// (launch_router_fused), one partial row per 128-token tile.  MOE_B300_ROUTER=separate keeps
+// the logits GEMM and the Top-k pass apart.
+bool router_fused(const moe_config& c) {
+  if (c.dtype != MOE_DTYPE_BF16 || c.routing != MOE_ROUTE_TOKEN_CHOICE) return false;
+  if (c.E < 32 || c.E > 256 || c.E % 32 || c.k > 8 || c.T <= kRouterSplitMaxT) return false;
+  const bool limit = c.score == MOE_SCORE_SIGMOID && c.n_groups > 1 &&
+                     c.topk_groups < c.n_groups;
+  if (limit && (c.E / c.n_groups) % 32) return false;
+  const char* env = getenv("MOE_B300_ROUTER");
+  return !(env && strcmp(env, "separate") == 0);
+}
+
+int aux_rows(const moe_config& c) {
+  if (router_fused(c)) return ceil_div(c.T, 128);
+  return route_cta(c) ? c.T : aux_blocks(c);
+}
+
+// The fused router's statistics rows for a given selection (moe_aux_stats), from logits in
+// global memory: the same 128-token tiles, the same token-to-thread mapping (a last tile of
+// <= 64 rows puts rows 16q..16q+15 on lanes 0..15 of warp q, as the M = 64 accumulator does)
+// and the same arithmetic, so both give the same bits.
+__global__ void __launch_bounds__(128) route_rows_stats_kernel(const float* __restrict__ g,
+                                                               const int32_t* __restrict__ idx,
+                                                               int T, RouteThreadCfg rc,
+                                                               float* part_P, int32_t* part_cnt,
+                                                               float* part_z) {
+  pdl_prologue();
+  __shared__ float s_P[4 * 256], s_C[4 * 256], s_Z[4];
+  const int E = rc.nc * 32;
+  const int tile = blockIdx.x;
+  const int row0 = tile * 128;
+  const int rows = min(128, T - row0);
+  const int q = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool half = rows <= 64;
+  const int row = half ? q * 16 + lane : q * 32 + lane;
+  const bool live = half ? (lane < 16 && row < rows) : (row < rows);
+  const size_t t = static_cast<size_t>(row0 + (live ? row : 0));
+  auto load = [&](int c, float (&v)[32]) {
+    const float4* src = reinterpret_cast<const float4*>(g + t * E + c * 32);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 f = live ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[4 * i] = f.x;
+      v[4 * i + 1] = f.y;
+      v[4 * i + 2] = f.z;
+      v[4 * i + 3] = f.w;
+    }
+  };
+  RouteThreadOut o;
+  route_thread(rc, nullptr, load, o);
+  int sel[kRouteMaxK];
+#pragma unroll
+  for (int j = 0; j < kRouteMaxK; ++j) sel[j] = (live && j < rc.k) ? idx[t * rc.k + j] : -1;
+#pragma unroll 1
+  for (int c = 0; c < rc.nc; ++c) {
+    float v[32], pr[32];
+    load(c, v);
+    token_probs(rc, o, v, pr);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (!live) pr[i] = 0.f;
+      v[i] = 0.f;
+    }
+    if (live) {
+#pragma unroll
+      for (int j = 0; j < kRouteMaxK; ++j) {
+        const int e = sel[j] - c * 32;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (j < rc.k && e == i) v[i] = 1.f;
+      }
+    }
+    const float ps = warp_column_sum(pr);
+    const float cs = warp_column_sum(v);
+    s_P[q * 256 + c * 32 + lane] = ps;
+    s_C[q * 256 + c * 32 + lane] = cs;
+  }
+  const float lse = o.m + logf(o.se);
+  const float zt = warp_sum(live ? lse * lse : 0.f);
+  if (lane == 0) s_Z[q] = zt;
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += 128) {
+    part_P[static_cast<size_t>(tile) * E + e] =
+        ((s_P[e] + s_P[256 + e]) + s_P[512 + e]) + s_P[768 + e];
+    part_cnt[static_cast<size_t>(tile) * E + e] =
+        static_cast<int32_t>(s_C[e] + s_C[256 + e] + s_C[512 + e] + s_C[768 + e]);
+  }
+  if (threadIdx.x == 0) part_z[tile] = ((s_Z[0] + s_Z[1]) + s_Z[2]) + s_Z[3];
+}
 
 // Block-wide reductions over blockDim/32 warps (every thread gets the result); red holds one
 // value per warp and is free again on return.
@@ -836,6 +930,18 @@ cudaError_t launch_aux_stats(const moe_config& c, const float* logits, const int
                              float* part_z, int nblocks, float* f, float* P, float* l_balance,
                              float* z_loss, DevStatus* st, cudaStream_t s) {
   (void)st;
+  if (router_fused(c)) {              // the fused router's 128-token rows
+    const bool limit = c.score == MOE_SCORE_SIGMOID && c.n_groups > 1 &&
+                       c.topk_groups < c.n_groups;
+    RouteThreadCfg rc{c.E / 32, c.k, c.score, limit ? (c.E / c.n_groups) / 32 : 0,
+                      c.topk_groups, c.renormalize, c.route_scale, 0};
+    const int tiles = ceil_div(c.T, 128);
+    launch_pdl(route_rows_stats_kernel, tiles, 128, 0, s, logits, idx, c.T, rc, part_P,
+               part_cnt, part_z);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    return launch_aux_final(c, part_P, part_cnt, part_z, tiles, f, P, l_balance, z_loss, s);
+  }
   if (route_cta(c)) {                 // per-token rows, as the fused Top-k pass writes them
     launch_pdl(aux_token_kernel, c.T, 32 * ceil_div(c.E, 32), 0, s, logits, idx, c.E, c.k,
                c.score, part_P, part_cnt, part_z);
