@@ -679,3 +679,4 @@ def test_router_epilogue_matches_separate_passes(case, monkeypatch):
     monkeypatch.delenv("MOE_B300_ROUTER", raising=False)
     fwd = U.run_forward(wl, inp, cfg)
     assert (fwd["idx"] == i_f).all() and (fwd["w"] == w_f.astype(np.float64)).all()
+

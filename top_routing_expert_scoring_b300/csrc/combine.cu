@@ -131,14 +131,28 @@ __global__ void __launch_bounds__(256) combine_kernel(const TY* __restrict__ y,
     ws[j] = j < k ? w[(size_t)t * k + j] : 0.f;
   }
   if constexpr (sizeof(TY) == 2) {
-    // bf16 y: eight columns per lane and step, so every y load moves 16 bytes
+    // bf16 y: eight columns per lane and step, so every y load moves 16 bytes; all k row loads
+    // of a step are issued before the first multiply-add (then added in the order j = 0..k-1)
     for (int v = v0 + lane * 8; v < v1; v += 256) {
+      uint4 yv[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        yv[j] = rows[j] >= 0 ? __ldg(reinterpret_cast<const uint4*>(y + (size_t)rows[j] * d + v))
+                             : make_uint4(0u, 0u, 0u, 0u);
       float acc[8];
       load_shared4(shared, (size_t)t * d + v, acc);
       load_shared4(shared, (size_t)t * d + v + 4, acc + 4);
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (rows[j] >= 0) fma8(ws[j], y + (size_t)rows[j] * d + v, acc);
+      for (int j = 0; j < 8; ++j) {
+        if (rows[j] < 0) continue;
+        const uint32_t u[4] = {yv[j].x, yv[j].y, yv[j].z, yv[j].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[i]));
+          acc[2 * i] = fmaf(ws[j], f.x, acc[2 * i]);
+          acc[2 * i + 1] = fmaf(ws[j], f.y, acc[2 * i + 1]);
+        }
+      }
       store4<TOut>(out + (size_t)t * d + v, acc);
       store4<TOut>(out + (size_t)t * d + v + 4, acc + 4);
     }

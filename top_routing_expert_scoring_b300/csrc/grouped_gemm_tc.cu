@@ -43,15 +43,17 @@ constexpr int B_BOX = 128 * BK * 2;          // 16 KB, one TMA box of 128 rows
 constexpr int B_STAGE = 2 * B_BOX;           // up to 256 rows
 constexpr int TMEM_COLS = 512;               // 2 accumulators x 256 fp32 columns
 constexpr int THREADS = 192;
-constexpr int NBARS = 2 * STAGES + 5;        // full, empty, tmem full x2, tmem empty x2, drain
 // expert schedule in shared memory: the M-tile prefix in schedule order [257] and the
 // expert at each schedule position [256]
 constexpr int SCHED_BYTES = (257 + 256) * 4;
 constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * (A_STAGE + B_STAGE) + 256 + SCHED_BYTES;
-// router epilogue (ROUTE instantiation): selection bias [256], per-warp P and count rows
-// [4][256] each, per-warp z terms [4]
-constexpr int ROUTE_BYTES = (256 + 2 * 4 * 256 + 4) * 4;
-constexpr size_t SMEM_BYTES_ROUTE = SMEM_BYTES + ROUTE_BYTES;
+// router (ROUTE instantiation): a 3-stage ring, 16 epilogue warps (four per TMEM lane
+// quarter, each owning a quarter of a token's experts) and their shared memory (RouteSmem)
+constexpr int STAGES_ROUTE = 3;
+constexpr int THREADS_ROUTE = 64 + 32 * 4 * kRouteSubs;
+constexpr size_t SMEM_BYTES_ROUTE = 1024 + (size_t)STAGES_ROUTE * (A_STAGE + B_STAGE) + 256 +
+                                    SCHED_BYTES + sizeof(RouteSmem);
+static_assert(SMEM_BYTES_ROUTE <= 232448, "router shared memory");
 
 struct Params {
   const int32_t* offsets;   // [E+1]
@@ -78,6 +80,9 @@ struct Params {
   // expert order of the tile list: 0 = expert index order; 1 = interleaved by row count
   // (largest, smallest, second largest, second smallest, ...), see build_schedule
   int order;
+  // 1: a tile of <= 64 rows runs as an M = 64 MMA (accumulator rows 16q..16q+15 in lanes
+  // 32q..32q+15); 0: every tile is an M = 128 MMA
+  int tail64;
   // float32 epilogue only: instead of storing row r, add w[perm[r]] * row into token
   // perm[r] / scat_k of scat_out [T, ldo] (float32 vector reductions); rows with perm < 0 skip
   float* scat_out;
@@ -231,9 +236,11 @@ __device__ __forceinline__ int choose_tail_split(int total, int G) {
 // default kernel's code is unchanged.
 // ROUTE: the router GEMM with the routing epilogue (see Params::r_*).
 template <bool GATHER, bool ROUTE = false>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(ROUTE ? THREADS_ROUTE : THREADS, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, const Params p) {
+  constexpr int STAGES = ROUTE ? STAGES_ROUTE : tc::STAGES;
+  constexpr int NBARS = 2 * STAGES + 5;   // full, empty, tmem full x2, tmem empty x2, drain
   pdl_prologue();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -261,7 +268,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, 4);
+      mbar_init(tempty0 + 8 * a, ROUTE ? 4 * kRouteSubs : 4);   // epilogue warps
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -426,7 +433,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
       // an expert's last tile with <= 64 rows runs as an M = 64 MMA (half the tensor work)
       const TileInfo tm = decode_tile(tile, p, sc, total, split);
-      const uint32_t idesc = idesc_bf16_f32(tm.rows <= 64 ? 64 : BM, tm.bn);
+      const uint32_t idesc = idesc_bf16_f32(p.tail64 && tm.rows <= 64 ? 64 : BM, tm.bn);
       if (!wait_bounded(tempty0 + 8 * acc, aph ^ 1u, abort_flag, p.st, 2, true)) {
         ok = false;
         break;
@@ -461,37 +468,43 @@ __global__ void __launch_bounds__(THREADS, 1)
     wait_bounded(drain, 0u, abort_flag, p.st, 6, false);
   } else if (ROUTE && warp >= 2) {
     // ------------------------------- routing epilogue ---------------------------------------
+    // 16 warps: warp w reads TMEM lane quarter q = w % 4 (32 token slots) and owns the
+    // quarter `sub` of each token's 32-expert chunks; the per-token phases meet in shared
+    // memory (route_thread.cuh).  Barrier 1 spans these 512 threads; a tile's start is agreed
+    // on by all of them (bar.red), so a timeout stops every warp at the same point.
     const int q = warp & 3;
-    const int r = q * 32 + lane;
-    const int et = threadIdx.x - 64;        // 0..127 over the four epilogue warps
-    float* s_bias = reinterpret_cast<float*>(smem + STAGES * (A_STAGE + B_STAGE) + 256 +
-                                             SCHED_BYTES);
-    float* s_P = s_bias + 256;              // [4][256]
-    float* s_C = s_P + 4 * 256;             // [4][256] selection counts (exact in float32)
-    float* s_Z = s_C + 4 * 256;             // [4]
+    const int sub = (warp - 2) >> 2;
+    const int r = q * 32 + lane;            // token slot of this thread (unique)
+    const int et = threadIdx.x - 64;        // 0..511
+    RouteSmem& sm = *reinterpret_cast<RouteSmem*>(smem + STAGES * (A_STAGE + B_STAGE) + 256 +
+                                                  SCHED_BYTES);
     const int E = p.r_E;
-    for (int e = et; e < E; e += 128) s_bias[e] = p.r_bias ? p.r_bias[e] : 0.f;
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    RouteThreadCfg rc{E / 32, p.r_k, p.r_score, p.r_cpg, p.r_topk_groups, p.r_renorm,
-                      p.r_scale, 1};
+    for (int e = et; e < 256; e += 512) {
+      sm.bias[e] = (e < E && p.r_bias) ? p.r_bias[e] : 0.f;
+      sm.cnt[e] = 0;
+    }
+    asm volatile("bar.sync 1, 512;" ::: "memory");
+    const RouteThreadCfg rc{E / 32, p.r_k, p.r_score, p.r_cpg, p.r_topk_groups, p.r_renorm,
+                            p.r_scale, 1};
     int acc = 0;
     uint32_t aph = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
       const TileInfo ti = decode_tile(tile, p, sc, total, split);
-      int ok = 1;
+      uint32_t ok = 1;
       if (lane == 0) ok = wait_bounded(tfull0 + 8 * acc, aph, abort_flag, p.st, 4, true) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) {
-        // keep the four warps' named barriers matched (the others may be inside this tile),
-        // then stop; the status word already holds the timeout
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        break;
-      }
+      uint32_t all_ok;
+      asm volatile(
+          "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, 512, p;\n"
+          " selp.u32 %0, 1, 0, q;\n}\n"
+          : "=r"(all_ok)
+          : "r"(ok)
+          : "memory");
+      if (!all_ok) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * 256) +
                           (static_cast<uint32_t>(q * 32) << 16);
-      const bool half = ti.rows <= 64;
+      const bool half = p.tail64 && ti.rows <= 64;
       const int row = half ? q * 16 + lane : r;
       const bool live = half ? (lane < 16 && row < ti.rows) : (r < ti.rows);
       const size_t t = static_cast<size_t>(ti.row0 + row);
@@ -502,66 +515,43 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(u[i]);
       };
       // the logits, as the statistics and the backward read them
-#pragma unroll 1
-      for (int c = 0; c < E / 32; ++c) {
-        uint32_t u[32];
-        tmem_ld32(tb + c * 32, u);
-        if (live) {
-          uint4* dst = reinterpret_cast<uint4*>(p.r_logits + t * E + c * 32);
+      auto each = [&](int c, const float (&v)[32]) {
+        if (!live) return;
+        float4* dst = reinterpret_cast<float4*>(p.r_logits + t * E + c * 32);
 #pragma unroll
-          for (int v4 = 0; v4 < 8; ++v4)
-            dst[v4] = make_uint4(u[4 * v4], u[4 * v4 + 1], u[4 * v4 + 2], u[4 * v4 + 3]);
-        }
-      }
-      RouteThreadOut o;
-      route_thread(rc, s_bias, load, o);
-      if (live) {
-        for (int j = 0; j < p.r_k; ++j) {
-          p.r_idx[t * p.r_k + j] = o.idx[j];
-          p.r_w[t * p.r_k + j] = o.w[j];
-        }
-      }
-      // statistics terms: P contributions and selection counts summed over the warp's tokens
-      // per expert (fixed butterfly order), then over the four warps in order
-#pragma unroll 1
-      for (int c = 0; c < E / 32; ++c) {
-        float v[32], pr[32];
-        load(c, v);
-        token_probs(rc, o, v, pr);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          if (!live) pr[i] = 0.f;
-          v[i] = 0.f;
-        }
-        if (live) {
-#pragma unroll
-          for (int j = 0; j < kRouteMaxK; ++j) {
-            const int e = o.idx[j] - c * 32;
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (j < p.r_k && e == i) v[i] = 1.f;
-          }
-        }
-        const float ps = warp_column_sum(pr);
-        const float cs = warp_column_sum(v);
-        s_P[q * 256 + c * 32 + lane] = ps;
-        s_C[q * 256 + c * 32 + lane] = cs;
-      }
+        for (int i = 0; i < 8; ++i)
+          dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      };
+      route_phase_a(rc, sm, r, sub, load, each);
+      asm volatile("bar.sync 1, 512;" ::: "memory");
+      route_phase_b(rc, sm, r, sub, q, live, load);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
-      const float lse = o.m + logf(o.se);
-      const float zt = warp_sum(live ? lse * lse : 0.f);
-      if (lane == 0) s_Z[q] = zt;
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      for (int e = et; e < E; e += 128) {
-        p.r_part_P[static_cast<size_t>(tile) * E + e] =
-            ((s_P[e] + s_P[256 + e]) + s_P[512 + e]) + s_P[768 + e];
-        p.r_part_cnt[static_cast<size_t>(tile) * E + e] = static_cast<int32_t>(
-            s_C[e] + s_C[256 + e] + s_C[512 + e] + s_C[768 + e]);
+      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);   // this warp is done with TMEM
+      asm volatile("bar.sync 1, 512;" ::: "memory");
+      if (sub == 0) {
+        int idx[kRouteMaxK];
+        float wv[kRouteMaxK];
+        const float lse = route_phase_c(rc, sm, r, idx, wv);
+        if (live) {
+          for (int j = 0; j < p.r_k; ++j) {
+            p.r_idx[t * p.r_k + j] = idx[j];
+            p.r_w[t * p.r_k + j] = wv[j];
+            atomicAdd(&sm.cnt[idx[j]], 1);
+          }
+        }
+        const float zt = warp_sum(live ? lse * lse : 0.f);
+        if (lane == 0) sm.Z[q] = zt;
       }
-      if (et == 0) p.r_part_z[tile] = ((s_Z[0] + s_Z[1]) + s_Z[2]) + s_Z[3];
-      asm volatile("bar.sync 1, 128;" ::: "memory");
+      asm volatile("bar.sync 1, 512;" ::: "memory");
+      for (int e = et; e < E; e += 512) {
+        p.r_part_P[static_cast<size_t>(tile) * E + e] =
+            ((sm.P[0][e] + sm.P[1][e]) + sm.P[2][e]) + sm.P[3][e];
+        p.r_part_cnt[static_cast<size_t>(tile) * E + e] = sm.cnt[e];
+        sm.cnt[e] = 0;
+      }
+      if (et == 0) p.r_part_z[tile] = ((sm.Z[0] + sm.Z[1]) + sm.Z[2]) + sm.Z[3];
+      asm volatile("bar.sync 1, 512;" ::: "memory");
       acc ^= 1;
       if (acc == 0) aph ^= 1u;
     }
@@ -582,7 +572,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                           (static_cast<uint32_t>(q * 32) << 16);
       // M = 128: row r = 32q + lane sits in TMEM lane r.  M = 64: rows 16q .. 16q+15 sit in the
       // first 16 lanes of the warp's 32-lane quarter.
-      const bool half = ti.rows <= 64;
+      const bool half = p.tail64 && ti.rows <= 64;
       const int row = half ? q * 16 + lane : r;
       const bool live = half ? (lane < 16 && row < ti.rows) : (r < ti.rows);
       if (p.swiglu) {
@@ -799,6 +789,19 @@ static int expert_order() {
   return (env && strcmp(env, "index") == 0) ? 0 : 1;
 }
 
+// Gate/up GEMM on two-block (256-row) tiles (launch_gateup_dm) unless MOE_B300_GATEUP=single
+// asks for one-block tiles; both compute the same rows.
+static bool gateup_two_blocks() {
+  const char* env = getenv("MOE_B300_GATEUP");
+  return !(env && strcmp(env, "single") == 0);
+}
+
+// M = 64 MMAs for tiles of <= 64 rows unless MOE_B300_TAIL64=0 (the same rows either way).
+static int tail_m64() {
+  const char* env = getenv("MOE_B300_TAIL64");
+  return (env && strcmp(env, "0") == 0) ? 0 : 1;
+}
+
 static bool use_pair_kernel(const GroupedFFN& g) {
   if (g.d % 256 != 0) return false;
   const char* env = getenv("MOE_B300_GEMM");
@@ -847,8 +850,11 @@ cudaError_t launch_ffn_tc(const GroupedFFN& g, DevStatus* st, cudaStream_t s) {
   p1.gk = g.gather_k;
   p1.gx = static_cast<const __nv_bfloat16*>(g.gather_x);
   p1.order = expert_order();
+  p1.tail64 = tail_m64();
   p1.st = st;
-  cudaError_t err = launch_one(mx, mw13, p1, mt_upper * p1.n_tiles, s);
+  cudaError_t err = (!g.gather_perm && gateup_two_blocks())
+                        ? launch_gateup_dm(g, p1.order, st, s)
+                        : launch_one(mx, mw13, p1, mt_upper * p1.n_tiles, s);
   if (err != cudaSuccess) return err;
   Params p2 = p1;
   p2.K = g.F;
@@ -893,6 +899,7 @@ cudaError_t launch_router_tc(const moe_config& c, const void* x, const void* w_g
   p.out = logits;
   p.out_f32 = 1;
   p.ldo = c.E;
+  p.tail64 = 1;
   p.st = nullptr;
   return launch_one(mx, mw, p, ceil_div(c.T, BM) * p.n_tiles, s);
 }
@@ -932,13 +939,15 @@ cudaError_t launch_router_fused(const moe_config& c, const void* x, const void* 
   p.r_topk_groups = c.topk_groups;
   p.r_renorm = c.renormalize;
   p.r_scale = c.route_scale;
+  p.tail64 = 1;
   const void* fn = reinterpret_cast<const void*>(grouped_gemm_tc_kernel<false, true>);
   cudaError_t e = smem_attr_once(fn, static_cast<int>(SMEM_BYTES_ROUTE));
   if (e != cudaSuccess) return e;
   int grid = num_sms();
   const int tiles = ceil_div(c.T, BM);
   if (tiles < grid) grid = tiles;
-  launch_pdl(grouped_gemm_tc_kernel<false, true>, grid, THREADS, SMEM_BYTES_ROUTE, s, mx, mw, p);
+  launch_pdl(grouped_gemm_tc_kernel<false, true>, grid, THREADS_ROUTE, SMEM_BYTES_ROUTE, s, mx,
+             mw, p);
   return cudaGetLastError();
 }
 

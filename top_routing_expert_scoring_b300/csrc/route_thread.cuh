@@ -1,15 +1,21 @@
-// One token's routing, done by one thread over its row of logits read 32 experts at a time:
-// scoring, the group limit, Top-k with renormalisation and the token's load-balance
-// contributions ["MoE 路由数学" §2.1 and §3.2; "Systems for Mixture-of-Experts Models" §5.3
-// router walk-through].  The row comes from a loader (a TMEM chunk in the router GEMM's
-// epilogue, or global memory in route_rows_kernel), so the GEMM epilogue and the separate
-// kernels compute the same bits.
+// One token's routing, split over four threads that each own a quarter of its logits (whole
+// 32-expert chunks): scoring, the group limit, Top-k with renormalisation and the token's
+// load-balance contributions ["MoE 路由数学" §2.1 and §3.2; "Systems for Mixture-of-Experts
+// Models" §5.3 router walk-through].
 //
-// The arithmetic matches the warp-per-token kernels: sigmoid as 1 / (1 + expf(-g)), selection
-// keys s + b (sigmoid) or g (softmax), a group's score = its two largest keys added in float32,
-// the (key descending, index ascending) order everywhere, weights exp(g_j - g_top) / sum or
-// s_j / sum times the route scale.  Experts are read in index order, so equal keys keep the
-// lower index first.
+// The four threads of a token are lanes of four warps with the same TMEM lane quarter, so in
+// the router GEMM's epilogue each reads its chunks straight from the accumulator; the same
+// phases run from global memory in route_rows_stats_kernel, so the GEMM epilogue and the
+// separate statistics kernel compute the same bits.  Phases (shared memory between them):
+//   A  per thread: max logit, sum of exp(g - max) (kept online across its chunks), sum of
+//      sigmoids, and each chunk's two largest selection keys;
+//   B  per thread: the token's max, exp-sum and sigmoid-sum (its four parts combined in thread
+//      order), the group limit, the top-k of its kept chunks, and its P contributions;
+//   C  one thread per token: the k best of the four lists, and the weights.
+// The arithmetic matches the warp-per-token kernels where it decides: sigmoid as
+// 1 / (1 + expf(-g)), selection keys s + b (sigmoid) or g (softmax), a group's score = its two
+// largest keys added in float32, the (key descending, index ascending) order everywhere, and
+// weights exp(g_j - g_top) / sum or s_j / sum times the route scale.
 #pragma once
 
 #include "common.cuh"
@@ -18,6 +24,8 @@ namespace moe {
 
 constexpr int kRouteMaxChunks = 8;   // E <= 256
 constexpr int kRouteMaxK = 8;
+constexpr int kRouteSubs = 4;        // threads per token
+constexpr int kRouteTile = 128;      // tokens per tile
 
 struct RouteThreadCfg {
   int nc;             // E / 32
@@ -30,165 +38,47 @@ struct RouteThreadCfg {
   int select;         // 1: choose experts and weights; 0: statistics only (given selection)
 };
 
-// Result of one token's routing: the k selected experts in rank order with their weights, and
-// the token's statistics terms (its z term; P contributions are produced chunk by chunk by the
-// caller through token_probs).
-struct RouteThreadOut {
-  int idx[kRouteMaxK];
-  float w[kRouteMaxK];
-  float m;            // max logit
-  float se;           // sum_e exp(g_e - m)
-  float ss;           // sum_e sigmoid(g_e) (sigmoid scoring)
+// Shared memory of the phases for one tile of 128 tokens.
+struct RouteSmem {
+  float bias[256];
+  float stat[kRouteTile][kRouteSubs][3];          // per thread part: max, exp-sum, sigmoid-sum
+  float ctop[kRouteTile][kRouteMaxChunks][2];     // per chunk: two largest keys
+  float ckey[kRouteTile][kRouteSubs][kRouteMaxK]; // per thread part: its top-k list
+  int cidx[kRouteTile][kRouteSubs][kRouteMaxK];
+  float cval[kRouteTile][kRouteSubs][kRouteMaxK];
+  float P[4][256];                                // per TMEM lane quarter: column sums
+  int cnt[256];
+  float Z[4];
 };
 
 __device__ __forceinline__ float sigm(float g) { return 1.0f / (1.0f + expf(-g)); }
 
-// Passes 1 and 2 over the row.  Loader: void(int chunk, float (&v)[32]) returning experts
-// 32*chunk .. 32*chunk+31.  bias: shared-memory copy of the selection bias (sigmoid) or nullptr.
-template <typename Loader>
-__device__ __forceinline__ void route_thread(const RouteThreadCfg& rc, const float* bias,
-                                             Loader load, RouteThreadOut& o) {
-  const bool sig = rc.score == MOE_SCORE_SIGMOID;
-  // ---- pass 1: max logit, sum of sigmoids, per-chunk two largest keys ------------------
-  float m = -INFINITY, ss = 0.f;
-  float ct1[kRouteMaxChunks], ct2[kRouteMaxChunks];
-#pragma unroll
-  for (int c = 0; c < kRouteMaxChunks; ++c) {
-    ct1[c] = -INFINITY;
-    ct2[c] = -INFINITY;
-    if (c >= rc.nc) continue;
-    float v[32];
-    load(c, v);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      m = fmaxf(m, v[i]);
-      if (sig) {
-        const float s = sigm(v[i]);
-        ss += s;
-        if (rc.cpg > 0) {
-          const float key = s + bias[c * 32 + i];
-          if (key > ct1[c]) {
-            ct2[c] = ct1[c];
-            ct1[c] = key;
-          } else if (key > ct2[c]) {
-            ct2[c] = key;
-          }
-        }
-      }
-    }
-  }
-  // group limit: a group's score is the sum of its two largest keys; a group is kept when
-  // fewer than topk_groups groups rank before it (ties: lower group)
-  uint32_t kept = 0xffffffffu;
-  if (sig && rc.cpg > 0 && rc.select) {
-    float gsc[kRouteMaxChunks];
-#pragma unroll
-    for (int c = 0; c < kRouteMaxChunks; ++c) {
-      float a = -INFINITY, b = -INFINITY;       // two largest over the chunks of c's group
-#pragma unroll
-      for (int c2 = 0; c2 < kRouteMaxChunks; ++c2) {
-        if (c2 < rc.nc && c < rc.nc && c2 / rc.cpg == c / rc.cpg) {
-          const float x1 = ct1[c2], x2 = ct2[c2];
-          if (x1 > a) {
-            b = fmaxf(a, x2);
-            a = x1;
-          } else if (x1 > b) {
-            b = x1;
-          }
-        }
-      }
-      gsc[c] = a + b;
-    }
-    kept = 0u;
-#pragma unroll
-    for (int c = 0; c < kRouteMaxChunks; ++c) {
-      if (c >= rc.nc) continue;
-      const int q = c / rc.cpg;
-      int rank = 0;
-#pragma unroll
-      for (int c2 = 0; c2 < kRouteMaxChunks; ++c2)
-        if (c2 < rc.nc && c2 % rc.cpg == 0 && ranks_before(gsc[c2], c2 / rc.cpg, gsc[c], q))
-          ++rank;
-      if (rank < rc.topk_groups) kept |= 1u << c;
-    }
-  }
-  // ---- pass 2: sum of exp(g - m); Top-k over the kept experts -------------------------
-  float se = 0.f;
-  float bk[kRouteMaxK], bv[kRouteMaxK];
-  int bi[kRouteMaxK];
-#pragma unroll
-  for (int j = 0; j < kRouteMaxK; ++j) {
-    bk[j] = -INFINITY;
-    bv[j] = 0.f;
-    bi[j] = 0x7fffffff;
-  }
-#pragma unroll
-  for (int c = 0; c < kRouteMaxChunks; ++c) {
-    if (c >= rc.nc) continue;
-    float v[32];
-    load(c, v);
-    const bool live = (kept >> c) & 1u;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      se += expf(v[i] - m);
-      if (!rc.select || !live) continue;
-      const int e = c * 32 + i;
-      float key, val;
-      if (sig) {
-        val = sigm(v[i]);
-        key = val + bias[e];
-      } else {
-        val = v[i];
-        key = v[i];
-      }
-      if (ranks_before(key, e, bk[kRouteMaxK - 1], bi[kRouteMaxK - 1])) {
-        // insertion into the sorted list, from the bottom up
-#pragma unroll
-        for (int j = kRouteMaxK - 1; j >= 0; --j) {
-          const bool here = ranks_before(key, e, bk[j], bi[j]);
-          const bool above = j == 0 ? true : ranks_before(key, e, bk[j - 1], bi[j - 1]);
-          if (here) {
-            if (above && j > 0) {
-              bk[j] = bk[j - 1];
-              bi[j] = bi[j - 1];
-              bv[j] = bv[j - 1];
-            } else {
-              bk[j] = key;
-              bi[j] = e;
-              bv[j] = val;
-            }
-          }
-        }
-      }
-    }
-  }
-  o.m = m;
-  o.se = se;
-  o.ss = ss;
-  if (!rc.select) return;
-  // weights of the k selected experts, in rank order
-  float num[kRouteMaxK], den = 0.f;
-#pragma unroll
-  for (int j = 0; j < kRouteMaxK; ++j) {
-    num[j] = 0.f;
-    if (j >= rc.k) continue;
-    num[j] = sig ? bv[j] : expf(bv[j] - bv[0]);
-    den += num[j];
-  }
-  if (!rc.renorm) den = sig ? 1.f : se * expf(m - bv[0]);
-#pragma unroll
-  for (int j = 0; j < kRouteMaxK; ++j) {
-    o.idx[j] = bi[j];
-    o.w[j] = (num[j] / den) * rc.scale;
-  }
+__device__ __forceinline__ void route_chunk_range(const RouteThreadCfg& rc, int sub, int& c0,
+                                                  int& c1) {
+  c0 = sub * rc.nc / kRouteSubs;
+  c1 = (sub + 1) * rc.nc / kRouteSubs;
 }
 
-// Pass 3: the token's P contributions for one 32-expert chunk (softmax(g)_e, or s_e / sum s).
-__device__ __forceinline__ void token_probs(const RouteThreadCfg& rc, const RouteThreadOut& o,
-                                            const float (&v)[32], float (&p)[32]) {
+// Insertion of (key, e, val) into the descending list (bk, bi, bv) of kRouteMaxK entries, from
+// the bottom up; equal keys keep the lower index first.
+__device__ __forceinline__ void topk_insert(float key, int e, float val, float (&bk)[kRouteMaxK],
+                                            int (&bi)[kRouteMaxK], float (&bv)[kRouteMaxK]) {
 #pragma unroll
-  for (int i = 0; i < 32; ++i)
-    p[i] = rc.score == MOE_SCORE_SIGMOID ? sigm(v[i]) / o.ss : expf(v[i] - o.m) / o.se;
+  for (int j = kRouteMaxK - 1; j >= 0; --j) {
+    const bool here = ranks_before(key, e, bk[j], bi[j]);
+    const bool above = j == 0 ? true : ranks_before(key, e, bk[j - 1], bi[j - 1]);
+    if (here) {
+      if (above && j > 0) {
+        bk[j] = bk[j - 1];
+        bi[j] = bi[j - 1];
+        bv[j] = bv[j - 1];
+      } else {
+        bk[j] = key;
+        bi[j] = e;
+        bv[j] = val;
+      }
+    }
+  }
 }
 
 // Column sums of a warp's 32 x 32 block (lane = token, register = expert of the chunk):
@@ -207,6 +97,186 @@ __device__ __forceinline__ float warp_column_sum(float (&v)[32]) {
     }
   }
   return v[0];
+}
+
+// Phase A for this thread's chunks of token slot r.  Loader: void(int chunk, float (&v)[32]).
+// Also hands each chunk to `each(c, v)` (the epilogue writes the logits from there).
+template <typename Loader, typename Each>
+__device__ __forceinline__ void route_phase_a(const RouteThreadCfg& rc, RouteSmem& sm, int r,
+                                              int sub, Loader load, Each each) {
+  const bool sig = rc.score == MOE_SCORE_SIGMOID;
+  const bool limit = sig && rc.cpg > 0 && rc.select;
+  int c0, c1;
+  route_chunk_range(rc, sub, c0, c1);
+  float m = -INFINITY, se = 0.f, ss = 0.f;
+#pragma unroll 1
+  for (int c = c0; c < c1; ++c) {
+    float v[32];
+    load(c, v);
+    each(c, v);
+    float cm = v[0];
+#pragma unroll
+    for (int i = 1; i < 32; ++i) cm = fmaxf(cm, v[i]);
+    if (cm > m) {                      // online exp-sum: rescale to the new maximum
+      se = (m == -INFINITY) ? 0.f : se * expf(m - cm);
+      m = cm;
+    }
+    float a = -INFINITY, b = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      se += expf(v[i] - m);
+      if (sig) {
+        const float s = sigm(v[i]);
+        ss += s;
+        if (limit) {
+          const float key = s + sm.bias[c * 32 + i];
+          if (key > a) {
+            b = a;
+            a = key;
+          } else if (key > b) {
+            b = key;
+          }
+        }
+      }
+    }
+    sm.ctop[r][c][0] = a;
+    sm.ctop[r][c][1] = b;
+  }
+  sm.stat[r][sub][0] = m;
+  sm.stat[r][sub][1] = se;
+  sm.stat[r][sub][2] = ss;
+}
+
+// The token's max, exp-sum and sigmoid-sum from the four parts, in thread order.
+struct RouteTotals {
+  float m, se, ss;
+};
+__device__ __forceinline__ RouteTotals route_totals(const RouteSmem& sm, int r) {
+  RouteTotals t{-INFINITY, 0.f, 0.f};
+#pragma unroll
+  for (int s = 0; s < kRouteSubs; ++s) t.m = fmaxf(t.m, sm.stat[r][s][0]);
+#pragma unroll
+  for (int s = 0; s < kRouteSubs; ++s) {
+    const float ms = sm.stat[r][s][0];
+    if (ms != -INFINITY) t.se += sm.stat[r][s][1] * expf(ms - t.m);
+    t.ss += sm.stat[r][s][2];
+  }
+  return t;
+}
+
+// Phase B: the group limit (kept chunks), the top-k of this thread's kept chunks into the
+// candidate lists, and this thread's P contributions (column sums of the warp's 32 tokens
+// into sm.P[q]).  live: the slot holds a token.
+template <typename Loader>
+__device__ __forceinline__ void route_phase_b(const RouteThreadCfg& rc, RouteSmem& sm, int r,
+                                              int sub, int q, bool live, Loader load) {
+  const bool sig = rc.score == MOE_SCORE_SIGMOID;
+  const bool limit = sig && rc.cpg > 0 && rc.select;
+  const RouteTotals tot = route_totals(sm, r);
+  uint32_t kept = 0xffffffffu;
+  if (limit) {
+    float gsc[kRouteMaxChunks];
+    const int ng = rc.nc / rc.cpg;
+#pragma unroll 1
+    for (int g = 0; g < ng; ++g) {
+      float a = -INFINITY, b = -INFINITY;        // two largest over the group's chunks
+      for (int c = g * rc.cpg; c < (g + 1) * rc.cpg; ++c) {
+        const float x1 = sm.ctop[r][c][0], x2 = sm.ctop[r][c][1];
+        if (x1 > a) {
+          b = fmaxf(a, x2);
+          a = x1;
+        } else if (x1 > b) {
+          b = x1;
+        }
+      }
+      gsc[g] = a + b;
+    }
+    kept = 0u;
+#pragma unroll 1
+    for (int g = 0; g < ng; ++g) {
+      int rank = 0;
+      for (int g2 = 0; g2 < ng; ++g2) rank += ranks_before(gsc[g2], g2, gsc[g], g) ? 1 : 0;
+      if (rank < rc.topk_groups)
+        for (int c = g * rc.cpg; c < (g + 1) * rc.cpg; ++c) kept |= 1u << c;
+    }
+  }
+  int c0, c1;
+  route_chunk_range(rc, sub, c0, c1);
+  float bk[kRouteMaxK], bv[kRouteMaxK];
+  int bi[kRouteMaxK];
+#pragma unroll
+  for (int j = 0; j < kRouteMaxK; ++j) {
+    bk[j] = -INFINITY;
+    bv[j] = 0.f;
+    bi[j] = 0x7fffffff;
+  }
+  const float inv_ss = 1.0f / tot.ss, inv_se = 1.0f / tot.se;
+#pragma unroll 1
+  for (int c = c0; c < c1; ++c) {
+    float v[32], pr[32];
+    load(c, v);
+    const bool sel = rc.select && ((kept >> c) & 1u);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float s = sig ? sigm(v[i]) : 0.f;
+      pr[i] = live ? (sig ? s * inv_ss : expf(v[i] - tot.m) * inv_se) : 0.f;
+      if (sel) {
+        const int e = c * 32 + i;
+        const float key = sig ? s + sm.bias[e] : v[i];
+        const float val = sig ? s : v[i];
+        if (ranks_before(key, e, bk[kRouteMaxK - 1], bi[kRouteMaxK - 1]))
+          topk_insert(key, e, val, bk, bi, bv);
+      }
+    }
+    sm.P[q][c * 32 + (threadIdx.x & 31)] = warp_column_sum(pr);
+  }
+#pragma unroll
+  for (int j = 0; j < kRouteMaxK; ++j) {
+    sm.ckey[r][sub][j] = bk[j];
+    sm.cidx[r][sub][j] = bi[j];
+    sm.cval[r][sub][j] = bv[j];
+  }
+}
+
+// Phase C (one thread per token): the k best of the four candidate lists, in rank order, and
+// the weights.  Returns the token's lse for the z-loss.
+__device__ __forceinline__ float route_phase_c(const RouteThreadCfg& rc, const RouteSmem& sm,
+                                               int r, int (&idx)[kRouteMaxK],
+                                               float (&w)[kRouteMaxK]) {
+  const bool sig = rc.score == MOE_SCORE_SIGMOID;
+  const RouteTotals tot = route_totals(sm, r);
+  float bk[kRouteMaxK], bv[kRouteMaxK];
+  int bi[kRouteMaxK];
+#pragma unroll
+  for (int j = 0; j < kRouteMaxK; ++j) {
+    bk[j] = sm.ckey[r][0][j];
+    bi[j] = sm.cidx[r][0][j];
+    bv[j] = sm.cval[r][0][j];
+  }
+#pragma unroll 1
+  for (int s = 1; s < kRouteSubs; ++s) {
+    for (int j = 0; j < kRouteMaxK; ++j) {      // each list is sorted: stop at its first miss
+      const float key = sm.ckey[r][s][j];
+      const int e = sm.cidx[r][s][j];
+      if (!ranks_before(key, e, bk[kRouteMaxK - 1], bi[kRouteMaxK - 1])) break;
+      topk_insert(key, e, sm.cval[r][s][j], bk, bi, bv);
+    }
+  }
+  float num[kRouteMaxK], den = 0.f;
+#pragma unroll
+  for (int j = 0; j < kRouteMaxK; ++j) {
+    num[j] = 0.f;
+    if (j >= rc.k) continue;
+    num[j] = sig ? bv[j] : expf(bv[j] - bv[0]);
+    den += num[j];
+  }
+  if (!rc.renorm) den = sig ? 1.f : tot.se * expf(tot.m - bv[0]);
+#pragma unroll
+  for (int j = 0; j < kRouteMaxK; ++j) {
+    idx[j] = bi[j];
+    w[j] = (num[j] / den) * rc.scale;
+  }
+  return tot.m + logf(tot.se);
 }
 
 }  // namespace moe

@@ -538,25 +538,35 @@ int aux_rows(const moe_config& c) {
 }
 
 // The fused router's statistics rows for a given selection (moe_aux_stats), from logits in
-// global memory: the same 128-token tiles, the same token-to-thread mapping (a last tile of
-// <= 64 rows puts rows 16q..16q+15 on lanes 0..15 of warp q, as the M = 64 accumulator does)
-// and the same arithmetic, so both give the same bits.
-__global__ void __launch_bounds__(128) route_rows_stats_kernel(const float* __restrict__ g,
+// global memory: the same 128-token tiles, the same four threads per token (thread group w =
+// warp + 2 takes TMEM lane quarter w % 4 and chunk quarter w / 4, as in the epilogue), the
+// same token-to-slot mapping (a last tile of <= 64 rows puts rows 16q..16q+15 on lanes 0..15
+// of quarter q, as the M = 64 accumulator does) and the same phases, so both give the same
+// bits.
+__global__ void __launch_bounds__(512) route_rows_stats_kernel(const float* __restrict__ g,
                                                                const int32_t* __restrict__ idx,
                                                                int T, RouteThreadCfg rc,
                                                                float* part_P, int32_t* part_cnt,
                                                                float* part_z) {
   pdl_prologue();
-  __shared__ float s_P[4 * 256], s_C[4 * 256], s_Z[4];
+  extern __shared__ unsigned char route_rows_smem[];
+  RouteSmem& sm = *reinterpret_cast<RouteSmem*>(route_rows_smem);
   const int E = rc.nc * 32;
   const int tile = blockIdx.x;
-  const int row0 = tile * 128;
-  const int rows = min(128, T - row0);
-  const int q = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row0 = tile * kRouteTile;
+  const int rows = min(kRouteTile, T - row0);
+  const int w = (threadIdx.x >> 5) + 2, lane = threadIdx.x & 31;
+  const int q = w & 3, sub = (w - 2) >> 2;
+  const int r = q * 32 + lane;
   const bool half = rows <= 64;
-  const int row = half ? q * 16 + lane : q * 32 + lane;
-  const bool live = half ? (lane < 16 && row < rows) : (row < rows);
+  const int row = half ? q * 16 + lane : r;
+  const bool live = half ? (lane < 16 && row < rows) : (r < rows);
   const size_t t = static_cast<size_t>(row0 + (live ? row : 0));
+  for (int e = threadIdx.x; e < 256; e += 512) {
+    sm.bias[e] = 0.f;
+    sm.cnt[e] = 0;
+  }
+  __syncthreads();
   auto load = [&](int c, float (&v)[32]) {
     const float4* src = reinterpret_cast<const float4*>(g + t * E + c * 32);
 #pragma unroll
@@ -568,46 +578,25 @@ __global__ void __launch_bounds__(128) route_rows_stats_kernel(const float* __re
       v[4 * i + 3] = f.w;
     }
   };
-  RouteThreadOut o;
-  route_thread(rc, nullptr, load, o);
-  int sel[kRouteMaxK];
-#pragma unroll
-  for (int j = 0; j < kRouteMaxK; ++j) sel[j] = (live && j < rc.k) ? idx[t * rc.k + j] : -1;
-#pragma unroll 1
-  for (int c = 0; c < rc.nc; ++c) {
-    float v[32], pr[32];
-    load(c, v);
-    token_probs(rc, o, v, pr);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      if (!live) pr[i] = 0.f;
-      v[i] = 0.f;
-    }
-    if (live) {
-#pragma unroll
-      for (int j = 0; j < kRouteMaxK; ++j) {
-        const int e = sel[j] - c * 32;
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (j < rc.k && e == i) v[i] = 1.f;
-      }
-    }
-    const float ps = warp_column_sum(pr);
-    const float cs = warp_column_sum(v);
-    s_P[q * 256 + c * 32 + lane] = ps;
-    s_C[q * 256 + c * 32 + lane] = cs;
-  }
-  const float lse = o.m + logf(o.se);
-  const float zt = warp_sum(live ? lse * lse : 0.f);
-  if (lane == 0) s_Z[q] = zt;
+  route_phase_a(rc, sm, r, sub, load, [](int, const float (&)[32]) {});
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += 128) {
-    part_P[static_cast<size_t>(tile) * E + e] =
-        ((s_P[e] + s_P[256 + e]) + s_P[512 + e]) + s_P[768 + e];
-    part_cnt[static_cast<size_t>(tile) * E + e] =
-        static_cast<int32_t>(s_C[e] + s_C[256 + e] + s_C[512 + e] + s_C[768 + e]);
+  route_phase_b(rc, sm, r, sub, q, live, load);
+  __syncthreads();
+  if (sub == 0) {
+    const RouteTotals tot = route_totals(sm, r);
+    const float lse = tot.m + logf(tot.se);
+    if (live)
+      for (int j = 0; j < rc.k; ++j) atomicAdd(&sm.cnt[idx[t * rc.k + j]], 1);
+    const float zt = warp_sum(live ? lse * lse : 0.f);
+    if (lane == 0) sm.Z[q] = zt;
   }
-  if (threadIdx.x == 0) part_z[tile] = ((s_Z[0] + s_Z[1]) + s_Z[2]) + s_Z[3];
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += 512) {
+    part_P[static_cast<size_t>(tile) * E + e] =
+        ((sm.P[0][e] + sm.P[1][e]) + sm.P[2][e]) + sm.P[3][e];
+    part_cnt[static_cast<size_t>(tile) * E + e] = sm.cnt[e];
+  }
+  if (threadIdx.x == 0) part_z[tile] = ((sm.Z[0] + sm.Z[1]) + sm.Z[2]) + sm.Z[3];
 }
 
 // Block-wide reductions over blockDim/32 warps (every thread gets the result); red holds one
@@ -935,9 +924,12 @@ cudaError_t launch_aux_stats(const moe_config& c, const float* logits, const int
                        c.topk_groups < c.n_groups;
     RouteThreadCfg rc{c.E / 32, c.k, c.score, limit ? (c.E / c.n_groups) / 32 : 0,
                       c.topk_groups, c.renormalize, c.route_scale, 0};
-    const int tiles = ceil_div(c.T, 128);
-    launch_pdl(route_rows_stats_kernel, tiles, 128, 0, s, logits, idx, c.T, rc, part_P,
-               part_cnt, part_z);
+    const int tiles = ceil_div(c.T, kRouteTile);
+    cudaError_t ea = smem_attr_once(reinterpret_cast<const void*>(route_rows_stats_kernel),
+                                    static_cast<int>(sizeof(RouteSmem)));
+    if (ea != cudaSuccess) return ea;
+    launch_pdl(route_rows_stats_kernel, tiles, 512, sizeof(RouteSmem), s, logits, idx, c.T, rc,
+               part_P, part_cnt, part_z);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     return launch_aux_final(c, part_P, part_cnt, part_z, tiles, f, P, l_balance, z_loss, s);
