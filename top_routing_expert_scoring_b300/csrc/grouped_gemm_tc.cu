@@ -789,13 +789,6 @@ static int expert_order() {
   return (env && strcmp(env, "index") == 0) ? 0 : 1;
 }
 
-// Gate/up GEMM on two-block (256-row) tiles (launch_gateup_dm) unless MOE_B300_GATEUP=single
-// asks for one-block tiles; both compute the same rows.
-static bool gateup_two_blocks() {
-  const char* env = getenv("MOE_B300_GATEUP");
-  return !(env && strcmp(env, "single") == 0);
-}
-
 // M = 64 MMAs for tiles of <= 64 rows unless MOE_B300_TAIL64=0 (the same rows either way).
 static int tail_m64() {
   const char* env = getenv("MOE_B300_TAIL64");
@@ -852,9 +845,7 @@ cudaError_t launch_ffn_tc(const GroupedFFN& g, DevStatus* st, cudaStream_t s) {
   p1.order = expert_order();
   p1.tail64 = tail_m64();
   p1.st = st;
-  cudaError_t err = (!g.gather_perm && gateup_two_blocks())
-                        ? launch_gateup_dm(g, p1.order, st, s)
-                        : launch_one(mx, mw13, p1, mt_upper * p1.n_tiles, s);
+  cudaError_t err = launch_one(mx, mw13, p1, mt_upper * p1.n_tiles, s);
   if (err != cudaSuccess) return err;
   Params p2 = p1;
   p2.K = g.F;

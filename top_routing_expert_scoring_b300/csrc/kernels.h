@@ -130,9 +130,6 @@ bool ffn_uses_pair(const GroupedFFN& g);
 // falls back to single when d % 256 != 0).
 cudaError_t launch_ffn_tc(const GroupedFFN& g, DevStatus* st, cudaStream_t s);
 cudaError_t launch_ffn_tc2(const GroupedFFN& g, DevStatus* st, cudaStream_t s);
-// The gate/up GEMM alone on 256-row (two-block) tiles of the single-CTA tensor-core kernel
-// family (grouped_gemm_dm.cu); order: 1 = experts interleaved by row count, 0 = index order.
-cudaError_t launch_gateup_dm(const GroupedFFN& g, int order, DevStatus* st, cudaStream_t s);
 cudaError_t launch_ffn_simt(const GroupedFFN& g, bool f32, DevStatus* st, cudaStream_t s);
 
 // Decode-sized batches: swap-AB tensor-core GEMMs (weights on M, tokens on N) over the routed
