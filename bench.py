@@ -45,7 +45,8 @@ def load_peaks():
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the expert GEMM launches of
 # one step, keyed by (workload, T), from an ncu capture of the bench command on the current
 # kernel build; a workload without a capture on the current build reports null.
-GEMM_TRAFFIC_BYTES = {}
+GEMM_TRAFFIC_BYTES = {("v3", 8192): (16806827520 + 266584064) + (7862200576 + 929650176)
+                      + (890786048 + 29044480) + (90960896 + 183969792)}
 
 
 def workload_flops_bytes(wl):
@@ -483,18 +484,33 @@ def router_backward_sweep(args):
         torch.cuda.empty_cache()
 
 
+def router_in_gemm(wl):
+    """The library's rule for running scoring and Top-k in the router GEMM's epilogue: a bf16
+    token-choice router with E a multiple of 32 up to 256, k <= 8, more than 512 tokens, and
+    groups (if limited) of whole 32-expert chunks; MOE_B300_ROUTER=separate turns it off."""
+    if wl.dtype != "bf16" or wl.routing != "token_choice":
+        return False
+    if wl.E < 32 or wl.E > 256 or wl.E % 32 or wl.k > 8 or wl.T <= 512:
+        return False
+    limit = wl.score == "sigmoid" and wl.n_groups > 1 and wl.topk_groups < wl.n_groups
+    if limit and (wl.E // wl.n_groups) % 32:
+        return False
+    return os.environ.get("MOE_B300_ROUTER") != "separate"
+
+
 def launches_per_step(wl):
-    """Our kernels per forward: router logits, Top-k (+statistics partials), dispatch (1 kernel
-    for T <= 256, else 4), 2 expert GEMMs, 2 shared-expert GEMMs, combine, statistics final.
-    A k <= 2 bf16 layer without shared experts and with a float32 output has no combine kernel:
-    the down GEMM adds the weighted rows into the output itself."""
+    """Our kernels per forward: router logits and Top-k (+statistics partials; one kernel when
+    the router GEMM's epilogue does the Top-k), dispatch (1 kernel for T <= 256, else 4),
+    2 expert GEMMs, 2 shared-expert GEMMs, combine, statistics final.  A k <= 2 bf16 layer
+    without shared experts and with a float32 output has no combine kernel: the down GEMM adds
+    the weighted rows into the output itself."""
     shared = wl.F_sh > 0
     if wl.routing == "expert_choice":
         return 1 + 5 + 2 + 2 + (2 if shared else 0) + 1 + 2
     combine_in_gemm = (wl.k <= 2 and not shared and wl.dtype == "bf16"
                        and os.environ.get("MOE_B300_COMBINE") != "separate")
-    return (1 + 1 + (1 if wl.T <= 256 else 4) + 2 + (2 if shared else 0)
-            + (0 if combine_in_gemm else 1) + 1)
+    return ((1 if router_in_gemm(wl) else 2) + (1 if wl.T <= 256 else 4) + 2
+            + (2 if shared else 0) + (0 if combine_in_gemm else 1) + 1)
 
 
 class Prefill:
