@@ -45,8 +45,8 @@ def load_peaks():
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the expert GEMM launches of
 # one step, keyed by (workload, T), from an ncu capture of the bench command on the current
 # kernel build; a workload without a capture on the current build reports null.
-GEMM_TRAFFIC_BYTES = {("v3", 8192): (16806827520 + 266584064) + (7862200576 + 929650176)
-                      + (890786048 + 29044480) + (90960896 + 183969792)}
+GEMM_TRAFFIC_BYTES = {("v3", 8192): (16798419968 + 266171136) + (7862379776 + 929392896)
+                      + (509447680 + 27314688) + (75314176 + 183981824)}
 
 
 def workload_flops_bytes(wl):

@@ -178,8 +178,17 @@ __device__ __forceinline__ PairTile decode_pair(int tile, const Params& p, const
     row_end = p.offsets[lo + 1];
   }
   const int tt = tile - base * p.n_tiles;
-  ti.nt = tt / mt_e;
-  const int mt = tt - ti.nt * mt_e;
+  int mt;
+  if (p.uniform_rows >= 0) {
+    // one group (shared experts): N fastest, so a pair tile's rows are read once from DRAM and
+    // reused from L2 by all N tiles while the (small) weights stay in L2
+    mt = tt / p.n_tiles;
+    ti.nt = tt - mt * p.n_tiles;
+  } else {
+    // ragged experts: M fastest, so the CTAs of an expert's M tiles share one weight tile
+    ti.nt = tt / mt_e;
+    mt = tt - ti.nt * mt_e;
+  }
   ti.row0 = row_base + mt * PM;
   ti.rows = min(PM, row_end - ti.row0);
   return ti;
