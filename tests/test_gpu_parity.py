@@ -112,6 +112,10 @@ SMALL = {
                                     renormalize=False),
     "router_fused_sigmoid_one_group": dict(name="v3", T=900, d=256, E=64, k=6, F=128,
                                            F_shared=128, n_groups=1, topk_groups=1),
+    # 153 tiles of 128 tokens on 148 CTAs: some CTAs route two tiles (double-buffered
+    # accumulators, epilogue state reused), and the last tile has 44 rows
+    "router_fused_two_tiles_per_cta": dict(name="v3", T=19500, d=128, E=64, k=4, F=128,
+                                           F_shared=128, n_groups=2, topk_groups=1),
     "one_expert": dict(name="mixtral", T=130, d=128, E=1, k=1, F=128),
     # prefill path with E = 1, k = 1 and d = 256 (decode regime needs <= 64 rows per expert)
     "one_expert_d256": dict(name="mixtral", T=300, d=256, E=1, k=1, F=128),
@@ -533,7 +537,7 @@ def test_forward_replays_in_a_cuda_graph():
 
 
 @pytest.mark.parametrize("case", ["v3_like", "softmax_cap", "decode_b8", "router_fused_v3_e256",
-                                  "router_fused_e96_tail"])
+                                  "router_fused_e96_tail", "router_fused_two_tiles_per_cta"])
 def test_forward_timed_and_fused_statistics(case):
     # moe_forward_timed runs moe_forward's kernels (identical output) and brackets the expert
     # GEMMs with the caller's events; the statistics moe_forward fuses into its Top-k pass

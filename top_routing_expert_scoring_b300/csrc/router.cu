@@ -586,7 +586,10 @@ __global__ void __launch_bounds__(512) route_rows_stats_kernel(const float* __re
     const RouteTotals tot = route_totals(sm, r);
     const float lse = tot.m + logf(tot.se);
     if (live)
-      for (int j = 0; j < rc.k; ++j) atomicAdd(&sm.cnt[idx[t * rc.k + j]], 1);
+      for (int j = 0; j < rc.k; ++j) {
+        const int e = idx[t * rc.k + j];
+        if (e >= 0 && e < E) atomicAdd(&sm.cnt[e], 1);    // caller's indices: range-checked
+      }
     const float zt = warp_sum(live ? lse * lse : 0.f);
     if (lane == 0) sm.Z[q] = zt;
   }
