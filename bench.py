@@ -408,9 +408,9 @@ def router_backward_bytes_flops(wl):
 
 
 def router_backward_sweep(args):
-    """Router-side backward (dL/dg, dW_gate, dx) per workload: CUDA events around each call, L2
-    flushed (256 MB write) between calls outside the events.  The routing inputs come from the
-    forward's own router call."""
+    """Router-side backward (dL/dg, dW_gate, dx) per workload: CUDA events around each call
+    (replayed from a CUDA graph), L2 flushed (256 MB write) between calls outside the events.
+    The routing inputs come from the forward's own router call."""
     import torch
     import moe_inputs
     import top_routing_expert_scoring_b300 as m
@@ -449,6 +449,13 @@ def router_backward_sweep(args):
         for _ in range(max(3, args.warmup)):
             call()
         torch.cuda.synchronize()
+        # one CUDA graph per call, so that the events time the kernels and not the host's
+        # marshalling and launch of three short kernels
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            call()
+        graph.replay()
+        torch.cuda.synchronize()
         reps = args.backward_steps
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(reps)]
@@ -457,7 +464,7 @@ def router_backward_sweep(args):
             for a, b in ev:
                 flush.fill_(1)
                 a.record()
-                call()
+                graph.replay()
                 b.record()
             torch.cuda.synchronize()
         st = m.sync_status(ws)

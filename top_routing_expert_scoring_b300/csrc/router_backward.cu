@@ -35,8 +35,8 @@
 namespace moe {
 namespace {
 
-constexpr int kBwTokens = 16;     // tokens per CTA of the scores kernel (2 per warp)
-constexpr int kBwWarps = 8;
+constexpr int kBwTokens = 16;     // tokens per CTA of the scores kernel (one per warp)
+constexpr int kBwWarps = 16;
 // shared row of the transposed tile: 18 bf16 = 9 words, odd, so the 32 lanes writing 32
 // experts of one token hit 32 different banks
 constexpr int kTPad = kBwTokens + 2;
@@ -55,13 +55,16 @@ struct ScoresArgs {
   float* d_logits;        // nullable
   __nv_bfloat16* dg16;    // nullable: [T, E64]
   __nv_bfloat16* dgT;     // nullable: [E64, T64]
+  int* tile_counter;      // nullable: zeroed here for the gradient GEMM launch that follows
   DevStatus* st;
 };
 
 template <int V>
-__global__ void __launch_bounds__(kBwWarps * 32) router_bw_scores_kernel(const ScoresArgs a) {
+__global__ void __launch_bounds__(kBwWarps * 32, 2) router_bw_scores_kernel(const ScoresArgs a) {
   pdl_prologue();
+  if (a.tile_counter && blockIdx.x == 0 && threadIdx.x == 0) *a.tile_counter = 0;
   __shared__ __nv_bfloat16 sT[256][kTPad];
+  __shared__ int sSel[kBwWarps][256];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t_base = blockIdx.x * kBwTokens;
   const float inv_T = 1.0f / static_cast<float>(a.T);
@@ -81,6 +84,14 @@ __global__ void __launch_bounds__(kBwWarps * 32) router_bw_scores_kernel(const S
     float dg[V];
     if (t < a.T) {
       const float* gr = a.logits + static_cast<size_t>(t) * a.E;
+      // every load of the token is issued here, before any arithmetic: lane j holds choice j
+      // (k <= 8), broadcast below
+      int e_l = 0;
+      float dw_l = 0.0f;
+      if (a.d_w && lane < a.k) {
+        e_l = a.idx[static_cast<size_t>(t) * a.k + lane];
+        dw_l = a.d_w[static_cast<size_t>(t) * a.k + lane];
+      }
       float g[V];
       float m = -INFINITY;
 #pragma unroll
@@ -110,7 +121,7 @@ __global__ void __launch_bounds__(kBwWarps * 32) router_bw_scores_kernel(const S
       } else {
 #pragma unroll
         for (int i = 0; i < V; ++i)
-          v[i] = (lane + 32 * i) < a.E ? 1.0f / (1.0f + expf(-g[i])) : 0.0f;
+          v[i] = (lane + 32 * i) < a.E ? __frcp_rn(1.0f + expf(-g[i])) : 0.0f;
       }
 
       // gate-weight term: dL/dv on the selected experts
@@ -122,19 +133,24 @@ __global__ void __launch_bounds__(kBwWarps * 32) router_bw_scores_kernel(const S
         float sum_s = 0.0f, sum_dws = 0.0f;
 #pragma unroll
         for (int i = 0; i < V; ++i) dwv[i] = 0.0f;
+        // choice j of the token marks expert e_j in the warp's row of slots (j + 1; the
+        // last choice naming an expert wins), then each lane reads its own experts' slots
+        int* slot = sSel[warp];
+#pragma unroll
+        for (int i = 0; i < V; ++i) slot[lane + 32 * i] = 0;
+        __syncwarp();
+        if (lane < a.k) {
+          if (e_l < 0 || e_l >= a.E) record_error(a.st, MOE_ERR_ARG, t);
+          else atomicMax(&slot[e_l], lane + 1);
+        }
+        __syncwarp();
         bool sel[V];
 #pragma unroll
-        for (int i = 0; i < V; ++i) sel[i] = false;
-        for (int j = 0; j < a.k; ++j) {
-          const int e = a.idx[static_cast<size_t>(t) * a.k + j];
-          const float dwj = a.d_w[static_cast<size_t>(t) * a.k + j];
-          if (e < 0 || e >= a.E) {
-            if (lane == 0) record_error(a.st, MOE_ERR_ARG, t);
-            continue;
-          }
-#pragma unroll
-          for (int i = 0; i < V; ++i)
-            if (lane + 32 * i == e) { sel[i] = true; dwv[i] = dwj; }
+        for (int i = 0; i < V; ++i) {
+          const int j1 = slot[lane + 32 * i];
+          const float dwj = __shfl_sync(0xffffffffu, dw_l, j1 > 0 ? j1 - 1 : 0);
+          sel[i] = j1 > 0;
+          dwv[i] = sel[i] ? dwj : 0.0f;
         }
 #pragma unroll
         for (int i = 0; i < V; ++i)
@@ -142,10 +158,12 @@ __global__ void __launch_bounds__(kBwWarps * 32) router_bw_scores_kernel(const S
         sum_s = warp_sum(sum_s);
         sum_dws = warp_sum(sum_dws);
         // w_j = scale * v_j / sum_S v: dL/dv_j = scale * (d_w_j - sum_S d_w v / sum_S v) / sum_S v
+        const float inv_ss = 1.0f / sum_s;
+        const float mean_dw = sum_dws * inv_ss;
 #pragma unroll
         for (int i = 0; i < V; ++i)
           if (sel[i])
-            dv[i] = a.renorm ? a.route_scale * (dwv[i] - sum_dws / sum_s) / sum_s
+            dv[i] = a.renorm ? a.route_scale * (dwv[i] - mean_dw) * inv_ss
                              : a.route_scale * dwv[i];
       }
 
@@ -227,12 +245,16 @@ constexpr int A_STAGE = BM * BK * 2;          // 16 KB
 constexpr int B_STAGE = 256 * BK * 2;         // up to 32 KB
 constexpr int MN_ATOM = 64 * BK * 2;          // one 64-column MN-major box: 8 KB
 constexpr int TMEM_COLS = 512;
-constexpr int THREADS = 192;
-constexpr int NBARS = 2 * STAGES + 5;
+constexpr int EPI_WARPS = 8;                  // two per TMEM lane quarter, one column half each
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int NQ = 4;                         // tile ids queued from the producer
+// full, empty, tmem full x2, tmem empty x2, drain, tile queue full x NQ, empty x NQ
+constexpr int NBARS = 2 * STAGES + 5 + 2 * NQ;
 constexpr int STAGE_OUT = 32 * 32 * 4;       // one 32-row x 32-column fp32 chunk, 4 KB
-// ring | per epilogue warp two chunk buffers (1024-byte aligned, 128-byte swizzle) | barriers
+// ring | per epilogue warp one chunk buffer (1024-byte aligned, 128-byte swizzle) | barriers
 constexpr size_t SMEM_BYTES =
-    1024 + (size_t)STAGES * (A_STAGE + B_STAGE) + 4 * 2 * STAGE_OUT + 256;
+    1024 + (size_t)STAGES * (A_STAGE + B_STAGE) + EPI_WARPS * STAGE_OUT + 256;
+static_assert(SMEM_BYTES <= 232448, "shared memory of one CTA");
 
 struct Params {
   int M, N, KB;           // rows of D, MMA N, K blocks of 64
@@ -242,6 +264,17 @@ struct Params {
   int out_mode;           // 0: out[m * ldo + n]; 1: out[(split * n_valid + n) * ldo + m]
   int ldo, n_valid;
   DevStatus* st;
+};
+
+// One launch runs up to two GEMMs (the dW and dx products of one backward call): tile ids
+// [0, ntiles[0]) belong to job 0, the next ntiles[1] to job 1.  CTAs take tile ids from a
+// global counter (zeroed by the kernel before), so the long dW tiles, handed out first, and
+// the short dx tiles spread over the GPU together: dW's reads of x overlap dx's writes.
+struct Jobs {
+  Params p[2];
+  int ntiles[2];
+  int njobs;
+  int* counter;
 };
 
 // Descriptor of an MN-major operand with the 128-byte swizzle: 64-element (128-byte) rows
@@ -272,9 +305,12 @@ __device__ __forceinline__ Tile tile_of(int tile, const Params& p) {
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
-    router_grad_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                            const __grid_constant__ CUtensorMap tmB,
-                            const __grid_constant__ CUtensorMap tmO, const Params p) {
+    router_grad_gemm_kernel(const __grid_constant__ CUtensorMap tmA0,
+                            const __grid_constant__ CUtensorMap tmB0,
+                            const __grid_constant__ CUtensorMap tmO0,
+                            const __grid_constant__ CUtensorMap tmA1,
+                            const __grid_constant__ CUtensorMap tmB1,
+                            const __grid_constant__ CUtensorMap tmO1, const Jobs J) {
   pdl_prologue();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -282,9 +318,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_STAGE;
   uint8_t* sOut = sB + STAGES * B_STAGE;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + 4 * 2 * STAGE_OUT);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + EPI_WARPS * STAGE_OUT);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* queue = reinterpret_cast<volatile int*>(tmem_slot + 2);   // [NQ] tile ids
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t full0 = smem_u32(bars);
@@ -292,6 +329,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tfull0 = empty0 + 8 * STAGES;
   const uint32_t tempty0 = tfull0 + 16;
   const uint32_t drain = tempty0 + 16;
+  const uint32_t qfull0 = drain + 8;
+  const uint32_t qempty0 = qfull0 + 8 * NQ;
+  const Params* P = J.p;
+  const int total = J.ntiles[0] + (J.njobs > 1 ? J.ntiles[1] : 0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -300,9 +341,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, 4);
+      mbar_init(tempty0 + 8 * a, EPI_WARPS);
     }
     mbar_init(drain, 1);
+    for (int q = 0; q < NQ; ++q) {
+      mbar_init(qfull0 + 8 * q, 1);        // the producer publishes a tile id
+      mbar_init(qempty0 + 8 * q, 1 + EPI_WARPS);   // the MMA issuer and every epilogue warp took it
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -317,17 +362,41 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int total = p.m_tiles * p.n_tiles * p.splits;
+
+  // the i-th tile id this CTA works on (consumers): -1 ends the sequence
+  auto next_tile = [&](int i, DevStatus* st, int where) -> int {
+    const int q = i % NQ;
+    if (!wait_bounded(qfull0 + 8 * q, static_cast<uint32_t>((i / NQ) & 1), abort_flag, st,
+                      where, true))
+      return -2;
+    const int t = queue[q];
+    return t;
+  };
 
   if (warp == 0 && lane == 0) {
     // ------------------------------- TMA producer -------------------------------------------
     int stage = 0;
     uint32_t ph = 0;
     uint32_t issued = 0, last_par = 0;
-    const uint32_t bytes = A_STAGE + p.N * BK * 2;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-      const Tile ti = tile_of(tile, p);
+    for (int i = 0; ok; ++i) {
+      int tile = atomicAdd(J.counter, 1);
+      if (tile >= total) tile = -1;
+      const int q = i % NQ;
+      if (!wait_bounded(qempty0 + 8 * q, static_cast<uint32_t>(((i / NQ) & 1) ^ 1), abort_flag,
+                        P[0].st, 27, true)) {
+        ok = false;
+        break;
+      }
+      queue[q] = tile;
+      mbar_arrive(qfull0 + 8 * q);
+      if (tile < 0) break;
+      const int job = tile < J.ntiles[0] ? 0 : 1;
+      const Params& p = P[job];
+      const CUtensorMap* tmA = job ? &tmA1 : &tmA0;
+      const CUtensorMap* tmB = job ? &tmB1 : &tmB0;
+      const Tile ti = tile_of(tile - (job ? J.ntiles[0] : 0), p);
+      const uint32_t bytes = A_STAGE + p.N * BK * 2;
       const int m0 = ti.mt * BM, n0 = ti.nt * p.N;
       for (int kb = ti.kb0; kb < ti.kb1; ++kb) {
         if (!wait_bounded(empty0 + 8 * stage, ph ^ 1u, abort_flag, p.st, 21, true)) {
@@ -339,16 +408,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t a_dst = smem_u32(sA + stage * A_STAGE);
         const uint32_t b_dst = smem_u32(sB + stage * B_STAGE);
         if (p.a_mn) {
-          tma_load_2d(a_dst, &tmA, fb, m0, kb * BK);
-          tma_load_2d(a_dst + MN_ATOM, &tmA, fb, m0 + 64, kb * BK);
+          tma_load_2d(a_dst, tmA, fb, m0, kb * BK);
+          tma_load_2d(a_dst + MN_ATOM, tmA, fb, m0 + 64, kb * BK);
         } else {
-          tma_load_2d(a_dst, &tmA, fb, kb * BK, m0);
+          tma_load_2d(a_dst, tmA, fb, kb * BK, m0);
         }
         if (p.b_mn) {
-          for (int i = 0; i < p.N / 64; ++i)
-            tma_load_2d(b_dst + i * MN_ATOM, &tmB, fb, n0 + 64 * i, kb * BK);
+          for (int i2 = 0; i2 < p.N / 64; ++i2)
+            tma_load_2d(b_dst + i2 * MN_ATOM, tmB, fb, n0 + 64 * i2, kb * BK);
         } else {
-          tma_load_2d(b_dst, &tmB, fb, kb * BK, n0);
+          tma_load_2d(b_dst, tmB, fb, kb * BK, n0);
         }
         issued |= 1u << stage;
         last_par = (last_par & ~(1u << stage)) | (ph << stage);
@@ -361,18 +430,23 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (!ok) {
       for (int s = 0; s < STAGES; ++s)
         if ((issued >> s) & 1u)
-          wait_bounded(full0 + 8 * s, (last_par >> s) & 1u, abort_flag, p.st, 25, false);
+          wait_bounded(full0 + 8 * s, (last_par >> s) & 1u, abort_flag, P[0].st, 25, false);
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------- MMA issuer ---------------------------------------------
-    const uint32_t idesc = idesc_bf16_f32(BM, p.N) | (static_cast<uint32_t>(p.a_mn) << 15) |
-                           (static_cast<uint32_t>(p.b_mn) << 16);
     const uint32_t a_lbo = MN_ATOM, b_lbo = MN_ATOM;
     int stage = 0, acc = 0;
     uint32_t ph = 0, aph = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-      const Tile ti = tile_of(tile, p);
+    for (int i = 0; ok; ++i) {
+      const int tile = next_tile(i, P[0].st, 28);
+      mbar_arrive(qempty0 + 8 * (i % NQ));
+      if (tile < 0) break;
+      const int job = tile < J.ntiles[0] ? 0 : 1;
+      const Params& p = P[job];
+      const Tile ti = tile_of(tile - (job ? J.ntiles[0] : 0), p);
+      const uint32_t idesc = idesc_bf16_f32(BM, p.N) | (static_cast<uint32_t>(p.a_mn) << 15) |
+                             (static_cast<uint32_t>(p.b_mn) << 16);
       if (!wait_bounded(tempty0 + 8 * acc, aph ^ 1u, abort_flag, p.st, 22, true)) {
         ok = false;
         break;
@@ -405,17 +479,27 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (acc == 0) aph ^= 1u;
     }
     tc_commit(drain);
-    wait_bounded(drain, 0u, abort_flag, p.st, 26, false);
+    wait_bounded(drain, 0u, abort_flag, P[0].st, 26, false);
   } else if (warp >= 2) {
     // ------------------------------- epilogue -----------------------------------------------
-    const int q = warp & 3;
+    const int q = warp & 3;                     // TMEM lane quarter this warp may read
+    const int h = (warp - 2) >> 2;              // column half
     const int r = q * 32 + lane;
-    const uint32_t out_buf0 = smem_u32(sOut) + (warp - 2) * 2 * STAGE_OUT;
-    int ob = 0;
+    const uint32_t buf = smem_u32(sOut) + (warp - 2) * STAGE_OUT;
     int acc = 0;
     uint32_t aph = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const Tile ti = tile_of(tile, p);
+    for (int i = 0;; ++i) {
+      int tile = 0;
+      if (lane == 0) {
+        tile = next_tile(i, P[0].st, 29);
+        mbar_arrive(qempty0 + 8 * (i % NQ));
+      }
+      tile = __shfl_sync(0xffffffffu, tile, 0);
+      if (tile < 0) break;
+      const int job = tile < J.ntiles[0] ? 0 : 1;
+      const Params& p = P[job];
+      const CUtensorMap* tmO = job ? &tmO1 : &tmO0;
+      const Tile ti = tile_of(tile - (job ? J.ntiles[0] : 0), p);
       int ok = 1;
       if (lane == 0) ok = wait_bounded(tfull0 + 8 * acc, aph, abort_flag, p.st, 24, true) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -427,15 +511,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool live = m < p.M;
       const int n0 = ti.nt * p.N;
 #pragma unroll 1
-      for (int c = 0; c < p.N / 32; ++c) {
+      for (int c = h * (p.N / 64); c < (h + 1) * (p.N / 64); ++c) {
         uint32_t vr[32];
         tmem_ld32(tb + c * 32, vr);
         if (p.out_mode == 0) {
-          // The warp's 32 rows x 32 columns go to one of its two shared buffers in the
+          // The warp's 32 rows x 32 columns go to its shared buffer in the
           // 128-byte-swizzled layout (16-byte chunk j of row i at chunk j ^ (i & 7):
           // conflict-free), then leave as one TMA store; rows past M are clipped by the TMA.
-          const uint32_t buf = out_buf0 + ob * STAGE_OUT;
-          if (lane == 0) bulk_wait_read<1>();     // the store that used this buffer has read it
+          if (lane == 0) bulk_wait_read<0>();     // the previous store has read the buffer
           __syncwarp();
 #pragma unroll
           for (int j = 0; j < 8; ++j)
@@ -447,19 +530,18 @@ __global__ void __launch_bounds__(THREADS, 1)
           fence_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmO, buf, n0 + c * 32, ti.mt * BM + q * 32);
+            tma_store_2d(tmO, buf, n0 + c * 32, ti.mt * BM + q * 32);
             bulk_commit();
           }
-          ob ^= 1;
         } else if (live) {
           // column n of this row goes to row n of the transposed partial: lanes hold
           // consecutive m, so each store instruction writes 128 contiguous bytes
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int n = n0 + c * 32 + i;
+          for (int i2 = 0; i2 < 32; ++i2) {
+            const int n = n0 + c * 32 + i2;
             if (n < p.n_valid)
               p.out[(static_cast<size_t>(ti.s) * p.n_valid + n) * p.ldo + m] =
-                  __uint_as_float(vr[i]);
+                  __uint_as_float(vr[i2]);
           }
         }
       }
@@ -482,15 +564,26 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
-                   const Params& p, cudaStream_t s) {
+// One launch of up to two GEMMs (jobs); counter: a workspace int zeroed by the kernel before.
+cudaError_t launch(const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap* o,
+                   const Params* p, int njobs, int* counter, cudaStream_t s) {
   cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(router_grad_gemm_kernel),
                                  static_cast<int>(SMEM_BYTES));
   if (e != cudaSuccess) return e;
-  const int total = p.m_tiles * p.n_tiles * p.splits;
+  Jobs J{};
+  int total = 0;
+  for (int j = 0; j < njobs; ++j) {
+    J.p[j] = p[j];
+    J.ntiles[j] = p[j].m_tiles * p[j].n_tiles * p[j].splits;
+    total += J.ntiles[j];
+  }
+  J.njobs = njobs;
+  J.counter = counter;
+  const int k1 = njobs > 1 ? 1 : 0;
   int grid = num_sms();
   if (total < grid) grid = total;
-  launch_pdl(router_grad_gemm_kernel, grid, THREADS, SMEM_BYTES, s, a, b, o, p);
+  launch_pdl(router_grad_gemm_kernel, grid, THREADS, SMEM_BYTES, s, a[0], b[0], o[0], a[k1], b[k1],
+             o[k1], J);
   return cudaGetLastError();
 }
 
@@ -554,7 +647,7 @@ __global__ void bias_update_kernel(const float* __restrict__ f, float* __restric
 // Host side
 // ---------------------------------------------------------------------------------------------
 struct BwLayout {
-  size_t status, dg16, dgT, part, dg32, total;
+  size_t status, counter, dg16, dgT, part, dg32, total;
   int splits;
 };
 
@@ -593,6 +686,7 @@ BwLayout bw_layout(const moe_config& c) {
   };
   const size_t T = c.T, E = c.E, d = c.d_model, E64 = e64_of(c.E), T64 = t64_of(c.T);
   L.status = take(sizeof(DevStatus));
+  L.counter = take(sizeof(int));
   if (c.dtype == MOE_DTYPE_BF16) {
     L.splits = dw_splits(c);
     L.dg16 = take(T * E64 * 2);
@@ -680,6 +774,7 @@ int moe_router_backward(const moe_config* c, const void* x, const void* w_gate,
     a.d_logits = d_logits;
     a.dg16 = d_x ? at_bw<__nv_bfloat16>(ws, L.dg16) : nullptr;
     a.dgT = at_bw<__nv_bfloat16>(ws, L.dgT);
+    a.tile_counter = at_bw<int>(ws, L.counter);
   } else {
     dg32 = d_logits ? d_logits : at_bw<float>(ws, L.dg32);
     a.d_logits = dg32;
@@ -697,26 +792,52 @@ int moe_router_backward(const moe_config* c, const void* x, const void* w_gate,
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
   }
 
-  // dW_gate = dg^T x: M = d (x MN-major), N = E64 (dg^T K-major), K = T
-  CUtensorMap ma, mb;
-  if (!tc::make_map_box(&ma, x, (uint64_t)T, (uint64_t)d, 64) ||
-      !tc::make_map_strided(&mb, a.dgT, (uint64_t)E64, (uint64_t)T, (uint64_t)T64, E64))
+  // One launch for both gradient GEMMs (tiles handed out by a counter, dW's first):
+  //   dW_gate = dg^T x: M = d (x MN-major), N = E64 (dg^T K-major), K = T, split along K
+  //   dx = dg W_gate:   M = T (dg K-major), N = 256 (or 128) columns of d (W_gate MN-major),
+  //                     K = E64
+  CUtensorMap ma[2], mb[2], mo[2];
+  rg::Params p[2] = {};
+  if (!tc::make_map_box(&ma[0], x, (uint64_t)T, (uint64_t)d, 64) ||
+      !tc::make_map_strided(&mb[0], a.dgT, (uint64_t)E64, (uint64_t)T, (uint64_t)T64, E64))
     return MOE_ERR_CUDA;
-  rg::Params p{};
-  p.M = d;
-  p.N = E64;
-  p.KB = ceil_div(T, rg::BK);
-  p.a_mn = 1;
-  p.b_mn = 0;
-  p.m_tiles = d / rg::BM;
-  p.n_tiles = 1;
-  p.splits = L.splits;
-  p.out_mode = 1;
-  p.ldo = d;
-  p.n_valid = E;
-  p.st = dst;
-  p.out = L.splits > 1 ? at_bw<float>(ws, L.part) : d_w_gate;
-  e = rg::launch(ma, mb, mb, p, s);   // transposed-partial mode: no store map
+  mo[0] = mb[0];                      // transposed-partial mode: no store map
+  p[0].M = d;
+  p[0].N = E64;
+  p[0].KB = ceil_div(T, rg::BK);
+  p[0].a_mn = 1;
+  p[0].b_mn = 0;
+  p[0].m_tiles = d / rg::BM;
+  p[0].n_tiles = 1;
+  p[0].splits = L.splits;
+  p[0].out_mode = 1;
+  p[0].ldo = d;
+  p[0].n_valid = E;
+  p[0].st = dst;
+  p[0].out = L.splits > 1 ? at_bw<float>(ws, L.part) : d_w_gate;
+  int njobs = 1;
+  if (d_x) {
+    const int bn = d % 256 == 0 ? 256 : 128;
+    if (!tc::make_map_box(&ma[1], a.dg16, (uint64_t)T, (uint64_t)E64, 128) ||
+        !tc::make_map_box(&mb[1], w_gate, (uint64_t)E, (uint64_t)d, 64) ||
+        !tc::make_map_f32_store(&mo[1], d_x, (uint64_t)T, (uint64_t)d))
+      return MOE_ERR_CUDA;
+    p[1].M = T;
+    p[1].N = bn;
+    p[1].KB = E64 / rg::BK;
+    p[1].a_mn = 0;
+    p[1].b_mn = 1;
+    p[1].m_tiles = ceil_div(T, rg::BM);
+    p[1].n_tiles = d / bn;
+    p[1].splits = 1;
+    p[1].out = d_x;
+    p[1].out_mode = 0;
+    p[1].ldo = d;
+    p[1].n_valid = d;
+    p[1].st = dst;
+    njobs = 2;
+  }
+  e = rg::launch(ma, mb, mo, p, njobs, at_bw<int>(ws, L.counter), s);
   if (e == cudaSuccess && L.splits > 1) {
     const long long n4 = (long long)E * d / 4;
     launch_pdl(splitk_reduce_kernel, num_sms() * 4, 256, 0, s, at_bw<const float4>(ws, L.part),
@@ -725,33 +846,6 @@ int moe_router_backward(const moe_config* c, const void* x, const void* w_gate,
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-
-  // dx = dg W_gate: M = T (dg K-major), N = 256 (or 128) columns of d (W_gate MN-major), K = E64
-  if (d_x) {
-    const int bn = d % 256 == 0 ? 256 : 128;
-    CUtensorMap mx2, mw2;
-    if (!tc::make_map_box(&mx2, a.dg16, (uint64_t)T, (uint64_t)E64, 128) ||
-        !tc::make_map_box(&mw2, w_gate, (uint64_t)E, (uint64_t)d, 64))
-      return MOE_ERR_CUDA;
-    CUtensorMap mo;
-    if (!tc::make_map_f32_store(&mo, d_x, (uint64_t)T, (uint64_t)d)) return MOE_ERR_CUDA;
-    rg::Params q{};
-    q.M = T;
-    q.N = bn;
-    q.KB = E64 / rg::BK;
-    q.a_mn = 0;
-    q.b_mn = 1;
-    q.m_tiles = ceil_div(T, rg::BM);
-    q.n_tiles = d / bn;
-    q.splits = 1;
-    q.out = d_x;
-    q.out_mode = 0;
-    q.ldo = d;
-    q.n_valid = d;
-    q.st = dst;
-    e = rg::launch(mx2, mw2, mo, q, s);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-  }
   return MOE_OK;
 }
 
