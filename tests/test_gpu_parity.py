@@ -429,13 +429,17 @@ PAIR_CASES = {
     "rows1024": dict(name="mixtral", T=2048, d=256, E=4, k=2, F=384),
     # few rows per expert (pairs with an empty half), several N tiles in both GEMMs
     "rows_small": dict(name="mixtral", T=300, d=512, E=8, k=2, F=256),
+    # ~256 rows per expert under the selection bias: last pair tiles of <= 128 rows (M = 128
+    # pair MMAs) beside ones of 129..255 rows (M = 256, padded)
+    "rows256": dict(name="v3", T=512, d=256, E=16, k=8, F=256, n_shared=0),
 }
 
 
-@pytest.mark.parametrize("kernel", ["single", "pair"])
+@pytest.mark.parametrize("kernel", ["single", "pair", "pair_m256_only"])
 @pytest.mark.parametrize("case", sorted(PAIR_CASES))
 def test_expert_gemm_kernels(case, kernel, monkeypatch):
-    monkeypatch.setenv("MOE_B300_GEMM", kernel)
+    monkeypatch.setenv("MOE_B300_GEMM", "single" if kernel == "single" else "pair")
+    monkeypatch.setenv("MOE_B300_PAIR_HALF", "0" if kernel == "pair_m256_only" else "1")
     m = U.lib()
     spec = dict(PAIR_CASES[case])
     wl = moe_inputs.workload(spec.pop("name"), **spec)

@@ -121,6 +121,48 @@ def test_fp8_layer_error_against_bf16_layer(case):
     assert 0.01 < rel < 0.10, rel
 
 
+@pytest.mark.parametrize("case", [dict(name="v3", T=24, d=128, E=16, F=128, F_shared=128),
+                                  dict(name="mixtral", T=20, d=128, E=8, F=256,
+                                       capacity_factor=1.0)])
+def test_fp8_layer_is_the_layer_on_dequantised_operands(case):
+    """The FP8 layer is the plain layer evaluated on dequantised operands: x quantised per
+    token, every weight row per row, h (rounded to float32) per row before the down product.
+    Composed here with numpy products from the row quantiser alone (pinned above against
+    torch's E4M3 conversion), so a scale applied twice, or to the wrong axis, or an operand
+    left unquantised, moves the output by whole quantisation steps."""
+    wl, h = _small(**case)
+    wq = O.fp8_expert_weights(h["w13"], h["w2"], h["ws13"], h["ws2"])
+    got, r = O.moe_forward_fp8(wl, h["x"], h["w_gate"], h["bias"], wq)
+    xc, xs = O.quantize_rows_fp8(h["x"].astype(np.float32))
+    xq = xc * xs[:, None]
+
+    def ffn(rows, W13, W2):
+        F = W13.shape[0] // 2
+        a, b = rows @ W13[:F].T, rows @ W13[F:].T
+        hh = (a / (1.0 + np.exp(-a)) * b).astype(np.float32)
+        hc, hs = O.quantize_rows_fp8(hh)
+        return (hc * hs[:, None]) @ W2.T
+
+    disp = O.dispatch(r["idx"], wl.E, O.capacity(wl.capacity_factor, wl.k, wl.T, wl.E))
+    want = np.zeros_like(got) if wq["ws13"] is None else ffn(xq, wq["ws13"], wq["ws2"])
+    n_routed = 0
+    for t in range(wl.T):
+        for j in range(wl.k):
+            if disp["row_of"][t, j] >= 0:
+                e = int(r["idx"][t, j])
+                want[t] += r["w"][t, j] * ffn(xq[t:t + 1], wq["w13"][e], wq["w2"][e])[0]
+                n_routed += 1
+    assert n_routed > 0
+    if wl.capacity_factor:
+        assert disp["n_dropped"] > 0 or n_routed == wl.T * wl.k
+    scale = np.sqrt(np.mean(want ** 2))
+    assert np.max(np.abs(got - want)) <= 1e-9 * scale
+    # and it is not the unquantised layer: the comparison above resolves quantisation steps
+    plain = O.moe_forward(wl, h["x"], h["w_gate"], h["bias"], h["w13"], h["w2"], h["ws13"],
+                          h["ws2"])["out"]
+    assert np.max(np.abs(plain - want)) > 1e-3 * scale
+
+
 def test_fp8_layer_token_subset_matches_full():
     wl, h = _small("v3", T=24, d=128, E=16, F=128, F_shared=128)
     wq = O.fp8_expert_weights(h["w13"], h["w2"], h["ws13"], h["ws2"])

@@ -9,14 +9,21 @@
 // traffic.  Both CTAs' loads complete on the leader CTA's barrier; the leader issues the MMAs
 // and its commits arrive on both CTAs' barriers; each CTA drains its own 128 accumulator rows.
 //
-// A pair tile is 256 rows of one expert; an expert with an odd number of 128-row blocks pays
-// one block of padding, so the host uses this kernel when experts average >= 512 rows.
+// A pair tile is 256 rows of one expert.  With `half128` set, an expert's last pair tile of at
+// most 128 rows runs as an M = 128 pair MMA instead: 64 rows per CTA, the same halved B
+// traffic, and the padding of a 128-row tile.  Each CTA's accumulator then holds its 64 rows
+// twice over the lanes: row i's first N/2 columns in TMEM lane i, its last N/2 columns in lane
+// 64 + i, both at TMEM columns 0 .. N/2-1.  For SwiGLU each CTA's B half is therefore 64 gate
+// rows followed by the 64 matching up rows, so that one thread holds gate and up of the same
+// 64 output columns.
 //
 // Every wait is bounded.  On expiry a CTA raises its own and its peer's abort flags and
 // records MOE_ERR_TIMEOUT; the pair then stops, the leader reconciles and waits for every
 // load still in flight to either CTA's shared memory, waits for its MMAs, and both CTAs free
 // TMEM and return.
 #include <cuda.h>
+#include <cstdlib>
+#include <cstring>
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -56,6 +63,7 @@ struct Params {
   void* out;
   int out_f32;
   int ldo;
+  int half128;              // an expert's last tile of <= 128 rows runs as an M = 128 pair
   DevStatus* st;
 };
 
@@ -196,7 +204,8 @@ __device__ __forceinline__ PairTile decode_pair(int tile, const Params& p, const
 
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
-                            const __grid_constant__ CUtensorMap tmB, const Params p) {
+                            const __grid_constant__ CUtensorMap tmB,
+                            const __grid_constant__ CUtensorMap tmB64, const Params p) {
   pdl_prologue();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -265,7 +274,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = true;
     for (int tile = cid; ok && tile < total; tile += ncl) {
       const PairTile ti = decode_pair(tile, p, prefix);
-      const int a_row = ti.row0 + static_cast<int>(rank) * BM;
+      // M = 128 pair tiles take 64 rows per CTA (the box still loads 128; the MMA reads 64)
+      const bool half = p.half128 && ti.rows <= BM;
+      const int a_row = ti.row0 + static_cast<int>(rank) * (half ? 64 : BM);
+      // SwiGLU M = 128: gate rows 64*rank .. +63 of the N tile, then the matching up rows
+      const int g_row = ti.e * p.b_rows + ti.nt * 128 + static_cast<int>(rank) * 64;
+      const bool split_b = half && p.swiglu;
       const int b_row = p.swiglu
                             ? ti.e * p.b_rows + ti.nt * 128 + (rank ? p.up_off : 0)
                             : ti.e * p.b_rows + ti.nt * 256 + static_cast<int>(rank) * 128;
@@ -278,7 +292,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t fb = full_leader0 + 8 * stage;
         const uint32_t sa = smem_u32(stage_mem + stage * STAGE);
         tma_load_2d_pair(sa, &tmA, fb, kb * BK, a_row);
-        tma_load_2d_pair(sa + A_STAGE, &tmB, fb, kb * BK, b_row);
+        if (split_b) {
+          tma_load_2d_pair(sa + A_STAGE, &tmB64, fb, kb * BK, g_row);
+          tma_load_2d_pair(sa + A_STAGE + B_STAGE / 2, &tmB64, fb, kb * BK, g_row + p.up_off);
+        } else {
+          tma_load_2d_pair(sa + A_STAGE, &tmB, fb, kb * BK, b_row);
+        }
         issued[stage] += 1;
         if (++stage == STAGES) {
           stage = 0;
@@ -288,11 +307,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == 1 && lane == 0 && leader) {
     // ------------------------------- MMA issuer (leader only) -------------------------------
-    const uint32_t idesc = idesc_bf16_f32(PM, 256);
+    const uint32_t idesc_full = idesc_bf16_f32(PM, 256);
+    const uint32_t idesc_half = idesc_bf16_f32(BM, 256);
     int stage = 0, acc = 0;
     uint32_t ph = 0, aph = 0;
     bool ok = true;
     for (int tile = cid; ok && tile < total; tile += ncl) {
+      const int rows = decode_pair(tile, p, prefix).rows;
+      const uint32_t idesc = p.half128 && rows <= BM ? idesc_half : idesc_full;
       if (!wait_pair(tempty0 + 8 * acc, aph ^ 1u, abort_flag, peer_flag, p.st, 12, true)) {
         ok = false;
         break;
@@ -341,16 +363,25 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const uint32_t tb = tmem_base + static_cast<uint32_t>(acc * 256) +
                           (static_cast<uint32_t>(q * 32) << 16);
-      const int row_in_pair = static_cast<int>(rank) * BM + r;
+      // M = 128 pair tile: warp q holds rows 32 (q & 1) + lane of this CTA's 64, and the
+      // (q >> 1)-th half of the tile's columns at TMEM columns 0 .. 127
+      const bool half = p.half128 && ti.rows <= BM;
+      const int hq = half ? (q >> 1) : 0;
+      const int row_in_pair = half ? static_cast<int>(rank) * 64 + 32 * (q & 1) + lane
+                                   : static_cast<int>(rank) * BM + r;
       const bool live = row_in_pair < ti.rows;
       const size_t grow = static_cast<size_t>(ti.row0 + row_in_pair);
       if (p.swiglu) {
-        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo + ti.nt * 128;
+        // gate column j at TMEM column j, up at j + 128 (M = 128: 64 columns, up at j + 64)
+        __nv_bfloat16* orow =
+            static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo + ti.nt * 128 + hq * 64;
+        const int nch = half ? 2 : 4;
+        const uint32_t up = half ? 64 : 128;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < nch; ++c) {
           uint32_t gr[32], ur[32];
           tmem_ld32(tb + c * 32, gr);
-          tmem_ld32(tb + 128 + c * 32, ur);
+          tmem_ld32(tb + up + c * 32, ur);
           uint32_t packed[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -370,9 +401,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       } else if (p.out_f32) {
-        float* orow = static_cast<float*>(p.out) + grow * p.ldo + ti.nt * 256;
+        float* orow = static_cast<float*>(p.out) + grow * p.ldo + ti.nt * 256 + hq * 128;
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < (half ? 4 : 8); ++c) {
           uint32_t vr[32];
           tmem_ld32(tb + c * 32, vr);
           if (live) {
@@ -383,9 +414,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       } else {
-        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo + ti.nt * 256;
+        __nv_bfloat16* orow =
+            static_cast<__nv_bfloat16*>(p.out) + grow * p.ldo + ti.nt * 256 + hq * 128;
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < (half ? 4 : 8); ++c) {
           uint32_t vr[32];
           tmem_ld32(tb + c * 32, vr);
           uint32_t packed[16];
@@ -443,8 +475,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 }  // namespace tc2
 
 // Pair kernel for one GEMM; `b_rows`, `n_tiles` etc. follow tc2::Params.
-cudaError_t launch_tc2(const CUtensorMap& a, const CUtensorMap& b, const tc2::Params& p,
-                       int upper_pair_tiles, cudaStream_t s) {
+cudaError_t launch_tc2(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b64,
+                       const tc2::Params& p, int upper_pair_tiles, cudaStream_t s) {
   using namespace tc2;
   cudaError_t e0 = smem_attr_once(reinterpret_cast<const void*>(grouped_gemm_tc2_kernel),
                                   static_cast<int>(SMEM_BYTES));
@@ -466,15 +498,22 @@ cudaError_t launch_tc2(const CUtensorMap& a, const CUtensorMap& b, const tc2::Pa
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_tc2_kernel, a, b, p);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_tc2_kernel, a, b, b64, p);
+}
+
+// M = 128 pair tiles for an expert's last <= 128 rows: on unless MOE_B300_PAIR_HALF=0.
+static int pair_half128() {
+  const char* env = getenv("MOE_B300_PAIR_HALF");
+  return (env && strcmp(env, "0") == 0) ? 0 : 1;
 }
 
 // Both SwiGLU GEMMs on CTA pairs.  Requires F % 128 == 0 and d % 256 == 0.
 cudaError_t launch_ffn_tc2(const GroupedFFN& g, DevStatus* st, cudaStream_t s) {
   using namespace tc2;
-  CUtensorMap mx, mw13, mh, mw2;
+  CUtensorMap mx, mw13, mw13_64, mh, mw2;
   if (!tc::make_map(&mx, g.x, (uint64_t)g.max_rows, (uint64_t)g.d) ||
       !tc::make_map(&mw13, g.w13, (uint64_t)g.E * 2 * g.F, (uint64_t)g.d) ||
+      !tc::make_map_box(&mw13_64, g.w13, (uint64_t)g.E * 2 * g.F, (uint64_t)g.d, 64) ||
       !tc::make_map(&mh, g.h, (uint64_t)g.max_rows, (uint64_t)g.F) ||
       !tc::make_map(&mw2, g.w2, (uint64_t)g.E * g.d, (uint64_t)g.F))
     return cudaErrorInvalidValue;
@@ -492,8 +531,9 @@ cudaError_t launch_ffn_tc2(const GroupedFFN& g, DevStatus* st, cudaStream_t s) {
   p1.out = g.h;
   p1.out_f32 = 0;
   p1.ldo = g.F;
+  p1.half128 = pair_half128();
   p1.st = st;
-  cudaError_t err = launch_tc2(mx, mw13, p1, pt_upper * p1.n_tiles, s);
+  cudaError_t err = launch_tc2(mx, mw13, mw13_64, p1, pt_upper * p1.n_tiles, s);
   if (err != cudaSuccess) return err;
   Params p2 = p1;
   p2.K = g.F;
@@ -504,7 +544,7 @@ cudaError_t launch_ffn_tc2(const GroupedFFN& g, DevStatus* st, cudaStream_t s) {
   p2.out = g.y;
   p2.out_f32 = g.y_bf16 ? 0 : 1;
   p2.ldo = g.d;
-  return launch_tc2(mh, mw2, p2, pt_upper * p2.n_tiles, s);
+  return launch_tc2(mh, mw2, mw2, p2, pt_upper * p2.n_tiles, s);
 }
 
 }  // namespace moe
