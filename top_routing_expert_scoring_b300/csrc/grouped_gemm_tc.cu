@@ -490,8 +490,10 @@ __global__ void __launch_bounds__(ROUTE ? THREADS_ROUTE : THREADS, 1)
     uint32_t aph = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
       const TileInfo ti = decode_tile(tile, p, sc, total, split);
+      // one thread waits for the accumulator; the barrier below releases the other 511
       uint32_t ok = 1;
-      if (lane == 0) ok = wait_bounded(tfull0 + 8 * acc, aph, abort_flag, p.st, 4, true) ? 1 : 0;
+      if (warp == 2 && lane == 0)
+        ok = wait_bounded(tfull0 + 8 * acc, aph, abort_flag, p.st, 4, true) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       uint32_t all_ok;
       asm volatile(

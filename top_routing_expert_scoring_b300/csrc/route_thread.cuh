@@ -38,20 +38,23 @@ struct RouteThreadCfg {
   int select;         // 1: choose experts and weights; 0: statistics only (given selection)
 };
 
-// Shared memory of the phases for one tile of 128 tokens.
+// Shared memory of the phases for one tile of 128 tokens.  The token slot is the innermost
+// index everywhere, so the 32 lanes of a warp (32 consecutive slots) touch 32 consecutive words.
 struct RouteSmem {
   float bias[256];
-  float stat[kRouteTile][kRouteSubs][3];          // per thread part: max, exp-sum, sigmoid-sum
-  float ctop[kRouteTile][kRouteMaxChunks][2];     // per chunk: two largest keys
-  float ckey[kRouteTile][kRouteSubs][kRouteMaxK]; // per thread part: its top-k list
-  int cidx[kRouteTile][kRouteSubs][kRouteMaxK];
-  float cval[kRouteTile][kRouteSubs][kRouteMaxK];
+  float stat[kRouteSubs][3][kRouteTile];          // per thread part: max, exp-sum, sigmoid-sum
+  float ctop[kRouteMaxChunks][2][kRouteTile];     // per chunk: two largest keys
+  float ckey[kRouteSubs][kRouteMaxK][kRouteTile]; // per thread part: its top-k list
+  int cidx[kRouteSubs][kRouteMaxK][kRouteTile];
+  float cval[kRouteSubs][kRouteMaxK][kRouteTile];
   float P[4][256];                                // per TMEM lane quarter: column sums
   int cnt[256];
   float Z[4];
 };
 
-__device__ __forceinline__ float sigm(float g) { return 1.0f / (1.0f + expf(-g)); }
+// 1 / (1 + e^-g); __frcp_rn is the correctly rounded reciprocal, the same bits as the
+// division 1.0f / x, without its general-divisor path
+__device__ __forceinline__ float sigm(float g) { return __frcp_rn(1.0f + expf(-g)); }
 
 __device__ __forceinline__ void route_chunk_range(const RouteThreadCfg& rc, int sub, int& c0,
                                                   int& c1) {
@@ -139,12 +142,12 @@ __device__ __forceinline__ void route_phase_a(const RouteThreadCfg& rc, RouteSme
         }
       }
     }
-    sm.ctop[r][c][0] = a;
-    sm.ctop[r][c][1] = b;
+    sm.ctop[c][0][r] = a;
+    sm.ctop[c][1][r] = b;
   }
-  sm.stat[r][sub][0] = m;
-  sm.stat[r][sub][1] = se;
-  sm.stat[r][sub][2] = ss;
+  sm.stat[sub][0][r] = m;
+  sm.stat[sub][1][r] = se;
+  sm.stat[sub][2][r] = ss;
 }
 
 // The token's max, exp-sum and sigmoid-sum from the four parts, in thread order.
@@ -154,12 +157,12 @@ struct RouteTotals {
 __device__ __forceinline__ RouteTotals route_totals(const RouteSmem& sm, int r) {
   RouteTotals t{-INFINITY, 0.f, 0.f};
 #pragma unroll
-  for (int s = 0; s < kRouteSubs; ++s) t.m = fmaxf(t.m, sm.stat[r][s][0]);
+  for (int s = 0; s < kRouteSubs; ++s) t.m = fmaxf(t.m, sm.stat[s][0][r]);
 #pragma unroll
   for (int s = 0; s < kRouteSubs; ++s) {
-    const float ms = sm.stat[r][s][0];
-    if (ms != -INFINITY) t.se += sm.stat[r][s][1] * expf(ms - t.m);
-    t.ss += sm.stat[r][s][2];
+    const float ms = sm.stat[s][0][r];
+    if (ms != -INFINITY) t.se += sm.stat[s][1][r] * expf(ms - t.m);
+    t.ss += sm.stat[s][2][r];
   }
   return t;
 }
@@ -181,7 +184,7 @@ __device__ __forceinline__ void route_phase_b(const RouteThreadCfg& rc, RouteSme
     for (int g = 0; g < ng; ++g) {
       float a = -INFINITY, b = -INFINITY;        // two largest over the group's chunks
       for (int c = g * rc.cpg; c < (g + 1) * rc.cpg; ++c) {
-        const float x1 = sm.ctop[r][c][0], x2 = sm.ctop[r][c][1];
+        const float x1 = sm.ctop[c][0][r], x2 = sm.ctop[c][1][r];
         if (x1 > a) {
           b = fmaxf(a, x2);
           a = x1;
@@ -232,9 +235,9 @@ __device__ __forceinline__ void route_phase_b(const RouteThreadCfg& rc, RouteSme
   }
 #pragma unroll
   for (int j = 0; j < kRouteMaxK; ++j) {
-    sm.ckey[r][sub][j] = bk[j];
-    sm.cidx[r][sub][j] = bi[j];
-    sm.cval[r][sub][j] = bv[j];
+    sm.ckey[sub][j][r] = bk[j];
+    sm.cidx[sub][j][r] = bi[j];
+    sm.cval[sub][j][r] = bv[j];
   }
 }
 
@@ -249,17 +252,17 @@ __device__ __forceinline__ float route_phase_c(const RouteThreadCfg& rc, const R
   int bi[kRouteMaxK];
 #pragma unroll
   for (int j = 0; j < kRouteMaxK; ++j) {
-    bk[j] = sm.ckey[r][0][j];
-    bi[j] = sm.cidx[r][0][j];
-    bv[j] = sm.cval[r][0][j];
+    bk[j] = sm.ckey[0][j][r];
+    bi[j] = sm.cidx[0][j][r];
+    bv[j] = sm.cval[0][j][r];
   }
 #pragma unroll 1
   for (int s = 1; s < kRouteSubs; ++s) {
     for (int j = 0; j < kRouteMaxK; ++j) {      // each list is sorted: stop at its first miss
-      const float key = sm.ckey[r][s][j];
-      const int e = sm.cidx[r][s][j];
+      const float key = sm.ckey[s][j][r];
+      const int e = sm.cidx[s][j][r];
       if (!ranks_before(key, e, bk[kRouteMaxK - 1], bi[kRouteMaxK - 1])) break;
-      topk_insert(key, e, sm.cval[r][s][j], bk, bi, bv);
+      topk_insert(key, e, sm.cval[s][j][r], bk, bi, bv);
     }
   }
   float num[kRouteMaxK], den = 0.f;
