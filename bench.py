@@ -494,7 +494,8 @@ def router_backward_sweep(args):
 def router_in_gemm(wl):
     """The library's rule for running scoring and Top-k in the router GEMM's epilogue: a bf16
     token-choice router with E a multiple of 32 up to 256, k <= 8, more than 512 tokens, and
-    groups (if limited) of whole 32-expert chunks; MOE_B300_ROUTER=separate turns it off."""
+    groups (if limited) of whole 32-expert chunks; by default only from 128 experts up.
+    MOE_B300_ROUTER=fused takes it for every such router, =separate for none."""
     if wl.dtype != "bf16" or wl.routing != "token_choice":
         return False
     if wl.E < 32 or wl.E > 256 or wl.E % 32 or wl.k > 8 or wl.T <= 512:
@@ -502,7 +503,10 @@ def router_in_gemm(wl):
     limit = wl.score == "sigmoid" and wl.n_groups > 1 and wl.topk_groups < wl.n_groups
     if limit and (wl.E // wl.n_groups) % 32:
         return False
-    return os.environ.get("MOE_B300_ROUTER") != "separate"
+    env = os.environ.get("MOE_B300_ROUTER")
+    if env in ("fused", "separate"):
+        return env == "fused"
+    return wl.E >= 128
 
 
 def launches_per_step(wl):

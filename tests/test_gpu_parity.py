@@ -122,8 +122,16 @@ SMALL = {
 }
 
 
+def _router_env(case, monkeypatch):
+    """The router_fused_* cases take the router GEMM with the routing epilogue whatever their E
+    (by default only routers of >= 128 experts do)."""
+    if case.startswith("router_fused_"):
+        monkeypatch.setenv("MOE_B300_ROUTER", "fused")
+
+
 @pytest.mark.parametrize("case", sorted(SMALL))
-def test_small_layer_parity(case):
+def test_small_layer_parity(case, monkeypatch):
+    _router_env(case, monkeypatch)
     spec = dict(SMALL[case])
     wl = moe_inputs.workload(spec.pop("name"), **spec)
     inp = _inputs(wl)
@@ -542,10 +550,11 @@ def test_forward_replays_in_a_cuda_graph():
 
 @pytest.mark.parametrize("case", ["v3_like", "softmax_cap", "decode_b8", "router_fused_v3_e256",
                                   "router_fused_e96_tail", "router_fused_two_tiles_per_cta"])
-def test_forward_timed_and_fused_statistics(case):
+def test_forward_timed_and_fused_statistics(case, monkeypatch):
     # moe_forward_timed runs moe_forward's kernels (identical output) and brackets the expert
     # GEMMs with the caller's events; the statistics moe_forward fuses into its Top-k pass
     # equal moe_aux_stats on the same logits and selection bit for bit
+    _router_env(case, monkeypatch)
     m = U.lib()
     spec = dict(SMALL[case])
     wl = moe_inputs.workload(spec.pop("name"), **spec)
@@ -663,10 +672,7 @@ def test_router_epilogue_matches_separate_passes(case, monkeypatch):
     T, E, k = wl.T, wl.E, wl.k
     runs = {}
     for mode in ("fused", "separate"):
-        if mode == "separate":
-            monkeypatch.setenv("MOE_B300_ROUTER", "separate")
-        else:
-            monkeypatch.delenv("MOE_B300_ROUTER", raising=False)
+        monkeypatch.setenv("MOE_B300_ROUTER", mode)
         ws = m.workspace(cfg)
         logits = torch.empty((T, E), dtype=torch.float32, device=DEV)
         idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
@@ -684,7 +690,7 @@ def test_router_epilogue_matches_separate_passes(case, monkeypatch):
     same = (i_f == i_s).all(axis=1)
     assert (same | near).all()
     assert np.abs(w_f[same] - w_s[same]).max() <= U.WEIGHT_ATOL
-    monkeypatch.delenv("MOE_B300_ROUTER", raising=False)
+    monkeypatch.setenv("MOE_B300_ROUTER", "fused")
     fwd = U.run_forward(wl, inp, cfg)
     assert (fwd["idx"] == i_f).all() and (fwd["w"] == w_f.astype(np.float64)).all()
 
