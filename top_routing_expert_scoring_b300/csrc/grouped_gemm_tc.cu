@@ -802,10 +802,12 @@ static bool use_pair_kernel(const GroupedFFN& g) {
   const char* env = getenv("MOE_B300_GEMM");
   if (env && strcmp(env, "single") == 0) return false;
   if (env && strcmp(env, "pair") == 0) return true;
-  // One group (shared experts): pairs carry no padding and run ~4% faster.  Ragged groups pay
-  // on average half a 128-row block per expert for 256-row pair tiles, so pairs only win once
-  // experts average >= 2048 rows.
-  if (g.uniform_rows >= 0) return g.uniform_rows >= 512;
+  // One group (shared experts): measured on the DeepSeekMoE-16B layer (two shared experts,
+  // T = 8192) the single-CTA kernel makes the step 1% faster (its last partial wave runs as
+  // N = 128 halves; the pair kernel's down GEMM has 3.5 waves of pair tiles), and on the V3
+  // layer the two are within noise.  Ragged groups pay on average half a 128-row block per
+  // expert for 256-row pair tiles, so pairs only win once experts average >= 2048 rows.
+  if (g.uniform_rows >= 0) return false;
   return (long long)g.max_rows / g.E >= 2048;
 }
 
