@@ -274,6 +274,40 @@ def test_expert_choice_entry_point():
     assert (rows.cpu().numpy() == csr["rows"]).all()
 
 
+@pytest.mark.parametrize("T", [777, 50000])
+@pytest.mark.parametrize("kind", ["normal", "few_levels"])
+def test_expert_choice_selection_on_given_logits(T, kind):
+    # the selection alone, bit for bit against the oracle: T = 777 keeps the expert's keys in
+    # shared memory, T = 50000 reads them from global memory in every radix pass; "few_levels"
+    # logits take 7 values only, so each expert's C-th key is tied with thousands of tokens and
+    # the lowest token indices must win
+    m = U.lib()
+    E, k = 16, 2
+    wl = moe_inputs.workload("dsmoe16b_ec", T=T, d=256, E=E, k=k, F=256, F_shared=128)
+    cfg = U.config_of(wl)
+    rng = np.random.default_rng(11 + T)
+    if kind == "normal":
+        g32 = rng.standard_normal((T, E)).astype(np.float32)
+    else:
+        g32 = rng.integers(-3, 4, size=(T, E)).astype(np.float32)
+    C = T * k // E
+    ws = m.workspace(cfg)
+    logits = torch.from_numpy(g32).to(DEV)
+    tok = torch.empty((E, C), dtype=torch.int32, device=DEV)
+    tw = torch.empty((E, C), dtype=torch.float32, device=DEV)
+    ptr = torch.empty(T + 1, dtype=torch.int32, device=DEV)
+    rows = torch.empty(E * C, dtype=torch.int32, device=DEV)
+    m.moe_expert_choice(cfg, logits, tok, tw, ptr, rows, ws)
+    torch.cuda.synchronize()
+    assert m.sync_status(ws) == 0
+    tokens, weights, _ = O.expert_choice_route(g32, k)
+    csr = O.expert_choice_csr(tokens, T)
+    assert (tok.cpu().numpy() == tokens).all()
+    assert np.abs(tw.cpu().numpy() - weights).max() <= U.WEIGHT_ATOL
+    assert (ptr.cpu().numpy() == csr["ptr"]).all()
+    assert (rows.cpu().numpy() == csr["rows"]).all()
+
+
 # ---------------------------------------------------------------------------------------------
 # failure paths (no fault: bounded waits and argument checks)
 # ---------------------------------------------------------------------------------------------

@@ -72,10 +72,18 @@ __global__ void __launch_bounds__(256) dispatch_scan_kernel(int32_t* __restrict_
   const int e = threadIdx.x;
   int total = 0;
   if (e < E) {
-    for (int b = 0; b < nblk; ++b) {
-      const int c = blk_cnt[(size_t)b * E + e];
-      blk_cnt[(size_t)b * E + e] = total;
-      total += c;
+    // 16 blocks' counts in flight at a time, then their exclusive bases in block order
+    constexpr int kBatch = 16;
+    for (int b0 = 0; b0 < nblk; b0 += kBatch) {
+      int c[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j)
+        c[j] = b0 + j < nblk ? blk_cnt[(size_t)(b0 + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        if (b0 + j < nblk) blk_cnt[(size_t)(b0 + j) * E + e] = total;
+        total += c[j];
+      }
     }
   }
   const int kp = e < E ? min(total, capacity) : 0;

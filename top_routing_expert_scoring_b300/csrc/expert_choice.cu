@@ -3,8 +3,9 @@
 // in its column (ties -> lower token index).  The weight of a chosen (token, expert) pair is
 // the token's softmax probability of that expert.
 //
-//   K1  per expert (one CTA): radix select of the C-th largest key over the column, then the
-//       chosen tokens in ascending token order (block prefix sums, no atomics in the order);
+//   K1  per expert (one CTA): radix select of the C-th largest key over the column (kept in
+//       shared memory), then the chosen tokens in ascending token order (block prefix sums,
+//       no atomics in the order);
 //   K2  per token: how many experts chose it;  K3: exclusive scan -> tok_ptr;
 //   K4  per token: its rows e*C + i in ascending expert order (CSR used by the combine).
 #include "common.cuh"
@@ -13,6 +14,7 @@
 namespace moe {
 
 constexpr int kEcThreads = 1024;
+constexpr int kEcSmemT = 40960;        // tokens whose keys the selection keeps in shared memory
 
 __device__ __forceinline__ uint32_t orderable(float f) {
   if (f == 0.0f) f = 0.0f;                 // -0.0 ranks equal to +0.0
@@ -63,6 +65,45 @@ __global__ void __launch_bounds__(256) token_softmax_stats(const float* __restri
   if (lane == 0) ms[t] = make_float2(m, s);
 }
 
+// The bin of the 256-bin histogram `hist` that holds the `remaining`-th largest key, counting
+// from the top bin, and how many keys of that bin are still to be taken.  All threads call it;
+// the first 256 threads scan the bins from the top (a suffix sum) in parallel.
+__device__ __forceinline__ void ec_pick_bin(const int* hist, int remaining, int* s_scan,
+                                            int* s_sel) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int v = 0, incl = 0;
+  if (tid < 256) {
+    v = hist[255 - tid];                   // thread j holds bin 255 - j
+    incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_scan[warp] = incl;
+  }
+  __syncthreads();
+  if (tid < 256) {
+    int before = 0;
+    for (int w = 0; w < warp; ++w) before += s_scan[w];
+    incl += before;
+    // keys in bins above this one: incl - v; the wanted key lies here when they fall short
+    // of `remaining` and this bin reaches it (the lowest bin takes whatever is left)
+    const int above = incl - v;
+    if (above < remaining && (incl >= remaining || tid == 255)) {
+      s_sel[0] = 255 - tid;
+      s_sel[1] = remaining - above;
+    }
+  }
+  __syncthreads();
+}
+
+// Expert choice, one CTA per expert: the C largest keys of the expert's logit column (ties to
+// the lower token index) by a 4-pass radix select on the orderable bits, then the chosen
+// tokens in ascending token order.  With T <= kEcSmemT the column is read from global memory
+// once and kept in shared memory as keys; the histograms aggregate equal bins within a warp
+// (one shared atomic per distinct bin), since the top byte of the keys falls into few bins.
+template <bool CACHED>
 __global__ void __launch_bounds__(kEcThreads) ec_select_kernel(const float* __restrict__ g, int T,
                                                               int E, int C,
                                                               const float2* __restrict__ ms,
@@ -70,31 +111,35 @@ __global__ void __launch_bounds__(kEcThreads) ec_select_kernel(const float* __re
                                                               float* __restrict__ ec_w,
                                                               int32_t* __restrict__ posmap) {
   pdl_prologue();
+  extern __shared__ uint32_t s_keys[];     // [T] when CACHED
   __shared__ int hist[256];
   __shared__ int s_warp[64];
   __shared__ int s_sel[2];
   const int e = blockIdx.x;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
+  auto key_of = [&](int t) -> uint32_t {
+    return CACHED ? s_keys[t] : orderable(g[(size_t)t * E + e]);
+  };
+  if (CACHED) {
+    for (int t = tid; t < T; t += kEcThreads) s_keys[t] = orderable(g[(size_t)t * E + e]);
+  }
   uint32_t prefix = 0, mask = 0;
   int remaining = C;
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = tid; i < 256; i += kEcThreads) hist[i] = 0;
     __syncthreads();
-    for (int t = tid; t < T; t += kEcThreads) {
-      const uint32_t u = orderable(g[(size_t)t * E + e]);
-      if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 0xFFu], 1);
-    }
-    __syncthreads();
-    if (tid == 0) {
-      int acc = 0, b = 255;
-      for (; b > 0; --b) {
-        if (acc + hist[b] >= remaining) break;
-        acc += hist[b];
+    for (int base = 0; base < T; base += kEcThreads) {
+      const int t = base + tid;
+      int bin = -1;
+      if (t < T) {
+        const uint32_t u = key_of(t);
+        if ((u & mask) == prefix) bin = static_cast<int>((u >> shift) & 0xFFu);
       }
-      s_sel[0] = b;
-      s_sel[1] = remaining - acc;
+      const uint32_t same = __match_any_sync(0xffffffffu, bin);
+      if (bin >= 0 && lane == __ffs(same) - 1) atomicAdd(&hist[bin], __popc(same));
     }
     __syncthreads();
+    ec_pick_bin(hist, remaining, s_warp, s_sel);
     prefix |= static_cast<uint32_t>(s_sel[0]) << shift;
     mask |= 0xFFu << shift;
     remaining = s_sel[1];
@@ -105,7 +150,7 @@ __global__ void __launch_bounds__(kEcThreads) ec_select_kernel(const float* __re
   for (int base = 0; base < T; base += kEcThreads) {
     const int t = base + tid;
     uint32_t u = 0;
-    if (t < T) u = orderable(g[(size_t)t * E + e]);
+    if (t < T) u = key_of(t);
     const int is_eq = (t < T && u == prefix) ? 1 : 0;
     int eq_total;
     const int eq_rank = eq_before + block_exclusive_scan(is_eq, s_warp, eq_total);
@@ -139,13 +184,26 @@ __global__ void __launch_bounds__(kEcThreads) ec_scan_kernel(const int32_t* __re
                                                             int T, int32_t* __restrict__ ptr) {
   pdl_prologue();
   __shared__ int s_warp[64];
+  // each thread takes kPer consecutive tokens per round: their counts are loaded together,
+  // summed, and the block scan of the sums places each thread's run
+  constexpr int kPer = 8;
   int run = 0;
-  for (int base = 0; base < T; base += kEcThreads) {
-    const int t = base + threadIdx.x;
-    const int v = t < T ? cnt[t] : 0;
+  for (int base = 0; base < T; base += kEcThreads * kPer) {
+    const int t0 = base + threadIdx.x * kPer;
+    int v[kPer];
+    int sum = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      v[j] = t0 + j < T ? cnt[t0 + j] : 0;
+      sum += v[j];
+    }
     int tot;
-    const int ex = block_exclusive_scan(v, s_warp, tot);
-    if (t < T) ptr[t] = run + ex;
+    int ex = run + block_exclusive_scan(sum, s_warp, tot);
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      if (t0 + j < T) ptr[t0 + j] = ex;
+      ex += v[j];
+    }
     run += tot;
   }
   if (threadIdx.x == 0) ptr[T] = run;
@@ -172,7 +230,17 @@ cudaError_t launch_expert_choice(const moe_config& c, const float* logits, int32
   (void)st;
   const int C = (int)((long long)c.T * c.k / c.E);
   launch_pdl(token_softmax_stats, ceil_div(c.T * 32, 256), 256, 0, s, logits, c.T, c.E, ms);
-  launch_pdl(ec_select_kernel, c.E, kEcThreads, 0, s, logits, c.T, c.E, C, ms, ec_tokens, ec_w, posmap);
+  if (c.T <= kEcSmemT) {
+    const int smem = c.T * 4;
+    cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(ec_select_kernel<true>),
+                                   kEcSmemT * 4);
+    if (e != cudaSuccess) return e;
+    launch_pdl(ec_select_kernel<true>, c.E, kEcThreads, smem, s, logits, c.T, c.E, C, ms,
+               ec_tokens, ec_w, posmap);
+  } else {
+    launch_pdl(ec_select_kernel<false>, c.E, kEcThreads, 0, s, logits, c.T, c.E, C, ms,
+               ec_tokens, ec_w, posmap);
+  }
   launch_pdl(ec_count_kernel, ceil_div(c.T, 256), 256, 0, s, posmap, c.T, c.E, tok_cnt);
   launch_pdl(ec_scan_kernel, 1, kEcThreads, 0, s, tok_cnt, c.T, tok_ptr);
   launch_pdl(ec_fill_kernel, ceil_div(c.T, 256), 256, 0, s, posmap, c.T, c.E, C, tok_ptr, tok_rows);
