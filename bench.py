@@ -45,8 +45,8 @@ def load_peaks():
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the expert GEMM launches of
 # one step, keyed by (workload, T), from an ncu capture of the bench command on the current
 # kernel build; a workload without a capture on the current build reports null.
-GEMM_TRAFFIC_BYTES = {("v3", 8192): (16809521664 + 266929664) + (7863550720 + 929537024)
-                      + (517201408 + 27765504) + (76913152 + 184267008)}
+GEMM_TRAFFIC_BYTES = {("v3", 8192): (16824082688 + 266261504) + (7862229760 + 929332992)
+                      + (891870464 + 29169920) + (87099392 + 183482624)}
 
 
 def workload_flops_bytes(wl):
