@@ -518,10 +518,9 @@ bool route_cta(const moe_config& c) {
   return c.routing == MOE_ROUTE_TOKEN_CHOICE && c.E > 32 && c.T <= kRouteCtaMaxT;
 }
 
-// Prefill batches of a bf16 router with E a multiple of 32 (<= 256) and groups of whole 32-expert
-// chunks: the router GEMM's epilogue does the scoring, the Top-k and the statistics terms
-// (launch_router_fused), one partial row per 128-token tile.  MOE_B300_ROUTER=separate keeps
-// the logits GEMM and the Top-k pass apart.
+// Prefill batches of a bf16 router with E a multiple of 32 (<= 256, by default >= 128) and
+// groups of whole 32-expert chunks: the router GEMM's epilogue does the scoring, the Top-k and
+// the statistics terms (launch_router_fused), one partial row per 128-token tile.
 constexpr int kRouterFusedMinE = 128;
 
 bool router_fused(const moe_config& c) {
