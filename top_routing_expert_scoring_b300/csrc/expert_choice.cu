@@ -145,19 +145,63 @@ __global__ void __launch_bounds__(kEcThreads) ec_select_kernel(const float* __re
     remaining = s_sel[1];
     __syncthreads();
   }
-  // prefix = key of the C-th largest; `remaining` tokens equal to it are taken (lowest index)
-  int eq_before = 0, sel_before = 0;
-  for (int base = 0; base < T; base += kEcThreads) {
-    const int t = base + tid;
-    uint32_t u = 0;
-    if (t < T) u = key_of(t);
-    const int is_eq = (t < T && u == prefix) ? 1 : 0;
-    int eq_total;
-    const int eq_rank = eq_before + block_exclusive_scan(is_eq, s_warp, eq_total);
-    const int chosen = (t < T && (u > prefix || (is_eq && eq_rank < remaining))) ? 1 : 0;
-    int sel_total;
-    const int pos = sel_before + block_exclusive_scan(chosen, s_warp, sel_total);
-    if (t < T) {
+  // prefix = key of the C-th largest; `remaining` tokens equal to it are taken (lowest index).
+  // Warp w owns the contiguous token range [w * per, (w + 1) * per): it counts its keys above
+  // and equal to the prefix, one scan over the 32 warps places each warp's equal keys and
+  // chosen tokens, and each warp then writes its range in token order (ballot prefixes), so
+  // the chosen set and its order are those of a sequential walk over the tokens.
+  constexpr int kWarps = kEcThreads / 32;
+  __shared__ int s_eqb[kWarps], s_selb[kWarps];
+  const int warp = tid >> 5;
+  const int per = (T + kWarps - 1) / kWarps;
+  const int t_lo = warp * per, t_hi = min(T, t_lo + per);
+  int n_gt = 0, n_eq = 0;
+  for (int b = t_lo; b < t_hi; b += 32) {
+    const int t = b + lane;
+    const uint32_t u = t < t_hi ? key_of(t) : 0u;
+    n_gt += __popc(__ballot_sync(0xffffffffu, t < t_hi && u > prefix));
+    n_eq += __popc(__ballot_sync(0xffffffffu, t < t_hi && u == prefix));
+  }
+  if (lane == 0) {
+    s_eqb[warp] = n_eq;
+    s_selb[warp] = n_gt;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // equal keys before each warp, then the chosen count of each warp, both scanned in order
+    const int eq_w = s_eqb[lane];
+    int incl = eq_w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int eq_before = incl - eq_w;
+    const int take_eq = max(0, min(eq_w, remaining - eq_before));
+    const int sel_w = s_selb[lane] + take_eq;
+    int sincl = sel_w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, sincl, o);
+      if (lane >= o) sincl += y;
+    }
+    s_eqb[lane] = eq_before;
+    s_selb[lane] = sincl - sel_w;
+  }
+  __syncthreads();
+  int eq_seen = s_eqb[warp], pos_base = s_selb[warp];
+  const uint32_t below = (1u << lane) - 1u;
+  for (int b = t_lo; b < t_hi; b += 32) {
+    const int t = b + lane;
+    const bool live = t < t_hi;
+    const uint32_t u = live ? key_of(t) : 0u;
+    const bool is_eq = live && u == prefix;
+    const uint32_t eq_mask = __ballot_sync(0xffffffffu, is_eq);
+    const int eq_rank = eq_seen + __popc(eq_mask & below);
+    const bool chosen = live && (u > prefix || (is_eq && eq_rank < remaining));
+    const uint32_t ch_mask = __ballot_sync(0xffffffffu, chosen);
+    const int pos = pos_base + __popc(ch_mask & below);
+    if (live) {
       posmap[(size_t)e * T + t] = chosen ? pos : -1;
       if (chosen) {
         ec_tokens[(size_t)e * C + pos] = t;
@@ -165,8 +209,8 @@ __global__ void __launch_bounds__(kEcThreads) ec_select_kernel(const float* __re
         ec_w[(size_t)e * C + pos] = expf(g[(size_t)t * E + e] - st.x) / st.y;
       }
     }
-    eq_before += eq_total;
-    sel_before += sel_total;
+    eq_seen += __popc(eq_mask);
+    pos_base += __popc(ch_mask);
   }
 }
 
