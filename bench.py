@@ -768,6 +768,8 @@ def main():
     ap.add_argument("--backward-steps", type=int, default=50)
     ap.add_argument("--tokens", type=int, default=0,
                     help="override T (smaller cases for profiler captures; not a bench line)")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override E (smaller cases for profiler captures; not a bench line)")
     args = ap.parse_args()
 
     if args.decode_sweep:
@@ -786,6 +788,8 @@ def main():
     wl = moe_inputs.workload(args.workload)
     if args.tokens:
         wl = wl.replace(T=args.tokens)
+    if args.experts:
+        wl = wl.replace(E=args.experts)
     peaks, peak_kind = load_peaks()
     config = workload_config(wl, world)
 
