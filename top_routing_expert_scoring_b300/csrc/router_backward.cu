@@ -12,12 +12,14 @@
 //   1. router_bw_scores_kernel: one warp per token recomputes p (and s), lse and the chain rule
 //      of the scoring function in fp32; writes dL/dg as fp32 and, for the tensor-core GEMMs,
 //      as bf16 in both [T, E64] and [E64, T] layouts (E64 = E rounded up to 64, zero padded).
-//   2. dW_gate = dg^T x: router_grad_gemm_kernel with M = d (x read MN-major: T is the
-//      reduction axis and x's row index), N = E64 (dg^T K-major), K = T, split along K into
-//      fixed slices whose float32 partials are summed in slice order (deterministic).
-//   3. dx = dg W_gate: the same kernel with M = T (dg K-major), N = 256 columns of d
-//      (W_gate read MN-major), K = E64.
-// The float32 configuration runs steps 2 and 3 as plain SIMT loops.
+//   2. One router_grad_gemm_kernel launch for both gradient products, its tiles taken from a
+//      counter (dW's first):
+//      dW_gate = dg^T x with M = d (x read MN-major: T is the reduction axis and x's row
+//      index), N = E64 (dg^T K-major), K = T, split along K into fixed slices;
+//      dx = dg W_gate with M = T (dg K-major), N = 256 columns of d (W_gate read MN-major),
+//      K = E64.
+//   3. splitk_reduce_kernel sums dW's float32 slices in slice order (deterministic).
+// The float32 configuration runs the two products as plain SIMT loops.
 //
 // The bias update ("Systems for Mixture-of-Experts Models" §3.4; update_bias code block of the
 // "Mixture of Experts 架构" page): b_i -= gamma when expert i's load exceeds the mean load
