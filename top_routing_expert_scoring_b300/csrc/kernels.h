@@ -124,10 +124,10 @@ struct GroupedFFN {
 };
 // true when launch_ffn_tc would run the CTA-pair kernel for g (which needs materialised rows)
 bool ffn_uses_pair(const GroupedFFN& g);
-// Tensor-core path.  Picks the CTA-pair kernel (cta_group::2, 256-row tiles) for one group of
-// >= 512 rows or for experts averaging >= 2048 rows (d % 256 == 0), else the single-CTA
-// kernel; the environment variable MOE_B300_GEMM=single|pair|auto overrides the choice (pair
-// falls back to single when d % 256 != 0).
+// Tensor-core path.  Picks the CTA-pair kernel (cta_group::2, 256-row tiles) for ragged
+// experts averaging >= 2048 rows (d % 256 == 0), else the single-CTA kernel (always for one
+// group of rows, the shared experts); the environment variable MOE_B300_GEMM=single|pair|auto
+// overrides the choice (pair falls back to single when d % 256 != 0).
 cudaError_t launch_ffn_tc(const GroupedFFN& g, DevStatus* st, cudaStream_t s);
 cudaError_t launch_ffn_tc2(const GroupedFFN& g, DevStatus* st, cudaStream_t s);
 cudaError_t launch_ffn_simt(const GroupedFFN& g, bool f32, DevStatus* st, cudaStream_t s);
