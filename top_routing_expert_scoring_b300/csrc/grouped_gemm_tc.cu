@@ -524,9 +524,22 @@ __global__ void __launch_bounds__(ROUTE ? THREADS_ROUTE : THREADS, 1)
         for (int i = 0; i < 8; ++i)
           dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
       };
+      // chunk c of this thread's token row, from the logits phase A wrote (the barrier below
+      // orders those writes before these reads)
+      auto load_row = [&](int c, float (&v)[32]) {
+        const float4* src = reinterpret_cast<const float4*>(p.r_logits + t * E + c * 32);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 f = src[i];
+          v[4 * i] = f.x;
+          v[4 * i + 1] = f.y;
+          v[4 * i + 2] = f.z;
+          v[4 * i + 3] = f.w;
+        }
+      };
       route_phase_a(rc, sm, r, sub, load, each);
       asm volatile("bar.sync 1, 512;" ::: "memory");
-      route_phase_b(rc, sm, r, sub, q, live, load);
+      route_phase_b(rc, sm, r, sub, q, live, load, load_row);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8 * acc);   // this warp is done with TMEM

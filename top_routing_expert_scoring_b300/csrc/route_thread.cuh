@@ -167,12 +167,16 @@ __device__ __forceinline__ RouteTotals route_totals(const RouteSmem& sm, int r) 
   return t;
 }
 
-// Phase B: the group limit (kept chunks), the top-k of this thread's kept chunks into the
-// candidate lists, and this thread's P contributions (column sums of the warp's 32 tokens
-// into sm.P[q]).  live: the slot holds a token.
-template <typename Loader>
+// Phase B: the group limit (kept chunks), this thread's P contributions (column sums of the
+// warp's 32 tokens into sm.P[q]) over its own chunks, and the top-k of its share of the
+// token's kept chunks into the candidate lists.  The kept chunks are dealt out in chunk order
+// (the j-th to thread part j mod 4), so every part of a token gets the same count whichever
+// groups the token keeps, and a warp's threads insert in step; load_row(c, v) reads chunk c of
+// the thread's own token row (any chunk, per thread).  live: the slot holds a token.
+template <typename Loader, typename RowLoader>
 __device__ __forceinline__ void route_phase_b(const RouteThreadCfg& rc, RouteSmem& sm, int r,
-                                              int sub, int q, bool live, Loader load) {
+                                              int sub, int q, bool live, Loader load,
+                                              RowLoader load_row) {
   const bool sig = rc.score == MOE_SCORE_SIGMOID;
   const bool limit = sig && rc.cpg > 0 && rc.select;
   const RouteTotals tot = route_totals(sm, r);
@@ -218,20 +222,42 @@ __device__ __forceinline__ void route_phase_b(const RouteThreadCfg& rc, RouteSme
   for (int c = c0; c < c1; ++c) {
     float v[32], pr[32];
     load(c, v);
-    const bool sel = rc.select && ((kept >> c) & 1u);
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       const float s = sig ? sigm(v[i]) : 0.f;
       pr[i] = live ? (sig ? s * inv_ss : expf(v[i] - tot.m) * inv_se) : 0.f;
-      if (sel) {
-        const int e = c * 32 + i;
-        const float key = sig ? s + sm.bias[e] : v[i];
-        const float val = sig ? s : v[i];
-        if (ranks_before(key, e, bk[kRouteMaxK - 1], bi[kRouteMaxK - 1]))
-          topk_insert(key, e, val, bk, bi, bv);
-      }
     }
     sm.P[q][c * 32 + (threadIdx.x & 31)] = warp_column_sum(pr);
+  }
+  if (rc.select) {
+    // this part's share of the kept chunks: every kRouteSubs-th set bit, from bit `sub`
+    uint32_t mine = 0u;
+    {
+      uint32_t rest = live ? kept & ((rc.nc >= 32) ? 0xffffffffu : ((1u << rc.nc) - 1u)) : 0u;
+      for (int j = 0; rest; ++j) {
+        const uint32_t low = rest & (0u - rest);
+        if ((j % kRouteSubs) == sub) mine |= low;
+        rest ^= low;
+      }
+    }
+#pragma unroll 1
+    while (__any_sync(0xffffffffu, mine != 0u)) {
+      if (mine) {
+        const int c = __ffs(mine) - 1;
+        mine &= mine - 1u;
+        float v[32];
+        load_row(c, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int e = c * 32 + i;
+          const float s = sig ? sigm(v[i]) : 0.f;
+          const float key = sig ? s + sm.bias[e] : v[i];
+          const float val = sig ? s : v[i];
+          if (ranks_before(key, e, bk[kRouteMaxK - 1], bi[kRouteMaxK - 1]))
+            topk_insert(key, e, val, bk, bi, bv);
+        }
+      }
+    }
   }
 #pragma unroll
   for (int j = 0; j < kRouteMaxK; ++j) {

@@ -587,7 +587,7 @@ __global__ void __launch_bounds__(512) route_rows_stats_kernel(const float* __re
   };
   route_phase_a(rc, sm, r, sub, load, [](int, const float (&)[32]) {});
   __syncthreads();
-  route_phase_b(rc, sm, r, sub, q, live, load);
+  route_phase_b(rc, sm, r, sub, q, live, load, load);
   __syncthreads();
   if (sub == 0) {
     const RouteTotals tot = route_totals(sm, r);
