@@ -274,15 +274,15 @@ def test_expert_choice_entry_point():
     assert (rows.cpu().numpy() == csr["rows"]).all()
 
 
-@pytest.mark.parametrize("T", [777, 50000])
+@pytest.mark.parametrize("T,E,k", [(777, 16, 2), (50000, 16, 2), (4096, 256, 8), (300, 96, 5)])
 @pytest.mark.parametrize("kind", ["normal", "few_levels"])
-def test_expert_choice_selection_on_given_logits(T, kind):
+def test_expert_choice_selection_on_given_logits(T, E, k, kind):
     # the selection alone, bit for bit against the oracle: T = 777 keeps the expert's keys in
-    # shared memory, T = 50000 reads them from global memory in every radix pass; "few_levels"
+    # shared memory, T = 50000 reads them from global memory in every radix pass; E = 256 and
+    # E = 96 (C not a multiple of anything in particular) run many CTAs; "few_levels"
     # logits take 7 values only, so each expert's C-th key is tied with thousands of tokens and
     # the lowest token indices must win
     m = U.lib()
-    E, k = 16, 2
     wl = moe_inputs.workload("dsmoe16b_ec", T=T, d=256, E=E, k=k, F=256, F_shared=128)
     cfg = U.config_of(wl)
     rng = np.random.default_rng(11 + T)
