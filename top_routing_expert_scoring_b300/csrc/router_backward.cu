@@ -650,16 +650,17 @@ __global__ void bias_update_kernel(const float* __restrict__ f, float* __restric
 // ---------------------------------------------------------------------------------------------
 struct BwLayout {
   size_t status, counter, dg16, dgT, part, dg32, total;
-  int splits;
+  int splits;         // K slices of dW when the launch also runs dx
+  int splits_alone;   // K slices of dW when it runs alone (no dx requested)
 };
 
 constexpr size_t kAlignBw = 256;
 size_t align_bw(size_t v) { return (v + kAlignBw - 1) & ~(kAlignBw - 1); }
 
-// K slices of the dW GEMM.  Cost in units of one K block of one tile: waves x (blocks per
-// slice + 4 for the pipeline fill), plus the partials' write and read expressed in the same
-// unit (one wave-wide K block moves num_sms x 16 KB of x).
-int dw_splits(const moe_config& c) {
+// K slices of the dW GEMM when it runs alone.  Cost in units of one K block of one tile:
+// waves x (blocks per slice + 4 for the pipeline fill), plus the partials' write and read
+// expressed in the same unit (one wave-wide K block moves num_sms x 16 KB of x).
+int dw_splits_alone(const moe_config& c) {
   const int m_tiles = c.d_model / rg::BM;
   const int KB = ceil_div(c.T, rg::BK);
   const int sms = num_sms();
@@ -678,6 +679,23 @@ int dw_splits(const moe_config& c) {
   return best;
 }
 
+// K slices of the dW GEMM sharing its launch with dx, whose tiles fill the SMs around the dW
+// tiles: the fewest slices whose tile (K blocks per slice) is no longer than the launch's
+// balanced length, all dW and dx work over the SMs, with a dx tile (its 128 KB float32
+// epilogue) counted as 7 K blocks of dW (measured rates).  Fewer slices write and reduce fewer
+// partials: measured, V3 1 slice 107 us against 111 with 2, Mixtral 2 slices 33.5 us against
+// 34.9 with 4, DeepSeekMoE 4 slices equal to 9.
+int dw_splits_merged(const moe_config& c) {
+  const int m_tiles = c.d_model / rg::BM;
+  const int KB = ceil_div(c.T, rg::BK);
+  const int bn = c.d_model % 256 == 0 ? 256 : 128;
+  const double dx_units = (double)ceil_div(c.T, rg::BM) * (c.d_model / bn) * (bn == 256 ? 7.0 : 3.5);
+  const double balanced = ((double)m_tiles * KB + dx_units) / num_sms();
+  for (int s = 1; s <= 32 && s <= KB; ++s)
+    if (ceil_div(KB, s) <= balanced) return s;
+  return KB < 32 ? KB : 32;
+}
+
 BwLayout bw_layout(const moe_config& c) {
   BwLayout L{};
   size_t o = 0;
@@ -690,12 +708,15 @@ BwLayout bw_layout(const moe_config& c) {
   L.status = take(sizeof(DevStatus));
   L.counter = take(sizeof(int));
   if (c.dtype == MOE_DTYPE_BF16) {
-    L.splits = dw_splits(c);
+    L.splits = dw_splits_merged(c);
+    L.splits_alone = dw_splits_alone(c);
     L.dg16 = take(T * E64 * 2);
     L.dgT = take(E64 * T64 * 2);
-    L.part = take(L.splits > 1 ? (size_t)L.splits * E * d * 4 : 0);
+    const int smax = L.splits > L.splits_alone ? L.splits : L.splits_alone;
+    L.part = take(smax > 1 ? (size_t)smax * E * d * 4 : 0);
   } else {
     L.splits = 1;
+    L.splits_alone = 1;
     L.dg32 = take(T * E * 4);
   }
   L.total = o;
@@ -811,12 +832,13 @@ int moe_router_backward(const moe_config* c, const void* x, const void* w_gate,
   p[0].b_mn = 0;
   p[0].m_tiles = d / rg::BM;
   p[0].n_tiles = 1;
-  p[0].splits = L.splits;
+  const int splits = d_x ? L.splits : L.splits_alone;
+  p[0].splits = splits;
   p[0].out_mode = 1;
   p[0].ldo = d;
   p[0].n_valid = E;
   p[0].st = dst;
-  p[0].out = L.splits > 1 ? at_bw<float>(ws, L.part) : d_w_gate;
+  p[0].out = splits > 1 ? at_bw<float>(ws, L.part) : d_w_gate;
   int njobs = 1;
   if (d_x) {
     const int bn = d % 256 == 0 ? 256 : 128;
@@ -840,11 +862,11 @@ int moe_router_backward(const moe_config* c, const void* x, const void* w_gate,
     njobs = 2;
   }
   e = rg::launch(ma, mb, mo, p, njobs, at_bw<int>(ws, L.counter), s);
-  if (e == cudaSuccess && L.splits > 1) {
+  if (e == cudaSuccess && splits > 1) {
     const long long n4 = (long long)E * d / 4;
     launch_pdl(splitk_reduce_kernel, num_sms() * 4, 256, 0, s, at_bw<const float4>(ws, L.part),
                                                         reinterpret_cast<float4*>(d_w_gate), n4,
-                                                        L.splits);
+                                                        splits);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return MOE_ERR_CUDA;
