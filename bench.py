@@ -42,11 +42,11 @@ def load_peaks():
     return PEAKS_FALLBACK, "fallback"
 
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the expert GEMM launches of
-# one step, keyed by (workload, T), from an ncu capture of the bench command on the current
-# kernel build; a workload without a capture on the current build reports null.
-GEMM_TRAFFIC_BYTES = {("v3", 8192): (16824082688 + 266261504) + (7862229760 + 929332992)
-                      + (891870464 + 29169920) + (87099392 + 183482624)}
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the expert GEMM launches that
+# the roofline times (the routed gate/up and down launches of one step), keyed by (workload,
+# T, E), from an ncu capture of the bench command on the current kernel build; a workload
+# without a capture on the current build reports null.
+GEMM_TRAFFIC_BYTES = {("v3", 8192, 256): (16824082688 + 266261504) + (7862229760 + 929332992)}
 
 
 def workload_flops_bytes(wl):
@@ -56,11 +56,25 @@ def workload_flops_bytes(wl):
     bytes = touched expert weights + router weights + x read + out write.
     """
     T, d, E, k, F, Fs = wl.T, wl.d, wl.E, wl.k, wl.F, wl.F_sh
-    ffn = T * k * 3 * 2 * d * F + T * 3 * 2 * d * Fs
+    routed = T * k * 3 * 2 * d * F
+    ffn = routed + T * 3 * 2 * d * Fs
     router = T * 2 * d * E
     weights = (E * 3 * d * F + 3 * d * Fs + E * d) * 2
     act = 2 * T * d * 2
-    return {"flops": ffn + router, "ffn_flops": ffn, "bytes": weights + act}
+    return {"flops": ffn + router, "ffn_flops": ffn, "routed_flops": routed,
+            "bytes": weights + act}
+
+
+def shared_on_side_stream(wl):
+    """Mirrors the library's rule: a bf16 prefill layer's shared experts run on a side stream
+    beside the router and the gather (outside the expert-stage events) unless
+    MOE_B300_SHARED=serial runs them after the routed GEMMs (inside the events)."""
+    if wl.F_sh <= 0 or wl.dtype != "bf16" or os.environ.get("MOE_B300_SHARED") == "serial":
+        return False
+    path = os.environ.get("MOE_B300_PATH")
+    decode = (wl.routing != "expert_choice" and wl.d % 256 == 0
+              and (path == "decode" or (path != "prefill" and wl.T * wl.k <= 64 * wl.E)))
+    return not decode
 
 
 class _Nvml:
@@ -594,23 +608,29 @@ def choose_peak(peaks, peak_kind, clocks):
 
 
 def prefill_figures(wl, ms_step, gemm_ms, clocks, peaks, peak_kind):
-    """Roofline of the expert GEMM stage (routed + shared SwiGLU FLOPs over the CUDA-event time
-    of those launches) and of the whole layer."""
+    """Roofline of the expert GEMM stage (the SwiGLU FLOPs of the launches between the two
+    CUDA events on the launching stream: the routed gate/up and down, plus the shared experts'
+    two when they run on that stream after them) and of the whole layer."""
     fb = workload_flops_bytes(wl)
+    side = shared_on_side_stream(wl)
+    stage_flops = fb["routed_flops"] if side else fb["ffn_flops"]
     gemm_avg = sum(gemm_ms) / len(gemm_ms)
-    tflops = fb["ffn_flops"] / (gemm_avg / 1e3) / 1e12
+    tflops = stage_flops / (gemm_avg / 1e3) / 1e12
     peak, peak_name = choose_peak(peaks, peak_kind, clocks)
     layer_roof_ms = max(fb["flops"] / (peak * 1e12),
                         fb["bytes"] / (peaks["hbm_gbs"] * 1e9)) * 1e3
-    kernel = ("whole expert-choice forward" if wl.routing == "expert_choice" else
-              "grouped GEMM kernel (routed gate/up + down launches, then the shared experts' "
-              "gate/up + down launches, of one step)")
+    kernel = ("grouped GEMM kernel: the routed gate/up + down launches of one step"
+              + ("; the shared experts' two launches run on a side stream beside the router and "
+                 "the gather, outside the timed pair" if side else
+                 (", then the shared experts' gate/up + down launches" if wl.F_sh > 0 else "")))
     return {
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
-                     "frac": tflops / peak, "traffic": GEMM_TRAFFIC_BYTES.get((wl.name, wl.T)),
-                     "traffic_unit": "bytes per step (the expert GEMM launches)",
+                     "frac": tflops / peak,
+                     "traffic": (GEMM_TRAFFIC_BYTES.get((wl.name, wl.T, wl.E))
+                                 if side or wl.F_sh == 0 else None),
+                     "traffic_unit": "bytes per step (the timed expert GEMM launches)",
                      "kernel": kernel, "peak_kind": peak_name,
-                     "flops_per_step": fb["ffn_flops"]},
+                     "flops_per_step": stage_flops},
         "layer_roofline": {"roofline_ms": layer_roof_ms, "frac": layer_roof_ms / ms_step,
                            "flops_per_step": fb["flops"], "bytes_per_step": fb["bytes"]},
         "stage_ms": {"expert_ffn": gemm_avg, "rest": ms_step - gemm_avg},

@@ -17,8 +17,9 @@
  * Conventions (every entry point):
  *   - Returns 0 (MOE_OK) or a negative MOE_ERR_* status; moe_status_string() gives its text.
  *   - Every pointer argument is DEVICE memory owned by the caller unless stated otherwise.
- *     The library allocates and frees nothing and never synchronises the stream; all work is
- *     enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *     The library allocates and frees no memory and never synchronises the stream; all work
+ *     is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream), except as
+ *     moe_forward states for the shared experts.
  *   - Tensors are row-major and contiguous.  "bf16" tensors hold IEEE bfloat16; with
  *     cfg->dtype == MOE_DTYPE_F32 the same tensors hold float32 instead.
  *   - Arguments are validated on the host before any launch (MOE_ERR_ARG / SHAPE /
@@ -204,7 +205,13 @@ int moe_expert_choice(const moe_config* cfg, const float* logits, int32_t* ec_to
  *   x [T,d], w_gate [E,d], bias [E] or NULL, w13, w2, ws13/ws2 (NULL when d_ff_shared == 0)
  *   out [T,d] in cfg->out_dtype (required)
  *   optional outputs (NULL to skip): topk_idx [T,k], topk_w [T,k], f [E], P [E],
- *   l_balance [1], z_loss [1], n_dropped [1] (token choice) */
+ *   l_balance [1], z_loss [1], n_dropped [1] (token choice)
+ * A bf16 prefill layer with shared experts runs their two GEMMs on a side stream of the
+ * library's (one per device and host thread, with two events, created on the first such call
+ * and kept for the thread's life): forked from `stream` before the router and joined back into
+ * it before the routed GEMMs, so the call still orders like one enqueue on `stream` and can be
+ * captured into a CUDA graph.  Creating them can fail (MOE_ERR_CUDA).  The environment variable
+ * MOE_B300_SHARED=serial keeps every launch on `stream`. */
 int moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const float* bias,
                 const void* w13, const void* w2, const void* ws13, const void* ws2, void* out,
                 int32_t* topk_idx, float* topk_w, float* f, float* P, float* l_balance,

@@ -555,11 +555,23 @@ def test_dispatch_oracle_indices_bitexact(T):
     assert torch.equal(x_perm[:nk].cpu(), inp["x"].cpu()[src])
 
 
-def test_forward_replays_in_a_cuda_graph():
-    # every launch of moe_forward is stream-ordered and allocation-free, so a captured forward
-    # replays with identical results
+GRAPH_CASES = {
+    "decode_b16": dict(name="v3", T=16, d=256, E=64, F=256, F_shared=256),
+    # prefill with shared experts: their GEMMs fork onto the side stream and join back
+    "prefill_shared_side": dict(name="v3", T=700, d=256, E=64, F=256, F_shared=256),
+    "expert_choice_shared_side": dict(name="dsmoe16b_ec", T=512, d=256, E=16, k=4, F=128,
+                                      F_shared=256),
+}
+
+
+@pytest.mark.parametrize("case", list(GRAPH_CASES))
+def test_forward_replays_in_a_cuda_graph(case):
+    # every launch of moe_forward is stream-ordered and allocation-free (a side stream forked
+    # from the caller's and joined back is captured with it), so a captured forward replays
+    # with identical results
     m = U.lib()
-    wl = moe_inputs.workload("v3", T=16, d=256, E=64, F=256, F_shared=256)
+    spec = dict(GRAPH_CASES[case])
+    wl = moe_inputs.workload(spec.pop("name"), **spec)
     cfg = U.config_of(wl)
     inp = _inputs(wl)
     ws = m.workspace(cfg)
@@ -580,6 +592,29 @@ def test_forward_replays_in_a_cuda_graph():
     torch.cuda.synchronize()
     assert m.sync_status(ws) == 0
     assert torch.equal(out, eager)
+
+
+@pytest.mark.parametrize("spec", [
+    dict(name="v3", T=700, d=256, E=64, F=256, F_shared=256, capacity_factor=1.25),
+    dict(name="dsmoe16b", T=1500, d=256, E=64, F=128, F_shared=256),
+    dict(name="dsmoe16b_ec", T=512, d=256, E=16, k=4, F=128, F_shared=256),
+    dict(name="v3", T=8192, d=512, E=256, F=128, F_shared=256),
+])
+def test_shared_side_stream_equals_serial(monkeypatch, spec):
+    """Prefill shared experts on the side stream (forked before the router, joined before the
+    routed GEMMs) run the same kernels on the same operands as the serial order: the layer's
+    outputs and statistics are bit-identical."""
+    wl = moe_inputs.workload(**spec)
+    inp = _inputs(wl)
+    monkeypatch.setenv("MOE_B300_SHARED", "serial")
+    a = U.run_forward(wl, inp)
+    monkeypatch.delenv("MOE_B300_SHARED")
+    b = U.run_forward(wl, inp)
+    assert torch.equal(a["out"], b["out"])
+    assert (a["idx"] == b["idx"]).all() and (a["w"] == b["w"]).all()
+    for key in ("f", "P"):
+        assert (a[key] == b[key]).all(), key
+    assert a["l_balance"] == b["l_balance"] and a["z_loss"] == b["z_loss"]
 
 
 @pytest.mark.parametrize("case", ["v3_like", "softmax_cap", "decode_b8", "router_fused_v3_e256",

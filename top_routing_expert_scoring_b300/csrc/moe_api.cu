@@ -1,6 +1,7 @@
 // C ABI of the MoE layer forward: argument checks, workspace layout and the launch sequence.
 // Every entry point validates on the host, enqueues on the caller's stream and returns; the
-// library allocates nothing and never synchronises (except moe_sync_status, which exists to).
+// library allocates no memory and never synchronises (except moe_sync_status, which exists
+// to).  The fused forward forks its shared experts onto a side stream and joins them back.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -89,6 +90,47 @@ bool combine_fused(const moe_config& c, bool dec) {
   if (ffn_uses_pair(probe)) return false;
   const char* env = getenv("MOE_B300_COMBINE");
   return !(env && strcmp(env, "separate") == 0);
+}
+
+// Prefill shared experts on a side stream, forked before the router and joined before the
+// routed GEMMs: the shared experts' two GEMMs read only x, so they run while the router (one
+// CTA per 128 tokens), the dispatch and the row gather hold few SMs or no tensor pipes.  The
+// routed GEMMs reuse the h buffer after the join.  MOE_B300_SHARED=serial runs them after the
+// routed GEMMs on the caller's stream instead.
+bool shared_overlap(const moe_config& c, bool dec) {
+  if (dec || c.d_ff_shared <= 0 || c.dtype != MOE_DTYPE_BF16) return false;
+  const char* env = getenv("MOE_B300_SHARED");
+  return !(env && strcmp(env, "serial") == 0);
+}
+
+// The side stream and its fork and join events: one set per device and host thread, created on
+// first use and kept for the life of the thread.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+SideStream* side_stream() {
+  constexpr int kMaxDevices = 64;
+  thread_local SideStream per_dev[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  SideStream& ss = per_dev[dev];
+  if (!ss.s) {
+    cudaStream_t st = nullptr;
+    cudaEvent_t a = nullptr, b = nullptr;
+    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&a, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&b, cudaEventDisableTiming) != cudaSuccess) {
+      if (a) cudaEventDestroy(a);
+      cudaStreamDestroy(st);
+      return nullptr;
+    }
+    ss.fork = a;
+    ss.join = b;
+    ss.s = st;
+  }
+  return &ss;
 }
 
 bool decode_split_possible(const moe_config& c) {
@@ -533,9 +575,29 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
   };
 
   cudaError_t e = cudaSuccess;
-  if (!(c->routing == MOE_ROUTE_TOKEN_CHOICE && router_fused(*c))) {
+  const bool tc = c->routing == MOE_ROUTE_TOKEN_CHOICE;
+  SideStream* side = nullptr;
+  if (shared && shared_overlap(*c, tc && decode_regime(*c))) {
+    if (!(side = side_stream())) return MOE_ERR_CUDA;
+    if (cudaEventRecord(side->fork, s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  // the shared experts' GEMMs on the side stream, issued right after the router's first launch
+  // so that the router's CTAs take their SMs first
+  auto launch_side = [&]() -> int {
+    if (!side) return MOE_OK;
+    if (cudaStreamWaitEvent(side->s, side->fork, 0) != cudaSuccess) return MOE_ERR_CUDA;
+    const int r = run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13, ws2,
+                          shared, ws, L, side->s);
+    if (r) return r;
+    return cudaEventRecord(side->join, side->s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  };
+  auto join_side = [&]() {
+    return side ? cudaStreamWaitEvent(s, side->join, 0) : cudaSuccess;
+  };
+  if (!(tc && router_fused(*c))) {
     e = launch_router_logits(*c, x, w_gate, g, s, at<float>(ws, L.router_part), dst);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if ((st = launch_side())) return st;
   }
 
   if (c->routing == MOE_ROUTE_TOKEN_CHOICE) {
@@ -544,10 +606,13 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
     // Top-k with the load-balance partials of the same pass (in the router GEMM's epilogue for
     // prefill batches of a wide router); the partials are reduced by an extra CTA of the small
     // dispatch (T <= 256), else after the combine, off the path to the output
-    if (router_fused(*c))
+    if (router_fused(*c)) {
       e = launch_router_fused(*c, x, w_gate, bias, g, idx, w, part_P, part_cnt, part_z, dst, s);
-    else
+      if (e != cudaSuccess) return MOE_ERR_CUDA;
+      if ((st = launch_side())) return st;
+    } else {
       e = launch_route_topk(*c, g, bias, idx, w, dst, s, part_P, part_cnt, part_z);
+    }
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     const bool dec = decode_regime(*c);
     const bool fuse = gather_fused(*c, dec);
@@ -604,7 +669,7 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
       const bool scat = combine_fused(*c, dec);
       if (scat && cudaMemsetAsync(out, 0, (size_t)c->T * c->d_model * 4, s) != cudaSuccess)
         return MOE_ERR_CUDA;
-      if (mark(ev_begin) != cudaSuccess) return MOE_ERR_CUDA;
+      if (join_side() != cudaSuccess || mark(ev_begin) != cudaSuccess) return MOE_ERR_CUDA;
       // y leaves the down GEMM in bf16 when a combine pass reads it back
       const bool ybf = !scat && bf16(*c);
       if ((st = run_ffn(*c, at<void>(ws, L.x_perm), b.offsets, b.mtile_prefix, -1, c->E,
@@ -613,8 +678,9 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
                         scat ? static_cast<float*>(out) : nullptr, scat ? b.perm : nullptr,
                         scat ? w : nullptr, ybf)))
         return st;
-      if (shared && (st = run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13,
-                                  ws2, shared, ws, L, s)))
+      if (shared && !side &&
+          (st = run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13, ws2,
+                        shared, ws, L, s)))
         return st;
       if (mark(ev_end) != cudaSuccess) return MOE_ERR_CUDA;
       if (!scat) {
@@ -640,15 +706,16 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
   if ((e = launch_gather_ec(*c, ec_tokens, x, at<void>(ws, L.x_perm), at<int32_t>(ws, L.offsets),
                             at<int32_t>(ws, L.mtp), s)) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (mark(ev_begin) != cudaSuccess) return MOE_ERR_CUDA;
+  if (join_side() != cudaSuccess || mark(ev_begin) != cudaSuccess) return MOE_ERR_CUDA;
   const bool ybf = bf16(*c);
   if ((st = run_ffn(*c, at<void>(ws, L.x_perm), at<int32_t>(ws, L.offsets),
                     at<int32_t>(ws, L.mtp), -1, c->E, c->d_ff, c->E * C, w13, w2,
                     at<float>(ws, L.y_perm), ws, L, s, nullptr, nullptr, nullptr, nullptr,
                     nullptr, ybf)))
     return st;
-  if (shared && (st = run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13, ws2,
-                              shared, ws, L, s)))
+  if (shared && !side &&
+      (st = run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13, ws2, shared,
+                    ws, L, s)))
     return st;
   if (mark(ev_end) != cudaSuccess) return MOE_ERR_CUDA;
   if ((e = launch_combine_ec(*c, at<void>(ws, L.y_perm), ybf, at<int32_t>(ws, L.tok_ptr),
