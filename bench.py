@@ -7,8 +7,9 @@ One step = one whole layer forward (router GEMM, scoring/Top-k, statistics, disp
 SwiGLU expert GEMMs, shared experts, combine) over one batch of synthetic tokens already in HBM.
 The headline workload is the largest single-GPU layer, the DeepSeek-V3-shaped prefill layer
 (T=8192, d=7168, 256 routed experts + 1 shared, top-8 of 8 groups keep 4).  The timed step is
-moe_forward_timed: moe_forward's kernels, with two CUDA events recorded around the expert GEMM
-launches (routed, then shared) so that the grouped GEMM's share is measured live.
+moe_forward_timed: moe_forward's kernels, with two CUDA events recorded around the routed expert
+GEMM launches (the shared experts' two run on a side stream beside the router, outside them) so
+that the grouped GEMM's share is measured live.
 After the headline, the same JSON line carries the other prefill layers (`per_config`: the
 Mixtral-8x7B-shaped layer balanced and collapsed, DeepSeekMoE-16B token choice and expert
 choice) and the decode-batch sweep (`decode`: B = 1, 8, 64, 256 on the V3- and Mixtral-shaped

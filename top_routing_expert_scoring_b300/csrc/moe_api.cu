@@ -577,14 +577,15 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
   cudaError_t e = cudaSuccess;
   const bool tc = c->routing == MOE_ROUTE_TOKEN_CHOICE;
   SideStream* side = nullptr;
-  if (shared && shared_overlap(*c, tc && decode_regime(*c))) {
+  const bool side_ffn = shared && shared_overlap(*c, tc && decode_regime(*c));
+  if (side_ffn) {
     if (!(side = side_stream())) return MOE_ERR_CUDA;
     if (cudaEventRecord(side->fork, s) != cudaSuccess) return MOE_ERR_CUDA;
   }
   // the shared experts' GEMMs on the side stream, issued right after the router's first launch
   // so that the router's CTAs take their SMs first
   auto launch_side = [&]() -> int {
-    if (!side) return MOE_OK;
+    if (!side_ffn) return MOE_OK;
     if (cudaStreamWaitEvent(side->s, side->fork, 0) != cudaSuccess) return MOE_ERR_CUDA;
     const int r = run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13, ws2,
                           shared, ws, L, side->s);
@@ -678,7 +679,7 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
                         scat ? static_cast<float*>(out) : nullptr, scat ? b.perm : nullptr,
                         scat ? w : nullptr, ybf)))
         return st;
-      if (shared && !side &&
+      if (shared && !side_ffn &&
           (st = run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13, ws2,
                         shared, ws, L, s)))
         return st;
@@ -713,7 +714,7 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
                     at<float>(ws, L.y_perm), ws, L, s, nullptr, nullptr, nullptr, nullptr,
                     nullptr, ybf)))
     return st;
-  if (shared && !side &&
+  if (shared && !side_ffn &&
       (st = run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13, ws2, shared,
                     ws, L, s)))
     return st;
