@@ -94,9 +94,9 @@ bool combine_fused(const moe_config& c, bool dec) {
 
 // Prefill shared experts on a side stream, forked before the router and joined before the
 // routed GEMMs: the shared experts' two GEMMs read only x, so they run while the router (one
-// CTA per 128 tokens), the dispatch and the row gather hold few SMs or no tensor pipes.  The
-// routed GEMMs reuse the h buffer after the join.  MOE_B300_SHARED=serial runs them after the
-// routed GEMMs on the caller's stream instead.
+// CTA per 128 tokens), the dispatch and the row gather hold few SMs or no tensor pipes.  Their
+// h rows sit after the routed rows' h in the workspace, so the two never share bytes.
+// MOE_B300_SHARED=serial runs them after the routed GEMMs on the caller's stream instead.
 bool shared_overlap(const moe_config& c, bool dec) {
   if (dec || c.d_ff_shared <= 0 || c.dtype != MOE_DTYPE_BF16) return false;
   const char* env = getenv("MOE_B300_SHARED");
@@ -415,7 +415,7 @@ int run_ffn(const moe_config& c, const void* xin, const int32_t* offsets, const 
             float* y, void* ws, const Layout& L, cudaStream_t s,
             const int32_t* gather_perm = nullptr, const void* gather_x = nullptr,
             float* scatter_out = nullptr, const int32_t* scatter_perm = nullptr,
-            const float* scatter_w = nullptr, bool y_bf16 = false) {
+            const float* scatter_w = nullptr, bool y_bf16 = false, void* h = nullptr) {
   GroupedFFN g{};
   g.y_bf16 = y_bf16 && bf16(c) ? 1 : 0;
   g.gather_perm = gather_perm;
@@ -434,7 +434,7 @@ int run_ffn(const moe_config& c, const void* xin, const int32_t* offsets, const 
   g.max_rows = max_rows;
   g.w13 = w13;
   g.w2 = w2;
-  g.h = at<void>(ws, L.h);
+  g.h = h ? h : at<void>(ws, L.h);
   g.y = y;
   DevStatus* st = at<DevStatus>(ws, L.status);
   cudaError_t e = bf16(c) ? launch_ffn_tc(g, st, s) : launch_ffn_simt(g, true, st, s);
@@ -582,18 +582,27 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
     if (!(side = side_stream())) return MOE_ERR_CUDA;
     if (cudaEventRecord(side->fork, s) != cudaSuccess) return MOE_ERR_CUDA;
   }
+  // the shared experts' h rows sit after the routed rows' h, so the two never share bytes
+  void* shared_h = at<uint8_t>(ws, L.h) + (size_t)rows_max(*c) * c->d_ff * 2;
   // the shared experts' GEMMs on the side stream, issued right after the router's first launch
   // so that the router's CTAs take their SMs first
   auto launch_side = [&]() -> int {
     if (!side_ffn) return MOE_OK;
     if (cudaStreamWaitEvent(side->s, side->fork, 0) != cudaSuccess) return MOE_ERR_CUDA;
     const int r = run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13, ws2,
-                          shared, ws, L, side->s);
+                          shared, ws, L, side->s, nullptr, nullptr, nullptr, nullptr, nullptr,
+                          false, shared_h);
     if (r) return r;
     return cudaEventRecord(side->join, side->s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
   };
   auto join_side = [&]() {
     return side ? cudaStreamWaitEvent(s, side->join, 0) : cudaSuccess;
+  };
+  // without the side stream the shared FFN runs after the routed GEMMs
+  auto shared_after = [&]() -> int {
+    if (!shared || side_ffn) return MOE_OK;
+    return run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13, ws2, shared,
+                   ws, L, s);
   };
   if (!(tc && router_fused(*c))) {
     e = launch_router_logits(*c, x, w_gate, g, s, at<float>(ws, L.router_part), dst);
@@ -679,10 +688,7 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
                         scat ? static_cast<float*>(out) : nullptr, scat ? b.perm : nullptr,
                         scat ? w : nullptr, ybf)))
         return st;
-      if (shared && !side_ffn &&
-          (st = run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13, ws2,
-                        shared, ws, L, s)))
-        return st;
+      if ((st = shared_after())) return st;
       if (mark(ev_end) != cudaSuccess) return MOE_ERR_CUDA;
       if (!scat) {
         e = ybf ? launch_combine_bf16y(*c, at<void>(ws, L.y_perm), b.row_of, w, shared, out, s)
@@ -714,10 +720,7 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
                     at<float>(ws, L.y_perm), ws, L, s, nullptr, nullptr, nullptr, nullptr,
                     nullptr, ybf)))
     return st;
-  if (shared && !side_ffn &&
-      (st = run_ffn(*c, x, nullptr, nullptr, c->T, 1, c->d_ff_shared, c->T, ws13, ws2, shared,
-                    ws, L, s)))
-    return st;
+  if ((st = shared_after())) return st;
   if (mark(ev_end) != cudaSuccess) return MOE_ERR_CUDA;
   if ((e = launch_combine_ec(*c, at<void>(ws, L.y_perm), ybf, at<int32_t>(ws, L.tok_ptr),
                              at<int32_t>(ws, L.tok_rows), ec_w, shared, out, s)) != cudaSuccess)
