@@ -594,6 +594,47 @@ def test_forward_replays_in_a_cuda_graph(case):
     assert torch.equal(out, eager)
 
 
+def test_first_forward_captured_in_a_new_thread():
+    """A host thread whose first prefill forward with shared experts is captured into a graph:
+    the side stream is not created during the capture, so the shared experts run on the
+    captured stream, and the replay equals the eager forward bit for bit."""
+    import threading
+    m = U.lib()
+    wl = moe_inputs.workload("v3", T=700, d=256, E=64, F=256, F_shared=256)
+    cfg = U.config_of(wl)
+    inp = _inputs(wl)
+    ws = m.workspace(cfg)
+    out = torch.empty((wl.T, wl.d), dtype=torch.float32, device=DEV)
+
+    def fwd():
+        m.moe_forward(cfg, inp["x"], inp["w_gate"], inp["bias"], inp["w13"], inp["w2"],
+                      inp["ws13"], inp["ws2"], out, ws=ws)
+    fwd()
+    torch.cuda.synchronize()
+    eager = out.clone()
+    out.zero_()
+    torch.cuda.synchronize()
+    box = {}
+    dev_index = torch.cuda.current_device()
+
+    def worker():
+        try:
+            torch.cuda.set_device(dev_index)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fwd()
+            g.replay()
+            torch.cuda.synchronize()
+        except Exception as exc:      # reported on the test's thread
+            box["err"] = exc
+    t = threading.Thread(target=worker)
+    t.start()
+    t.join()
+    assert "err" not in box, box.get("err")
+    assert m.sync_status(ws) == 0
+    assert torch.equal(out, eager)
+
+
 @pytest.mark.parametrize("spec", [
     dict(name="v3", T=700, d=256, E=64, F=256, F_shared=256, capacity_factor=1.25),
     dict(name="dsmoe16b", T=1500, d=256, E=64, F=128, F_shared=256),

@@ -104,27 +104,37 @@ bool shared_overlap(const moe_config& c, bool dec) {
 }
 
 // The side stream and its fork and join events: one set per device and host thread, created on
-// first use and kept for the life of the thread.
+// first use and kept for the life of the thread.  They are not created while the caller's
+// stream is being captured into a graph (creation could end a global-mode capture); the call
+// then runs the shared experts on the caller's stream (same kernels, same results).
 struct SideStream {
   cudaStream_t s = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
 };
 
-SideStream* side_stream() {
+SideStream* side_stream(cudaStream_t caller) {
   constexpr int kMaxDevices = 64;
   thread_local SideStream per_dev[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   SideStream& ss = per_dev[dev];
   if (!ss.s) {
+    // a failed query or creation leaves no error behind for the launches that follow
+    auto give_up = []() -> SideStream* {
+      (void)cudaGetLastError();
+      return nullptr;
+    };
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(caller, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+      return give_up();
     cudaStream_t st = nullptr;
     cudaEvent_t a = nullptr, b = nullptr;
-    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return give_up();
     if (cudaEventCreateWithFlags(&a, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&b, cudaEventDisableTiming) != cudaSuccess) {
       if (a) cudaEventDestroy(a);
       cudaStreamDestroy(st);
-      return nullptr;
+      return give_up();
     }
     ss.fork = a;
     ss.join = b;
@@ -576,12 +586,10 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
 
   cudaError_t e = cudaSuccess;
   const bool tc = c->routing == MOE_ROUTE_TOKEN_CHOICE;
-  SideStream* side = nullptr;
-  const bool side_ffn = shared && shared_overlap(*c, tc && decode_regime(*c));
-  if (side_ffn) {
-    if (!(side = side_stream())) return MOE_ERR_CUDA;
-    if (cudaEventRecord(side->fork, s) != cudaSuccess) return MOE_ERR_CUDA;
-  }
+  SideStream* side = shared && shared_overlap(*c, tc && decode_regime(*c)) ? side_stream(s)
+                                                                           : nullptr;
+  const bool side_ffn = side != nullptr;
+  if (side_ffn && cudaEventRecord(side->fork, s) != cudaSuccess) return MOE_ERR_CUDA;
   // the shared experts' h rows sit after the routed rows' h, so the two never share bytes
   void* shared_h = at<uint8_t>(ws, L.h) + (size_t)rows_max(*c) * c->d_ff * 2;
   // the shared experts' GEMMs on the side stream, issued right after the router's first launch
