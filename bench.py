@@ -47,7 +47,13 @@ def load_peaks():
 # the roofline times (the routed gate/up and down launches of one step), keyed by (workload,
 # T, E), from an ncu capture of the bench command on the current kernel build; a workload
 # without a capture on the current build reports null.
-GEMM_TRAFFIC_BYTES = {("v3", 8192, 256): (16824082688 + 266261504) + (7862229760 + 929332992)}
+GEMM_TRAFFIC_BYTES = {
+    ("v3", 8192, 256): (16824082688 + 266261504) + (7862229760 + 929332992),
+    ("mixtral", 4096, 8): (1948641024 + 226491136) + (1553855744 + 122539776),
+    ("mixtral_collapsed", 4096, 8): (1963653888 + 229137664) + (1768455936 + 124471808),
+    ("dsmoe16b", 8192, 64): (953357056 + 125698560) + (517015552 + 171648256),
+    ("dsmoe16b_ec", 8192, 64): (939601152 + 123286272) + (507836160 + 171243520),
+}
 
 
 def workload_flops_bytes(wl):
