@@ -29,3 +29,35 @@ def test_reference_arm_prints_one_contract_line():
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_prefill_roofline_counts_the_launches_between_the_stage_events(monkeypatch):
+    """With the shared experts on the side stream (a bf16 prefill layer's default) the stage
+    events bracket the routed GEMM launches only, so the roofline counts the routed SwiGLU
+    FLOPs; MOE_B300_SHARED=serial puts the shared launches inside the events and counts both.
+    The launches' measured DRAM traffic is reported only for the set it was captured on."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import moe_inputs
+    wl = moe_inputs.workload("dsmoe16b")
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+    clocks = {"sm_mhz": 2032, "sm_max_mhz": 2032}
+    fb = bench.workload_flops_bytes(wl)
+    routed = wl.T * wl.k * 3 * 2 * wl.d * wl.F
+    assert fb["routed_flops"] == routed
+    assert fb["ffn_flops"] == routed + wl.T * 3 * 2 * wl.d * wl.F_sh
+    monkeypatch.delenv("MOE_B300_SHARED", raising=False)
+    monkeypatch.delenv("MOE_B300_PATH", raising=False)
+    side = bench.prefill_figures(wl, 1.0, [0.5, 0.5], clocks, peaks, "measured")
+    assert side["roofline"]["flops_per_step"] == routed
+    assert abs(side["roofline"]["achieved"] - routed / 0.5e-3 / 1e12) < 1e-6
+    assert side["roofline"]["traffic"] == bench.GEMM_TRAFFIC_BYTES[("dsmoe16b", 8192, 64)]
+    monkeypatch.setenv("MOE_B300_SHARED", "serial")
+    serial = bench.prefill_figures(wl, 1.0, [0.5, 0.5], clocks, peaks, "measured")
+    assert serial["roofline"]["flops_per_step"] == fb["ffn_flops"]
+    assert serial["roofline"]["traffic"] is None
+    # a decode-sized batch never uses the side stream
+    monkeypatch.delenv("MOE_B300_SHARED")
+    assert not bench.shared_on_side_stream(wl.replace(T=64))
+    assert bench.shared_on_side_stream(wl)
+    assert not bench.shared_on_side_stream(moe_inputs.workload("mixtral"))
