@@ -208,7 +208,7 @@ int moe_expert_choice(const moe_config* cfg, const float* logits, int32_t* ec_to
  *   l_balance [1], z_loss [1], n_dropped [1] (token choice)
  * A bf16 prefill layer with shared experts runs their two GEMMs on a side stream of the
  * library's (one per device and host thread, with two events, created on the first such call
- * and kept for the thread's life): forked from `stream` before the router and joined back into
+ * and never destroyed): forked from `stream` before the router and joined back into
  * it before the routed GEMMs, so the call still orders like one enqueue on `stream` and can be
  * captured into a CUDA graph.  If they cannot be created, or the first such call comes while
  * `stream` is being captured, the shared experts run on `stream` after the routed GEMMs (same

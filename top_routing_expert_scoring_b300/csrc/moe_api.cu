@@ -104,7 +104,8 @@ bool shared_overlap(const moe_config& c, bool dec) {
 }
 
 // The side stream and its fork and join events: one set per device and host thread, created on
-// first use and kept for the life of the thread.  They are not created while the caller's
+// first use and never destroyed (no CUDA call runs from a destructor at thread or process
+// exit, when the runtime may already be gone).  They are not created while the caller's
 // stream is being captured into a graph (creation could end a global-mode capture); the call
 // then runs the shared experts on the caller's stream (same kernels, same results).
 struct SideStream {
