@@ -61,3 +61,19 @@ def test_prefill_roofline_counts_the_launches_between_the_stage_events(monkeypat
     assert not bench.shared_on_side_stream(wl.replace(T=64))
     assert bench.shared_on_side_stream(wl)
     assert not bench.shared_on_side_stream(moe_inputs.workload("mixtral"))
+
+
+def test_peak_follows_the_power_cap_of_the_timed_region():
+    """Burst peak at full clock; the sustained (power-capped) peak when the median clock sat
+    below 95% of the maximum or the power-cap reason held for at least half of the samples."""
+    sys.path.insert(0, ROOT)
+    import bench
+    peaks = {"bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+    full = {"sm_mhz": 2032, "sm_max_mhz": 2032, "reason_share": {"sw_power_cap": 0.1}}
+    assert bench.choose_peak(peaks, "measured", full)[0] == 1800.0
+    slow = {"sm_mhz": 1837, "sm_max_mhz": 2032, "reason_share": {}}
+    assert bench.choose_peak(peaks, "measured", slow)[0] == 1400.0
+    capped = {"sm_mhz": 1935, "sm_max_mhz": 2032, "reason_share": {"sw_power_cap": 0.9}}
+    peak, kind = bench.choose_peak(peaks, "measured", capped)
+    assert peak == 1400.0 and "90%" in kind
+    assert bench.choose_peak(peaks, "measured", {"sm_mhz": None})[0] == 1800.0
