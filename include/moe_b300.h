@@ -219,10 +219,11 @@ int moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const 
                 float* z_loss, int32_t* n_dropped, void* ws, void* stream);
 
 /* moe_forward that also records two caller-created CUDA events (cudaEvent_t, timing enabled)
- * on `stream` around the expert GEMM launches: the routed experts' grouped GEMMs followed by
- * the shared experts' GEMMs (prefill), or the routed and shared experts' decode GEMMs.  Same
- * kernels and results as moe_forward; for measuring the GEMM share of a forward.  Both events
- * are required. */
+ * on `stream` around the expert GEMM launches on `stream`: the routed experts' grouped GEMMs,
+ * followed by the shared experts' GEMMs when those run on `stream` (prefill without the side
+ * stream), or the routed and shared experts' decode GEMMs.  With the side stream the shared
+ * experts' GEMMs run beside the router, outside the events.  Same kernels and results as
+ * moe_forward; for measuring the GEMM share of a forward.  Both events are required. */
 int moe_forward_timed(const moe_config* cfg, const void* x, const void* w_gate, const float* bias,
                       const void* w13, const void* w2, const void* ws13, const void* ws2,
                       void* out, int32_t* topk_idx, float* topk_w, float* f, float* P,
