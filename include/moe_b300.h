@@ -210,7 +210,9 @@ int moe_expert_choice(const moe_config* cfg, const float* logits, int32_t* ec_to
  * library's (one per device and host thread, with two events, created on the first such call
  * and never destroyed): forked from `stream` before the router and joined back into
  * it before the routed GEMMs, so the call still orders like one enqueue on `stream` and can be
- * captured into a CUDA graph.  If they cannot be created, or the first such call comes while
+ * captured into a CUDA graph.  Calls from one host thread on different streams share the side
+ * stream, so their shared-expert GEMMs run in call order.  If they cannot be created, or the
+ * first such call comes while
  * `stream` is being captured, the shared experts run on `stream` after the routed GEMMs (same
  * kernels, same results).  The environment variable MOE_B300_SHARED=serial always does so. */
 int moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const float* bias,
