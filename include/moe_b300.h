@@ -212,9 +212,9 @@ int moe_expert_choice(const moe_config* cfg, const float* logits, int32_t* ec_to
  * it before the routed GEMMs, so the call still orders like one enqueue on `stream` and can be
  * captured into a CUDA graph.  Calls from one host thread on different streams share the side
  * stream, so their shared-expert GEMMs run in call order.  If they cannot be created, or the
- * first such call comes while
- * `stream` is being captured, the shared experts run on `stream` after the routed GEMMs (same
- * kernels, same results).  The environment variable MOE_B300_SHARED=serial always does so. */
+ * first such call comes while `stream` is being captured, the shared experts run on `stream`
+ * after the routed GEMMs (same kernels, same results).  The environment variable
+ * MOE_B300_SHARED=serial always does so. */
 int moe_forward(const moe_config* cfg, const void* x, const void* w_gate, const float* bias,
                 const void* w13, const void* w2, const void* ws13, const void* ws2, void* out,
                 int32_t* topk_idx, float* topk_w, float* f, float* P, float* l_balance,
