@@ -4,6 +4,7 @@
 // to).  The fused forward forks its shared experts onto a side stream and joins them back.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -150,26 +151,43 @@ bool decode_split_possible(const moe_config& c) {
 
 // K slices of a decode GEMM.  The expected experts touched by T tokens, E(1 - (1 - k/E)^T)
 // ("Systems for MoE Models" §1.4), plus the shared experts, give the tile count; each slice
-// count ks is costed in units of one K block streamed by every SM:
-//   ceil(tiles * ks / SMs) * (ceil(kblocks / ks) + 1)          waves x (blocks per tile + fill)
-//   + (ks - 1) * 2 * partial_bytes / (SMs * 32 KB)             extra partials written and read
-// and the cheapest (fewest slices on ties) is taken, at most kMaxSplit.  With 8 or more waves
-// unsplit the tail wave is a small share of a weight stream that runs at full bandwidth
-// anyway, and slicing only adds partials and a finalize pass: one slice (measured on
-// DeepSeek-V3- and Mixtral-shaped decode batches).
+// count ks is costed in units of one K block streamed by every SM at the HBM rate.  The
+// kernel streams weights, so a round of n < SMs active CTAs (the last, partial one) runs each
+// CTA faster than a full round, up to kSmRate times an SM's share of the HBM rate (one CTA's
+// ring of TMA loads in flight sets that ceiling; fitted to Mixtral-shaped down GEMMs, whose
+// one unsplit round of 32 CTAs ran ~1.5x an SM's share):
+//   full rounds x blocks per tile + blocks per tile / min(kSmRate, SMs / n)   the weight stream
+//   + 1                                                                       the ring's fill
+//   + (ks - 1) * 2 * partial_bytes / (SMs * 32 KB)                            extra partials
+// and the cheapest (fewest slices on ties) is taken, at most kMaxSplit.  A round that already
+// holds most of the SMs thus gains nothing from slicing.  With 8 or more rounds unsplit the
+// tail is a small share of the stream: one slice.  MOE_B300_SPLITMODEL=waves restores the
+// earlier cost, rounds x (blocks per tile + 1), which charges every round as a full one.
+constexpr double kSmRate = 1.5;
+
 int split_by_waves(const moe_config& c, int tiles_per_entry, int kblocks, double partial_bytes) {
   const double touched = c.E * (1.0 - std::pow(1.0 - (double)c.k / c.E, (double)c.T));
   const double entries = touched + (c.d_ff_shared > 0 ? 1.0 : 0.0);
   const long long tiles = (long long)std::ceil(entries * tiles_per_entry);
   const int sms = num_sms();
   if (tiles >= 8ll * sms) return 1;
+  const char* env = getenv("MOE_B300_SPLITMODEL");
+  const bool waves_model = env && strcmp(env, "waves") == 0;
   const double unit = (double)sms * 32768.0;     // one 256-row weight K block on every SM
   int best = 1;
   double best_cost = 1e300;
   for (int ks = 1; ks <= kMaxSplit && ks <= kblocks; ++ks) {
-    const double waves = (double)((tiles * ks + sms - 1) / sms);
-    const double cost = waves * (double)((kblocks + ks - 1) / ks + 1) +
-                        (ks - 1) * 2.0 * partial_bytes / unit;
+    const long long n = tiles * ks;
+    const double kb = (double)((kblocks + ks - 1) / ks);
+    double stream;
+    if (waves_model) {
+      stream = (double)((n + sms - 1) / sms) * (kb + 1.0);
+    } else {
+      const long long rest = n % sms;
+      stream = (double)(n / sms) * kb + 1.0;
+      if (rest) stream += kb / std::min(kSmRate, (double)sms / (double)rest);
+    }
+    const double cost = stream + (ks - 1) * 2.0 * partial_bytes / unit;
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = ks;
@@ -178,8 +196,19 @@ int split_by_waves(const moe_config& c, int tiles_per_entry, int kblocks, double
   return best;
 }
 
-int decode_split(const moe_config& c, int tiles_per_entry, int kblocks, double partial_bytes) {
+// K slices of the bf16 decode gate/up (which = 1) or down (which = 2) GEMM.  The environment
+// variables MOE_B300_KSPLIT1 / MOE_B300_KSPLIT2 fix the count (clamped to 1..kMaxSplit and the
+// K blocks), for measuring the cost model against other choices.
+int decode_split(const moe_config& c, int tiles_per_entry, int kblocks, double partial_bytes,
+                 int which) {
   if (!decode_split_possible(c)) return 1;
+  const char* env = getenv(which == 1 ? "MOE_B300_KSPLIT1" : "MOE_B300_KSPLIT2");
+  if (env && *env) {
+    int ks = atoi(env);
+    if (ks > kMaxSplit) ks = kMaxSplit;
+    if (ks > kblocks) ks = kblocks;
+    return ks < 1 ? 1 : ks;
+  }
   return split_by_waves(c, tiles_per_entry, kblocks, partial_bytes);
 }
 
@@ -502,7 +531,7 @@ int moe_expert_ffn(const moe_config* c, const void* x_perm, const int32_t* offse
     g.h = at<void>(ws, L.h);
     g.y = y_perm;
     g.ksplit1 = decode_split(*c, c->d_ff / 128, c->d_model / 64,
-                             (double)g.max_rows * 2 * c->d_ff * 4);
+                             (double)g.max_rows * 2 * c->d_ff * 4, 1);
     g.ksplit2 = 1;                          // the caller's y_perm holds one slice
     g.gu = g.ksplit1 > 1 ? at<float>(ws, L.dec_gu) : nullptr;
     g.y_part_stride = (size_t)rows_max(*c) * c->d_model;
@@ -667,12 +696,12 @@ int forward_impl(const moe_config* c, const void* x, const void* w_gate, const f
       g.h = at<void>(ws, L.h);
       const int Fmx = c->d_ff > c->d_ff_shared ? c->d_ff : c->d_ff_shared;
       g.ksplit1 = decode_split(*c, c->d_ff / 128, c->d_model / 64,
-                               (double)g.max_rows * 2 * Fmx * 4);
+                               (double)g.max_rows * 2 * Fmx * 4, 1);
       // every K slice must hold at least one 64-wide block of both the routed and shared K
       const int kb2 = (c->d_ff_shared > 0 && c->d_ff_shared < c->d_ff ? c->d_ff_shared
                                                                       : c->d_ff) / 64;
       g.ksplit2 = decode_split(*c, c->d_model / 256, kb2,
-                               (double)(rows_max(*c) + (shared ? c->T : 0)) * c->d_model * 4);
+                               (double)(rows_max(*c) + (shared ? c->T : 0)) * c->d_model * 4, 2);
       g.gu = g.ksplit1 > 1 ? at<float>(ws, L.dec_gu) : nullptr;
       g.y = g.ksplit2 > 1 ? at<float>(ws, L.dec_y) : at<float>(ws, L.y_perm);
       g.shared_out = g.ksplit2 > 1 ? at<float>(ws, L.dec_sh) : shared;
