@@ -141,6 +141,22 @@ def test_small_layer_parity(case, monkeypatch):
     print(case, report)
 
 
+@pytest.mark.parametrize("case,ks1,ks2", [("decode_b8", 3, 3), ("decode_b8", 8, 1),
+                                         ("decode_b1", 5, 3), ("decode_collapsed_b256", 3, 3)])
+def test_decode_forced_k_slices(case, ks1, ks2, monkeypatch):
+    """The decode GEMMs with K cut into slice counts the cost model may not pick (uneven
+    slices of the K blocks, and a count above the K blocks, clamped), partials summed in slice
+    order: the layer against the oracle under the same bar."""
+    monkeypatch.setenv("MOE_B300_KSPLIT1", str(ks1))
+    monkeypatch.setenv("MOE_B300_KSPLIT2", str(ks2))
+    spec = dict(SMALL[case])
+    wl = moe_inputs.workload(spec.pop("name"), **spec)
+    inp = _inputs(wl)
+    report = {}
+    _full_check(wl, inp, report, U.OUT_TOL_BF16)
+    print(case, ks1, ks2, report)
+
+
 @pytest.mark.parametrize("case", ["v3_like", "softmax_cap"])
 def test_bf16_output(case, monkeypatch):
     # the layer output rounded once to bf16: the bound adds that rounding (2^-8 |out|).  The
