@@ -605,12 +605,13 @@ class Prefill:
 def choose_peak(peaks, peak_kind, clocks):
     """Burst bf16 peak while the GPU held its clock; the sustained (power-capped) peak when the
     timed region ran under the power cap: its median SM clock sat materially below the maximum,
-    or the power-cap reason was active in at least half of its clock samples (a cap flag raised
-    now and then at full clock does not count)."""
-    low = bool(clocks.get("sm_mhz") and clocks.get("sm_max_mhz")
-               and clocks["sm_mhz"] < 0.95 * clocks["sm_max_mhz"])
+    or the power-cap reason was active in at least half of its clock samples while the median
+    clock sat below the maximum (a cap flag at full clock does not count)."""
+    mhz, top = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    low = bool(mhz and top and mhz < 0.95 * top)
+    below = bool(mhz and top and mhz < 0.99 * top)
     cap_share = clocks.get("reason_share", {}).get("sw_power_cap", 0.0)
-    if (low or cap_share >= 0.5) and "bf16_tflops_sustained" in peaks:
+    if (low or (below and cap_share >= 0.5)) and "bf16_tflops_sustained" in peaks:
         why = ("timed region ran below 95% of the maximum SM clock" if low else
                f"power cap active in {cap_share:.0%} of the timed region's clock samples")
         return float(peaks["bf16_tflops_sustained"]), f"{peak_kind} bf16 sustained ({why})"

@@ -65,7 +65,8 @@ def test_prefill_roofline_counts_the_launches_between_the_stage_events(monkeypat
 
 def test_peak_follows_the_power_cap_of_the_timed_region():
     """Burst peak at full clock; the sustained (power-capped) peak when the median clock sat
-    below 95% of the maximum or the power-cap reason held for at least half of the samples."""
+    below 95% of the maximum, or the power-cap reason held for at least half of the samples
+    while the median clock sat below the maximum."""
     sys.path.insert(0, ROOT)
     import bench
     peaks = {"bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
@@ -77,3 +78,6 @@ def test_peak_follows_the_power_cap_of_the_timed_region():
     peak, kind = bench.choose_peak(peaks, "measured", capped)
     assert peak == 1400.0 and "90%" in kind
     assert bench.choose_peak(peaks, "measured", {"sm_mhz": None})[0] == 1800.0
+    # the cap flag raised while the clock held its maximum does not count
+    held = {"sm_mhz": 2032, "sm_max_mhz": 2032, "reason_share": {"sw_power_cap": 1.0}}
+    assert bench.choose_peak(peaks, "measured", held)[0] == 1800.0
